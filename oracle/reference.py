@@ -1,0 +1,383 @@
+"""Plain, slow CPU oracle for the trainable sparse-attention hot path.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path may import, call or
+execute this module: only the tests, the package's ``smoke()`` check and the
+bench's CPU-baseline / reference arm use it.  It shares no code with the CUDA
+library (no kernels, headers, tables or helpers); both sides are fed from the
+seeded generators in ``synth``.
+
+Everything is computed in float64 from the exact values of the bf16 inputs.
+The one place where floating point decides an integer (which keys the top-k
+selects) is taken in fp32, the precision the kernels decide in: each indexer
+score is computed in fp64 and rounded to fp32 once.
+
+Sources (web pages, cited by title and section):
+  [QSA]  Megatron-LM issue #7060 "Add trainable QSA sparse attention with a
+         TileLang backend" -- indexer, exact block top-k with a lexicographic
+         (score, block_id) key, Sparse-GQA, bounded-memory streaming, BSHD/THD.
+  [DSA]  Megatron-LM PR #3674 "Enable DSA CP/absorbed/THD paths with TileLang
+         fused ops" -- absorbed MLA, sparse MLA fwd/bwd kernels, indexer kernels,
+         logits cleaning, packed THD masking.
+  [NOPE] Megatron-LM PR #7617 "Support NoPE shapes and unaligned top-k in
+         TileLang sparse MLA" -- q [T,H,576], kv latent with values in the first
+         512 channels, -1 invalid sentinel, explicit softmax scale, the dense
+         [b, heads, sq, sk] masked-softmax fallback, all-invalid rows.
+
+Readings where the pages are silent (each is also listed in the design notes):
+  * indexer score = score_scale * sum_h w[t,h] * ReLU(q_I[t,h] . k_I[s]); the
+    candidate keys of query t are s <= t inside t's sequence (self included);
+  * indexer heads are split into ``groups`` contiguous sets (one per kv group);
+  * a block's score is the max over its causal tokens; future blocks are not
+    candidates; masked entries are never selected, even when fewer than k;
+  * -0.0 equals +0.0; rows come out sorted by (score desc, index asc), -1 last;
+  * indices are positions local to their sequence;
+  * LSE is the natural log; an all-invalid row gives o = 0 and lse = -inf;
+  * sparse MLA does not re-mask the indices it is given (no causal test);
+    sparse GQA keeps only tokens s <= t of the selected blocks.
+
+Parity pins: every function here is checked in ``tests/test_oracle_pins.py``
+against closed forms, textbook dense attention, brute force, hand-derived
+golden rows and finite differences.
+"""
+from __future__ import annotations
+
+import math
+from typing import Iterable, List, Optional, Sequence
+
+import numpy as np
+
+NEG_INF = -math.inf
+
+
+# --------------------------------------------------------------------------
+# small helpers (shapes and sequence bookkeeping only)
+# --------------------------------------------------------------------------
+
+def as_f64(x) -> np.ndarray:
+    """Widen an array-like (numpy, or a CPU torch tensor of any float dtype) to fp64 exactly."""
+    if hasattr(x, "detach"):
+        import torch  # local import: only for tensor inputs
+        x = x.detach().to("cpu", torch.float64).numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def as_i64(x) -> np.ndarray:
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().numpy()
+    return np.asarray(x, dtype=np.int64)
+
+
+def seq_bounds(cu_seqlens: Sequence[int], t: int):
+    """(start, length) of the sequence that holds packed token row t."""
+    cu = list(cu_seqlens)
+    for b in range(len(cu) - 1):
+        if cu[b] <= t < cu[b + 1]:
+            return cu[b], cu[b + 1] - cu[b]
+    raise IndexError(f"token {t} outside cu_seqlens {cu}")
+
+
+def max_seqlen(cu_seqlens: Sequence[int]) -> int:
+    cu = list(cu_seqlens)
+    return max(cu[b + 1] - cu[b] for b in range(len(cu) - 1))
+
+
+# --------------------------------------------------------------------------
+# indexer score  ([QSA] "Describe the solution": trainable indexer, ReLU scores;
+# [DSA] "Changes": fused indexer forward + logits cleaning)
+# --------------------------------------------------------------------------
+
+def indexer_token_scores(q_idx, k_idx, w, cu_seqlens, rows: Iterable[int], groups: int = 1,
+                         score_scale: float = 1.0, width: Optional[int] = None) -> np.ndarray:
+    """Token-level indexer scores for the query rows ``rows``.
+
+    I_g[t, s] = score_scale * sum_{h in group g} w[t,h] * max(q_I[t,h,:] . k_I[s,:], 0)
+    for local key positions s <= p(t) of t's sequence, computed in fp64 and
+    rounded once to fp32; every other column is -inf (a "cleaned" logit that can
+    never be selected).  -0.0 is canonicalised to +0.0.
+
+    Returns float32 [len(rows), groups, width], width defaulting to the longest
+    sequence.
+    """
+    qI, kI, W = as_f64(q_idx), as_f64(k_idx), as_f64(w)
+    T, H_I, _ = qI.shape
+    if H_I % groups:
+        raise ValueError("H_I must be a multiple of groups")
+    hg = H_I // groups
+    rows = list(rows)
+    width = max_seqlen(cu_seqlens) if width is None else width
+    out = np.full((len(rows), groups, width), -np.inf, dtype=np.float32)
+    for i, t in enumerate(rows):
+        s0, n = seq_bounds(cu_seqlens, t)
+        p = t - s0
+        dots = qI[t] @ kI[s0:s0 + p + 1].T                  # [H_I, p+1]
+        relu = np.maximum(dots, 0.0)
+        for g in range(groups):
+            hs = slice(g * hg, (g + 1) * hg)
+            acc = W[t, hs] @ relu[hs]                          # [p+1], fp64
+            sc = (score_scale * acc).astype(np.float32)
+            sc[sc == 0] = np.float32(0.0)                      # -0.0 -> +0.0
+            out[i, g, :p + 1] = sc
+    return out
+
+
+def indexer_block_scores(q_idx, k_idx, w, cu_seqlens, rows: Iterable[int], block_size: int,
+                         groups: int = 1, score_scale: float = 1.0,
+                         width: Optional[int] = None) -> np.ndarray:
+    """Block-level scores ([QSA] "Describe the solution": exact block top-k over a
+    [sequence, sequence/block_size] score matrix).
+
+    B_g[t, b] = max over local tokens s in block b with s <= p(t) of I_g[t, s]
+    (the fp32 token scores above).  Blocks that start after p(t) are -inf.
+    """
+    Lmax = max_seqlen(cu_seqlens)
+    nblk = -(-Lmax // block_size) if width is None else width
+    tok = indexer_token_scores(q_idx, k_idx, w, cu_seqlens, rows, groups, score_scale, Lmax)
+    out = np.full((tok.shape[0], groups, nblk), -np.inf, dtype=np.float32)
+    for i, t in enumerate(rows):
+        s0, _ = seq_bounds(cu_seqlens, t)
+        p = t - s0
+        for b in range(p // block_size + 1):
+            lo, hi = b * block_size, min((b + 1) * block_size, p + 1)
+            out[i, :, b] = tok[i, :, lo:hi].max(axis=1)
+    return out
+
+
+# --------------------------------------------------------------------------
+# deterministic exact top-k ([QSA] "Describe the solution": lexicographic
+# (score, block_id) key; "Additional context": deterministic tie-breaking)
+# --------------------------------------------------------------------------
+
+def topk_lex(row, k: int) -> np.ndarray:
+    """The k best finite entries of one fp32 row under the total order
+    (score descending, index ascending); -inf entries are not candidates.
+    Output int32 [k], sorted in that order, -1 after the last candidate."""
+    r = np.asarray(row, dtype=np.float32)
+    cand = np.nonzero(r != -np.inf)[0]
+    vals = r[cand]
+    order = np.lexsort((cand, -vals))        # primary: -score ascending; then index ascending
+    sel = cand[order[:k]]
+    out = np.full(k, -1, dtype=np.int32)
+    out[:sel.size] = sel
+    return out
+
+
+def topk_rows(scores, k: int) -> np.ndarray:
+    """topk_lex applied to every row of a [..., L] fp32 array."""
+    s = np.asarray(scores, dtype=np.float32)
+    flat = s.reshape(-1, s.shape[-1])
+    out = np.stack([topk_lex(r, k) for r in flat]) if flat.shape[0] else np.zeros((0, k), np.int32)
+    return out.reshape(s.shape[:-1] + (k,))
+
+
+def qsa_topk(q_idx, k_idx, w, cu_seqlens, rows: Iterable[int], topk: int, groups: int = 1,
+             block_size: int = 1, score_scale: float = 1.0) -> np.ndarray:
+    """Indexer then top-k, per query row: int32 [len(rows), groups, topk]."""
+    rows = list(rows)
+    if block_size == 1:
+        sc = indexer_token_scores(q_idx, k_idx, w, cu_seqlens, rows, groups, score_scale)
+    else:
+        sc = indexer_block_scores(q_idx, k_idx, w, cu_seqlens, rows, block_size, groups, score_scale)
+    return topk_rows(sc, topk)
+
+
+# --------------------------------------------------------------------------
+# sparse MLA ([DSA] "Changes": sparse MLA forward/backward over the absorbed
+# latent; [NOPE] "What does this PR do?" and the backport's "Why"/"Change":
+# q [T,H,576], kv latent, value = key[..., :512], -1 slots masked)
+# --------------------------------------------------------------------------
+
+def _valid_rows(idx_row: np.ndarray, n: int) -> np.ndarray:
+    sel = idx_row[idx_row >= 0]
+    if sel.size and sel.max() >= n:
+        raise IndexError("index beyond its sequence")
+    return sel
+
+
+def sparse_mla_fwd_dense(q, kv, idx, cu_seqlens, scale: float, d_v: int = 512):
+    """Dense-masked definition (the [b, heads, sq, sk] masked softmax fallback of
+    [NOPE]): for every (t, h) a logit row over all keys of t's sequence that is
+    -inf except at t's selected indices; softmax in fp64; o = P @ kv[:, :d_v];
+    lse = log(sum exp) (natural log).  All-invalid rows give o = 0, lse = -inf.
+    Returns (o [T,H,d_v], lse [T,H]) in float64."""
+    Q, KV, I = as_f64(q), as_f64(kv), as_i64(idx)
+    T, H, _ = Q.shape
+    o = np.zeros((T, H, d_v))
+    lse = np.full((T, H), -np.inf)
+    for t in range(T):
+        s0, n = seq_bounds(cu_seqlens, t)
+        sel = _valid_rows(I[t], n)
+        if sel.size == 0:
+            continue
+        mask = np.zeros(n, dtype=bool)
+        mask[sel] = True
+        logits = np.full((H, n), -np.inf)
+        full = scale * (Q[t] @ KV[s0:s0 + n].T)
+        logits[:, mask] = full[:, mask]
+        m = logits.max(axis=1, keepdims=True)
+        e = np.exp(logits - m)
+        l = e.sum(axis=1, keepdims=True)
+        o[t] = (e / l) @ KV[s0:s0 + n, :d_v]
+        lse[t] = (m + np.log(l))[:, 0]
+    return o, lse
+
+
+def sparse_mla_fwd(q, kv, idx, cu_seqlens, scale: float, d_v: int = 512,
+                   rows: Optional[Iterable[int]] = None):
+    """Gather form of the same forward: softmax over the valid slots of idx[t]
+    (slot order as given).  Equal to the dense-masked form when a row holds no
+    duplicate index.  ``rows`` restricts the work to some query rows (others
+    are left at o = 0, lse = -inf)."""
+    Q, KV, I = as_f64(q), as_f64(kv), as_i64(idx)
+    T, H, _ = Q.shape
+    o = np.zeros((T, H, d_v))
+    lse = np.full((T, H), -np.inf)
+    for t in (range(T) if rows is None else rows):
+        s0, n = seq_bounds(cu_seqlens, t)
+        sel = _valid_rows(I[t], n)
+        if sel.size == 0:
+            continue
+        K = KV[s0 + sel]                                    # [nk, D]
+        S = scale * (Q[t] @ K.T)                            # [H, nk]
+        m = S.max(axis=1, keepdims=True)
+        e = np.exp(S - m)
+        l = e.sum(axis=1, keepdims=True)
+        o[t] = (e / l) @ K[:, :d_v]
+        lse[t] = (m + np.log(l))[:, 0]
+    return o, lse
+
+
+def sparse_mla_bwd(q, kv, idx, cu_seqlens, scale: float, dout, d_v: int = 512,
+                   rows: Optional[Iterable[int]] = None):
+    """Analytic gradient of the sparse MLA forward, in fp64.
+
+    With P = exp(scale*S - lse), dP = dO . V^T, Dlt = sum_c dO*o,
+    dS = P * (dP - Dlt):  dQ = scale * dS . K;
+    dKV[idx] += scale * dS^T . Q  (all channels)  +  P^T . dO  (first d_v channels).
+    Gradients reaching -1 slots are dropped.  ``rows`` restricts the sum to some
+    query rows: exact whenever dO is zero on every other row.
+    Returns (dq [T,H,D], dkv [T,D]) float64."""
+    Q, KV, I, dO = as_f64(q), as_f64(kv), as_i64(idx), as_f64(dout)
+    T, H, D = Q.shape
+    rows = list(range(T)) if rows is None else list(rows)
+    o, lse = sparse_mla_fwd(Q, KV, I, cu_seqlens, scale, d_v, rows)
+    dq = np.zeros_like(Q)
+    dkv = np.zeros_like(KV)
+    for t in rows:
+        s0, n = seq_bounds(cu_seqlens, t)
+        sel = _valid_rows(I[t], n)
+        if sel.size == 0:
+            continue
+        g = s0 + sel
+        K = KV[g]
+        S = scale * (Q[t] @ K.T)
+        P = np.exp(S - lse[t][:, None])
+        dP = dO[t] @ K[:, :d_v].T
+        Dlt = (dO[t] * o[t]).sum(axis=1)
+        dS = P * (dP - Dlt[:, None])
+        dq[t] = scale * (dS @ K)
+        np.add.at(dkv, g, scale * (dS.T @ Q[t]))
+        np.add.at(dkv[:, :d_v], g, P.T @ dO[t])
+    return dq, dkv
+
+
+def mla_bwd_delta(o, dout) -> np.ndarray:
+    """Dlt[t,h] = sum_c dO[t,h,c] * o[t,h,c] (the backward's preprocess)."""
+    return (as_f64(o) * as_f64(dout)).sum(axis=-1)
+
+
+# --------------------------------------------------------------------------
+# block Sparse-GQA ([QSA] "Describe the solution": Sparse-GQA forward and
+# backward over exact block top-k selections; BSHD and packed THD)
+# --------------------------------------------------------------------------
+
+def _gqa_tokens(blk_row: np.ndarray, p: int, n: int, block_size: int) -> np.ndarray:
+    """Local token positions attended by a query at local position p: every
+    token s <= p inside a selected block (a set; duplicates count once)."""
+    sel = blk_row[blk_row >= 0]
+    if sel.size and (sel.max() * block_size >= n):
+        raise IndexError("block beyond its sequence")
+    mask = np.zeros(n, dtype=bool)
+    for b in sel:
+        mask[b * block_size: min((b + 1) * block_size, p + 1)] = True
+    return np.nonzero(mask)[0]
+
+
+def sparse_gqa_fwd(q, k, v, blk_idx, cu_seqlens, block_size: int, scale: float,
+                   rows: Optional[Iterable[int]] = None):
+    """o[t,h] = softmax over the tokens of the selected blocks of group g(h) =
+    h // (Hq/Hkv) (causal inside the query's own block) of scale * q.k, times v.
+    Returns (o [T,Hq,d], lse [T,Hq]) float64; empty selections give 0 / -inf."""
+    Q, K, V, I = as_f64(q), as_f64(k), as_f64(v), as_i64(blk_idx)
+    T, Hq, d = Q.shape
+    Hkv = K.shape[1]
+    G = Hq // Hkv
+    o = np.zeros((T, Hq, V.shape[2]))
+    lse = np.full((T, Hq), -np.inf)
+    for t in (range(T) if rows is None else rows):
+        s0, n = seq_bounds(cu_seqlens, t)
+        p = t - s0
+        for g in range(Hkv):
+            tok = _gqa_tokens(I[t, g], p, n, block_size)
+            if tok.size == 0:
+                continue
+            Kg, Vg = K[s0 + tok, g], V[s0 + tok, g]
+            hs = slice(g * G, (g + 1) * G)
+            S = scale * (Q[t, hs] @ Kg.T)
+            m = S.max(axis=1, keepdims=True)
+            e = np.exp(S - m)
+            l = e.sum(axis=1, keepdims=True)
+            o[t, hs] = (e / l) @ Vg
+            lse[t, hs] = (m + np.log(l))[:, 0]
+    return o, lse
+
+
+def sparse_gqa_bwd(q, k, v, blk_idx, cu_seqlens, block_size: int, scale: float, dout,
+                   rows: Optional[Iterable[int]] = None):
+    """Analytic gradient of sparse_gqa_fwd (fp64): dq, dk, dv, with dk/dv summed
+    over all query heads of the group and all queries that attend a token."""
+    Q, K, V, I, dO = as_f64(q), as_f64(k), as_f64(v), as_i64(blk_idx), as_f64(dout)
+    T, Hq, d = Q.shape
+    Hkv = K.shape[1]
+    G = Hq // Hkv
+    rows = list(range(T)) if rows is None else list(rows)
+    o, lse = sparse_gqa_fwd(Q, K, V, I, cu_seqlens, block_size, scale, rows)
+    dq, dk, dv = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+    for t in rows:
+        s0, n = seq_bounds(cu_seqlens, t)
+        p = t - s0
+        for g in range(Hkv):
+            tok = _gqa_tokens(I[t, g], p, n, block_size)
+            if tok.size == 0:
+                continue
+            gi = s0 + tok
+            Kg, Vg = K[gi, g], V[gi, g]
+            hs = slice(g * G, (g + 1) * G)
+            S = scale * (Q[t, hs] @ Kg.T)
+            P = np.exp(S - lse[t, hs][:, None])
+            dP = dO[t, hs] @ Vg.T
+            Dlt = (dO[t, hs] * o[t, hs]).sum(axis=1)
+            dS = P * (dP - Dlt[:, None])
+            dq[t, hs] = scale * (dS @ Kg)
+            dk[gi, g] += scale * (dS.T @ Q[t, hs])
+            dv[gi, g] += P.T @ dO[t, hs]
+    return dq, dk, dv
+
+
+# --------------------------------------------------------------------------
+# the two exact paddings of [NOPE] ("What does this PR do?"; backport "Change")
+# --------------------------------------------------------------------------
+
+def pad_nope(x, width: int = 576) -> np.ndarray:
+    """Zero-pad the last (channel) axis of a 512-wide NoPE tensor to ``width``."""
+    X = as_f64(x)
+    pad = [(0, 0)] * (X.ndim - 1) + [(0, width - X.shape[-1])]
+    return np.pad(X, pad)
+
+
+def pad_topk(idx, multiple: int = 64) -> np.ndarray:
+    """Pad the slot axis to a multiple of ``multiple`` with the -1 sentinel."""
+    I = as_i64(idx)
+    k = I.shape[-1]
+    kp = -(-k // multiple) * multiple
+    pad = [(0, 0)] * (I.ndim - 1) + [(0, kp - k)]
+    return np.pad(I, pad, constant_values=-1)
