@@ -98,8 +98,8 @@ def indexer_token_scores(q_idx, k_idx, w, cu_seqlens, rows: Iterable[int], group
     Returns float32 [len(rows), groups, width], width defaulting to the longest
     sequence.
     """
-    qI, kI, W = as_f64(q_idx), as_f64(k_idx), as_f64(w)
-    T, H_I, _ = qI.shape
+    kI = as_f64(k_idx)
+    H_I = q_idx.shape[1]
     if H_I % groups:
         raise ValueError("H_I must be a multiple of groups")
     hg = H_I // groups
@@ -109,11 +109,12 @@ def indexer_token_scores(q_idx, k_idx, w, cu_seqlens, rows: Iterable[int], group
     for i, t in enumerate(rows):
         s0, n = seq_bounds(cu_seqlens, t)
         p = t - s0
-        dots = qI[t] @ kI[s0:s0 + p + 1].T                  # [H_I, p+1]
+        dots = as_f64(q_idx[t]) @ kI[s0:s0 + p + 1].T      # [H_I, p+1]
         relu = np.maximum(dots, 0.0)
+        w_t = as_f64(w[t])
         for g in range(groups):
             hs = slice(g * hg, (g + 1) * hg)
-            acc = W[t, hs] @ relu[hs]                          # [p+1], fp64
+            acc = w_t[hs] @ relu[hs]                           # [p+1], fp64
             sc = (score_scale * acc).astype(np.float32)
             sc[sc == 0] = np.float32(0.0)                      # -0.0 -> +0.0
             out[i, g, :p + 1] = sc
@@ -221,28 +222,35 @@ def sparse_mla_fwd_dense(q, kv, idx, cu_seqlens, scale: float, d_v: int = 512):
     return o, lse
 
 
+def sparse_mla_row(q_t, kv, idx_t, s0: int, n: int, scale: float, d_v: int = 512):
+    """One query row of the gather form: softmax over the valid slots of idx_t
+    (slot order as given) of scale * q_t . kv[s0 + idx]; returns (o [H, d_v], lse [H])."""
+    Qt, I = as_f64(q_t), as_i64(idx_t)
+    H = Qt.shape[0]
+    sel = _valid_rows(I, n)
+    if sel.size == 0:
+        return np.zeros((H, d_v)), np.full(H, -np.inf)
+    K = as_f64(kv[s0 + sel]) if not isinstance(kv, np.ndarray) else kv[s0 + sel]   # [nk, D]
+    S = scale * (Qt @ K.T)                                 # [H, nk]
+    m = S.max(axis=1, keepdims=True)
+    e = np.exp(S - m)
+    l = e.sum(axis=1, keepdims=True)
+    return (e / l) @ K[:, :d_v], (m + np.log(l))[:, 0]
+
+
 def sparse_mla_fwd(q, kv, idx, cu_seqlens, scale: float, d_v: int = 512,
                    rows: Optional[Iterable[int]] = None):
-    """Gather form of the same forward: softmax over the valid slots of idx[t]
-    (slot order as given).  Equal to the dense-masked form when a row holds no
-    duplicate index.  ``rows`` restricts the work to some query rows (others
-    are left at o = 0, lse = -inf)."""
-    Q, KV, I = as_f64(q), as_f64(kv), as_i64(idx)
-    T, H, _ = Q.shape
-    o = np.zeros((T, H, d_v))
-    lse = np.full((T, H), -np.inf)
-    for t in (range(T) if rows is None else rows):
+    """Gather form of the same forward, equal to the dense-masked form when a
+    row holds no duplicate index.  Returns (o [T,H,d_v], lse [T,H]) float64, or
+    for ``rows`` the compact (o [len(rows),H,d_v], lse [len(rows),H])."""
+    KV = as_f64(kv)
+    T, H = q.shape[0], q.shape[1]
+    rr = range(T) if rows is None else list(rows)
+    o = np.zeros((len(rr), H, d_v))
+    lse = np.full((len(rr), H), -np.inf)
+    for i, t in enumerate(rr):
         s0, n = seq_bounds(cu_seqlens, t)
-        sel = _valid_rows(I[t], n)
-        if sel.size == 0:
-            continue
-        K = KV[s0 + sel]                                    # [nk, D]
-        S = scale * (Q[t] @ K.T)                            # [H, nk]
-        m = S.max(axis=1, keepdims=True)
-        e = np.exp(S - m)
-        l = e.sum(axis=1, keepdims=True)
-        o[t] = (e / l) @ K[:, :d_v]
-        lse[t] = (m + np.log(l))[:, 0]
+        o[i], lse[i] = sparse_mla_row(q[t], KV, idx[t], s0, n, scale, d_v)
     return o, lse
 
 
@@ -254,29 +262,30 @@ def sparse_mla_bwd(q, kv, idx, cu_seqlens, scale: float, dout, d_v: int = 512,
     dS = P * (dP - Dlt):  dQ = scale * dS . K;
     dKV[idx] += scale * dS^T . Q  (all channels)  +  P^T . dO  (first d_v channels).
     Gradients reaching -1 slots are dropped.  ``rows`` restricts the sum to some
-    query rows: exact whenever dO is zero on every other row.
-    Returns (dq [T,H,D], dkv [T,D]) float64."""
-    Q, KV, I, dO = as_f64(q), as_f64(kv), as_i64(idx), as_f64(dout)
-    T, H, D = Q.shape
-    rows = list(range(T)) if rows is None else list(rows)
-    o, lse = sparse_mla_fwd(Q, KV, I, cu_seqlens, scale, d_v, rows)
-    dq = np.zeros_like(Q)
+    query rows (exact whenever dO is zero on every other row) and makes dq
+    compact [len(rows), H, D].  Returns (dq, dkv [T_kv, D]) float64."""
+    KV = as_f64(kv)
+    T, H, D = q.shape
+    rr = list(range(T)) if rows is None else list(rows)
+    dq = np.zeros((len(rr), H, D))
     dkv = np.zeros_like(KV)
-    for t in rows:
+    for i, t in enumerate(rr):
         s0, n = seq_bounds(cu_seqlens, t)
-        sel = _valid_rows(I[t], n)
+        sel = _valid_rows(as_i64(idx[t]), n)
         if sel.size == 0:
             continue
+        Qt, dOt = as_f64(q[t]), as_f64(dout[t])
+        o_t, lse_t = sparse_mla_row(Qt, KV, idx[t], s0, n, scale, d_v)
         g = s0 + sel
         K = KV[g]
-        S = scale * (Q[t] @ K.T)
-        P = np.exp(S - lse[t][:, None])
-        dP = dO[t] @ K[:, :d_v].T
-        Dlt = (dO[t] * o[t]).sum(axis=1)
+        S = scale * (Qt @ K.T)
+        P = np.exp(S - lse_t[:, None])
+        dP = dOt @ K[:, :d_v].T
+        Dlt = (dOt * o_t).sum(axis=1)
         dS = P * (dP - Dlt[:, None])
-        dq[t] = scale * (dS @ K)
-        np.add.at(dkv, g, scale * (dS.T @ Q[t]))
-        np.add.at(dkv[:, :d_v], g, P.T @ dO[t])
+        dq[i] = scale * (dS @ K)
+        np.add.at(dkv, g, scale * (dS.T @ Qt))
+        np.add.at(dkv[:, :d_v], g, P.T @ dOt)
     return dq, dkv
 
 
@@ -302,64 +311,79 @@ def _gqa_tokens(blk_row: np.ndarray, p: int, n: int, block_size: int) -> np.ndar
     return np.nonzero(mask)[0]
 
 
+def sparse_gqa_row(q_t, K, V, blk_t, s0: int, p: int, n: int, block_size: int, scale: float):
+    """One query row: per kv group g, softmax over the attended tokens of
+    scale * q[h] . k[., g] for the group's heads, times v.  Returns (o [Hq,d], lse [Hq])."""
+    Qt, I = as_f64(q_t), as_i64(blk_t)
+    Hq = Qt.shape[0]
+    Hkv = K.shape[1]
+    G = Hq // Hkv
+    o = np.zeros((Hq, V.shape[2]))
+    lse = np.full(Hq, -np.inf)
+    for g in range(Hkv):
+        tok = _gqa_tokens(I[g], p, n, block_size)
+        if tok.size == 0:
+            continue
+        Kg, Vg = K[s0 + tok, g], V[s0 + tok, g]
+        hs = slice(g * G, (g + 1) * G)
+        S = scale * (Qt[hs] @ Kg.T)
+        m = S.max(axis=1, keepdims=True)
+        e = np.exp(S - m)
+        l = e.sum(axis=1, keepdims=True)
+        o[hs] = (e / l) @ Vg
+        lse[hs] = (m + np.log(l))[:, 0]
+    return o, lse
+
+
 def sparse_gqa_fwd(q, k, v, blk_idx, cu_seqlens, block_size: int, scale: float,
                    rows: Optional[Iterable[int]] = None):
     """o[t,h] = softmax over the tokens of the selected blocks of group g(h) =
     h // (Hq/Hkv) (causal inside the query's own block) of scale * q.k, times v.
-    Returns (o [T,Hq,d], lse [T,Hq]) float64; empty selections give 0 / -inf."""
-    Q, K, V, I = as_f64(q), as_f64(k), as_f64(v), as_i64(blk_idx)
-    T, Hq, d = Q.shape
-    Hkv = K.shape[1]
-    G = Hq // Hkv
-    o = np.zeros((T, Hq, V.shape[2]))
-    lse = np.full((T, Hq), -np.inf)
-    for t in (range(T) if rows is None else rows):
+    Returns (o [T,Hq,d], lse [T,Hq]) float64 (compact for ``rows``); empty
+    selections give 0 / -inf."""
+    K, V = as_f64(k), as_f64(v)
+    T, Hq = q.shape[0], q.shape[1]
+    rr = range(T) if rows is None else list(rows)
+    o = np.zeros((len(rr), Hq, V.shape[2]))
+    lse = np.full((len(rr), Hq), -np.inf)
+    for i, t in enumerate(rr):
         s0, n = seq_bounds(cu_seqlens, t)
-        p = t - s0
-        for g in range(Hkv):
-            tok = _gqa_tokens(I[t, g], p, n, block_size)
-            if tok.size == 0:
-                continue
-            Kg, Vg = K[s0 + tok, g], V[s0 + tok, g]
-            hs = slice(g * G, (g + 1) * G)
-            S = scale * (Q[t, hs] @ Kg.T)
-            m = S.max(axis=1, keepdims=True)
-            e = np.exp(S - m)
-            l = e.sum(axis=1, keepdims=True)
-            o[t, hs] = (e / l) @ Vg
-            lse[t, hs] = (m + np.log(l))[:, 0]
+        o[i], lse[i] = sparse_gqa_row(q[t], K, V, blk_idx[t], s0, t - s0, n, block_size, scale)
     return o, lse
 
 
 def sparse_gqa_bwd(q, k, v, blk_idx, cu_seqlens, block_size: int, scale: float, dout,
                    rows: Optional[Iterable[int]] = None):
-    """Analytic gradient of sparse_gqa_fwd (fp64): dq, dk, dv, with dk/dv summed
-    over all query heads of the group and all queries that attend a token."""
-    Q, K, V, I, dO = as_f64(q), as_f64(k), as_f64(v), as_i64(blk_idx), as_f64(dout)
-    T, Hq, d = Q.shape
+    """Analytic gradient of sparse_gqa_fwd (fp64): dq (compact for ``rows``),
+    dk, dv, with dk/dv summed over all query heads of the group and all queries
+    that attend a token (exact for ``rows`` when dO is zero elsewhere)."""
+    K, V = as_f64(k), as_f64(v)
+    T, Hq, d = q.shape
     Hkv = K.shape[1]
     G = Hq // Hkv
-    rows = list(range(T)) if rows is None else list(rows)
-    o, lse = sparse_gqa_fwd(Q, K, V, I, cu_seqlens, block_size, scale, rows)
-    dq, dk, dv = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
-    for t in rows:
+    rr = list(range(T)) if rows is None else list(rows)
+    dq = np.zeros((len(rr), Hq, d))
+    dk, dv = np.zeros_like(K), np.zeros_like(V)
+    for i, t in enumerate(rr):
         s0, n = seq_bounds(cu_seqlens, t)
         p = t - s0
+        Qt, dOt, I = as_f64(q[t]), as_f64(dout[t]), as_i64(blk_idx[t])
+        o_t, lse_t = sparse_gqa_row(Qt, K, V, I, s0, p, n, block_size, scale)
         for g in range(Hkv):
-            tok = _gqa_tokens(I[t, g], p, n, block_size)
+            tok = _gqa_tokens(I[g], p, n, block_size)
             if tok.size == 0:
                 continue
             gi = s0 + tok
             Kg, Vg = K[gi, g], V[gi, g]
             hs = slice(g * G, (g + 1) * G)
-            S = scale * (Q[t, hs] @ Kg.T)
-            P = np.exp(S - lse[t, hs][:, None])
-            dP = dO[t, hs] @ Vg.T
-            Dlt = (dO[t, hs] * o[t, hs]).sum(axis=1)
+            S = scale * (Qt[hs] @ Kg.T)
+            P = np.exp(S - lse_t[hs][:, None])
+            dP = dOt[hs] @ Vg.T
+            Dlt = (dOt[hs] * o_t[hs]).sum(axis=1)
             dS = P * (dP - Dlt[:, None])
-            dq[t, hs] = scale * (dS @ Kg)
-            dk[gi, g] += scale * (dS.T @ Q[t, hs])
-            dv[gi, g] += P.T @ dO[t, hs]
+            dq[i, hs] = scale * (dS @ Kg)
+            dk[gi, g] += scale * (dS.T @ Qt[hs])
+            dv[gi, g] += P.T @ dOt[hs]
     return dq, dk, dv
 
 

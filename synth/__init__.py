@@ -216,3 +216,49 @@ WORKLOADS: Dict[str, Workload] = {
     "mla_t65536_h128": Workload("mla_t65536_h128", "mla", [65536], H=128, D=576, topk=2048,
                                 scale=1 / math.sqrt(192), H_I=64, d_I=128),
 }
+
+
+def spread_topk_indices(cu_seqlens, topk: int, seed: int, device="cpu") -> torch.Tensor:
+    """Distinct causal local indices spread over each query's range, built with
+    tensor ops (fast at T = 65536 on the device).
+
+    Query at local position p: if p+1 <= topk every key 0..p appears once (in a
+    rotated order) and the rest is -1; otherwise slot j holds
+    (floor(j*(p+1)/topk) + r_t) mod (p+1) with a seeded per-row rotation r_t.
+    """
+    g = gen(seed, device)
+    T = cu_seqlens[-1]
+    cu = torch.tensor(cu_seqlens, device=device, dtype=torch.int64)
+    t = torch.arange(T, device=device, dtype=torch.int64)
+    seq = torch.searchsorted(cu, t, right=True) - 1
+    n_cand = t - cu[seq] + 1                                   # p + 1
+    rot = (torch.rand((T,), generator=g, device=device) * n_cand.to(torch.float32)).to(torch.int64)
+    rot = torch.minimum(rot, n_cand - 1)
+    j = torch.arange(topk, device=device, dtype=torch.int64)[None, :]
+    wide = n_cand[:, None] > topk
+    base = torch.where(wide, (j * n_cand[:, None]) // topk, j)
+    idx = (base + rot[:, None]) % n_cand[:, None]
+    idx = torch.where(wide | (j < n_cand[:, None]), idx, torch.full_like(idx, -1))
+    return idx.to(torch.int32).contiguous()
+
+
+def spread_block_indices(cu_seqlens, Hkv: int, nsel: int, block_size: int, seed: int,
+                         device="cpu") -> torch.Tensor:
+    """Causal distinct local block ids per (query, kv group), spread over the
+    query's causal blocks with a seeded per-row rotation; -1 padded.
+    int32 [T, Hkv, nsel], built with tensor ops."""
+    g = gen(seed, device)
+    T = cu_seqlens[-1]
+    cu = torch.tensor(cu_seqlens, device=device, dtype=torch.int64)
+    t = torch.arange(T, device=device, dtype=torch.int64)
+    seq = torch.searchsorted(cu, t, right=True) - 1
+    nb = (t - cu[seq]) // block_size + 1                      # causal blocks of each query
+    rot = (torch.rand((T, Hkv), generator=g, device=device) * nb[:, None].to(torch.float32)).to(torch.int64)
+    rot = torch.minimum(rot, nb[:, None] - 1)
+    j = torch.arange(nsel, device=device, dtype=torch.int64)[None, None, :]
+    nbb = nb[:, None, None]
+    wide = nbb > nsel
+    base = torch.where(wide, (j * nbb) // nsel, j)
+    b = (base + rot[:, :, None]) % nbb
+    b = torch.where(wide | (j < nbb), b, torch.full_like(b, -1))
+    return b.to(torch.int32).contiguous()

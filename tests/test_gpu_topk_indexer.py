@@ -1,0 +1,182 @@
+"""GPU parity: indexer scores, exact top-k and the streaming indexer + top-k,
+against the CPU oracle, through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth
+from _util import compare_topk_rows, indexer_score_bound
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tsa():
+    import trainable_sparse_attention_gb300 as m
+    m.build()
+    m.load_library()
+    return m
+
+
+DEV = "cuda"
+
+
+# ------------------------------------------------------------ top-k from scores
+
+@pytest.mark.parametrize("rows,L,k", [(64, 50, 7), (64, 333, 64), (32, 4096, 2048), (16, 5000, 65),
+                                      (8, 20011, 2048), (4, 65536, 2048), (8, 70000, 4096), (3, 9000, 1)])
+def test_topk_from_scores_bit_exact(tsa, rows, L, k):
+    s = synth.tie_stress_scores(rows, L, seed=rows + L + k)
+    got = tsa.qsa_topk_from_scores(s.to(DEV), k).cpu().numpy()
+    ref = O.topk_rows(s.numpy(), k)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_topk_from_scores_all_masked_and_tiny_rows(tsa):
+    s = torch.full((5, 10), -math.inf)
+    s[1, 3] = 0.0
+    s[2, :] = -0.0
+    s[3, 9] = -1.0
+    s[4, ::2] = 2.0
+    got = tsa.qsa_topk_from_scores(s.to(DEV), 4).cpu().numpy()
+    np.testing.assert_array_equal(got, O.topk_rows(s.numpy(), 4))
+    assert np.all(got[0] == -1)
+
+
+def test_topk_from_scores_distinct_random(tsa):
+    g = torch.Generator().manual_seed(5)
+    s = torch.randn((12, 30000), generator=g)
+    got = tsa.qsa_topk_from_scores(s.to(DEV), 1000).cpu().numpy()
+    np.testing.assert_array_equal(got, O.topk_rows(s.numpy(), 1000))
+
+
+def test_topk_deterministic_replay_under_contention(tsa):
+    s = synth.tie_stress_scores(256, 12000, seed=9).to(DEV)
+    a = tsa.qsa_topk_from_scores(s, 2048)
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        big = torch.randn(4096, 4096, device=DEV)
+        for _ in range(4):
+            big = big @ big.T
+            big = big / big.norm()
+    b = tsa.qsa_topk_from_scores(s, 2048)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+# ------------------------------------------------------------ indexer scores
+
+@pytest.mark.parametrize("H_I,d_I,groups,cu", [(4, 64, 1, [0, 256]), (8, 128, 1, [0, 300, 1000]),
+                                               (8, 128, 4, [0, 130, 700]), (64, 128, 1, [0, 520]),
+                                               (16, 64, 2, [0, 1, 257, 390])])
+def test_indexer_scores_exact_inputs_bit_exact(tsa, H_I, d_I, groups, cu):
+    T = cu[-1]
+    x = synth.indexer_inputs(T, H_I, d_I, seed=H_I + d_I + groups, integer=True)
+    got = tsa.qsa_indexer_scores(x["q_idx"].to(DEV), x["k_idx"].to(DEV), x["w"].to(DEV), cu,
+                                 groups=groups).cpu().numpy()
+    ref = O.indexer_token_scores(x["q_idx"], x["k_idx"], x["w"], cu, range(T), groups)
+    np.testing.assert_array_equal(got, ref)
+
+
+@pytest.mark.parametrize("H_I,d_I,groups,bs,cu", [(4, 64, 1, 1, [0, 256]), (8, 128, 4, 64, [0, 300, 1000]),
+                                                  (64, 128, 1, 1, [0, 700]), (8, 128, 1, 32, [0, 450])])
+def test_indexer_scores_randn_within_bound(tsa, H_I, d_I, groups, bs, cu):
+    T = cu[-1]
+    x = synth.indexer_inputs(T, H_I, d_I, seed=3, zero_key_frac=0.3)
+    got = tsa.qsa_indexer_scores(x["q_idx"].to(DEV), x["k_idx"].to(DEV), x["w"].to(DEV), cu, groups=groups,
+                                 block_size=bs, score_scale=0.5).cpu().numpy()
+    if bs == 1:
+        ref = O.indexer_token_scores(x["q_idx"], x["k_idx"], x["w"], cu, range(T), groups, 0.5)
+    else:
+        ref = O.indexer_block_scores(x["q_idx"], x["k_idx"], x["w"], cu, range(T), bs, groups, 0.5)
+    assert np.array_equal(np.isneginf(got), np.isneginf(ref)), "candidate pattern differs"
+    fin = np.isfinite(ref)
+    for t in range(0, T, 37):
+        tol = 0.5 * indexer_score_bound(x["q_idx"], x["k_idx"], x["w"], cu, t, groups)
+        for g in range(groups):
+            f = fin[t, g]
+            err = np.max(np.abs(got[t, g][f].astype(np.float64) - ref[t, g][f])) if f.any() else 0.0
+            assert err <= tol[g] + 1e-30, (t, g, err, tol[g])
+    # exact zeros (zero keys) are exact on both sides
+    assert np.array_equal(got[fin] == 0, ref[fin] == 0)
+
+
+# ------------------------------------------------------------ streaming indexer + top-k
+
+@pytest.mark.parametrize("H_I,d_I,groups,bs,topk,cu", [
+    (4, 64, 1, 1, 64, [0, 256]),
+    (8, 128, 1, 1, 2048, [0, 700, 2600]),
+    (64, 128, 1, 1, 128, [0, 1100]),
+    (8, 128, 4, 64, 32, [0, 900, 3000]),
+    (8, 128, 1, 1, 65, [0, 5, 300]),
+])
+def test_qsa_topk_exact_inputs_bit_exact(tsa, H_I, d_I, groups, bs, topk, cu):
+    T = cu[-1]
+    x = synth.indexer_inputs(T, H_I, d_I, seed=11, integer=True)
+    got = tsa.qsa_topk(x["q_idx"].to(DEV), x["k_idx"].to(DEV), x["w"].to(DEV), cu, topk, groups=groups,
+                       block_size=bs).cpu().numpy()
+    ref = O.qsa_topk(x["q_idx"], x["k_idx"], x["w"], cu, range(T), topk, groups, bs)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_qsa_topk_zero_tie_stress_t4096(tsa):
+    """T=4096, 8 indexer heads, d_I=128, 30% zero keys, 16 dead queries, k=2048."""
+    cu = [0, 4096]
+    x = synth.indexer_inputs(4096, 8, 128, seed=2, zero_key_frac=0.3, dead_queries=16)
+    got = tsa.qsa_topk(x["q_idx"].to(DEV), x["k_idx"].to(DEV), x["w"].to(DEV), cu, 2048).cpu().numpy()
+    dead = np.nonzero(np.all(x["q_idx"].float().numpy() == 0, axis=(1, 2)))[0]
+    rows = sorted(set(list(range(0, 4096, 97)) + [0, 1, 2047, 2048, 4095] + dead.tolist()))
+    sc = O.indexer_token_scores(x["q_idx"], x["k_idx"], x["w"], cu, rows)
+    mism = 0
+    for i, t in enumerate(rows):
+        tol = indexer_score_bound(x["q_idx"], x["k_idx"], x["w"], cu, t)[0]
+        mism += compare_topk_rows(got[t, 0], sc[i, 0], 2048, tol)
+    for t in dead:  # all-zero rows: pure index order
+        want = np.arange(min(t + 1, 2048))
+        np.testing.assert_array_equal(got[t, 0, :want.size], want)
+    assert mism <= 0.001 * len(rows) * 2048
+
+
+def test_qsa_topk_deterministic(tsa):
+    cu = [0, 3000]
+    x = synth.indexer_inputs(3000, 8, 128, seed=4, zero_key_frac=0.3)
+    args = (x["q_idx"].to(DEV), x["k_idx"].to(DEV), x["w"].to(DEV), cu, 512)
+    a = tsa.qsa_topk(*args)
+    b = tsa.qsa_topk(*args)
+    assert torch.equal(a, b)
+
+
+@pytest.mark.slow
+def test_qsa_topk_t65536_sampled(tsa):
+    """T=65536, 64 indexer heads, d_I=128, k=2048; sampled rows vs the oracle."""
+    T = 65536
+    cu = [0, T]
+    x = synth.indexer_inputs(T, 64, 128, seed=5, device=DEV)
+    got = tsa.qsa_topk(x["q_idx"], x["k_idx"], x["w"], cu, 2048)
+    rows = [0, 1, 2046, 2047, 2048, 30000, 65535] + list(range(1000, T, 9973))
+    xc = {k: v.cpu() for k, v in x.items()}
+    sc = O.indexer_token_scores(xc["q_idx"], xc["k_idx"], xc["w"], cu, rows)
+    g = got.cpu().numpy()
+    for i, t in enumerate(rows):
+        tol = indexer_score_bound(xc["q_idx"], xc["k_idx"], xc["w"], cu, t)[0]
+        compare_topk_rows(g[t, 0], sc[i, 0], 2048, tol)
+
+
+@pytest.mark.slow
+def test_qsa_topk_block_thd32768_sampled(tsa):
+    """Packed THD of 4 sequences (4096/8192/12288/8192), 8 heads in 4 groups,
+    block_size 64, top-32 blocks; sampled rows vs the oracle."""
+    cu = synth.cu_seqlens_thd([4096, 8192, 12288, 8192])
+    T = cu[-1]
+    x = synth.indexer_inputs(T, 8, 128, seed=6, device=DEV)
+    got = tsa.qsa_topk(x["q_idx"], x["k_idx"], x["w"], cu, 32, groups=4, block_size=64).cpu().numpy()
+    rows = [0, 63, 64, 4095, 4096, 4097, 12287, 12288, 24575, 24576, 32767] + list(range(500, T, 1999))
+    xc = {k: v.cpu() for k, v in x.items()}
+    sc = O.indexer_block_scores(xc["q_idx"], xc["k_idx"], xc["w"], cu, rows, 64, 4)
+    for i, t in enumerate(rows):
+        tol = indexer_score_bound(xc["q_idx"], xc["k_idx"], xc["w"], cu, t, 4)
+        for g in range(4):
+            compare_topk_rows(got[t, g], sc[i, g], 32, tol[g])

@@ -1,0 +1,410 @@
+// C-ABI entry points of libtsa: argument validation, workspace carving and
+// kernel launches.  No entry point allocates device memory or falls back to a
+// different implementation: unsupported shapes are refused with a status code.
+#include <cstdarg>
+#include <cstdio>
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <string>
+
+#include "kernels.cuh"
+
+using namespace tsa;
+
+namespace {
+
+// Error flag word raised by kernels (never a trap); read by tsa_read_flags.
+__device__ unsigned int g_flags = 0;
+
+unsigned int* flags_ptr() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_flags) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return static_cast<unsigned int*>(p);
+}
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int cuda_status(cudaError_t e, const char* where) {
+  if (e == cudaSuccess) return TSA_OK;
+  return fail(TSA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+#define TSA_CHECK_CUDA(expr, where)            \
+  do {                                         \
+    cudaError_t _e = (expr);                   \
+    if (_e != cudaSuccess) return cuda_status(_e, where); \
+  } while (0)
+
+// Validate cu_seqlens and fill the kernel-side table.
+int make_seqs(const int32_t* cu, int num_seqs, SeqTable* st, int64_t* T_out) {
+  if (cu == nullptr) return fail(TSA_ERR_INVALID_ARG, "cu_seqlens is null");
+  if (num_seqs < 1 || num_seqs > TSA_MAX_SEQS)
+    return fail(TSA_ERR_INVALID_ARG, "num_seqs=%d outside [1, %d]", num_seqs, TSA_MAX_SEQS);
+  if (cu[0] != 0) return fail(TSA_ERR_INVALID_ARG, "cu_seqlens[0]=%d, expected 0", cu[0]);
+  st->num_seqs = num_seqs;
+  st->max_len = 0;
+  st->cu[0] = 0;
+  for (int i = 1; i <= num_seqs; ++i) {
+    if (cu[i] < cu[i - 1]) return fail(TSA_ERR_INVALID_ARG, "cu_seqlens not non-decreasing at %d", i);
+    st->cu[i] = cu[i];
+    int len = cu[i] - cu[i - 1];
+    if (len > st->max_len) st->max_len = len;
+  }
+  *T_out = cu[num_seqs];
+  return TSA_OK;
+}
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int check_indexer_shape(int H_I, int d_I, int groups, int block_size) {
+  if (!is_pow2(H_I) || H_I < 2 || H_I > 128)
+    return fail(TSA_ERR_UNSUPPORTED, "H_I=%d: need a power of two in [2, 128]", H_I);
+  if (d_I != 64 && d_I != 128) return fail(TSA_ERR_UNSUPPORTED, "d_I=%d: need 64 or 128", d_I);
+  if (groups < 1 || H_I % groups != 0 || H_I / groups < 2)
+    return fail(TSA_ERR_UNSUPPORTED, "groups=%d: need H_I/groups >= 2 and integral", groups);
+  if (block_size != 1 && block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128)
+    return fail(TSA_ERR_UNSUPPORTED, "block_size=%d: need 1, 16, 32, 64 or 128", block_size);
+  return TSA_OK;
+}
+
+int64_t score_width(int max_len, int block_size) {
+  return block_size == 1 ? max_len : (max_len + block_size - 1) / block_size;
+}
+
+// Query rows per streamed chunk: the chunk's scores stay within ~64 MB (L2-sized).
+int64_t chunk_rows(int max_len, int groups, int block_size) {
+  int64_t w = score_width(max_len, block_size);
+  if (w < 1) w = 1;
+  int64_t c = (int64_t(64) << 20) / (4 * w * groups);
+  c = (c / 128) * 128;
+  if (c < 128) c = 128;
+  if (c > max_len) c = max_len;
+  if (c < 1) c = 1;
+  return c;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* tsa_status_string(int status) {
+  switch (status) {
+    case TSA_OK: return "TSA_OK";
+    case TSA_ERR_INVALID_ARG: return "TSA_ERR_INVALID_ARG: invalid argument";
+    case TSA_ERR_UNSUPPORTED: return "TSA_ERR_UNSUPPORTED: shape or option not built";
+    case TSA_ERR_WORKSPACE: return "TSA_ERR_WORKSPACE: workspace missing or too small";
+    case TSA_ERR_CUDA: return "TSA_ERR_CUDA: CUDA runtime error";
+    case TSA_ERR_INDEX_RANGE: return "TSA_ERR_INDEX_RANGE: index outside its sequence";
+    case TSA_ERR_TIMEOUT: return "TSA_ERR_TIMEOUT: bounded device wait expired";
+    default: return "unknown tsa status";
+  }
+}
+
+const char* tsa_last_error(void) { return g_last_error.c_str(); }
+
+int tsa_version(void) { return 1; }
+
+int tsa_read_flags(uint32_t* flags, int clear, void* stream) {
+  if (flags == nullptr) return fail(TSA_ERR_INVALID_ARG, "flags is null");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned int v = 0;
+  TSA_CHECK_CUDA(cudaMemcpyFromSymbolAsync(&v, g_flags, sizeof(v), 0, cudaMemcpyDeviceToHost, s), "read flags");
+  TSA_CHECK_CUDA(cudaStreamSynchronize(s), "read flags sync");
+  if (clear) {
+    unsigned int z = 0;
+    TSA_CHECK_CUDA(cudaMemcpyToSymbolAsync(g_flags, &z, sizeof(z), 0, cudaMemcpyHostToDevice, s), "clear flags");
+    TSA_CHECK_CUDA(cudaStreamSynchronize(s), "clear flags sync");
+  }
+  *flags = v;
+  return TSA_OK;
+}
+
+// ---------------------------------------------------------------- indexer
+
+int qsa_indexer_scores(const void* q_idx, const void* k_idx, const float* w, const int32_t* cu_seqlens,
+                       int num_seqs, int H_I, int d_I, int groups, int block_size, float score_scale,
+                       int64_t q_begin, int64_t q_count, float* scores, int64_t width, void* stream) {
+  SeqTable st;
+  int64_t T;
+  int rc = make_seqs(cu_seqlens, num_seqs, &st, &T);
+  if (rc) return rc;
+  if ((rc = check_indexer_shape(H_I, d_I, groups, block_size))) return rc;
+  if (q_begin < 0 || q_count < 0 || q_begin + q_count > T)
+    return fail(TSA_ERR_INVALID_ARG, "query range [%lld, %lld) outside [0, %lld)", (long long)q_begin,
+                (long long)(q_begin + q_count), (long long)T);
+  if (width < score_width(st.max_len, block_size))
+    return fail(TSA_ERR_INVALID_ARG, "width=%lld < %lld", (long long)width,
+                (long long)score_width(st.max_len, block_size));
+  if (q_count == 0) return TSA_OK;
+  if (!q_idx || !k_idx || !w || !scores) return fail(TSA_ERR_INVALID_ARG, "null tensor pointer");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  TSA_CHECK_CUDA(launch_fill(scores, q_count * groups * width, -INFINITY, s), "fill");
+  for (int b = 0; b < num_seqs; ++b) {
+    int64_t lo = std::max<int64_t>(q_begin, st.cu[b]);
+    int64_t hi = std::min<int64_t>(q_begin + q_count, st.cu[b + 1]);
+    if (lo >= hi) continue;
+    IndexerArgs a;
+    a.q = static_cast<const __nv_bfloat16*>(q_idx);
+    a.k = static_cast<const __nv_bfloat16*>(k_idx);
+    a.w = w;
+    a.H_I = H_I; a.d_I = d_I; a.groups = groups; a.bs = block_size;
+    a.score_scale = score_scale;
+    a.seq_start = st.cu[b];
+    a.p_begin = static_cast<int>(lo - st.cu[b]);
+    a.nq = static_cast<int>(hi - lo);
+    a.out = scores + (lo - q_begin) * groups * width;
+    a.width = width;
+    TSA_CHECK_CUDA(launch_indexer(a, s), "indexer launch");
+  }
+  return TSA_OK;
+}
+
+// ---------------------------------------------------------------- top-k
+
+int qsa_topk_from_scores(const float* scores, int64_t rows, int64_t width, int64_t ld, int topk,
+                         int32_t* indices, void* stream) {
+  if (rows < 0 || width < 0 || ld < width) return fail(TSA_ERR_INVALID_ARG, "bad rows/width/ld");
+  if (width > 0x7fffffffLL) return fail(TSA_ERR_UNSUPPORTED, "width beyond 2^31-1");
+  if (rows > 0x7fffffffLL) return fail(TSA_ERR_UNSUPPORTED, "rows beyond 2^31-1");
+  if (topk < 1 || topk > kTopkMaxK) return fail(TSA_ERR_UNSUPPORTED, "topk=%d outside [1, %d]", topk, kTopkMaxK);
+  if (rows == 0) return TSA_OK;
+  if (!scores || !indices) return fail(TSA_ERR_INVALID_ARG, "null tensor pointer");
+  TopkRows a;
+  a.scores = scores; a.ld = ld; a.width = width; a.mode = 0; a.groups = 1; a.bs = 1; a.p0 = 0;
+  a.out = indices; a.out_ld = topk; a.k = topk;
+  return cuda_status(launch_topk_rows(a, rows, static_cast<cudaStream_t>(stream)), "topk launch");
+}
+
+size_t qsa_topk_workspace_size(const int32_t* cu_seqlens, int num_seqs, int groups, int block_size) {
+  SeqTable st;
+  int64_t T;
+  if (make_seqs(cu_seqlens, num_seqs, &st, &T) || groups < 1 || block_size < 1) return 0;
+  int64_t C = chunk_rows(st.max_len, groups, block_size);
+  return static_cast<size_t>(C * groups * score_width(st.max_len, block_size) * sizeof(float));
+}
+
+int qsa_topk(const void* q_idx, const void* k_idx, const float* w, const int32_t* cu_seqlens, int num_seqs,
+             int H_I, int d_I, int groups, int block_size, float score_scale, int topk, int32_t* indices,
+             void* workspace, size_t workspace_bytes, void* stream) {
+  SeqTable st;
+  int64_t T;
+  int rc = make_seqs(cu_seqlens, num_seqs, &st, &T);
+  if (rc) return rc;
+  if ((rc = check_indexer_shape(H_I, d_I, groups, block_size))) return rc;
+  if (topk < 1 || topk > kTopkMaxK) return fail(TSA_ERR_UNSUPPORTED, "topk=%d outside [1, %d]", topk, kTopkMaxK);
+  if (T == 0) return TSA_OK;
+  if (!q_idx || !k_idx || !w || !indices) return fail(TSA_ERR_INVALID_ARG, "null tensor pointer");
+  size_t need = qsa_topk_workspace_size(cu_seqlens, num_seqs, groups, block_size);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(TSA_ERR_WORKSPACE, "workspace %zu bytes < %zu", workspace_bytes, need);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t C = chunk_rows(st.max_len, groups, block_size);
+  const int64_t width = score_width(st.max_len, block_size);
+  float* scratch = static_cast<float*>(workspace);
+  for (int b = 0; b < num_seqs; ++b) {
+    const int len = st.cu[b + 1] - st.cu[b];
+    for (int64_t p0 = 0; p0 < len; p0 += C) {
+      const int nq = static_cast<int>(std::min<int64_t>(C, len - p0));
+      IndexerArgs a;
+      a.q = static_cast<const __nv_bfloat16*>(q_idx);
+      a.k = static_cast<const __nv_bfloat16*>(k_idx);
+      a.w = w;
+      a.H_I = H_I; a.d_I = d_I; a.groups = groups; a.bs = block_size;
+      a.score_scale = score_scale;
+      a.seq_start = st.cu[b];
+      a.p_begin = static_cast<int>(p0);
+      a.nq = nq;
+      a.out = scratch;
+      a.width = width;
+      TSA_CHECK_CUDA(launch_indexer(a, s), "indexer launch");
+      TopkRows r;
+      r.scores = scratch; r.ld = width; r.width = width;
+      r.mode = block_size == 1 ? 1 : 2;
+      r.groups = groups; r.bs = block_size; r.p0 = p0;
+      r.out = indices + (st.cu[b] + p0) * groups * topk;
+      r.out_ld = topk;
+      r.k = topk;
+      TSA_CHECK_CUDA(launch_topk_rows(r, (int64_t)nq * groups, s), "topk launch");
+    }
+  }
+  return TSA_OK;
+}
+
+// ---------------------------------------------------------------- sparse MLA
+
+static int check_mla(int64_t T, int H, int d_qk, int topk) {
+  if (H < 1 || H > 128) return fail(TSA_ERR_UNSUPPORTED, "H=%d outside [1, 128]", H);
+  if (d_qk != 512 && d_qk != 576) return fail(TSA_ERR_UNSUPPORTED, "d_qk=%d: need 512 or 576", d_qk);
+  if (topk < 1) return fail(TSA_ERR_INVALID_ARG, "topk=%d < 1", topk);
+  if (T > 0x7fffffffLL) return fail(TSA_ERR_UNSUPPORTED, "T beyond 2^31-1");
+  return TSA_OK;
+}
+
+int sparse_mla_fwd(const void* q, const void* kv, const int32_t* indices, const int32_t* cu_seqlens, int num_seqs,
+                   int H, int d_qk, int topk, float softmax_scale, void* out, float* lse, void* stream) {
+  MlaFwdArgs a;
+  int64_t T;
+  int rc = make_seqs(cu_seqlens, num_seqs, &a.st, &T);
+  if (rc) return rc;
+  if ((rc = check_mla(T, H, d_qk, topk))) return rc;
+  if (T == 0) return TSA_OK;
+  if (!q || !kv || !indices || !out || !lse) return fail(TSA_ERR_INVALID_ARG, "null tensor pointer");
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.kv = static_cast<const __nv_bfloat16*>(kv);
+  a.idx = indices;
+  a.T = static_cast<int>(T); a.H = H; a.topk = topk;
+  a.scale_log2 = softmax_scale * kLog2e;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.lse = lse;
+  a.flags = flags_ptr();
+  return cuda_status(launch_mla_fwd(a, d_qk, static_cast<cudaStream_t>(stream)), "mla fwd launch");
+}
+
+size_t sparse_mla_bwd_workspace_size(int64_t T, int H, int d_qk) {
+  if (T < 0 || H < 1 || d_qk < 1) return 0;
+  size_t a = static_cast<size_t>(T) * d_qk * sizeof(float);
+  a = (a + 255) & ~size_t(255);
+  return a + static_cast<size_t>(T) * H * sizeof(float);
+}
+
+int sparse_mla_bwd(const void* q, const void* kv, const int32_t* indices, const void* out, const float* lse,
+                   const void* dout, const int32_t* cu_seqlens, int num_seqs, int H, int d_qk, int topk,
+                   float softmax_scale, void* dq, void* dkv, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+  MlaBwdArgs a;
+  int64_t T;
+  int rc = make_seqs(cu_seqlens, num_seqs, &a.st, &T);
+  if (rc) return rc;
+  if ((rc = check_mla(T, H, d_qk, topk))) return rc;
+  if (T == 0) return TSA_OK;
+  if (!q || !kv || !indices || !out || !lse || !dout || !dq || !dkv)
+    return fail(TSA_ERR_INVALID_ARG, "null tensor pointer");
+  size_t need = sparse_mla_bwd_workspace_size(T, H, d_qk);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(TSA_ERR_WORKSPACE, "workspace %zu bytes < %zu", workspace_bytes, need);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  size_t dkv_bytes = (static_cast<size_t>(T) * d_qk * sizeof(float) + 255) & ~size_t(255);
+  float* dkv_acc = static_cast<float*>(workspace);
+  float* dlt = reinterpret_cast<float*>(static_cast<char*>(workspace) + dkv_bytes);
+  TSA_CHECK_CUDA(cudaMemsetAsync(dkv_acc, 0, static_cast<size_t>(T) * d_qk * sizeof(float), s), "memset");
+  TSA_CHECK_CUDA(launch_bwd_delta(static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout),
+                                  dlt, T * H, 512, s), "delta launch");
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.kv = static_cast<const __nv_bfloat16*>(kv);
+  a.idx = indices;
+  a.lse = lse;
+  a.dlt = dlt;
+  a.dout = static_cast<const __nv_bfloat16*>(dout);
+  a.T = static_cast<int>(T); a.H = H; a.topk = topk;
+  a.scale = softmax_scale;
+  a.scale_log2 = softmax_scale * kLog2e;
+  a.dq = static_cast<__nv_bfloat16*>(dq);
+  a.dkv_acc = dkv_acc;
+  TSA_CHECK_CUDA(launch_mla_bwd(a, d_qk, s), "mla bwd launch");
+  TSA_CHECK_CUDA(launch_f32_to_bf16(dkv_acc, static_cast<__nv_bfloat16*>(dkv), T * d_qk, s), "convert launch");
+  return TSA_OK;
+}
+
+// ---------------------------------------------------------------- sparse GQA
+
+static int check_gqa(int64_t T, int Hq, int Hkv, int d, int block_size, int nsel) {
+  if (Hkv < 1 || Hq < Hkv || Hq % Hkv != 0 || Hq / Hkv > 16)
+    return fail(TSA_ERR_UNSUPPORTED, "Hq=%d Hkv=%d: need Hq = G*Hkv with 1 <= G <= 16", Hq, Hkv);
+  if (d != 64 && d != 128) return fail(TSA_ERR_UNSUPPORTED, "d=%d: need 64 or 128", d);
+  if (block_size != 32 && block_size != 64) return fail(TSA_ERR_UNSUPPORTED, "block_size=%d: need 32 or 64", block_size);
+  if (nsel < 1) return fail(TSA_ERR_INVALID_ARG, "nsel=%d < 1", nsel);
+  if (T > 0x7fffffffLL) return fail(TSA_ERR_UNSUPPORTED, "T beyond 2^31-1");
+  return TSA_OK;
+}
+
+int sparse_gqa_fwd(const void* q, const void* k, const void* v, const int32_t* block_indices,
+                   const int32_t* cu_seqlens, int num_seqs, int Hq, int Hkv, int d, int block_size, int nsel,
+                   float softmax_scale, void* out, float* lse, void* stream) {
+  GqaArgs a;
+  memset(static_cast<void*>(&a), 0, sizeof(a) - sizeof(SeqTable));
+  int64_t T;
+  int rc = make_seqs(cu_seqlens, num_seqs, &a.st, &T);
+  if (rc) return rc;
+  if ((rc = check_gqa(T, Hq, Hkv, d, block_size, nsel))) return rc;
+  if (T == 0) return TSA_OK;
+  if (!q || !k || !v || !block_indices || !out || !lse) return fail(TSA_ERR_INVALID_ARG, "null tensor pointer");
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k = static_cast<const __nv_bfloat16*>(k);
+  a.v = static_cast<const __nv_bfloat16*>(v);
+  a.blk = block_indices;
+  a.T = static_cast<int>(T); a.Hq = Hq; a.Hkv = Hkv; a.G = Hq / Hkv; a.nsel = nsel;
+  a.scale = softmax_scale;
+  a.scale_log2 = softmax_scale * kLog2e;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.lse = lse;
+  a.flags = flags_ptr();
+  return cuda_status(launch_gqa(a, block_size, d, false, static_cast<cudaStream_t>(stream)), "gqa fwd launch");
+}
+
+size_t sparse_gqa_bwd_workspace_size(int64_t T, int Hq, int Hkv, int d) {
+  if (T < 0 || Hq < 1 || Hkv < 1 || d < 1) return 0;
+  size_t one = (static_cast<size_t>(T) * Hkv * d * sizeof(float) + 255) & ~size_t(255);
+  return 2 * one + static_cast<size_t>(T) * Hq * sizeof(float);
+}
+
+int sparse_gqa_bwd(const void* q, const void* k, const void* v, const int32_t* block_indices, const void* out,
+                   const float* lse, const void* dout, const int32_t* cu_seqlens, int num_seqs, int Hq, int Hkv,
+                   int d, int block_size, int nsel, float softmax_scale, void* dq, void* dk, void* dv,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+  GqaArgs a;
+  memset(static_cast<void*>(&a), 0, sizeof(a) - sizeof(SeqTable));
+  int64_t T;
+  int rc = make_seqs(cu_seqlens, num_seqs, &a.st, &T);
+  if (rc) return rc;
+  if ((rc = check_gqa(T, Hq, Hkv, d, block_size, nsel))) return rc;
+  if (T == 0) return TSA_OK;
+  if (!q || !k || !v || !block_indices || !out || !lse || !dout || !dq || !dk || !dv)
+    return fail(TSA_ERR_INVALID_ARG, "null tensor pointer");
+  size_t need = sparse_gqa_bwd_workspace_size(T, Hq, Hkv, d);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(TSA_ERR_WORKSPACE, "workspace %zu bytes < %zu", workspace_bytes, need);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  size_t one_elems = static_cast<size_t>(T) * Hkv * d;
+  size_t one = (one_elems * sizeof(float) + 255) & ~size_t(255);
+  float* dk_acc = static_cast<float*>(workspace);
+  float* dv_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + one);
+  float* dlt = reinterpret_cast<float*>(static_cast<char*>(workspace) + 2 * one);
+  TSA_CHECK_CUDA(cudaMemsetAsync(workspace, 0, 2 * one, s), "memset");
+  TSA_CHECK_CUDA(launch_bwd_delta(static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout),
+                                  dlt, T * Hq, d, s), "delta launch");
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k = static_cast<const __nv_bfloat16*>(k);
+  a.v = static_cast<const __nv_bfloat16*>(v);
+  a.blk = block_indices;
+  a.lse_in = lse;
+  a.dlt = dlt;
+  a.dout = static_cast<const __nv_bfloat16*>(dout);
+  a.T = static_cast<int>(T); a.Hq = Hq; a.Hkv = Hkv; a.G = Hq / Hkv; a.nsel = nsel;
+  a.scale = softmax_scale;
+  a.scale_log2 = softmax_scale * kLog2e;
+  a.dq = static_cast<__nv_bfloat16*>(dq);
+  a.dk_acc = dk_acc;
+  a.dv_acc = dv_acc;
+  a.flags = flags_ptr();
+  TSA_CHECK_CUDA(launch_gqa(a, block_size, d, true, s), "gqa bwd launch");
+  TSA_CHECK_CUDA(launch_f32_to_bf16(dk_acc, static_cast<__nv_bfloat16*>(dk), (int64_t)one_elems, s), "convert");
+  TSA_CHECK_CUDA(launch_f32_to_bf16(dv_acc, static_cast<__nv_bfloat16*>(dv), (int64_t)one_elems, s), "convert");
+  return TSA_OK;
+}
+
+}  // extern "C"

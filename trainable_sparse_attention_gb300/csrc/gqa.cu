@@ -1,0 +1,389 @@
+// Block Sparse-GQA forward and backward.
+//
+// Megatron-LM issue #7060 "Add trainable QSA sparse attention with a TileLang
+// backend" ("Describe the solution you'd like": Sparse-GQA forward and
+// backward kernels over exact block top-k selections, BSHD and packed THD).
+//
+// One CTA per (query t, kv group g) holds the group's Hq/Hkv query heads in a
+// 16-row MMA tile; each selected block (block_size tokens of the group's k and
+// v, causal inside the query's own block) streams through a double-buffered
+// cp.async pipeline.  Forward: online softmax, natural-log LSE.  Backward:
+// recompute P from the LSE, dQ in registers, dK/dV tile contributions
+// scattered with red.global.add.v2.f32 into fp32 workspaces, then converted.
+#include "kernels.cuh"
+
+namespace tsa {
+
+
+// BS tokens per block, DH head dim.  4 warps.
+template <int BS, int DH>
+struct GqaSmem {
+  static constexpr int RS = DH + 8;
+  static constexpr int PRS = BS + 8;
+};
+
+template <int BS, int DH>
+__global__ void __launch_bounds__(128) gqa_fwd_mma_kernel(const __grid_constant__ GqaArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  constexpr int RS = DH + 8, PRS = BS + 8;
+  constexpr int KPW = BS / 4;        // keys per warp in S
+  constexpr int NKT = KPW / 8;       // n-tiles per warp in S
+  constexpr int CPW = DH / 4;        // channels per warp in PV
+  constexpr int NTV = CPW / 8;
+  __nv_bfloat16* Qs = reinterpret_cast<__nv_bfloat16*>(smem_raw);  // [16][RS]
+  __nv_bfloat16* Ks = Qs + 16 * RS;                                 // [2][BS][RS]
+  __nv_bfloat16* Vs = Ks + 2 * BS * RS;                             // [2][BS][RS]
+  __nv_bfloat16* Ps = Vs + 2 * BS * RS;                             // [16][PRS]
+  float* red_max = reinterpret_cast<float*>(Ps + 16 * PRS);         // [4][16]
+  float* red_sum = red_max + 64;
+  int* s_blk = reinterpret_cast<int*>(red_sum + 64);                // [2]
+
+  const int t = blockIdx.x, gk = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int gq = lane >> 2, c4 = lane & 3;
+  const int sq = seq_of(a.st, t);
+  const int s0 = a.st.cu[sq];
+  const int n = a.st.cu[sq + 1] - s0;
+  const int p = t - s0;
+  const int h0 = gk * a.G;
+  const int* blk_row = a.blk + ((int64_t)t * a.Hkv + gk) * a.nsel;
+  constexpr int CPR = DH / 8;
+
+  for (int i = tid; i < 16 * CPR; i += 128) {
+    int r = i / CPR, ch = i % CPR;
+    bool ok = r < a.G;
+    const __nv_bfloat16* src = a.q + ((int64_t)t * a.Hq + h0 + (ok ? r : 0)) * DH + ch * 8;
+    cp_async16(smem_u32(Qs + r * RS + ch * 8), src, ok ? 16u : 0u);
+  }
+  auto gather = [&](int j, int buf) {
+    int b = __ldg(blk_row + j);
+    bool bok = b >= 0 && b * BS < n;
+    if (b >= 0 && b * BS >= n && tid == 0) raise_flag(a.flags, TSA_FLAG_INDEX_RANGE);
+    for (int i = tid; i < BS * CPR; i += 128) {
+      int r = i / CPR, ch = i % CPR;
+      int pos = b * BS + r;
+      bool ok = bok && pos <= p;
+      int64_t row = ((int64_t)(s0 + (ok ? pos : 0)) * a.Hkv + gk) * DH + ch * 8;
+      cp_async16(smem_u32(Ks + (buf * BS + r) * RS + ch * 8), a.k + row, ok ? 16u : 0u);
+      cp_async16(smem_u32(Vs + (buf * BS + r) * RS + ch * 8), a.v + row, ok ? 16u : 0u);
+    }
+    if (tid == 0) s_blk[buf] = bok ? b : -1;
+  };
+  gather(0, 0);
+  cp_async_commit();
+
+  const float NEG_INF = __int_as_float(0xff800000);
+  float m_r[2] = {NEG_INF, NEG_INF}, l_r[2] = {0.f, 0.f};
+  float o[NTV][4];
+#pragma unroll
+  for (int i = 0; i < NTV; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+  for (int j = 0; j < a.nsel; ++j) {
+    const int buf = j & 1;
+    if (j + 1 < a.nsel) { gather(j + 1, buf ^ 1); cp_async_commit(); cp_async_wait<1>(); }
+    else { cp_async_wait<0>(); }
+    __syncthreads();
+    const int b = s_blk[buf];
+    const __nv_bfloat16* Kb = Ks + buf * BS * RS;
+    const __nv_bfloat16* Vb = Vs + buf * BS * RS;
+    float s[NKT][4];
+#pragma unroll
+    for (int i = 0; i < NKT; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < DH / 16; ks += 2) {
+      uint32_t a0, a1, a2, a3, a4, a5, a6, a7;
+      ldsm_x4(smem_u32(Qs + (lane & 15) * RS + ks * 16 + (lane >> 4) * 8), a0, a1, a2, a3);
+      ldsm_x4(smem_u32(Qs + (lane & 15) * RS + (ks + 1) * 16 + (lane >> 4) * 8), a4, a5, a6, a7);
+#pragma unroll
+      for (int nk = 0; nk < NKT; ++nk) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(smem_u32(Kb + (warp * KPW + nk * 8 + (lane & 7)) * RS + ks * 16 + (lane >> 3) * 8), b0, b1, b2, b3);
+        mma_bf16(s[nk], a0, a1, a2, a3, b0, b1);
+        mma_bf16(s[nk], a4, a5, a6, a7, b2, b3);
+      }
+    }
+    float mx0 = NEG_INF, mx1 = NEG_INF;
+#pragma unroll
+    for (int nk = 0; nk < NKT; ++nk) {
+      int key = warp * KPW + nk * 8 + 2 * c4;
+      bool v0 = b >= 0 && b * BS + key <= p, v1 = b >= 0 && b * BS + key + 1 <= p;
+      s[nk][0] = v0 ? s[nk][0] * a.scale_log2 : NEG_INF;
+      s[nk][1] = v1 ? s[nk][1] * a.scale_log2 : NEG_INF;
+      s[nk][2] = v0 ? s[nk][2] * a.scale_log2 : NEG_INF;
+      s[nk][3] = v1 ? s[nk][3] * a.scale_log2 : NEG_INF;
+      mx0 = fmaxf(mx0, fmaxf(s[nk][0], s[nk][1]));
+      mx1 = fmaxf(mx1, fmaxf(s[nk][2], s[nk][3]));
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    if (c4 == 0) { red_max[warp * 16 + gq] = mx0; red_max[warp * 16 + gq + 8] = mx1; }
+    __syncthreads();
+    float mnew[2], muse[2], alpha[2];
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      int row = gq + rr * 8;
+      float tm = fmaxf(fmaxf(red_max[row], red_max[16 + row]), fmaxf(red_max[32 + row], red_max[48 + row]));
+      mnew[rr] = fmaxf(m_r[rr], tm);
+      muse[rr] = mnew[rr] == NEG_INF ? 0.f : mnew[rr];
+      alpha[rr] = exp2f(m_r[rr] - muse[rr]);
+    }
+    float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+    for (int nk = 0; nk < NKT; ++nk) {
+      float p0 = exp2f(s[nk][0] - muse[0]), p1 = exp2f(s[nk][1] - muse[0]);
+      float p2 = exp2f(s[nk][2] - muse[1]), p3 = exp2f(s[nk][3] - muse[1]);
+      ps0 += p0 + p1;
+      ps1 += p2 + p3;
+      int key = warp * KPW + nk * 8 + 2 * c4;
+      *reinterpret_cast<uint32_t*>(Ps + gq * PRS + key) = pack_bf16(p0, p1);
+      *reinterpret_cast<uint32_t*>(Ps + (gq + 8) * PRS + key) = pack_bf16(p2, p3);
+    }
+    ps0 += __shfl_xor_sync(0xffffffffu, ps0, 1);
+    ps0 += __shfl_xor_sync(0xffffffffu, ps0, 2);
+    ps1 += __shfl_xor_sync(0xffffffffu, ps1, 1);
+    ps1 += __shfl_xor_sync(0xffffffffu, ps1, 2);
+    if (c4 == 0) { red_sum[warp * 16 + gq] = ps0; red_sum[warp * 16 + gq + 8] = ps1; }
+    __syncthreads();
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      int row = gq + rr * 8;
+      float ts = (red_sum[row] + red_sum[16 + row]) + (red_sum[32 + row] + red_sum[48 + row]);
+      l_r[rr] = l_r[rr] * alpha[rr] + ts;
+      m_r[rr] = mnew[rr];
+    }
+#pragma unroll
+    for (int nt = 0; nt < NTV; ++nt) {
+      o[nt][0] *= alpha[0]; o[nt][1] *= alpha[0];
+      o[nt][2] *= alpha[1]; o[nt][3] *= alpha[1];
+    }
+#pragma unroll
+    for (int ks = 0; ks < BS / 16; ++ks) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(smem_u32(Ps + (lane & 15) * PRS + ks * 16 + (lane >> 4) * 8), a0, a1, a2, a3);
+#pragma unroll
+      for (int nt = 0; nt < NTV; nt += 2) {
+        uint32_t b0, b1, b2, b3;
+        int key = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        int ch = warp * CPW + nt * 8 + (lane >> 4) * 8;
+        ldsm_x4_t(smem_u32(Vb + key * RS + ch), b0, b1, b2, b3);
+        mma_bf16(o[nt], a0, a1, a2, a3, b0, b1);
+        mma_bf16(o[nt + 1], a0, a1, a2, a3, b2, b3);
+      }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    int r = gq + rr * 8;
+    if (r < a.G) {
+      float inv = l_r[rr] > 0.f ? 1.f / l_r[rr] : 0.f;
+      __nv_bfloat16* orow = a.out + ((int64_t)t * a.Hq + h0 + r) * DH + warp * CPW + 2 * c4;
+#pragma unroll
+      for (int nt = 0; nt < NTV; ++nt)
+        *reinterpret_cast<uint32_t*>(orow + nt * 8) = pack_bf16(o[nt][2 * rr] * inv, o[nt][2 * rr + 1] * inv);
+      if (warp == 0 && c4 == 0)
+        a.lse[(int64_t)t * a.Hq + h0 + r] = l_r[rr] > 0.f ? (m_r[rr] + log2f(l_r[rr])) * kLn2 : NEG_INF;
+    }
+  }
+}
+
+template <int BS, int DH>
+__global__ void __launch_bounds__(128) gqa_bwd_mma_kernel(const __grid_constant__ GqaArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  constexpr int RS = DH + 8, PRS = BS + 8;
+  constexpr int KPW = BS / 4;
+  constexpr int NKT = KPW / 8;
+  constexpr int CPW = DH / 4;
+  constexpr int NTV = CPW / 8;
+  __nv_bfloat16* Qs = reinterpret_cast<__nv_bfloat16*>(smem_raw);  // [16][RS]
+  __nv_bfloat16* dOs = Qs + 16 * RS;                                // [16][RS]
+  __nv_bfloat16* Ks = dOs + 16 * RS;                                // [2][BS][RS]
+  __nv_bfloat16* Vs = Ks + 2 * BS * RS;
+  __nv_bfloat16* Ps = Vs + 2 * BS * RS;                             // [16][PRS]
+  __nv_bfloat16* dSs = Ps + 16 * PRS;
+  int* s_blk = reinterpret_cast<int*>(dSs + 16 * PRS);
+
+  const int t = blockIdx.x, gk = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int gq = lane >> 2, c4 = lane & 3;
+  const int sq = seq_of(a.st, t);
+  const int s0 = a.st.cu[sq];
+  const int n = a.st.cu[sq + 1] - s0;
+  const int p = t - s0;
+  const int h0 = gk * a.G;
+  const int* blk_row = a.blk + ((int64_t)t * a.Hkv + gk) * a.nsel;
+  constexpr int CPR = DH / 8;
+  const float NEG_INF = __int_as_float(0xff800000);
+
+  for (int i = tid; i < 16 * CPR; i += 128) {
+    int r = i / CPR, ch = i % CPR;
+    bool ok = r < a.G;
+    int64_t off = ((int64_t)t * a.Hq + h0 + (ok ? r : 0)) * DH + ch * 8;
+    cp_async16(smem_u32(Qs + r * RS + ch * 8), a.q + off, ok ? 16u : 0u);
+    cp_async16(smem_u32(dOs + r * RS + ch * 8), a.dout + off, ok ? 16u : 0u);
+  }
+  auto gather = [&](int j, int buf) {
+    int b = __ldg(blk_row + j);
+    bool bok = b >= 0 && b * BS < n;
+    for (int i = tid; i < BS * CPR; i += 128) {
+      int r = i / CPR, ch = i % CPR;
+      int pos = b * BS + r;
+      bool ok = bok && pos <= p;
+      int64_t row = ((int64_t)(s0 + (ok ? pos : 0)) * a.Hkv + gk) * DH + ch * 8;
+      cp_async16(smem_u32(Ks + (buf * BS + r) * RS + ch * 8), a.k + row, ok ? 16u : 0u);
+      cp_async16(smem_u32(Vs + (buf * BS + r) * RS + ch * 8), a.v + row, ok ? 16u : 0u);
+    }
+    if (tid == 0) s_blk[buf] = bok ? b : -1;
+  };
+  gather(0, 0);
+  cp_async_commit();
+
+  float lse2[2], dl[2];
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    int r = gq + rr * 8;
+    float L = r < a.G ? a.lse_in[(int64_t)t * a.Hq + h0 + r] : NEG_INF;
+    lse2[rr] = L * kLog2e;
+    dl[rr] = r < a.G ? a.dlt[(int64_t)t * a.Hq + h0 + r] : 0.f;
+  }
+  float dq[NTV][4];
+#pragma unroll
+  for (int i = 0; i < NTV; ++i) dq[i][0] = dq[i][1] = dq[i][2] = dq[i][3] = 0.f;
+
+  for (int j = 0; j < a.nsel; ++j) {
+    const int buf = j & 1;
+    if (j + 1 < a.nsel) { gather(j + 1, buf ^ 1); cp_async_commit(); cp_async_wait<1>(); }
+    else { cp_async_wait<0>(); }
+    __syncthreads();
+    const int b = s_blk[buf];
+    const __nv_bfloat16* Kb = Ks + buf * BS * RS;
+    const __nv_bfloat16* Vb = Vs + buf * BS * RS;
+    if (b >= 0) {  // uniform across the CTA
+      float s[NKT][4], dp[NKT][4];
+#pragma unroll
+      for (int i = 0; i < NKT; ++i)
+        for (int e = 0; e < 4; ++e) s[i][e] = dp[i][e] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < DH / 16; ks += 2) {
+        uint32_t a0, a1, a2, a3, a4, a5, a6, a7, e0, e1, e2, e3, e4, e5, e6, e7;
+        ldsm_x4(smem_u32(Qs + (lane & 15) * RS + ks * 16 + (lane >> 4) * 8), a0, a1, a2, a3);
+        ldsm_x4(smem_u32(Qs + (lane & 15) * RS + (ks + 1) * 16 + (lane >> 4) * 8), a4, a5, a6, a7);
+        ldsm_x4(smem_u32(dOs + (lane & 15) * RS + ks * 16 + (lane >> 4) * 8), e0, e1, e2, e3);
+        ldsm_x4(smem_u32(dOs + (lane & 15) * RS + (ks + 1) * 16 + (lane >> 4) * 8), e4, e5, e6, e7);
+#pragma unroll
+        for (int nk = 0; nk < NKT; ++nk) {
+          uint32_t b0, b1, b2, b3;
+          int krow = warp * KPW + nk * 8 + (lane & 7);
+          ldsm_x4(smem_u32(Kb + krow * RS + ks * 16 + (lane >> 3) * 8), b0, b1, b2, b3);
+          mma_bf16(s[nk], a0, a1, a2, a3, b0, b1);
+          mma_bf16(s[nk], a4, a5, a6, a7, b2, b3);
+          ldsm_x4(smem_u32(Vb + krow * RS + ks * 16 + (lane >> 3) * 8), b0, b1, b2, b3);
+          mma_bf16(dp[nk], e0, e1, e2, e3, b0, b1);
+          mma_bf16(dp[nk], e4, e5, e6, e7, b2, b3);
+        }
+      }
+#pragma unroll
+      for (int nk = 0; nk < NKT; ++nk) {
+        int key = warp * KPW + nk * 8 + 2 * c4;
+        bool v0 = b * BS + key <= p, v1 = b * BS + key + 1 <= p;
+        float P[4], dS[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          int rr = i >> 1;
+          bool v = (i & 1) ? v1 : v0;
+          P[i] = (v && lse2[rr] != NEG_INF) ? exp2f(s[nk][i] * a.scale_log2 - lse2[rr]) : 0.f;
+          dS[i] = a.scale * P[i] * (dp[nk][i] - dl[rr]);
+        }
+        *reinterpret_cast<uint32_t*>(Ps + gq * PRS + key) = pack_bf16(P[0], P[1]);
+        *reinterpret_cast<uint32_t*>(Ps + (gq + 8) * PRS + key) = pack_bf16(P[2], P[3]);
+        *reinterpret_cast<uint32_t*>(dSs + gq * PRS + key) = pack_bf16(dS[0], dS[1]);
+        *reinterpret_cast<uint32_t*>(dSs + (gq + 8) * PRS + key) = pack_bf16(dS[2], dS[3]);
+      }
+      __syncthreads();
+      // dQ[:, warp channels] += dS K
+#pragma unroll
+      for (int ks = 0; ks < BS / 16; ++ks) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(smem_u32(dSs + (lane & 15) * PRS + ks * 16 + (lane >> 4) * 8), a0, a1, a2, a3);
+#pragma unroll
+        for (int nt = 0; nt < NTV; nt += 2) {
+          uint32_t b0, b1, b2, b3;
+          int key = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+          int ch = warp * CPW + nt * 8 + (lane >> 4) * 8;
+          ldsm_x4_t(smem_u32(Kb + key * RS + ch), b0, b1, b2, b3);
+          mma_bf16(dq[nt], a0, a1, a2, a3, b0, b1);
+          mma_bf16(dq[nt + 1], a0, a1, a2, a3, b2, b3);
+        }
+      }
+      // dK tile = dS^T Q, dV tile = P^T dO  ([BS keys x DH], K = 16 heads); warp owns CPW channels
+#pragma unroll 1
+      for (int nt = 0; nt < NTV; ++nt) {
+        const int ch0 = warp * CPW + nt * 8;
+        uint32_t bq0, bq1, bo0, bo1;
+        ldsm_x2_t(smem_u32(Qs + (lane & 15) * RS + ch0), bq0, bq1);
+        ldsm_x2_t(smem_u32(dOs + (lane & 15) * RS + ch0), bo0, bo1);
+#pragma unroll
+        for (int m2 = 0; m2 < BS / 16; ++m2) {
+          float ak[4] = {0.f, 0.f, 0.f, 0.f}, av[4] = {0.f, 0.f, 0.f, 0.f};
+          uint32_t a0, a1, a2, a3;
+          int hrow = (lane & 7) + (lane >> 4) * 8;
+          int kcol = m2 * 16 + ((lane >> 3) & 1) * 8;
+          ldsm_x4_t(smem_u32(dSs + hrow * PRS + kcol), a0, a1, a2, a3);
+          mma_bf16(ak, a0, a1, a2, a3, bq0, bq1);
+          ldsm_x4_t(smem_u32(Ps + hrow * PRS + kcol), a0, a1, a2, a3);
+          mma_bf16(av, a0, a1, a2, a3, bo0, bo1);
+          int pos0 = b * BS + m2 * 16 + gq, pos1 = pos0 + 8;
+          if (pos0 <= p) {
+            int64_t off = ((int64_t)(s0 + pos0) * a.Hkv + gk) * DH + ch0 + 2 * c4;
+            red_add_v2(a.dk_acc + off, ak[0], ak[1]);
+            red_add_v2(a.dv_acc + off, av[0], av[1]);
+          }
+          if (pos1 <= p) {
+            int64_t off = ((int64_t)(s0 + pos1) * a.Hkv + gk) * DH + ch0 + 2 * c4;
+            red_add_v2(a.dk_acc + off, ak[2], ak[3]);
+            red_add_v2(a.dv_acc + off, av[2], av[3]);
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    int r = gq + rr * 8;
+    if (r < a.G) {
+      __nv_bfloat16* drow = a.dq + ((int64_t)t * a.Hq + h0 + r) * DH + warp * CPW + 2 * c4;
+#pragma unroll
+      for (int nt = 0; nt < NTV; ++nt)
+        *reinterpret_cast<uint32_t*>(drow + nt * 8) = pack_bf16(dq[nt][2 * rr], dq[nt][2 * rr + 1]);
+    }
+  }
+}
+
+template <int BS, int DH>
+static cudaError_t launch_gqa_t(const GqaArgs& a, bool bwd, cudaStream_t stream) {
+  constexpr int RS = DH + 8, PRS = BS + 8;
+  dim3 grid(a.T, a.Hkv);
+  if (!bwd) {
+    size_t smem = sizeof(__nv_bfloat16) * (16 * RS + 4 * BS * RS + 16 * PRS) + sizeof(float) * 128 + 16;
+    cudaFuncSetAttribute(gqa_fwd_mma_kernel<BS, DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    gqa_fwd_mma_kernel<BS, DH><<<grid, 128, smem, stream>>>(a);
+  } else {
+    size_t smem = sizeof(__nv_bfloat16) * (32 * RS + 4 * BS * RS + 32 * PRS) + 16;
+    cudaFuncSetAttribute(gqa_bwd_mma_kernel<BS, DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    gqa_bwd_mma_kernel<BS, DH><<<grid, 128, smem, stream>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gqa(const GqaArgs& a, int bs, int d, bool bwd, cudaStream_t stream) {
+  if (a.T <= 0) return cudaSuccess;
+  if (bs == 64 && d == 128) return launch_gqa_t<64, 128>(a, bwd, stream);
+  if (bs == 64 && d == 64) return launch_gqa_t<64, 64>(a, bwd, stream);
+  if (bs == 32 && d == 128) return launch_gqa_t<32, 128>(a, bwd, stream);
+  return launch_gqa_t<32, 64>(a, bwd, stream);
+}
+
+}  // namespace tsa

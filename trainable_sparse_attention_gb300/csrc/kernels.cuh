@@ -1,0 +1,93 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include "common.cuh"
+
+namespace tsa {
+
+struct TopkRows {
+  const float* scores;  // row r starts at scores + r * ld
+  int64_t ld;
+  int64_t width;        // entries per row (upper bound on candidates)
+  int mode;             // 0: n = width; 1: causal tokens; 2: causal blocks
+  int groups;           // rows are (query, group) pairs in causal modes
+  int bs;               // block size (mode 2)
+  int64_t p0;           // local position of the query of row 0 (causal modes)
+  int32_t* out;         // row r writes out + r * out_ld
+  int64_t out_ld;
+  int k;
+};
+
+struct IndexerArgs {
+  const __nv_bfloat16* q;  // [T, H_I, d_I]
+  const __nv_bfloat16* k;  // [T, d_I]
+  const float* w;          // [T, H_I]
+  int H_I, d_I, groups, bs;
+  float score_scale;
+  int seq_start;   // packed row of the sequence's first token
+  int p_begin;     // local position of the launch's first query
+  int nq;          // queries in this launch
+  float* out;      // query q, group g -> out + (q*groups + g) * width
+  int64_t width;
+};
+
+struct MlaFwdArgs {
+  const __nv_bfloat16* q;   // [T, H, D]
+  const __nv_bfloat16* kv;  // [T, D]
+  const int32_t* idx;       // [T, topk]
+  int T, H, topk;
+  float scale_log2;         // softmax_scale * log2(e)
+  __nv_bfloat16* out;       // [T, H, 512]
+  float* lse;               // [T, H]
+  unsigned int* flags;      // device error flags
+  SeqTable st;
+};
+
+struct MlaBwdArgs {
+  const __nv_bfloat16* q;    // [T, H, D]
+  const __nv_bfloat16* kv;   // [T, D]
+  const int32_t* idx;        // [T, topk]
+  const float* lse;          // [T, H] natural log
+  const float* dlt;          // [T, H]
+  const __nv_bfloat16* dout; // [T, H, 512]
+  int T, H, topk;
+  float scale;               // softmax scale
+  float scale_log2;          // softmax scale * log2(e)
+  __nv_bfloat16* dq;         // [T, H, D]
+  float* dkv_acc;            // [T, D] fp32, zeroed by the caller
+  SeqTable st;
+};
+
+struct GqaArgs {
+  const __nv_bfloat16* q;   // [T, Hq, d]
+  const __nv_bfloat16* k;   // [T, Hkv, d]
+  const __nv_bfloat16* v;   // [T, Hkv, d]
+  const int32_t* blk;       // [T, Hkv, nsel]
+  const float* lse_in;      // bwd: [T, Hq]
+  const float* dlt;         // bwd: [T, Hq]
+  const __nv_bfloat16* dout;// bwd: [T, Hq, d]
+  int T, Hq, Hkv, G, nsel;
+  float scale, scale_log2;
+  __nv_bfloat16* out;       // fwd: [T, Hq, d]
+  float* lse;               // fwd: [T, Hq]
+  __nv_bfloat16* dq;        // bwd
+  float* dk_acc;            // bwd: [T, Hkv, d] fp32
+  float* dv_acc;
+  unsigned int* flags;      // device error flags
+  SeqTable st;
+};
+
+cudaError_t launch_topk_rows(const TopkRows& a, int64_t rows, cudaStream_t stream);
+cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t stream);
+cudaError_t launch_fill(float* p, int64_t n, float v, cudaStream_t stream);
+cudaError_t launch_mla_fwd(const MlaFwdArgs& a, int D, cudaStream_t stream);
+cudaError_t launch_mla_bwd(const MlaBwdArgs& a, int D, cudaStream_t stream);
+cudaError_t launch_bwd_delta(const __nv_bfloat16* o, const __nv_bfloat16* dout, float* dlt, int64_t rows, int dv,
+                             cudaStream_t stream);
+cudaError_t launch_f32_to_bf16(const float* src, __nv_bfloat16* dst, int64_t n, cudaStream_t stream);
+cudaError_t launch_gqa(const GqaArgs& a, int bs, int d, bool bwd, cudaStream_t stream);
+
+constexpr int kIndexerKTile = 128;  // keys per indexer tile (block sizes must divide it)
+constexpr int kTopkMaxK = 4096;
+
+}  // namespace tsa
