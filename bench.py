@@ -1,0 +1,416 @@
+"""Benchmark of the trainable sparse-attention hot path on GB300.
+
+Workload: long-context absorbed sparse MLA, one sequence of T = 65536 tokens,
+H = 128 heads, q/kv bf16 with 576 channels (values = first 512), top-2048,
+softmax scale 1/sqrt(192); streaming indexer with 64 heads, d_I = 128,
+w ~ U(0,1).  One step = the whole path over one batch:
+
+    qsa_topk (indexer score + exact top-k, streamed)  ->  sparse_mla_fwd
+    ->  sparse_mla_bwd (Dlt preprocess, dQ/dKV, dKV conversion)
+
+value = algorithmic TFLOP/s of the step (indexer GEMM + attention fwd + bwd,
+counted from the actual indices) with inputs resident in HBM; per-stage times,
+indexer queries/s and roofline fractions are reported alongside.  Inputs
+(~20 GB) exceed the 129 MB L2, so no flush is needed between steps.
+
+`--impl reference` times the CPU oracle on a bounded sample of the same
+workload on the host cores (the reference arm: the pages ship no runnable
+reference implementation).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+T_TOK = 65536
+H = 128
+D = 576
+DV = 512
+TOPK = 2048
+SCALE = 1.0 / math.sqrt(192)
+H_I = 64
+D_I = 128
+WORKLOAD = "mla_t65536_h128_topk2048"
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def flops_of(valid_per_row_total: int, causal_pairs: int):
+    """Algorithmic FLOPs: indexer GEMM over causal pairs; attention per valid
+    (query, key) pair and head: fwd 2*(576+512), bwd 2*(3*576+2*512)."""
+    f_idx = causal_pairs * H_I * D_I * 2
+    f_fwd = valid_per_row_total * H * 2 * (D + DV)
+    f_bwd = valid_per_row_total * H * 2 * (3 * D + 2 * DV)
+    return f_idx, f_fwd, f_bwd
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus: int):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allmax(x: float, world) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- oracle timing
+
+def oracle_sample(n_rows: int, seed: int = 123):
+    """Run the CPU oracle on n_rows query rows of the workload (indexer + top-k,
+    attention fwd and bwd per row) and return (seconds, algorithmic flops)."""
+    import numpy as np
+    import torch
+    import oracle as O
+    import synth
+
+    cu = [0, T_TOK]
+    rng = np.random.default_rng(seed)
+    rows = sorted(rng.choice(T_TOK, size=n_rows, replace=False).tolist())
+    # inputs for the sampled rows only (the oracle widens rows lazily); keys/kv in full
+    g = synth.gen(seed, "cpu")
+    k_idx = synth.randn_bf16((T_TOK, D_I), g, "cpu")
+    kv = synth.randn_bf16((T_TOK, D), g, "cpu")
+    q_rows = synth.randn_bf16((n_rows, H_I, D_I), g, "cpu")
+    w_rows = synth.uniform_f32((n_rows, H_I), g, "cpu")
+    q_att = synth.randn_bf16((n_rows, H, D), g, "cpu")
+    do_rows = synth.randn_bf16((n_rows, H, DV), g, "cpu")
+
+    class Rows:
+        """Row accessor: row t of the full tensor is the i-th sampled row."""
+        def __init__(self, data, shape):
+            self.data, self.shape, self.pos = data, shape, {t: i for i, t in enumerate(rows)}
+
+        def __getitem__(self, t):
+            return self.data[self.pos[t]]
+
+    qI = Rows(q_rows, (T_TOK, H_I, D_I))
+    W = Rows(w_rows, (T_TOK, H_I))
+    Q = Rows(q_att, (T_TOK, H, D))
+    dO = Rows(do_rows, (T_TOK, H, DV))
+    t0 = time.perf_counter()
+    sc = O.indexer_token_scores(qI, k_idx, W, cu, rows)
+    idx_rows = O.topk_rows(sc, TOPK)[:, 0, :]
+    I = Rows(torch.from_numpy(idx_rows), (T_TOK, TOPK))
+    O.sparse_mla_fwd(Q, kv, I, cu, SCALE, rows=rows)
+    O.sparse_mla_bwd(Q, kv, I, cu, SCALE, dO, rows=rows)
+    dt = time.perf_counter() - t0
+    valid = int((idx_rows >= 0).sum())
+    pairs = sum(t + 1 for t in rows)
+    f = sum(flops_of(valid, pairs))
+    return dt, f, rows
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    n_rows = args.ref_rows
+    times, fl = [], 0.0
+    for i in range(args.warmup + args.steps):
+        dt, f, _ = oracle_sample(n_rows, seed=1000 + i)
+        if i >= args.warmup:
+            times.append(dt)
+            fl = f
+    mean = sum(times) / len(times)
+    value = fl / mean / 1e12
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": "sparse-attn fwd/bwd + indexer/top-k algorithmic TFLOP/s",
+        "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": mean * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "T": T_TOK, "H": H, "d_qk": D, "topk": TOPK, "H_I": H_I, "d_I": D_I,
+                   "sample_rows_per_step": n_rows},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n_rows} random query rows of the T=65536 workload per step "
+                                   "(indexer+top-k, fwd, bwd), numpy fp64"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import torch
+    import synth
+    import trainable_sparse_attention_gb300 as tsa
+
+    rank, world, local = dist_setup(args.gpus)
+    tsa.build() if rank == 0 else None
+    barrier(world)
+    tsa.load_library()
+    dev = torch.device("cuda", local)
+    cu = [0, T_TOK]
+    peaks = load_peaks()
+
+    # inputs resident in HBM (seeded per rank: independent replicas)
+    x = synth.indexer_inputs(T_TOK, H_I, D_I, seed=5 + rank, device=dev)
+    m = synth.mla_inputs(T_TOK, H, D, seed=7 + rank, device=dev, with_grad_out=True)
+    q_i, k_i, w = x["q_idx"], x["k_idx"], x["w"]
+    q, kv, dout = m["q"], m["kv"], m["dout"]
+    del x, m
+    ws_topk = torch.empty(tsa.qsa_topk_workspace_size(cu), dtype=torch.uint8, device=dev)
+    ws_bwd = torch.empty(tsa.sparse_mla_bwd_workspace_size(T_TOK, H, D), dtype=torch.uint8, device=dev)
+    idx = torch.empty((T_TOK, 1, TOPK), dtype=torch.int32, device=dev)
+    out = torch.empty((T_TOK, H, DV), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T_TOK, H), dtype=torch.float32, device=dev)
+    dq = torch.empty_like(q)
+    dkv = torch.empty_like(kv)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        tsa.qsa_topk(q_i, k_i, w, cu, TOPK, workspace=ws_topk, out=idx)
+        if ev:
+            ev[1].record(stream)
+        tsa.sparse_mla_fwd(q, kv, idx.view(T_TOK, TOPK), cu, SCALE, out=out, lse=lse)
+        if ev:
+            ev[2].record(stream)
+        tsa.sparse_mla_bwd(q, kv, idx.view(T_TOK, TOPK), out, lse, dout, cu, SCALE, workspace=ws_bwd,
+                           dq=dq, dkv=dkv)
+        if ev:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    valid = int((idx >= 0).sum().item())
+    pairs = T_TOK * (T_TOK + 1) // 2
+    f_idx, f_fwd, f_bwd = flops_of(valid, pairs)
+    f_step = f_idx + f_fwd + f_bwd
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    launches0 = tsa.kernel_launches()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    launches = (tsa.kernel_launches() - launches0) // args.steps
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    total_ms = allmax(total_ms, world)
+    ms_step = total_ms / args.steps
+    st_idx = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+    st_fwd = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    st_bwd = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps
+    value = world * f_step / (ms_step * 1e-3) / 1e12
+    psus = peaks["bf16_tflops_sustained"]
+    stages = {
+        "indexer_topk": {"ms": st_idx, "tflops": f_idx / (st_idx * 1e-3) / 1e12,
+                         "queries_per_s": T_TOK / (st_idx * 1e-3),
+                         "frac_of_measured_bf16_sustained": f_idx / (st_idx * 1e-3) / 1e12 / psus},
+        "mla_fwd": {"ms": st_fwd, "tflops": f_fwd / (st_fwd * 1e-3) / 1e12,
+                    "frac_of_measured_bf16_sustained": f_fwd / (st_fwd * 1e-3) / 1e12 / psus},
+        "mla_bwd": {"ms": st_bwd, "tflops": f_bwd / (st_bwd * 1e-3) / 1e12,
+                    "frac_of_measured_bf16_sustained": f_bwd / (st_bwd * 1e-3) / 1e12 / psus},
+    }
+    dom = max(("indexer_topk", st_idx, f_idx), ("mla_fwd", st_fwd, f_fwd), ("mla_bwd", st_bwd, f_bwd),
+              key=lambda r: r[1])
+    achieved = dom[2] / (dom[1] * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": dom[0], "achieved": achieved, "peak": psus, "unit": "TFLOP/s",
+                "frac": achieved / psus, "traffic": None,
+                "peak_source": f"{peaks['source']} bf16 sustained (MEASURED_PEAKS.json)"}
+
+    # end to end through the public API with host buffers (pinned), copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, tsa, dev, cu, {"q_idx": q_i, "k_idx": k_i, "w": w, "q": q, "kv": kv, "dout": dout},
+                      f_step, world)
+
+    cpu = None
+    if rank == 0 and world >= 1 and not args.no_cpu_baseline:
+        dt, f, _ = oracle_sample(args.ref_rows)
+        cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{args.ref_rows} random query rows of the same workload (indexer+top-k, fwd, bwd), "
+                         f"numpy fp64, {dt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": "sparse-attn fwd/bwd + indexer/top-k algorithmic TFLOP/s", "value": value,
+            "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "T": T_TOK, "H": H, "d_qk": D, "d_v": DV, "topk": TOPK,
+                       "softmax_scale": "1/sqrt(192)", "H_I": H_I, "d_I": D_I, "parallelism": f"replicas{world}",
+                       "l2": "inputs (~20 GB) exceed L2; no flush"},
+            "stages": stages,
+            "indexer_topk_queries_per_s": world * T_TOK / (stages["indexer_topk"]["ms"] * 1e-3),
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": int(launches),
+            "clocks": clk,
+            "flops_per_step": {"indexer": f_idx, "fwd": f_fwd, "bwd": f_bwd, "valid_pairs": valid},
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, tsa, dev, cu, dev_inputs, f_step, world):
+    """Same step through the public API from pinned host buffers: H2D of every
+    input and D2H of every output inside the timed region."""
+    import torch
+    host_in = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in dev_inputs.items()}
+    for k, v in dev_inputs.items():
+        host_in[k].copy_(v)
+    outs_shape = {"idx": ((T_TOK, 1, TOPK), torch.int32), "out": ((T_TOK, H, DV), torch.bfloat16),
+                  "lse": ((T_TOK, H), torch.float32), "dq": ((T_TOK, H, D), torch.bfloat16),
+                  "dkv": ((T_TOK, D), torch.bfloat16)}
+    host_out = {k: torch.empty(s, dtype=d, pin_memory=True) for k, (s, d) in outs_shape.items()}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    stream = torch.cuda.current_stream()
+    ws_topk = torch.empty(tsa.qsa_topk_workspace_size(cu), dtype=torch.uint8, device=dev)
+    ws_bwd = torch.empty(tsa.sparse_mla_bwd_workspace_size(T_TOK, H, D), dtype=torch.uint8, device=dev)
+    d_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+
+    def e2e_step():
+        for k in host_in:
+            d_in[k].copy_(host_in[k], non_blocking=True)
+        idx = tsa.qsa_topk(d_in["q_idx"], d_in["k_idx"], d_in["w"], cu, TOPK, workspace=ws_topk)
+        i2 = idx.view(T_TOK, TOPK)
+        out, lse = tsa.sparse_mla_fwd(d_in["q"], d_in["kv"], i2, cu, SCALE)
+        dq, dkv = tsa.sparse_mla_bwd(d_in["q"], d_in["kv"], i2, out, lse, d_in["dout"], cu, SCALE, workspace=ws_bwd)
+        for k, t in (("idx", idx), ("out", out), ("lse", lse), ("dq", dq), ("dkv", dkv)):
+            host_out[k].copy_(t, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    steps = max(1, min(args.steps, 3))
+    barrier(world)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = allmax(a.elapsed_time(b) / steps, world)
+    del d_in, host_in, host_out
+    torch.cuda.empty_cache()
+    return {"value": world * f_step / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--ref-rows", type=int, default=96, help="oracle rows per CPU sample")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

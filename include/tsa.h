@@ -62,6 +62,10 @@ const char* tsa_status_string(int status);
 const char* tsa_last_error(void);
 int tsa_version(void);
 
+/* Number of CUDA kernels this library has launched since it was loaded (all
+ * devices, all threads).  Host-side counter; used to account for launches. */
+unsigned long long tsa_kernel_launches(void);
+
 /* Copy the device flags (bitwise OR of TSA_FLAG_*) to *flags after
  * synchronising `stream`; clear them when clear != 0. */
 int tsa_read_flags(uint32_t* flags, int clear, void* stream);

@@ -20,7 +20,8 @@ def lib():
 def declared_functions():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    names = re.findall(r"^\s*(?:const\s+)?(?:int|size_t|char\s*\*|const char\s*\*)\s*\**\s*(\w+)\s*\(", src, re.M)
+    names = re.findall(r"^\s*(?:const\s+)?(?:int|size_t|unsigned long long|char\s*\*|const char\s*\*)\s*\**\s*(\w+)\s*\(",
+                       src, re.M)
     return sorted(set(names))
 
 

@@ -102,10 +102,14 @@ def test_mla_nope_and_topk_padding_are_exact(tsa):
     b = _run_fwd_bwd(tsa, pad, idx_p, cu, scale)
     assert torch.equal(a["out"], b["out"]) and torch.equal(a["lse"], b["lse"])
     assert torch.equal(a["dq"], b["dq"][..., :512])
-    assert torch.equal(a["dkv"], b["dkv"][..., :512])
+    # dKV is accumulated with atomics (summation order not fixed): equal up to
+    # fp32 reordering and the final bf16 rounding
+    assert rel_l2(a["dkv"], b["dkv"][..., :512]) <= 1e-3
     assert torch.all(b["dq"][..., 512:] == 0) and torch.all(b["dkv"][..., 512:] == 0)
     o_ref, l_ref = O.sparse_mla_fwd(m["q"], m["kv"], idx, cu, scale)
     check_out_lse(a["out"], a["lse"], o_ref, l_ref)
+    dq_ref, dkv_ref = O.sparse_mla_bwd(m["q"], m["kv"], idx, cu, scale, m["dout"])
+    assert rel_l2(a["dq"], dq_ref) <= TOL_GRAD and rel_l2(a["dkv"], dkv_ref) <= TOL_GRAD
 
 
 def test_mla_forward_deterministic_under_contention(tsa):

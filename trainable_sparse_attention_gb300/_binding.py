@@ -28,6 +28,7 @@ SIGNATURES = {
     "tsa_status_string": (ctypes.c_char_p, [c_int]),
     "tsa_last_error": (ctypes.c_char_p, []),
     "tsa_version": (c_int, []),
+    "tsa_kernel_launches": (ctypes.c_ulonglong, []),
     "tsa_read_flags": (c_int, [ctypes.POINTER(ctypes.c_uint32), c_int, c_void_p]),
     "qsa_indexer_scores": (c_int, [c_void_p, c_void_p, c_void_p, c_i32p, c_int, c_int, c_int, c_int, c_int,
                                    c_float, c_int64, c_int64, c_void_p, c_int64, c_void_p]),
@@ -274,6 +275,11 @@ def sparse_gqa_bwd(q, k, v, block_indices, out, lse, dout, cu_seqlens, block_siz
                                                 softmax_scale, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
                                                 workspace.numel(), _stream(stream)))
     return dq, dk, dv
+
+
+def kernel_launches() -> int:
+    """Kernels libtsa has launched since it was loaded."""
+    return int(load_library().tsa_kernel_launches())
 
 
 def read_flags(clear: bool = True, stream=None) -> int:

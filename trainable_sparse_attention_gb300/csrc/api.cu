@@ -4,6 +4,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <string>
@@ -48,6 +49,16 @@ int cuda_status(cudaError_t e, const char* where) {
   do {                                         \
     cudaError_t _e = (expr);                   \
     if (_e != cudaSuccess) return cuda_status(_e, where); \
+  } while (0)
+
+// Kernels launched by this library since load (every launch_* starts one kernel).
+std::atomic<unsigned long long> g_launches{0};
+
+#define TSA_LAUNCH(expr, where)                \
+  do {                                         \
+    cudaError_t _e = (expr);                   \
+    if (_e != cudaSuccess) return cuda_status(_e, where); \
+    g_launches.fetch_add(1, std::memory_order_relaxed); \
   } while (0)
 
 // Validate cu_seqlens and fill the kernel-side table.
@@ -119,6 +130,8 @@ const char* tsa_last_error(void) { return g_last_error.c_str(); }
 
 int tsa_version(void) { return 1; }
 
+unsigned long long tsa_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
 int tsa_read_flags(uint32_t* flags, int clear, void* stream) {
   if (flags == nullptr) return fail(TSA_ERR_INVALID_ARG, "flags is null");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -153,7 +166,7 @@ int qsa_indexer_scores(const void* q_idx, const void* k_idx, const float* w, con
   if (q_count == 0) return TSA_OK;
   if (!q_idx || !k_idx || !w || !scores) return fail(TSA_ERR_INVALID_ARG, "null tensor pointer");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  TSA_CHECK_CUDA(launch_fill(scores, q_count * groups * width, -INFINITY, s), "fill");
+  TSA_LAUNCH(launch_fill(scores, q_count * groups * width, -INFINITY, s), "fill");
   for (int b = 0; b < num_seqs; ++b) {
     int64_t lo = std::max<int64_t>(q_begin, st.cu[b]);
     int64_t hi = std::min<int64_t>(q_begin + q_count, st.cu[b + 1]);
@@ -169,7 +182,7 @@ int qsa_indexer_scores(const void* q_idx, const void* k_idx, const float* w, con
     a.nq = static_cast<int>(hi - lo);
     a.out = scores + (lo - q_begin) * groups * width;
     a.width = width;
-    TSA_CHECK_CUDA(launch_indexer(a, s), "indexer launch");
+    TSA_LAUNCH(launch_indexer(a, s), "indexer launch");
   }
   return TSA_OK;
 }
@@ -187,7 +200,8 @@ int qsa_topk_from_scores(const float* scores, int64_t rows, int64_t width, int64
   TopkRows a;
   a.scores = scores; a.ld = ld; a.width = width; a.mode = 0; a.groups = 1; a.bs = 1; a.p0 = 0;
   a.out = indices; a.out_ld = topk; a.k = topk;
-  return cuda_status(launch_topk_rows(a, rows, static_cast<cudaStream_t>(stream)), "topk launch");
+  TSA_LAUNCH(launch_topk_rows(a, rows, static_cast<cudaStream_t>(stream)), "topk launch");
+  return TSA_OK;
 }
 
 size_t qsa_topk_workspace_size(const int32_t* cu_seqlens, int num_seqs, int groups, int block_size) {
@@ -231,7 +245,7 @@ int qsa_topk(const void* q_idx, const void* k_idx, const float* w, const int32_t
       a.nq = nq;
       a.out = scratch;
       a.width = width;
-      TSA_CHECK_CUDA(launch_indexer(a, s), "indexer launch");
+      TSA_LAUNCH(launch_indexer(a, s), "indexer launch");
       TopkRows r;
       r.scores = scratch; r.ld = width; r.width = width;
       r.mode = block_size == 1 ? 1 : 2;
@@ -239,7 +253,7 @@ int qsa_topk(const void* q_idx, const void* k_idx, const float* w, const int32_t
       r.out = indices + (st.cu[b] + p0) * groups * topk;
       r.out_ld = topk;
       r.k = topk;
-      TSA_CHECK_CUDA(launch_topk_rows(r, (int64_t)nq * groups, s), "topk launch");
+      TSA_LAUNCH(launch_topk_rows(r, (int64_t)nq * groups, s), "topk launch");
     }
   }
   return TSA_OK;
@@ -272,7 +286,8 @@ int sparse_mla_fwd(const void* q, const void* kv, const int32_t* indices, const 
   a.out = static_cast<__nv_bfloat16*>(out);
   a.lse = lse;
   a.flags = flags_ptr();
-  return cuda_status(launch_mla_fwd(a, d_qk, static_cast<cudaStream_t>(stream)), "mla fwd launch");
+  TSA_LAUNCH(launch_mla_fwd(a, d_qk, static_cast<cudaStream_t>(stream)), "mla fwd launch");
+  return TSA_OK;
 }
 
 size_t sparse_mla_bwd_workspace_size(int64_t T, int H, int d_qk) {
@@ -302,7 +317,7 @@ int sparse_mla_bwd(const void* q, const void* kv, const int32_t* indices, const 
   float* dkv_acc = static_cast<float*>(workspace);
   float* dlt = reinterpret_cast<float*>(static_cast<char*>(workspace) + dkv_bytes);
   TSA_CHECK_CUDA(cudaMemsetAsync(dkv_acc, 0, static_cast<size_t>(T) * d_qk * sizeof(float), s), "memset");
-  TSA_CHECK_CUDA(launch_bwd_delta(static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout),
+  TSA_LAUNCH(launch_bwd_delta(static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout),
                                   dlt, T * H, 512, s), "delta launch");
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.kv = static_cast<const __nv_bfloat16*>(kv);
@@ -315,8 +330,8 @@ int sparse_mla_bwd(const void* q, const void* kv, const int32_t* indices, const 
   a.scale_log2 = softmax_scale * kLog2e;
   a.dq = static_cast<__nv_bfloat16*>(dq);
   a.dkv_acc = dkv_acc;
-  TSA_CHECK_CUDA(launch_mla_bwd(a, d_qk, s), "mla bwd launch");
-  TSA_CHECK_CUDA(launch_f32_to_bf16(dkv_acc, static_cast<__nv_bfloat16*>(dkv), T * d_qk, s), "convert launch");
+  TSA_LAUNCH(launch_mla_bwd(a, d_qk, s), "mla bwd launch");
+  TSA_LAUNCH(launch_f32_to_bf16(dkv_acc, static_cast<__nv_bfloat16*>(dkv), T * d_qk, s), "convert launch");
   return TSA_OK;
 }
 
@@ -353,7 +368,8 @@ int sparse_gqa_fwd(const void* q, const void* k, const void* v, const int32_t* b
   a.out = static_cast<__nv_bfloat16*>(out);
   a.lse = lse;
   a.flags = flags_ptr();
-  return cuda_status(launch_gqa(a, block_size, d, false, static_cast<cudaStream_t>(stream)), "gqa fwd launch");
+  TSA_LAUNCH(launch_gqa(a, block_size, d, false, static_cast<cudaStream_t>(stream)), "gqa fwd launch");
+  return TSA_OK;
 }
 
 size_t sparse_gqa_bwd_workspace_size(int64_t T, int Hq, int Hkv, int d) {
@@ -385,7 +401,7 @@ int sparse_gqa_bwd(const void* q, const void* k, const void* v, const int32_t* b
   float* dv_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + one);
   float* dlt = reinterpret_cast<float*>(static_cast<char*>(workspace) + 2 * one);
   TSA_CHECK_CUDA(cudaMemsetAsync(workspace, 0, 2 * one, s), "memset");
-  TSA_CHECK_CUDA(launch_bwd_delta(static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout),
+  TSA_LAUNCH(launch_bwd_delta(static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout),
                                   dlt, T * Hq, d, s), "delta launch");
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.k = static_cast<const __nv_bfloat16*>(k);
@@ -401,9 +417,9 @@ int sparse_gqa_bwd(const void* q, const void* k, const void* v, const int32_t* b
   a.dk_acc = dk_acc;
   a.dv_acc = dv_acc;
   a.flags = flags_ptr();
-  TSA_CHECK_CUDA(launch_gqa(a, block_size, d, true, s), "gqa bwd launch");
-  TSA_CHECK_CUDA(launch_f32_to_bf16(dk_acc, static_cast<__nv_bfloat16*>(dk), (int64_t)one_elems, s), "convert");
-  TSA_CHECK_CUDA(launch_f32_to_bf16(dv_acc, static_cast<__nv_bfloat16*>(dv), (int64_t)one_elems, s), "convert");
+  TSA_LAUNCH(launch_gqa(a, block_size, d, true, s), "gqa bwd launch");
+  TSA_LAUNCH(launch_f32_to_bf16(dk_acc, static_cast<__nv_bfloat16*>(dk), (int64_t)one_elems, s), "convert");
+  TSA_LAUNCH(launch_f32_to_bf16(dv_acc, static_cast<__nv_bfloat16*>(dv), (int64_t)one_elems, s), "convert");
   return TSA_OK;
 }
 
