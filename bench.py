@@ -43,6 +43,13 @@ D_I = 128
 WORKLOAD = "mla_t65536_h128_topk2048"
 
 
+def set_T(t: int):
+    """Shrink the sequence (profiling captures only); the workload name says so."""
+    global T_TOK, WORKLOAD
+    T_TOK = int(t)
+    WORKLOAD = f"mla_t{T_TOK}_h128_topk2048"
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -403,10 +410,13 @@ def main():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--ref-rows", type=int, default=96, help="oracle rows per CPU sample")
+    ap.add_argument("--ref-rows", type=int, default=384, help="oracle rows per CPU sample")
+    ap.add_argument("--T", type=int, default=T_TOK, help="sequence length (smaller only for profiling captures)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    if args.T != T_TOK:
+        set_T(args.T)
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)
