@@ -129,6 +129,27 @@ int qsa_topk(const void* q_idx_dev, const void* k_idx_dev, const float* w_dev,
              size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * qsa_topk_no_alloc -- qsa_topk for callers that cannot provide scratch memory.
+ * (The pages have no counterpart: this is an interface convenience.)
+ *
+ *   Same arguments and result as qsa_topk, minus the workspace.  It is for
+ *   hosts that may not allocate device memory once running (fixed memory
+ *   budgets, allocation-free serving loops, plugin interfaces that pass only
+ *   input and output buffers).  The score scratch is a fixed 16 MiB device
+ *   array inside the library, held by every GPU that loads it until exit; the
+ *   library allocates nothing.  The first call on a device looks up that
+ *   array's address with the device current -- make it before any stream
+ *   capture.  All calls share the array: calls that overlap on the GPU race and
+ *   must be serialised by the caller.  A problem needing more than 16 MiB for
+ *   one query row of scores (groups * row width * 4 bytes) is refused with
+ *   TSA_ERR_UNSUPPORTED.  Output is bit-identical to qsa_topk's.
+ * ------------------------------------------------------------------------- */
+int qsa_topk_no_alloc(const void* q_idx_dev, const void* k_idx_dev, const float* w_dev,
+                      const int32_t* cu_seqlens, int num_seqs, int H_I, int d_I, int groups,
+                      int block_size, float score_scale, int topk, int32_t* indices_dev,
+                      void* stream);
+
+/* ---------------------------------------------------------------------------
  * sparse_mla_fwd -- absorbed sparse MLA forward.
  * [DSA "Changes": sparse MLA forward over the absorbed latent; NOPE "What
  * does this PR do?": q [T,H,576], kv latent [T,576], value = kv[..., :512],

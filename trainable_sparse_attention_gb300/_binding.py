@@ -36,6 +36,8 @@ SIGNATURES = {
     "qsa_topk_workspace_size": (c_size_t, [c_i32p, c_int, c_int, c_int]),
     "qsa_topk": (c_int, [c_void_p, c_void_p, c_void_p, c_i32p, c_int, c_int, c_int, c_int, c_int, c_float,
                          c_int, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "qsa_topk_no_alloc": (c_int, [c_void_p, c_void_p, c_void_p, c_i32p, c_int, c_int, c_int, c_int, c_int,
+                                  c_float, c_int, c_void_p, c_void_p]),
     "sparse_mla_fwd": (c_int, [c_void_p, c_void_p, c_void_p, c_i32p, c_int, c_int, c_int, c_int, c_float,
                                c_void_p, c_void_p, c_void_p]),
     "sparse_mla_bwd_workspace_size": (c_size_t, [c_int64, c_int, c_int]),

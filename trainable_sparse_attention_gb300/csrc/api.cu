@@ -111,6 +111,16 @@ int64_t chunk_rows(int max_len, int groups, int block_size) {
 
 }  // namespace
 
+namespace tsa {
+// For entry points defined in other translation units: record a detail
+// message for tsa_last_error() and account for a kernel launch.
+int note_error(int code, const char* msg) {
+  g_last_error = msg;
+  return code;
+}
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+}  // namespace tsa
+
 extern "C" {
 
 const char* tsa_status_string(int status) {
