@@ -192,6 +192,8 @@ int qsa_indexer_scores(const void* q_idx, const void* k_idx, const float* w, con
     a.nq = static_cast<int>(hi - lo);
     a.out = scores + (lo - q_begin) * groups * width;
     a.width = width;
+      a.T_total = static_cast<int>(T);
+      a.flags = flags_ptr();
     TSA_LAUNCH(launch_indexer(a, s), "indexer launch");
   }
   return TSA_OK;
@@ -255,6 +257,8 @@ int qsa_topk(const void* q_idx, const void* k_idx, const float* w, const int32_t
       a.nq = nq;
       a.out = scratch;
       a.width = width;
+      a.T_total = static_cast<int>(T);
+      a.flags = flags_ptr();
       TSA_LAUNCH(launch_indexer(a, s), "indexer launch");
       TopkRows r;
       r.scores = scratch; r.ld = width; r.width = width;

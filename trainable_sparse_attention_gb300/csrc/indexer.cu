@@ -179,8 +179,11 @@ size_t indexer_smem_bytes(int d_I, int H_I, int groups) {
 }
 
 // Scores for queries at local positions [p_begin, p_begin + nq) of one sequence.
+// Token-level scores run on the tcgen05 kernel (indexer_tc.cu); block scores
+// (max over a block's causal tokens) run here.
 cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t stream) {
   if (a.nq <= 0) return cudaSuccess;
+  if (a.T_total > 0 && indexer_tc_supported(a.H_I, a.d_I, a.groups, a.bs)) return launch_indexer_tc(a, stream);
   size_t smem = indexer_smem_bytes(a.d_I, a.H_I, a.groups);
   static bool attr_set = false;
   if (!attr_set) {

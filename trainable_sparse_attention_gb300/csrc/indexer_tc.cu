@@ -1,0 +1,269 @@
+// Indexer score on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+//   I_g[t,s] = score_scale * sum_{h in g} w[t,h] * ReLU(q_I[t,h] . k_I[s]),  s <= t
+//
+// Megatron-LM issue #7060 "Add trainable QSA sparse attention with a TileLang
+// backend" ("Describe the solution you'd like": trainable indexer, ReLU
+// scores, streaming bounded-memory runner) and Megatron-LM PR #3674 (fused
+// indexer forward + logits cleaning).
+//
+// One CTA owns QB = 256 / H_I consecutive queries (their q_I rows form the
+// MMA's B operand, N = 256 columns = (query, head)) and streams key tiles of
+// 128 keys (the A operand, M = 128) through a 4-stage TMA ring.  Keys sit on
+// TMEM lanes, so each epilogue thread owns one key and reduces the heads of a
+// group inside its own registers: ReLU, head weight and group sum never leave
+// the thread, and only causal scores are written ("cleaned" logits are never
+// produced).  The 2 x 256-column TMEM accumulator is double-buffered so the
+// epilogue of tile i overlaps the MMAs of tile i+1.
+//
+// Warp roles (192 threads): warps 0-3 epilogue (TMEM lanes 0-127), warp 4 TMA
+// producer, warp 5 TMEM allocator + MMA issuer (one elected thread).  Every
+// wait is bounded; a timeout raises TSA_FLAG_TIMEOUT and the CTA winds down,
+// releasing its TMEM.
+#include "kernels.cuh"
+#include "tc.cuh"
+
+namespace tsa {
+
+namespace {
+
+constexpr int IT_M = 128;
+constexpr int IT_N = 256;
+constexpr int IT_STAGES = 4;
+constexpr int IT_KT_PER_CTA = 16;
+constexpr int IT_THREADS = 192;
+
+template <int DI>
+struct ItLayout {
+  static constexpr int KB = DI / 64;                    // 128-byte column blocks along d_I
+  static constexpr int B_BYTES = KB * IT_N * 128;       // q_I block
+  static constexpr int A_BYTES = KB * IT_M * 128;       // one key tile
+  static constexpr int USED = 1024 + B_BYTES + IT_STAGES * A_BYTES + IT_N * 4 + 256;
+  // at least 120 KB so that a single CTA (the only TMEM owner) fits on an SM
+  static constexpr int SMEM = USED > 120 * 1024 ? USED : 120 * 1024;
+};
+
+}  // namespace
+
+template <int DI, int HG>
+__global__ void __launch_bounds__(IT_THREADS, 1)
+    indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ IndexerArgs a) {
+  using L = ItLayout<DI>;
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  unsigned char* gbase = smem_raw + (base - raw);
+  const uint32_t sB = base;
+  const uint32_t sA = base + L::B_BYTES;
+  float* Ws = reinterpret_cast<float*>(gbase + L::B_BYTES + IT_STAGES * L::A_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(Ws + IT_N);
+  uint64_t* full = bars;                       // [IT_STAGES]
+  uint64_t* empty = bars + IT_STAGES;          // [IT_STAGES]
+  uint64_t* bfull = bars + 2 * IT_STAGES;      // [1]
+  uint64_t* accf = bars + 2 * IT_STAGES + 1;   // [2]
+  uint64_t* acce = bars + 2 * IT_STAGES + 3;   // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * IT_STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int H_I = a.H_I;
+  const int QB = IT_N / H_I;
+  const int q0 = blockIdx.y * QB;
+  const int qn = min(QB, a.nq - q0);
+  const int p_first = a.p_begin + q0;
+  const int p_last = p_first + qn - 1;
+  const int kt0 = blockIdx.x * IT_KT_PER_CTA;
+  if (kt0 * IT_M > p_last) return;  // uniform: nothing causal for this CTA
+  const int ntiles = min(kt0 + IT_KT_PER_CTA, p_last / IT_M + 1) - kt0;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int i = 0; i < IT_STAGES; ++i) { tc::mbar_init(&full[i], 1); tc::mbar_init(&empty[i], 1); }
+    tc::mbar_init(bfull, 1);
+    for (int i = 0; i < 2; ++i) { tc::mbar_init(&accf[i], 1); tc::mbar_init(&acce[i], 4); }
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 5) tc::tmem_alloc(tmem_slot, 512);
+  for (int c = tid; c < IT_N; c += IT_THREADS) {
+    int qq = c / H_I, h = c % H_I;
+    Ws[c] = (qq < qn) ? a.w[(int64_t)(a.seq_start + p_first + qq) * H_I + h] : 0.f;
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tc::prefetch_tmap(&tm_q);
+      tc::prefetch_tmap(&tm_k);
+      tc::mbar_arrive_expect_tx(bfull, L::B_BYTES);
+      for (int c = 0; c < L::KB; ++c)
+        tc::tma_load_2d(sB + c * (IT_N * 128), &tm_q, bfull, c * 64, (a.seq_start + p_first) * H_I);
+      for (int it = 0; it < ntiles; ++it) {
+        const int st = it % IT_STAGES;
+        const uint32_t ph = (it / IT_STAGES) & 1;
+        if (!tc::mbar_wait(&empty[st], ph ^ 1u, abort_flag)) { *abort_flag = 1; break; }
+        tc::mbar_arrive_expect_tx(&full[st], L::A_BYTES);
+        const int row = a.seq_start + (kt0 + it) * IT_M;
+        for (int c = 0; c < L::KB; ++c)
+          tc::tma_load_2d(sA + st * L::A_BYTES + c * (IT_M * 128), &tm_k, &full[st], c * 64, row);
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(IT_M, IT_N);
+      bool ok = tc::mbar_wait(bfull, 0, abort_flag);
+      for (int it = 0; ok && it < ntiles; ++it) {
+        const int st = it % IT_STAGES;
+        const uint32_t ph = (it / IT_STAGES) & 1;
+        const int acc = it & 1;
+        const uint32_t aph = (it >> 1) & 1;
+        if (!tc::mbar_wait(&full[st], ph, abort_flag) || !tc::mbar_wait(&acce[acc], aph ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t d = tmem + acc * IT_N;
+#pragma unroll
+        for (int ks = 0; ks < DI / 16; ++ks) {
+          const int c = ks >> 2, kk = ks & 3;
+          const uint64_t ad = tc::desc_sw128(sA + st * L::A_BYTES + c * (IT_M * 128) + kk * 32);
+          const uint64_t bd = tc::desc_sw128(sB + c * (IT_N * 128) + kk * 32);
+          tc::mma_bf16_ss(d, ad, bd, idesc, ks > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(&empty[st]);
+        tc::mma_commit(&accf[acc]);
+      }
+      if (!ok) *abort_flag = 1;
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 0-3)
+    const int key_in_tile = warp * 32 + lane;
+    for (int it = 0; it < ntiles; ++it) {
+      const int acc = it & 1;
+      const uint32_t aph = (it >> 1) & 1;
+      if (!tc::mbar_wait(&accf[acc], aph, abort_flag)) { *abort_flag = 1; break; }
+      tc::fence_after_sync();
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + acc * IT_N;
+      const int s = (kt0 + it) * IT_M + key_in_tile;
+      float run = 0.f;  // running sum of the current (query, group) segment
+#pragma unroll 1
+      for (int cb = 0; cb < IT_N / 32; ++cb) {
+        uint32_t r[32];
+        __syncwarp();
+        tc::tmem_ld32(taddr + cb * 32, r);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          run = fmaf(Ws[cb * 32 + j], fmaxf(__uint_as_float(r[j]), 0.f), run);
+          const bool seg_done = (HG <= 32) ? ((j + 1) % HG == 0) : (j == 31 && ((cb + 1) * 32) % HG == 0);
+          if (seg_done) {
+            const int sg = (cb * 32 + j) / HG;
+            const int qq = sg / a.groups, gg = sg % a.groups;
+            if (qq < qn && s <= p_first + qq)
+              a.out[((int64_t)(q0 + qq) * a.groups + gg) * a.width + s] = run * a.score_scale + 0.f;
+            run = 0.f;
+          }
+        }
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&acce[acc]);
+    }
+  }
+
+  __syncthreads();
+  if (*abort_flag && tid == 0) raise_flag(a.flags, TSA_FLAG_TIMEOUT);
+  if (warp == 5) {
+    __syncwarp();
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+}  // namespace
+
+// 2-D bf16 tensor map over a row-major [rows, cols] array, 128-byte swizzle.
+cudaError_t make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                              uint32_t box_cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+bool indexer_tc_supported(int H_I, int d_I, int groups, int bs) {
+  if (bs != 1 || (d_I != 64 && d_I != 128)) return false;
+  if (H_I < 2 || H_I > IT_N || (IT_N % H_I) != 0) return false;
+  const int hg = H_I / groups;
+  return hg >= 2 && hg <= 128 && (hg & (hg - 1)) == 0 && hg * groups == H_I;
+}
+
+template <int DI, int HG>
+static cudaError_t launch_tc_t(const IndexerArgs& a, cudaStream_t stream) {
+  CUtensorMap tq, tk;
+  cudaError_t e = make_tmap_bf16_2d(&tq, a.q, (uint64_t)a.T_total * a.H_I, DI, IT_N, 64);
+  if (e != cudaSuccess) return e;
+  e = make_tmap_bf16_2d(&tk, a.k, (uint64_t)a.T_total, DI, IT_M, 64);
+  if (e != cudaSuccess) return e;
+  constexpr int smem = ItLayout<DI>::SMEM;
+  e = cudaFuncSetAttribute(indexer_tc_kernel<DI, HG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int QB = IT_N / a.H_I;
+  const int p_last = a.p_begin + a.nq - 1;
+  const int ktiles = p_last / IT_M + 1;
+  dim3 grid((ktiles + IT_KT_PER_CTA - 1) / IT_KT_PER_CTA, (a.nq + QB - 1) / QB);
+  indexer_tc_kernel<DI, HG><<<grid, IT_THREADS, smem, stream>>>(tq, tk, a);
+  return cudaGetLastError();
+}
+
+template <int DI>
+static cudaError_t launch_tc_d(const IndexerArgs& a, cudaStream_t stream) {
+  switch (a.H_I / a.groups) {
+    case 2: return launch_tc_t<DI, 2>(a, stream);
+    case 4: return launch_tc_t<DI, 4>(a, stream);
+    case 8: return launch_tc_t<DI, 8>(a, stream);
+    case 16: return launch_tc_t<DI, 16>(a, stream);
+    case 32: return launch_tc_t<DI, 32>(a, stream);
+    case 64: return launch_tc_t<DI, 64>(a, stream);
+    default: return launch_tc_t<DI, 128>(a, stream);
+  }
+}
+
+cudaError_t launch_indexer_tc(const IndexerArgs& a, cudaStream_t stream) {
+  if (a.nq <= 0) return cudaSuccess;
+  return a.d_I == 128 ? launch_tc_d<128>(a, stream) : launch_tc_d<64>(a, stream);
+}
+
+}  // namespace tsa

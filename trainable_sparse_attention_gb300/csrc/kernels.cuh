@@ -29,6 +29,8 @@ struct IndexerArgs {
   int nq;          // queries in this launch
   float* out;      // query q, group g -> out + (q*groups + g) * width
   int64_t width;
+  int T_total = 0;                 // packed rows of q_I / k_I (bounds of the TMA maps)
+  unsigned int* flags = nullptr;   // device error flags
 };
 
 struct MlaFwdArgs {
@@ -79,6 +81,9 @@ struct GqaArgs {
 
 cudaError_t launch_topk_rows(const TopkRows& a, int64_t rows, cudaStream_t stream);
 cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t stream);
+// tcgen05 indexer (token-level scores); launch_indexer routes to it when it applies.
+bool indexer_tc_supported(int H_I, int d_I, int groups, int bs);
+cudaError_t launch_indexer_tc(const IndexerArgs& a, cudaStream_t stream);
 cudaError_t launch_fill(float* p, int64_t n, float v, cudaStream_t stream);
 cudaError_t launch_mla_fwd(const MlaFwdArgs& a, int D, cudaStream_t stream);
 cudaError_t launch_mla_bwd(const MlaBwdArgs& a, int D, cudaStream_t stream);

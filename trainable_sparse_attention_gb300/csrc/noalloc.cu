@@ -125,6 +125,7 @@ extern "C" int qsa_topk_no_alloc(const void* q_idx, const void* k_idx, const flo
       a.nq = nq;
       a.out = static_cast<float*>(scratch);
       a.width = width;
+      a.T_total = cu_seqlens[num_seqs];
       cudaError_t e = launch_indexer(a, s);
       if (e != cudaSuccess) return note_error(TSA_ERR_CUDA, cudaGetErrorString(e));
       note_launch();
