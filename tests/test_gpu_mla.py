@@ -194,3 +194,43 @@ def test_mla_t65536_h128_sampled(tsa):
     dq_ref, dkv_ref = O.sparse_mla_bwd(m["q"], m["kv"], idx, cu, scale, m["dout"], rows=rows)
     assert rel_l2(dq[rows], dq_ref) <= TOL_GRAD
     assert rel_l2(dkv, dkv_ref) <= TOL_GRAD
+
+
+@pytest.mark.parametrize("D,topk,lengths", [
+    (576, 64, [300]),            # first 63 rows have fewer than 64 candidates
+    (576, 65, [130, 200]),       # ragged last tile, THD
+    (576, 1000, [700]),          # top-k wider than the sequence: -1 tails
+    (512, 96, [257]),            # NoPE layout
+    (576, 2048, [2100]),         # 64 tiles of 32 keys
+])
+def test_mla_h128_forward(tsa, D, topk, lengths):
+    """H = 128 (the tcgen05 cluster path): parity with the oracle on sampled rows,
+    all-invalid rows exact, bit-identical replay."""
+    cu = synth.cu_seqlens_thd(lengths)
+    T = cu[-1]
+    m = synth.mla_inputs(T, 128, D, seed=T + topk + D)
+    idx = synth.random_topk_indices(cu, topk, seed=topk, invalid_rows=[3, T - 1])
+    scale = 1 / math.sqrt(D)
+    q, kv, ids = m["q"].to(DEV), m["kv"].to(DEV), idx.to(DEV)
+    out, lse = tsa.sparse_mla_fwd(q, kv, ids, cu, scale)
+    out2, lse2 = tsa.sparse_mla_fwd(q, kv, ids, cu, scale)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+    rows = sorted(set([0, 1, 2, 3, 63, 64, T - 1] + list(range(5, T, max(1, T // 40)))))
+    o_ref, l_ref = O.sparse_mla_fwd(m["q"], m["kv"], idx, cu, scale, rows=rows)
+    check_out_lse(out, lse, o_ref, l_ref, rows=rows)
+    for r in (3, T - 1):
+        assert torch.all(out[r] == 0) and torch.all(torch.isneginf(lse[r]))
+
+
+def test_mla_h128_large_logits_rescale(tsa):
+    """Large, growing logits force the lazy running-max rescale of the output
+    accumulator; compare with the oracle."""
+    cu = [0, 600]
+    m = synth.mla_inputs(600, 128, 576, seed=11)
+    m["q"] = (m["q"].float() * 4).to(torch.bfloat16)
+    idx = synth.random_topk_indices(cu, 512, seed=11)
+    out, lse = tsa.sparse_mla_fwd(m["q"].to(DEV), m["kv"].to(DEV), idx.to(DEV), cu, 0.2)
+    rows = list(range(0, 600, 7)) + [599]
+    o_ref, l_ref = O.sparse_mla_fwd(m["q"], m["kv"], idx, cu, 0.2, rows=rows)
+    check_out_lse(out, lse, o_ref, l_ref, rows=rows)
