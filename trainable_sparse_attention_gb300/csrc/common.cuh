@@ -5,7 +5,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
-#include "../../include/tsa.h"
+#include "tsa.h"
 
 namespace tsa {
 
@@ -77,6 +77,26 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 __device__ __forceinline__ void red_add_v2(float* addr, float a, float b) {
   asm volatile("red.global.add.v2.f32 [%0], {%1, %2};\n" ::"l"(addr), "f"(a), "f"(b) : "memory");
+}
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+// Scatter-add of an m16n8 accumulator fragment (rows g and g+8, channels
+// 2*c4, 2*c4+1) with 16-byte vector atomics: lanes c4 and c4^1 swap halves so
+// the even lane adds 4 channels of row g and the odd lane 4 channels of row g+8.
+// row_g / row_g8 point at channel 0 of the fragment's two rows (or are null).
+__device__ __forceinline__ void red_frag_v4(float* row_g, float* row_g8, const float* acc, int c4) {
+  const bool odd = (c4 & 1) != 0;
+  const float s0 = odd ? acc[0] : acc[2], s1 = odd ? acc[1] : acc[3];
+  const float o0 = __shfl_xor_sync(0xffffffffu, s0, 1), o1 = __shfl_xor_sync(0xffffffffu, s1, 1);
+  if (!odd) {
+    if (row_g) red_add_v4(row_g + 2 * c4, acc[0], acc[1], o0, o1);
+  } else {
+    if (row_g8) red_add_v4(row_g8 + 2 * (c4 - 1), o0, o1, acc[2], acc[3]);
+  }
 }
 
 __device__ __forceinline__ float warp_max(float v) {

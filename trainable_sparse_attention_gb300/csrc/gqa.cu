@@ -334,17 +334,11 @@ __global__ void __launch_bounds__(128) gqa_bwd_mma_kernel(const __grid_constant_
           mma_bf16(ak, a0, a1, a2, a3, bq0, bq1);
           ldsm_x4_t(smem_u32(Ps + hrow * PRS + kcol), a0, a1, a2, a3);
           mma_bf16(av, a0, a1, a2, a3, bo0, bo1);
-          int pos0 = b * BS + m2 * 16 + gq, pos1 = pos0 + 8;
-          if (pos0 <= p) {
-            int64_t off = ((int64_t)(s0 + pos0) * a.Hkv + gk) * DH + ch0 + 2 * c4;
-            red_add_v2(a.dk_acc + off, ak[0], ak[1]);
-            red_add_v2(a.dv_acc + off, av[0], av[1]);
-          }
-          if (pos1 <= p) {
-            int64_t off = ((int64_t)(s0 + pos1) * a.Hkv + gk) * DH + ch0 + 2 * c4;
-            red_add_v2(a.dk_acc + off, ak[2], ak[3]);
-            red_add_v2(a.dv_acc + off, av[2], av[3]);
-          }
+          const int pos0 = b * BS + m2 * 16 + gq, pos1 = pos0 + 8;
+          const int64_t off0 = ((int64_t)(s0 + pos0) * a.Hkv + gk) * DH + ch0;
+          const int64_t off1 = ((int64_t)(s0 + pos1) * a.Hkv + gk) * DH + ch0;
+          red_frag_v4(pos0 <= p ? a.dk_acc + off0 : nullptr, pos1 <= p ? a.dk_acc + off1 : nullptr, ak, c4);
+          red_frag_v4(pos0 <= p ? a.dv_acc + off0 : nullptr, pos1 <= p ? a.dv_acc + off1 : nullptr, av, c4);
         }
       }
     }

@@ -234,9 +234,9 @@ __global__ void __launch_bounds__(128 * MW) mla_bwd_mma_kernel(const __grid_cons
         }
 #pragma unroll
         for (int m2 = 0; m2 < 2; ++m2) {
-          int r0 = rows_b[m2 * 16 + g], r1 = rows_b[m2 * 16 + g + 8];
-          if (r0 >= 0) red_add_v2(a.dkv_acc + (int64_t)r0 * D + ch0 + 2 * c4, acc[m2][0], acc[m2][1]);
-          if (r1 >= 0) red_add_v2(a.dkv_acc + (int64_t)r1 * D + ch0 + 2 * c4, acc[m2][2], acc[m2][3]);
+          const int r0 = rows_b[m2 * 16 + g], r1 = rows_b[m2 * 16 + g + 8];
+          red_frag_v4(r0 >= 0 ? a.dkv_acc + (int64_t)r0 * D + ch0 : nullptr,
+                      r1 >= 0 ? a.dkv_acc + (int64_t)r1 * D + ch0 : nullptr, acc[m2], c4);
         }
       }
     }

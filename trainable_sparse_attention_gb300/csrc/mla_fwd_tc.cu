@@ -1,5 +1,5 @@
-// Sparse MLA forward for H = 128 heads on tcgen05 (TMEM accumulators, TMA
-// gather4, 2-CTA cluster).
+// Sparse MLA forward for H = 128 heads on tcgen05 (TMEM accumulators, 2-CTA
+// cluster, cp.async gather into swizzled tiles).
 //
 // Megatron-LM PR #3674 "Enable DSA CP/absorbed/THD paths with TileLang fused
 // ops" (sparse MLA forward over the absorbed latent) and Megatron-LM PR #7617
@@ -11,19 +11,24 @@
 // logits.  So a CTA pair shares one query and splits the value channels
 // (CTA r owns O[:, 256r, 256r+256)).  Each CTA also owns the matching slice of
 // the 576 q/kv channels (CTA 0: [0,256), CTA 1: [256, D)), gathers only that
-// slice of the selected rows (TMA tile::gather4, 4 rows per instruction), and
-// computes the partial logits Q_r K_r^T over it.  The two 128 x 32 partials
-// are swapped through distributed shared memory and added; fp32 addition is
-// commutative, so both CTAs hold bit-identical logits and take identical
-// softmax decisions.  No MMA is repeated and every selected row is read once.
+// slice of the selected rows, and computes the partial logits Q_r K_r^T over
+// it.  The two 128 x 32 partials are swapped through distributed shared memory
+// and added; fp32 addition is commutative, so both CTAs hold bit-identical
+// logits and take identical softmax decisions.  No MMA is repeated and every
+// selected row is read once.
 //
 // Per CTA: TMEM columns [0,256) = O slice, [256,320) = two 32-key S buffers.
-// Warps 0-3: softmax (thread h = head h = TMEM lane h), warp 4: TMA producer
-// (q slice once, then a 4-stage ring of 32-key tiles), warp 5: TMEM owner and
-// single-thread MMA issuer (QK^T of tile j+1 is issued before PV of tile j).
-// The running max is rescaled lazily (only when it grows by more than 2^8), so
-// the O slice in TMEM is rarely touched.  Every wait is bounded; a timeout
-// raises TSA_FLAG_TIMEOUT and both CTAs wind down.
+// Warps 0-3: softmax (thread h = head h = TMEM lane h); warp 4: TMEM owner,
+// TMA load of the q slice and single-thread MMA issuer (QK^T of tile j+2 is
+// issued before PV of tile j); warps 5-8: cp.async gather of the selected rows
+// into a 4-stage ring of 32-key tiles.
+//
+// The softmax is software-pipelined: while tile j is normalised, the partial
+// logits of tile j+1 are already on their way to the peer (two exchange
+// buffers), and P is double-buffered so PV(j) never waits for the softmax of
+// tile j+1.  The running max is rescaled lazily (only when it grows by more
+// than 2^8), so the O slice in TMEM is rarely touched.  Every wait is bounded;
+// a timeout raises TSA_FLAG_TIMEOUT and both CTAs wind down.
 #include "kernels.cuh"
 #include "tc.cuh"
 
@@ -34,7 +39,7 @@ namespace {
 constexpr int MT_H = 128;        // heads = MMA M
 constexpr int MT_N = 32;         // keys per tile
 constexpr int MT_STAGES = 4;
-constexpr int MT_THREADS = 192;  // warps 0-3 softmax, 4 producer, 5 MMA
+constexpr int MT_THREADS = 288;  // warps 0-3 softmax, 4 MMA, 5-8 gather producers
 constexpr int MT_DV = 512;
 constexpr int MT_OCOLS = 256;    // value channels per CTA
 constexpr float kRescaleLog2 = 8.f;
@@ -47,40 +52,47 @@ struct MtLayout {
   static constexpr int Q_BYTES = KBMAX * MT_H * 128;
   static constexpr int KV_BLOCK = MT_N * 128;        // one 64-channel column block of a tile
   static constexpr int KV_STAGE = KBMAX * KV_BLOCK;
-  static constexpr int P_BYTES = MT_H * 128;
-  static constexpr int X_BYTES = MT_H * MT_N * 4;
+  static constexpr int P_BYTES = MT_H * 128;         // one P buffer (keys 0..31 of 128-byte rows)
+  static constexpr int X_BYTES = MT_H * MT_N * 4;    // one exchange buffer
   static constexpr int OFF_KV = Q_BYTES;
   static constexpr int OFF_P = OFF_KV + MT_STAGES * KV_STAGE;
-  static constexpr int OFF_X = OFF_P + P_BYTES;
-  static constexpr int OFF_BAR = OFF_X + X_BYTES;
+  static constexpr int OFF_X = OFF_P + 2 * P_BYTES;
+  static constexpr int OFF_BAR = OFF_X + 2 * X_BYTES;
   static constexpr int SMEM = 1024 + OFF_BAR + 512;
 };
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 }  // namespace
 
 template <int D>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
-    mla_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
-                      const __grid_constant__ MlaFwdArgs a) {
+    mla_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ MlaFwdArgs a) {
   using L = MtLayout<D>;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* gbase = smem_raw + (base - raw);
   const uint32_t sQ = base, sKV = base + L::OFF_KV, sP = base + L::OFF_P;
-  float* X = reinterpret_cast<float*>(gbase + L::OFF_X);  // [128][32] partial logits written by the peer
+  float* X = reinterpret_cast<float*>(gbase + L::OFF_X);  // [2][128][32] partial logits written by the peer
   uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + L::OFF_BAR);
   uint64_t* qfull = bars;
   uint64_t* kv_full = bars + 1;                       // [STAGES]
-  uint64_t* kv_empty = bars + 1 + MT_STAGES;          // [STAGES]
-  uint64_t* s_full = bars + 1 + 2 * MT_STAGES;        // [2]
+  uint64_t* kv_empty = kv_full + MT_STAGES;           // [STAGES]
+  uint64_t* s_full = kv_empty + MT_STAGES;            // [2]
   uint64_t* s_empty = s_full + 2;                     // [2]
-  uint64_t* p_full = s_empty + 2;
-  uint64_t* p_empty = p_full + 1;
-  uint64_t* xfull = p_empty + 1;                      // peer wrote my X
-  uint64_t* xfree = xfull + 1;                        // peer consumed what I wrote into its X
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xfree + 1);
+  uint64_t* p_full = s_empty + 2;                     // [2]
+  uint64_t* p_empty = p_full + 2;                     // [2] (PV of that buffer completed)
+  uint64_t* xfull = p_empty + 2;                      // [2] peer wrote my X[b]
+  uint64_t* xfree = xfull + 2;                        // [2] peer consumed what I wrote into its X[b]
+  uint64_t* mask_full = xfree + 2;                    // [STAGES] valid-slot bits of the stage written
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mask_full + MT_STAGES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint32_t* masks = tmem_slot + 2;                    // [STAGES] valid-slot bits of each staged tile
 
   const uint32_t rank = tc::cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
@@ -97,16 +109,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
 
   if (tid == 0) {
     tc::mbar_init(qfull, 1);
-    for (int i = 0; i < MT_STAGES; ++i) { tc::mbar_init(&kv_full[i], 1); tc::mbar_init(&kv_empty[i], 1); }
-    for (int i = 0; i < 2; ++i) { tc::mbar_init(&s_full[i], 1); tc::mbar_init(&s_empty[i], MT_H); }
-    tc::mbar_init(p_full, MT_H);
-    tc::mbar_init(p_empty, 1);
-    tc::mbar_init(xfull, MT_H);
-    tc::mbar_init(xfree, MT_H);
+    for (int i = 0; i < MT_STAGES; ++i) {
+      tc::mbar_init(&kv_full[i], 128);  // one asynchronous arrival per producer thread when its copies land
+      tc::mbar_init(&kv_empty[i], 1);
+      tc::mbar_init(&mask_full[i], 4);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&s_full[i], 1);
+      tc::mbar_init(&s_empty[i], MT_H);
+      tc::mbar_init(&p_full[i], MT_H);
+      tc::mbar_init(&p_empty[i], 1);
+      tc::mbar_init(&xfull[i], 4);  // one remote arrival per softmax warp of the peer
+      tc::mbar_init(&xfree[i], 4);
+    }
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
-  if (warp == 5) tc::tmem_alloc(tmem_slot, 512);
+  if (warp == 4) tc::tmem_alloc(tmem_slot, 512);
   tc::fence_before_sync();
   __syncthreads();
   __syncwarp();
@@ -114,37 +133,59 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      tc::prefetch_tmap(&tm_q);
-      tc::prefetch_tmap(&tm_kv);
-      tc::mbar_arrive_expect_tx(qfull, kb * MT_H * 128);
-      for (int c = 0; c < kb; ++c) tc::tma_load_2d(sQ + c * (MT_H * 128), &tm_q, qfull, ch0 + c * 64, t * MT_H);
-      for (int j = 0; j < ntiles; ++j) {
-        const int st = j % MT_STAGES;
-        if (!tc::mbar_wait(&kv_empty[st], ((j / MT_STAGES) & 1) ^ 1u, abort_flag)) { *abort_flag = 1; break; }
-        int rows[MT_N];
-#pragma unroll
-        for (int i = 0; i < MT_N; ++i) {
-          const int slot = j * MT_N + i;
-          const int id = slot < a.topk ? __ldg(idx_row + slot) : -1;
-          if (id >= n) raise_flag(a.flags, TSA_FLAG_INDEX_RANGE);
-          rows[i] = (id >= 0 && id < n) ? s0 + id : 0;  // invalid slots read a real row and are masked
-        }
-        tc::mbar_arrive_expect_tx(&kv_full[st], kb * L::KV_BLOCK);
-        const uint32_t dst = sKV + st * L::KV_STAGE;
-        for (int c = 0; c < kb; ++c) {
-#pragma unroll
-          for (int g = 0; g < MT_N / 4; ++g)
-            tc::tma_gather4(dst + c * L::KV_BLOCK + g * 512, &tm_kv, &kv_full[st], ch0 + c * 64, rows[4 * g],
-                            rows[4 * g + 1], rows[4 * g + 2], rows[4 * g + 3]);
-        }
+  if (warp >= 5) {
+    // ------------------------------------------------------------ gather producers (128 threads)
+    // 32 rows x 4 parts: each thread copies kb*2 16-byte chunks of one selected
+    // row straight into the 128-byte-swizzled K-major tile (cp.async).  Each
+    // thread's copies arrive on the stage's barrier asynchronously when they
+    // land (cp.async.mbarrier.arrive.noinc), so the producers never wait on
+    // their own copies: every free stage holds a tile in flight.  The MMA
+    // thread orders the landed data for the tensor cores with a proxy fence.
+    // The index of the next tile is loaded one iteration ahead.
+    const int pt = tid - 160;
+    const int row = pt >> 2, part = pt & 3;
+    const int per = kb * 2;
+    const char* kvb = reinterpret_cast<const char*>(a.kv);
+    bool ok = true;
+    int id_next = row < a.topk ? __ldg(idx_row + row) : -1;
+    for (int j = 0; j < ntiles; ++j) {
+      const int st = j % MT_STAGES;
+      const int id = id_next;
+      const int slot_next = (j + 1) * MT_N + row;
+      id_next = slot_next < a.topk ? __ldg(idx_row + slot_next) : -1;
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&kv_empty[st], ((j / MT_STAGES) & 1) ^ 1u, abort_flag))) {
+        ok = false;
+        break;
+      }
+      const bool valid = id >= 0 && id < n;
+      if (part == 0 && id >= n) raise_flag(a.flags, TSA_FLAG_INDEX_RANGE);
+      const char* src_row = kvb + ((int64_t)(valid ? s0 + id : 0) * D + ch0) * 2;
+      const uint32_t dst = sKV + st * L::KV_STAGE + row * 128;
+      for (int q = 0; q < per; ++q) {
+        const int c16 = part * per + q;
+        const int cb = c16 >> 3, jj = c16 & 7;
+        cp_async16(dst + cb * L::KV_BLOCK + ((jj ^ (row & 7)) << 4), src_row + c16 * 16, valid ? 16u : 0u);
+      }
+      cp_async_commit();
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&kv_full[st]))
+                   : "memory");
+      // valid-slot bits: lanes with part == 0 hold rows 8*(warp-5) + lane/4
+      const uint32_t bal = __ballot_sync(0xffffffffu, part == 0 && valid);
+      if (lane == 0) {
+        uint32_t byte = 0;
+        for (int r8 = 0; r8 < 8; ++r8) byte |= ((bal >> (4 * r8)) & 1u) << r8;
+        reinterpret_cast<volatile unsigned char*>(&masks[st])[warp - 5] = static_cast<unsigned char>(byte);
+        tc::mbar_arrive(&mask_full[st]);
       }
     }
-  } else if (warp == 5) {
-    // ------------------------------------------------------------ MMA issuer
+    cp_async_wait<0>();
+    if (!ok) *abort_flag = 1;
+  } else if (warp == 4) {
+    // ------------------------------------------------------------ q slice (TMA) + MMA issuer
     if (lane == 0) {
+      tc::prefetch_tmap(&tm_q);
+      tc::mbar_arrive_expect_tx(qfull, kb * MT_H * 128);
+      for (int c = 0; c < kb; ++c) tc::tma_load_2d(sQ + c * (MT_H * 128), &tm_q, qfull, ch0 + c * 64, t * MT_H);
       constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(MT_H, MT_N);
       constexpr uint32_t idesc_pv = tc::idesc_bf16_f32_bmn(MT_H, MT_OCOLS);
       bool ok = tc::mbar_wait(qfull, 0, abort_flag);
@@ -152,6 +193,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
         const int st = j % MT_STAGES, b = j & 1;
         if (!tc::mbar_wait(&kv_full[st], (j / MT_STAGES) & 1, abort_flag)) return false;
         if (!tc::mbar_wait(&s_empty[b], ((j >> 1) & 1) ^ 1u, abort_flag)) return false;
+        tc::fence_proxy_async_smem();  // the gathered tile was written through the generic proxy
         tc::fence_after_sync();
         const uint32_t d = tmem + MT_OCOLS + b * MT_N;
         for (int c = 0; c < kb; ++c) {
@@ -165,25 +207,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
         tc::mma_commit(&s_full[b]);
         return true;
       };
+      // QK^T runs two tiles ahead of PV: the softmax frees an S buffer as soon
+      // as it has read it, long before it produces that tile's P.
       if (ok && ntiles > 0) ok = issue_qk(0);
+      if (ok && ntiles > 1) ok = issue_qk(1);
       for (int j = 0; ok && j < ntiles; ++j) {
-        if (j + 1 < ntiles && !issue_qk(j + 1)) { ok = false; break; }
-        if (!tc::mbar_wait(p_full, j & 1, abort_flag)) { ok = false; break; }
+        if (j + 2 < ntiles && !issue_qk(j + 2)) { ok = false; break; }
+        const int pb = j & 1;
+        if (!tc::mbar_wait(&p_full[pb], (j >> 1) & 1, abort_flag)) { ok = false; break; }
         tc::fence_after_sync();
         const int st = j % MT_STAGES;
 #pragma unroll
         for (int ks = 0; ks < MT_N / 16; ++ks) {
-          const uint64_t ad = tc::desc_sw128(sP + ks * 32);
+          const uint64_t ad = tc::desc_sw128(sP + pb * L::P_BYTES + ks * 32);
           const uint64_t bd = tc::desc_sw128_mn(sKV + st * L::KV_STAGE + ks * 2048, L::KV_BLOCK);
           tc::mma_bf16_ss(tmem, ad, bd, idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
         }
         tc::mma_commit(&kv_empty[st]);
-        tc::mma_commit(p_empty);
+        tc::mma_commit(&p_empty[pb]);
       }
       if (!ok) *abort_flag = 1;
     }
   } else {
     // ------------------------------------------------------------ softmax (warps 0-3)
+    // Iteration j fetches tile j's partial logits from TMEM and sends them to
+    // the peer, then normalises tile j-1, whose peer half arrived meanwhile.
     const int h = tid;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const uint32_t x_peer_row = tc::mapa(smem_u32(X + h * MT_N), peer);
@@ -191,66 +239,99 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
     const uint32_t peer_xfree = tc::mapa(smem_u32(xfree), peer);
     float m_use = NEG_INF, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < ntiles; ++j) {
-      const int b = j & 1;
-      if (!__all_sync(0xffffffffu, tc::mbar_wait(&s_full[b], (j >> 1) & 1, abort_flag))) { ok = false; break; }
-      tc::fence_after_sync();
-      uint32_t r[32];
-      __syncwarp();
-      tc::tmem_ld32(tmem + lane_base + MT_OCOLS + b * MT_N, r);
-      tc::tmem_ld_wait();
-      tc::fence_before_sync();
-      tc::mbar_arrive(&s_empty[b]);
-      // swap partial logits with the peer CTA
-      if (!__all_sync(0xffffffffu, tc::mbar_wait_cluster(xfree, (j & 1) ^ 1u, abort_flag))) { ok = false; break; }
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        tc::st_cluster_v4(x_peer_row + q * 16, __uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                          __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
-      tc::mbar_arrive_remote(peer_xfull);
-      if (!__all_sync(0xffffffffu, tc::mbar_wait_cluster(xfull, j & 1, abort_flag))) { ok = false; break; }
-      float x2[32];
-      const float4* xr = reinterpret_cast<const float4*>(X + h * MT_N);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        float4 v = xr[q];
-        x2[4 * q] = __uint_as_float(r[4 * q]) + v.x;
-        x2[4 * q + 1] = __uint_as_float(r[4 * q + 1]) + v.y;
-        x2[4 * q + 2] = __uint_as_float(r[4 * q + 2]) + v.z;
-        x2[4 * q + 3] = __uint_as_float(r[4 * q + 3]) + v.w;
-      }
-      tc::mbar_arrive_remote(peer_xfree);
-      // mask, scale, lazy running max
-      float tmax = NEG_INF;
-#pragma unroll
-      for (int i = 0; i < MT_N; ++i) {
-        const int slot = j * MT_N + i;
-        const int id = slot < a.topk ? __ldg(idx_row + slot) : -1;
-        x2[i] = (id >= 0 && id < n) ? x2[i] * a.scale_log2 : NEG_INF;
-        tmax = fmaxf(tmax, x2[i]);
-      }
-      float alpha = 1.f;
-      const bool resc = tmax > m_use + kRescaleLog2;
-      if (resc) {
-        alpha = (m_use == NEG_INF) ? 0.f : exp2f(m_use - tmax);
-        m_use = tmax;
-        l *= alpha;
-      }
-      const float mu = (m_use == NEG_INF) ? 0.f : m_use;
-      uint32_t pk[MT_N / 2];
-      float psum = 0.f;
-#pragma unroll
-      for (int i = 0; i < MT_N; i += 2) {
-        const float p0 = exp2f(x2[i] - mu), p1 = exp2f(x2[i + 1] - mu);
-        psum += p0 + p1;
-        pk[i / 2] = pack_bf16(p0, p1);
-      }
-      l += psum;
-      // P and the O slice are free once PV of the previous tile has completed
-      if (j > 0) {
-        if (!__all_sync(0xffffffffu, tc::mbar_wait(p_empty, (j - 1) & 1, abort_flag))) { ok = false; break; }
+    uint32_t cur[32];
+    for (int j = 0; j <= ntiles; ++j) {
+      uint32_t nxt[32];
+      if (j < ntiles) {
+        const int b = j & 1;
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(&s_full[b], (j >> 1) & 1, abort_flag))) { ok = false; break; }
         tc::fence_after_sync();
-        if (__any_sync(0xffffffffu, resc)) {
+        __syncwarp();
+        tc::tmem_ld32(tmem + lane_base + MT_OCOLS + b * MT_N, nxt);
+        tc::tmem_ld_wait();
+        tc::fence_before_sync();
+        tc::mbar_arrive(&s_empty[b]);
+        if (!__all_sync(0xffffffffu, tc::mbar_wait_cluster(&xfree[b], ((j >> 1) & 1) ^ 1u, abort_flag))) {
+          ok = false;
+          break;
+        }
+        const uint32_t dst = x_peer_row + b * L::X_BYTES;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          tc::st_cluster_v4(dst + q * 16, __uint_as_float(nxt[4 * q]), __uint_as_float(nxt[4 * q + 1]),
+                            __uint_as_float(nxt[4 * q + 2]), __uint_as_float(nxt[4 * q + 3]));
+        __syncwarp();  // the warp's remote stores are ordered before its one release arrival
+        if (lane == 0) tc::mbar_arrive_remote(peer_xfull + b * 8);
+      }
+      if (j > 0) {
+        const int jj = j - 1, bb = jj & 1;
+        if (!__all_sync(0xffffffffu, tc::mbar_wait_cluster(&xfull[bb], (jj >> 1) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        float x2[32];
+        const float4* xr = reinterpret_cast<const float4*>(X + bb * (MT_H * MT_N) + h * MT_N);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 v = xr[q];
+          x2[4 * q] = __uint_as_float(cur[4 * q]) + v.x;
+          x2[4 * q + 1] = __uint_as_float(cur[4 * q + 1]) + v.y;
+          x2[4 * q + 2] = __uint_as_float(cur[4 * q + 2]) + v.z;
+          x2[4 * q + 3] = __uint_as_float(cur[4 * q + 3]) + v.w;
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive_remote(peer_xfree + bb * 8);
+        // valid-slot bits published by the producer with this stage
+        const int st = jj % MT_STAGES;
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(&mask_full[st], (jj / MT_STAGES) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        const uint32_t mask = masks[st];
+        float tmax = NEG_INF;
+        if (mask == 0xffffffffu) {
+#pragma unroll
+          for (int i = 0; i < MT_N; ++i) {
+            x2[i] *= a.scale_log2;
+            tmax = fmaxf(tmax, x2[i]);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < MT_N; ++i) {
+            x2[i] = ((mask >> i) & 1u) ? x2[i] * a.scale_log2 : NEG_INF;
+            tmax = fmaxf(tmax, x2[i]);
+          }
+        }
+        float alpha = 1.f;
+        const bool resc = tmax > m_use + kRescaleLog2;
+        if (resc) {
+          alpha = (m_use == NEG_INF) ? 0.f : ex2(m_use - tmax);
+          m_use = tmax;
+          l *= alpha;
+        }
+        const float mu = (m_use == NEG_INF) ? 0.f : m_use;
+        uint32_t pk[MT_N / 2];
+        float psum = 0.f;
+#pragma unroll
+        for (int i = 0; i < MT_N; i += 2) {
+          const float p0 = ex2(x2[i] - mu), p1 = ex2(x2[i + 1] - mu);
+          psum += p0 + p1;
+          pk[i / 2] = pack_bf16(p0, p1);
+        }
+        l += psum;
+        // P buffer bb is free once PV(jj-2) completed
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(&p_empty[bb], ((jj >> 1) & 1) ^ 1u, abort_flag))) {
+          ok = false;
+          break;
+        }
+        // a raised running max rescales the O slice, which PV(jj-1) must have finished
+        if (jj > 0 && __any_sync(0xffffffffu, resc)) {
+          const int pb = (jj - 1) & 1;
+          if (!__all_sync(0xffffffffu, tc::mbar_wait(&p_empty[pb], ((jj - 1) >> 1) & 1, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
           for (int cb = 0; cb < MT_OCOLS / 32; ++cb) {
             uint32_t o[32];
             tc::tmem_ld32(tmem + lane_base + cb * 32, o);
@@ -261,20 +342,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
           }
           tc::tmem_st_wait();
         }
-      }
-      // P row h: 32 bf16 = 4 x 16 B chunks in a 128-byte-swizzled K-major row
-      unsigned char* prow = gbase + L::OFF_P + h * 128;
+        // P row h: 32 bf16 = 4 x 16 B chunks in a 128-byte-swizzled K-major row
+        unsigned char* prow = gbase + L::OFF_P + bb * L::P_BYTES + h * 128;
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        *reinterpret_cast<uint4*>(prow + ((c ^ (h & 7)) << 4)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      tc::fence_proxy_async_smem();
-      tc::fence_before_sync();
-      tc::mbar_arrive(p_full);
+        for (int c = 0; c < 4; ++c)
+          *reinterpret_cast<uint4*>(prow + ((c ^ (h & 7)) << 4)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        tc::fence_proxy_async_smem();
+        tc::fence_before_sync();
+        tc::mbar_arrive(&p_full[bb]);
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) cur[i] = nxt[i];
     }
     if (!ok) *abort_flag = 1;
     // epilogue: O slice / l -> bf16, lse
-    const bool last_ok = ok && __all_sync(0xffffffffu, tc::mbar_wait(p_empty, (ntiles - 1) & 1, abort_flag));
+    const int lb = (ntiles - 1) & 1;
+    const bool last_ok =
+        ok && __all_sync(0xffffffffu, tc::mbar_wait(&p_empty[lb], ((ntiles - 1) >> 1) & 1, abort_flag));
     if (last_ok) {
       tc::fence_after_sync();
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -294,7 +379,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
       }
       if (rank == 0) a.lse[(int64_t)t * MT_H + h] = l > 0.f ? (m_use + log2f(l)) * kLn2 : NEG_INF;
     } else {
-      // nothing selected (or wound down): zero output slice, -inf lse
+      // wound down after a timeout: zero output slice, -inf lse
       __nv_bfloat16* orow = a.out + ((int64_t)t * MT_H + h) * MT_DV + ch0;
       for (int c = 0; c < MT_OCOLS; c += 8) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
       if (rank == 0) a.lse[(int64_t)t * MT_H + h] = NEG_INF;
@@ -306,7 +391,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
   if (*abort_flag && tid == 0) raise_flag(a.flags, TSA_FLAG_TIMEOUT);
   __syncwarp();
   tc::cluster_sync();  // the peer no longer writes into this CTA's shared memory
-  if (warp == 5) {
+  if (warp == 4) {
     __syncwarp();
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, 512);
@@ -318,15 +403,14 @@ cudaError_t make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, u
 
 template <int D>
 static cudaError_t launch_tc_t(const MlaFwdArgs& a, cudaStream_t stream) {
-  CUtensorMap tq, tkv;
+  CUtensorMap tq;
   cudaError_t e = make_tmap_bf16_2d(&tq, a.q, (uint64_t)a.T * MT_H, D, MT_H, 64);
   if (e != cudaSuccess) return e;
-  e = make_tmap_bf16_2d(&tkv, a.kv, (uint64_t)a.T, D, 1, 64);
-  if (e != cudaSuccess) return e;
   constexpr int smem = MtLayout<D>::SMEM;
+  static_assert(smem <= 227 * 1024, "shared memory budget");
   e = cudaFuncSetAttribute(mla_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  mla_fwd_tc_kernel<D><<<dim3(2 * a.T), MT_THREADS, smem, stream>>>(tq, tkv, a);
+  mla_fwd_tc_kernel<D><<<dim3(2 * a.T), MT_THREADS, smem, stream>>>(tq, a);
   return cudaGetLastError();
 }
 
