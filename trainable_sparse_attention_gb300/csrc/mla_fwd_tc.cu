@@ -87,9 +87,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
   uint64_t* s_empty = s_full + 2;                     // [2]
   uint64_t* p_full = s_empty + 2;                     // [2]
   uint64_t* p_empty = p_full + 2;                     // [2] (PV of that buffer completed)
-  uint64_t* xfull = p_empty + 2;                      // [2] peer wrote my X[b]
-  uint64_t* xfree = xfull + 2;                        // [2] peer consumed what I wrote into its X[b]
-  uint64_t* mask_full = xfree + 2;                    // [STAGES] valid-slot bits of the stage written
+  uint64_t* xfull = p_empty + 2;                      // [2] the peer's half of a tile landed in my X[b]
+  uint64_t* mask_full = xfull + 2;                    // [STAGES] valid-slot bits of the stage written
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mask_full + MT_STAGES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   uint32_t* masks = tmem_slot + 2;                    // [STAGES] valid-slot bits of each staged tile
@@ -119,11 +118,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
       tc::mbar_init(&s_empty[i], MT_H);
       tc::mbar_init(&p_full[i], MT_H);
       tc::mbar_init(&p_empty[i], 1);
-      tc::mbar_init(&xfull[i], 4);  // one remote arrival per softmax warp of the peer
-      tc::mbar_init(&xfree[i], 4);
+      tc::mbar_init(&xfull[i], 1);  // own expect_tx arrival + the peer's st.async bytes
     }
     *abort_flag = 0;
     tc::fence_barrier_init();
+    tc::mbar_arrive_expect_tx(&xfull[0], L::X_BYTES);  // tiles 0 and 1
+    tc::mbar_arrive_expect_tx(&xfull[1], L::X_BYTES);
   }
   if (warp == 4) tc::tmem_alloc(tmem_slot, 512);
   tc::fence_before_sync();
@@ -230,13 +230,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax (warps 0-3)
-    // Iteration j fetches tile j's partial logits from TMEM and sends them to
-    // the peer, then normalises tile j-1, whose peer half arrived meanwhile.
+    // Iteration j: fetch tile j's partial logits from TMEM, receive the peer's
+    // half of tile j-1, send this CTA's half of tile j (st.async, completing
+    // on the peer's barrier), then normalise tile j-1 while it travels.
     const int h = tid;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const uint32_t x_peer_row = tc::mapa(smem_u32(X + h * MT_N), peer);
     const uint32_t peer_xfull = tc::mapa(smem_u32(xfull), peer);
-    const uint32_t peer_xfree = tc::mapa(smem_u32(xfree), peer);
     float m_use = NEG_INF, l = 0.f;
     bool ok = true;
     uint32_t cur[32];
@@ -251,25 +251,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
         tc::tmem_ld_wait();
         tc::fence_before_sync();
         tc::mbar_arrive(&s_empty[b]);
-        if (!__all_sync(0xffffffffu, tc::mbar_wait_cluster(&xfree[b], ((j >> 1) & 1) ^ 1u, abort_flag))) {
-          ok = false;
-          break;
-        }
-        const uint32_t dst = x_peer_row + b * L::X_BYTES;
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          tc::st_cluster_v4(dst + q * 16, __uint_as_float(nxt[4 * q]), __uint_as_float(nxt[4 * q + 1]),
-                            __uint_as_float(nxt[4 * q + 2]), __uint_as_float(nxt[4 * q + 3]));
-        __syncwarp();  // the warp's remote stores are ordered before its one release arrival
-        if (lane == 0) tc::mbar_arrive_remote(peer_xfull + b * 8);
       }
+      // receive the peer's half of tile j-1 (published at the end of its previous iteration)
+      float x2[32];
       if (j > 0) {
         const int jj = j - 1, bb = jj & 1;
         if (!__all_sync(0xffffffffu, tc::mbar_wait_cluster(&xfull[bb], (jj >> 1) & 1, abort_flag))) {
           ok = false;
           break;
         }
-        float x2[32];
         const float4* xr = reinterpret_cast<const float4*>(X + bb * (MT_H * MT_N) + h * MT_N);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -279,8 +269,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
           x2[4 * q + 2] = __uint_as_float(cur[4 * q + 2]) + v.z;
           x2[4 * q + 3] = __uint_as_float(cur[4 * q + 3]) + v.w;
         }
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive_remote(peer_xfree + bb * 8);
+        // the next use of X[bb] is tile jj+2; the peer can send it only after
+        // all of this CTA's threads sent tile jj+1, i.e. after they read X[bb]
+        if (h == 0 && jj + 2 < ntiles) tc::mbar_arrive_expect_tx(&xfull[bb], L::X_BYTES);
+      }
+      // send this CTA's half of tile j: asynchronous stores that complete on
+      // the peer's barrier when they land (no fence, no remote arrival)
+      if (j < ntiles) {
+        const int b = j & 1;
+        const uint32_t dst = x_peer_row + b * L::X_BYTES;
+        const uint32_t rbar = peer_xfull + b * 8;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          tc::st_async_v4(dst + q * 16, rbar, __uint_as_float(nxt[4 * q]), __uint_as_float(nxt[4 * q + 1]),
+                          __uint_as_float(nxt[4 * q + 2]), __uint_as_float(nxt[4 * q + 3]));
+      }
+      if (j > 0) {
+        const int jj = j - 1, bb = jj & 1;
         // valid-slot bits published by the producer with this stage
         const int st = jj % MT_STAGES;
         if (!__all_sync(0xffffffffu, tc::mbar_wait(&mask_full[st], (jj / MT_STAGES) & 1, abort_flag))) {

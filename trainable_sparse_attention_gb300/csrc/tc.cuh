@@ -195,6 +195,14 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t raddr, float a, float b, 
   asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(raddr), "f"(a), "f"(b), "f"(c), "f"(d)
                : "memory");
 }
+// Asynchronous 16-byte store into another CTA's shared memory that, once it
+// lands, completes 16 transaction bytes on that CTA's mbarrier `rbar`.
+__device__ __forceinline__ void st_async_v4(uint32_t raddr, uint32_t rbar, float a, float b, float c, float d) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   raddr),
+               "f"(a), "f"(b), "f"(c), "f"(d), "r"(rbar)
+               : "memory");
+}
 // Arrive on an mbarrier of another CTA in the cluster, releasing prior writes.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t raddr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(raddr) : "memory");
