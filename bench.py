@@ -248,7 +248,7 @@ def run_gpu(args):
     q, kv, dout = m["q"], m["kv"], m["dout"]
     del x, m
     ws_topk = torch.empty(tsa.qsa_topk_workspace_size(cu), dtype=torch.uint8, device=dev)
-    ws_bwd = torch.empty(tsa.sparse_mla_bwd_workspace_size(T_TOK, H, D), dtype=torch.uint8, device=dev)
+    ws_bwd = torch.empty(tsa.sparse_mla_bwd_workspace_size(T_TOK, H, D, TOPK), dtype=torch.uint8, device=dev)
     idx = torch.empty((T_TOK, 1, TOPK), dtype=torch.int32, device=dev)
     out = torch.empty((T_TOK, H, DV), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((T_TOK, H), dtype=torch.float32, device=dev)
@@ -372,7 +372,7 @@ def run_e2e(args, tsa, dev, cu, dev_inputs, f_step, world):
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
     stream = torch.cuda.current_stream()
     ws_topk = torch.empty(tsa.qsa_topk_workspace_size(cu), dtype=torch.uint8, device=dev)
-    ws_bwd = torch.empty(tsa.sparse_mla_bwd_workspace_size(T_TOK, H, D), dtype=torch.uint8, device=dev)
+    ws_bwd = torch.empty(tsa.sparse_mla_bwd_workspace_size(T_TOK, H, D, TOPK), dtype=torch.uint8, device=dev)
     d_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
 
     def e2e_step():

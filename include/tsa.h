@@ -180,10 +180,13 @@ int sparse_mla_fwd(const void* q_dev, const void* kv_dev, const int32_t* indices
  *   dS = P*(dP - Dlt); dq = scale*dS.K;
  *   dkv[idx] += scale*dS^T.q (+ P^T.dO on the first 512 channels).
  *   dq_dev bf16 [T, H, d_qk], dkv_dev bf16 [T, d_qk] (fully overwritten).
- *   workspace: sparse_mla_bwd_workspace_size bytes (fp32 dkv + Dlt).
+ *   workspace: sparse_mla_bwd_workspace_size(T, H, d_qk, topk) bytes: fp32
+ *   dkv and Dlt, and for H = 128 a bf16 staging area for P and dS of one
+ *   chunk of queries (at most 1 GiB; the chunk shrinks as topk grows).
+ *   Returns 0 for T < 0, H < 1, d_qk < 1 or topk < 1.
  * Same support as sparse_mla_fwd.  dkv summation order is not fixed.
  * ------------------------------------------------------------------------- */
-size_t sparse_mla_bwd_workspace_size(int64_t T, int H, int d_qk);
+size_t sparse_mla_bwd_workspace_size(int64_t T, int H, int d_qk, int topk);
 int sparse_mla_bwd(const void* q_dev, const void* kv_dev, const int32_t* indices_dev,
                    const void* out_dev, const float* lse_dev, const void* dout_dev,
                    const int32_t* cu_seqlens, int num_seqs, int H, int d_qk, int topk,

@@ -234,3 +234,35 @@ def test_mla_h128_large_logits_rescale(tsa):
     rows = list(range(0, 600, 7)) + [599]
     o_ref, l_ref = O.sparse_mla_fwd(m["q"], m["kv"], idx, cu, 0.2, rows=rows)
     check_out_lse(out, lse, o_ref, l_ref, rows=rows)
+
+
+@pytest.mark.parametrize("D,topk,lengths", [
+    (576, 64, [300]),            # short rows: fewer candidates than slots
+    (576, 65, [130, 200]),       # THD; slots padded from 65 to 128 for the dKV GEMM
+    (576, 1000, [700]),          # -1 tails
+    (512, 96, [257]),            # NoPE layout: four 128-channel dKV blocks
+    (576, 2048, [2100]),         # three query chunks of the P/dS staging
+])
+def test_mla_h128_backward(tsa, D, topk, lengths):
+    """H = 128 backward (recompute of P/dS + tcgen05 dKV GEMM): dO is kept on
+    sampled rows only, so the oracle's dq of those rows and its full dkv are
+    exact references; dq of the other rows must be zero."""
+    cu = synth.cu_seqlens_thd(lengths)
+    T = cu[-1]
+    m = synth.mla_inputs(T, 128, D, seed=3 * T + topk + D, with_grad_out=True)
+    idx = synth.random_topk_indices(cu, topk, seed=topk + 1, invalid_rows=[3, T - 1])
+    scale = 1 / math.sqrt(D)
+    rows = sorted(set([0, 1, 3, 63, 64, T - 1] + list(range(5, T, max(1, T // 24)))))
+    mask = torch.zeros(T, dtype=torch.bool)
+    mask[rows] = True
+    m["dout"] = torch.where(mask[:, None, None], m["dout"], torch.zeros_like(m["dout"]))
+    r = _run_fwd_bwd(tsa, m, idx, cu, scale)
+    dq_ref, dkv_ref = O.sparse_mla_bwd(m["q"], m["kv"], idx, cu, scale, m["dout"], rows=rows)
+    dq = r["dq"].cpu()
+    assert rel_l2(dq[rows], dq_ref) <= TOL_GRAD
+    assert rel_l2(r["dkv"], dkv_ref) <= TOL_GRAD
+    others = torch.ones(T, dtype=torch.bool)
+    others[rows] = False
+    assert torch.all(dq[others] == 0)
+    untouched = torch.from_numpy(np.abs(np.asarray(dkv_ref)).sum(1) == 0)
+    assert torch.all(r["dkv"].cpu()[untouched] == 0)

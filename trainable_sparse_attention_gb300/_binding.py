@@ -40,7 +40,7 @@ SIGNATURES = {
                                   c_float, c_int, c_void_p, c_void_p]),
     "sparse_mla_fwd": (c_int, [c_void_p, c_void_p, c_void_p, c_i32p, c_int, c_int, c_int, c_int, c_float,
                                c_void_p, c_void_p, c_void_p]),
-    "sparse_mla_bwd_workspace_size": (c_size_t, [c_int64, c_int, c_int]),
+    "sparse_mla_bwd_workspace_size": (c_size_t, [c_int64, c_int, c_int, c_int]),
     "sparse_mla_bwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_i32p, c_int,
                                c_int, c_int, c_int, c_float, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "sparse_gqa_fwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_i32p, c_int, c_int, c_int, c_int,
@@ -201,8 +201,8 @@ def sparse_mla_fwd(q, kv, indices, cu_seqlens, softmax_scale: float, out=None, l
     return out, lse
 
 
-def sparse_mla_bwd_workspace_size(T: int, H: int, d_qk: int) -> int:
-    return int(load_library().sparse_mla_bwd_workspace_size(T, H, d_qk))
+def sparse_mla_bwd_workspace_size(T: int, H: int, d_qk: int, topk: int) -> int:
+    return int(load_library().sparse_mla_bwd_workspace_size(T, H, d_qk, topk))
 
 
 def sparse_mla_bwd(q, kv, indices, out, lse, dout, cu_seqlens, softmax_scale: float, workspace=None,
@@ -215,7 +215,7 @@ def sparse_mla_bwd(q, kv, indices, out, lse, dout, cu_seqlens, softmax_scale: fl
     topk = indices.shape[1]
     cu, nseq = _cu(cu_seqlens)
     lib = load_library()
-    need = int(lib.sparse_mla_bwd_workspace_size(T, H, D))
+    need = int(lib.sparse_mla_bwd_workspace_size(T, H, D, topk))
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     if dq is None:

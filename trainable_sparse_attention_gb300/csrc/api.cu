@@ -304,11 +304,27 @@ int sparse_mla_fwd(const void* q, const void* kv, const int32_t* indices, const 
   return TSA_OK;
 }
 
-size_t sparse_mla_bwd_workspace_size(int64_t T, int H, int d_qk) {
-  if (T < 0 || H < 1 || d_qk < 1) return 0;
-  size_t a = static_cast<size_t>(T) * d_qk * sizeof(float);
-  a = (a + 255) & ~size_t(255);
-  return a + static_cast<size_t>(T) * H * sizeof(float);
+// The 128-head backward stages P and dS of one chunk of queries in bf16
+// ([query][head][slot], slots rounded up to 128) for the dKV GEMM; the chunk
+// is sized so that the staging stays within kMlaStageBytes.
+static constexpr int64_t kMlaStageBytes = int64_t(1) << 30;
+
+static int64_t mla_kp(int topk) { return (static_cast<int64_t>(topk) + 127) / 128 * 128; }
+
+static int64_t mla_bwd_chunk(int64_t T, int H, int topk) {
+  if (H != 128) return 0;
+  const int64_t per_query = static_cast<int64_t>(H) * mla_kp(topk) * 2 * sizeof(__nv_bfloat16);
+  return std::max<int64_t>(1, std::min<int64_t>(T, kMlaStageBytes / per_query));
+}
+
+static size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
+
+size_t sparse_mla_bwd_workspace_size(int64_t T, int H, int d_qk, int topk) {
+  if (T < 0 || H < 1 || d_qk < 1 || topk < 1) return 0;
+  size_t a = align256(static_cast<size_t>(T) * d_qk * sizeof(float));
+  a += align256(static_cast<size_t>(T) * H * sizeof(float));
+  const int64_t chunk = mla_bwd_chunk(T, H, topk);
+  return a + static_cast<size_t>(chunk) * H * mla_kp(topk) * 2 * sizeof(__nv_bfloat16);
 }
 
 int sparse_mla_bwd(const void* q, const void* kv, const int32_t* indices, const void* out, const float* lse,
@@ -323,11 +339,12 @@ int sparse_mla_bwd(const void* q, const void* kv, const int32_t* indices, const 
   if (T == 0) return TSA_OK;
   if (!q || !kv || !indices || !out || !lse || !dout || !dq || !dkv)
     return fail(TSA_ERR_INVALID_ARG, "null tensor pointer");
-  size_t need = sparse_mla_bwd_workspace_size(T, H, d_qk);
+  size_t need = sparse_mla_bwd_workspace_size(T, H, d_qk, topk);
   if (workspace == nullptr || workspace_bytes < need)
     return fail(TSA_ERR_WORKSPACE, "workspace %zu bytes < %zu", workspace_bytes, need);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  size_t dkv_bytes = (static_cast<size_t>(T) * d_qk * sizeof(float) + 255) & ~size_t(255);
+  const size_t dkv_bytes = align256(static_cast<size_t>(T) * d_qk * sizeof(float));
+  const size_t dlt_bytes = align256(static_cast<size_t>(T) * H * sizeof(float));
   float* dkv_acc = static_cast<float*>(workspace);
   float* dlt = reinterpret_cast<float*>(static_cast<char*>(workspace) + dkv_bytes);
   TSA_CHECK_CUDA(cudaMemsetAsync(dkv_acc, 0, static_cast<size_t>(T) * d_qk * sizeof(float), s), "memset");
@@ -344,7 +361,33 @@ int sparse_mla_bwd(const void* q, const void* kv, const int32_t* indices, const 
   a.scale_log2 = softmax_scale * kLog2e;
   a.dq = static_cast<__nv_bfloat16*>(dq);
   a.dkv_acc = dkv_acc;
-  TSA_LAUNCH(launch_mla_bwd(a, d_qk, s), "mla bwd launch");
+  if (H == 128) {
+    // chunks of queries: P and dS (plus dQ) from the recompute kernel, then the dKV GEMM
+    const int64_t chunk = mla_bwd_chunk(T, H, topk);
+    const int64_t kp = mla_kp(topk);
+    auto* stage = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(workspace) + dkv_bytes + dlt_bytes);
+    a.kp = static_cast<int>(kp);
+    a.p_out = stage;
+    a.ds_out = stage + chunk * H * kp;
+    MlaBwdTcArgs b;
+    b.q = a.q;
+    b.dout = a.dout;
+    b.ds = a.ds_out;
+    b.p = a.p_out;
+    b.idx = indices;
+    b.T = a.T; b.D = d_qk; b.topk = topk; b.kp = a.kp;
+    b.dkv_acc = dkv_acc;
+    b.flags = flags_ptr();
+    b.st = a.st;
+    for (int64_t q0 = 0; q0 < T; q0 += chunk) {
+      const int nq = static_cast<int>(std::min(chunk, T - q0));
+      a.q0 = b.q0 = static_cast<int>(q0);
+      TSA_LAUNCH(launch_mla_bwd_emit(a, d_qk, nq, s), "mla bwd recompute launch");
+      TSA_LAUNCH(launch_mla_bwd_dkv_tc(b, nq, s), "mla bwd dkv launch");
+    }
+  } else {
+    TSA_LAUNCH(launch_mla_bwd(a, d_qk, s), "mla bwd launch");
+  }
   TSA_LAUNCH(launch_f32_to_bf16(dkv_acc, static_cast<__nv_bfloat16*>(dkv), T * d_qk, s), "convert launch");
   return TSA_OK;
 }

@@ -58,6 +58,26 @@ struct MlaBwdArgs {
   __nv_bfloat16* dq;         // [T, H, D]
   float* dkv_acc;            // [T, D] fp32, zeroed by the caller
   SeqTable st;
+  // Emit mode (H = 128): queries q0 .. q0+gridDim.x write P and dS (bf16) to
+  // p_out / ds_out [query - q0][head][kp] instead of scattering dKV themselves.
+  int q0 = 0;
+  int kp = 0;
+  __nv_bfloat16* p_out = nullptr;
+  __nv_bfloat16* ds_out = nullptr;
+};
+
+// Inputs of the tcgen05 dKV GEMM: P and dS of queries q0 .. q0+nq in bf16,
+// [query - q0][128 heads][kp slots], kp = topk rounded up to 128 (zero padded).
+struct MlaBwdTcArgs {
+  const __nv_bfloat16* q;     // [T, 128, D]
+  const __nv_bfloat16* dout;  // [T, 128, 512]
+  const __nv_bfloat16* ds;    // [nq, 128, kp]  scale * P * (dP - Dlt)
+  const __nv_bfloat16* p;     // [nq, 128, kp]
+  const int32_t* idx;         // [T, topk]
+  int T, D, topk, kp, q0;
+  float* dkv_acc;             // [T, D] fp32
+  unsigned int* flags;        // device error flags
+  SeqTable st;
 };
 
 struct GqaArgs {
@@ -88,6 +108,9 @@ cudaError_t launch_fill(float* p, int64_t n, float v, cudaStream_t stream);
 cudaError_t launch_mla_fwd(const MlaFwdArgs& a, int D, cudaStream_t stream);
 cudaError_t launch_mla_fwd_tc(const MlaFwdArgs& a, int D, cudaStream_t stream);
 cudaError_t launch_mla_bwd(const MlaBwdArgs& a, int D, cudaStream_t stream);
+// Emit mode of the backward for 128 heads: queries a.q0 .. a.q0+nq, P and dS to the workspace, dQ.
+cudaError_t launch_mla_bwd_emit(const MlaBwdArgs& a, int D, int nq, cudaStream_t stream);
+cudaError_t launch_mla_bwd_dkv_tc(const MlaBwdTcArgs& a, int nq, cudaStream_t stream);
 cudaError_t launch_bwd_delta(const __nv_bfloat16* o, const __nv_bfloat16* dout, float* dlt, int64_t rows, int dv,
                              cudaStream_t stream);
 cudaError_t launch_f32_to_bf16(const float* src, __nv_bfloat16* dst, int64_t n, cudaStream_t stream);
