@@ -367,6 +367,7 @@ int sparse_mla_bwd(const void* q, const void* kv, const int32_t* indices, const 
     const int64_t kp = mla_kp(topk);
     auto* stage = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(workspace) + dkv_bytes + dlt_bytes);
     a.kp = static_cast<int>(kp);
+    a.flags = flags_ptr();
     a.p_out = stage;
     a.ds_out = stage + chunk * H * kp;
     MlaBwdTcArgs b;
@@ -382,7 +383,8 @@ int sparse_mla_bwd(const void* q, const void* kv, const int32_t* indices, const 
     for (int64_t q0 = 0; q0 < T; q0 += chunk) {
       const int nq = static_cast<int>(std::min(chunk, T - q0));
       a.q0 = b.q0 = static_cast<int>(q0);
-      TSA_LAUNCH(launch_mla_bwd_emit(a, d_qk, nq, s), "mla bwd recompute launch");
+      TSA_LAUNCH(launch_mla_bwd_pds_tc(a, d_qk, nq, s), "mla bwd recompute launch");
+      TSA_LAUNCH(launch_mla_bwd_dq_tc(a, d_qk, nq, s), "mla bwd dq launch");
       TSA_LAUNCH(launch_mla_bwd_dkv_tc(b, nq, s), "mla bwd dkv launch");
     }
   } else {

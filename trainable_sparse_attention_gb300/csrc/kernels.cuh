@@ -64,6 +64,7 @@ struct MlaBwdArgs {
   int kp = 0;
   __nv_bfloat16* p_out = nullptr;
   __nv_bfloat16* ds_out = nullptr;
+  unsigned int* flags = nullptr;  // device error flags
 };
 
 // Inputs of the tcgen05 dKV GEMM: P and dS of queries q0 .. q0+nq in bf16,
@@ -111,6 +112,9 @@ cudaError_t launch_mla_bwd(const MlaBwdArgs& a, int D, cudaStream_t stream);
 // Emit mode of the backward for 128 heads: queries a.q0 .. a.q0+nq, P and dS to the workspace, dQ.
 cudaError_t launch_mla_bwd_emit(const MlaBwdArgs& a, int D, int nq, cudaStream_t stream);
 cudaError_t launch_mla_bwd_dkv_tc(const MlaBwdTcArgs& a, int nq, cudaStream_t stream);
+// tcgen05 recompute of P and dS (to a.p_out / a.ds_out) and dQ = dS K for queries a.q0 .. a.q0+nq.
+cudaError_t launch_mla_bwd_pds_tc(const MlaBwdArgs& a, int D, int nq, cudaStream_t stream);
+cudaError_t launch_mla_bwd_dq_tc(const MlaBwdArgs& a, int D, int nq, cudaStream_t stream);
 cudaError_t launch_bwd_delta(const __nv_bfloat16* o, const __nv_bfloat16* dout, float* dlt, int64_t rows, int dv,
                              cudaStream_t stream);
 cudaError_t launch_f32_to_bf16(const float* src, __nv_bfloat16* dst, int64_t n, cudaStream_t stream);
