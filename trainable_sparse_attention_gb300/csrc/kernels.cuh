@@ -58,8 +58,8 @@ struct MlaBwdArgs {
   __nv_bfloat16* dq;         // [T, H, D]
   float* dkv_acc;            // [T, D] fp32, zeroed by the caller
   SeqTable st;
-  // Emit mode (H = 128): queries q0 .. q0+gridDim.x write P and dS (bf16) to
-  // p_out / ds_out [query - q0][head][kp] instead of scattering dKV themselves.
+  // 128-head tcgen05 path: queries q0 .. q0+nq of one chunk, P and dS (bf16)
+  // staged in p_out / ds_out as [query - q0][head][kp].
   int q0 = 0;
   int kp = 0;
   __nv_bfloat16* p_out = nullptr;
@@ -109,8 +109,6 @@ cudaError_t launch_fill(float* p, int64_t n, float v, cudaStream_t stream);
 cudaError_t launch_mla_fwd(const MlaFwdArgs& a, int D, cudaStream_t stream);
 cudaError_t launch_mla_fwd_tc(const MlaFwdArgs& a, int D, cudaStream_t stream);
 cudaError_t launch_mla_bwd(const MlaBwdArgs& a, int D, cudaStream_t stream);
-// Emit mode of the backward for 128 heads: queries a.q0 .. a.q0+nq, P and dS to the workspace, dQ.
-cudaError_t launch_mla_bwd_emit(const MlaBwdArgs& a, int D, int nq, cudaStream_t stream);
 cudaError_t launch_mla_bwd_dkv_tc(const MlaBwdTcArgs& a, int nq, cudaStream_t stream);
 // tcgen05 recompute of P and dS (to a.p_out / a.ds_out) and dQ = dS K for queries a.q0 .. a.q0+nq.
 cudaError_t launch_mla_bwd_pds_tc(const MlaBwdArgs& a, int D, int nq, cudaStream_t stream);

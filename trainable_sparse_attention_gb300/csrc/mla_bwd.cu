@@ -11,9 +11,10 @@
 //
 // Three launches: (1) Dlt per (t, h); (2) one CTA per (query, head block)
 // recomputes S/P from the stored LSE, keeps dQ in registers and scatters its
-// dKV tile contribution with red.global.add.v2.f32 into an fp32 workspace;
-// (3) fp32 -> bf16 conversion of dKV.  Warp-level tensor-core (mma.sync)
-// variant.
+// dKV tile contribution with 16-byte vector reductions into an fp32
+// workspace; (3) fp32 -> bf16 conversion of dKV.  Warp-level tensor-core
+// (mma.sync) kernel for H < 128; 128 heads take the tcgen05 kernels
+// (mla_bwd_pds_tc.cu, mla_bwd_tc.cu) between the same first and last launch.
 #include "kernels.cuh"
 
 namespace tsa {
@@ -61,9 +62,8 @@ __global__ void f32_to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16*
   }
 }
 
-// MW m-tiles of 16 heads per CTA (HB = 16*MW heads), 4*MW warps.  EMIT: write
-// P and dS of each tile to a.p_out / a.ds_out and leave dKV to the dKV GEMM.
-template <int D, int MW, bool EMIT>
+// MW m-tiles of 16 heads per CTA (HB = 16*MW heads), 4*MW warps.
+template <int D, int MW>
 __global__ void __launch_bounds__(128 * MW) mla_bwd_mma_kernel(const __grid_constant__ MlaBwdArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   constexpr int HB = 16 * MW;
@@ -79,7 +79,7 @@ __global__ void __launch_bounds__(128 * MW) mla_bwd_mma_kernel(const __grid_cons
   __nv_bfloat16* dSs = Ps + HB * PRS;                               // [HB][PRS]
   int* s_rows = reinterpret_cast<int*>(dSs + HB * PRS);             // [2][32] kv row or -1
 
-  const int t = a.q0 + blockIdx.x;
+  const int t = blockIdx.x;
   const int h0 = blockIdx.y * HB;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c4 = lane & 3;
@@ -202,16 +202,6 @@ __global__ void __launch_bounds__(128 * MW) mla_bwd_mma_kernel(const __grid_cons
         }
       }
     }
-    if constexpr (EMIT) {
-      // P and dS rows of this CTA's heads for the 32 slots of the tile: 64 B per row and tensor
-      const int64_t grow = (int64_t)blockIdx.x * a.H + h0;
-      for (int i = tid; i < 2 * HB * 4; i += NTHR) {
-        const int which = i / (HB * 4), r = (i / 4) % HB, c = i % 4;
-        const __nv_bfloat16* src = (which ? dSs : Ps) + r * PRS + c * 8;
-        __nv_bfloat16* dst = (which ? a.ds_out : a.p_out) + (grow + r) * a.kp + jt * MB_KT + c * 8;
-        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
-      }
-    } else {
     // dKV tile [32 keys x D] = (scale dS)^T Q + P^T dO, channels split across warps
     {
       constexpr int CPW = D / NW;     // channels per warp
@@ -251,19 +241,7 @@ __global__ void __launch_bounds__(128 * MW) mla_bwd_mma_kernel(const __grid_cons
         }
       }
     }
-    }
     __syncthreads();
-  }
-  if constexpr (EMIT) {
-    // zero the padding slots [ntile * 32, kp) of this CTA's rows
-    const int pad0 = ntile * MB_KT;
-    const int padc = (a.kp - pad0) / 8;
-    const int64_t grow = (int64_t)blockIdx.x * a.H + h0;
-    for (int i = tid; i < 2 * HB * padc; i += NTHR) {
-      const int which = i / (HB * padc), r = (i / padc) % HB, c = i % padc;
-      __nv_bfloat16* dst = (which ? a.ds_out : a.p_out) + (grow + r) * a.kp + pad0 + c * 8;
-      *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-    }
   }
 
 #pragma unroll
@@ -286,12 +264,12 @@ static size_t mla_bwd_smem() {
          sizeof(int) * 2 * MB_KT;
 }
 
-template <int D, int MW, bool EMIT = false>
-static cudaError_t launch_bwd_main(const MlaBwdArgs& a, int nq, cudaStream_t stream) {
+template <int D, int MW>
+static cudaError_t launch_bwd_main(const MlaBwdArgs& a, cudaStream_t stream) {
   size_t smem = mla_bwd_smem<D, MW>();
-  cudaFuncSetAttribute(mla_bwd_mma_kernel<D, MW, EMIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  dim3 grid(nq, (a.H + 16 * MW - 1) / (16 * MW));
-  mla_bwd_mma_kernel<D, MW, EMIT><<<grid, 128 * MW, smem, stream>>>(a);
+  cudaFuncSetAttribute(mla_bwd_mma_kernel<D, MW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  dim3 grid(a.T, (a.H + 16 * MW - 1) / (16 * MW));
+  mla_bwd_mma_kernel<D, MW><<<grid, 128 * MW, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -315,14 +293,8 @@ cudaError_t launch_f32_to_bf16(const float* src, __nv_bfloat16* dst, int64_t n, 
 cudaError_t launch_mla_bwd(const MlaBwdArgs& a, int D, cudaStream_t stream) {
   if (a.T <= 0) return cudaSuccess;
   const bool wide = a.H > 16;
-  if (D == 576) return wide ? launch_bwd_main<576, 2>(a, a.T, stream) : launch_bwd_main<576, 1>(a, a.T, stream);
-  return wide ? launch_bwd_main<512, 2>(a, a.T, stream) : launch_bwd_main<512, 1>(a, a.T, stream);
-}
-
-cudaError_t launch_mla_bwd_emit(const MlaBwdArgs& a, int D, int nq, cudaStream_t stream) {
-  if (nq <= 0) return cudaSuccess;
-  if (a.H != 128 || a.kp % 128 != 0 || a.p_out == nullptr || a.ds_out == nullptr) return cudaErrorInvalidValue;
-  return D == 576 ? launch_bwd_main<576, 2, true>(a, nq, stream) : launch_bwd_main<512, 2, true>(a, nq, stream);
+  if (D == 576) return wide ? launch_bwd_main<576, 2>(a, stream) : launch_bwd_main<576, 1>(a, stream);
+  return wide ? launch_bwd_main<512, 2>(a, stream) : launch_bwd_main<512, 1>(a, stream);
 }
 
 }  // namespace tsa

@@ -9,20 +9,29 @@
 //   S = q K^T, P = exp(scale S - L), dP = dO V^T, dS = scale P (dP - Dlt),
 //   dQ = dS K.
 //
-// mla_bwd_pds_tc_kernel: one CTA per query.  The query's q rows (128 heads x
-// D) live in TMEM and are the A operand of S = q K^T, so shared memory holds
-// only dO (the A operand of dP = dO V^T, loaded once by TMA) and a two-stage
-// ring of gathered 32-key tiles of kv.  S and dP of a tile land in TMEM
-// (double-buffered); warps 0-3 (thread = head = TMEM lane) turn them into P
-// and dS and write both in bf16 to the staging area, [query][head][slot],
-// slots padded to kp with zeros.  No softmax state is carried between tiles:
-// L is known, so every tile is final when it is computed.
+// mla_bwd_sp_tc_kernel, two passes with one CTA per query.  A tcgen05 MMA
+// costs the same for N = 32 and N = 64 (about 45 cycles for M = 128), so the
+// selected rows are taken 64 at a time; q (576 channels) and dO (512) do not
+// both fit the 512 TMEM columns next to two 64-column accumulators, and dO in
+// shared memory would leave no room for a deep gather ring.  Hence:
+//   pass 1: S = q K^T with the q rows in TMEM (A operand), P = exp(scale S - L)
+//           written in bf16;
+//   pass 2: dP = dO V^T with the dO rows in TMEM, dS = scale P (dP - Dlt)
+//           from the bf16 P of pass 1, written in bf16.
+// Each pass streams its gathered 64-row tiles through a three-stage ring
+// (cp.async, 8 producer warps) and double-buffers the accumulator in TMEM;
+// warps 0-3 (thread = head = TMEM lane) write [query][head][slot] rows, slots
+// padded to kp with zeros.  No softmax state is carried between tiles: L is
+// known, so every tile is final when it is computed.
 //
 // mla_bwd_dq_tc_kernel: dQ = dS K over the gathered rows.  The 128 x D fp32
 // accumulator does not fit one SM's 512 TMEM columns for D = 576, so two CTAs
 // share a query, split by channel (CTA 0: [0, 256), CTA 1: [256, D)); each
 // gathers only its slice of the selected rows as the MN-major B operand and
 // streams the dS tiles (A, K-major) by TMA.
+//
+// All gathers copy a selected row with consecutive lanes on consecutive
+// 16-byte chunks, so the cp.async of a warp coalesce into whole lines.
 #include "kernels.cuh"
 #include "tc.cuh"
 
@@ -34,21 +43,17 @@ cudaError_t make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, u
 namespace {
 
 constexpr int PB_H = 128;        // heads = MMA M
-constexpr int PB_N = 32;         // keys per tile
-constexpr int PB_STAGES = 2;
-constexpr int PB_THREADS = 288;  // warps 0-3 P/dS, warp 4 MMA + TMA, warps 5-8 gather producers
-constexpr int PB_QC = 288;       // TMEM columns reserved for q (D / 2 packed bf16 pairs)
+constexpr int SP_H = PB_H;
+constexpr int SP_N = 64;         // keys per tile (MMA N)
+constexpr int SP_STAGES = 3;
+constexpr int SP_PRODUCERS = 256;
+constexpr int SP_THREADS = 160 + SP_PRODUCERS;  // warps 0-3 epilogue, warp 4 MMA, warps 5-12 gather
+constexpr int SP_ACC = 288;      // first TMEM column of the two accumulators (after the A operand)
 
-template <int D>
-struct PbLayout {
-  static constexpr int KB = D / 64;                  // 64-channel blocks of a kv row
-  static constexpr int DO_BYTES = 8 * PB_H * 128;    // dO, 8 boxes of 64 channels x 128 rows
-  static constexpr int KV_BLOCK = PB_N * 128;        // one 64-channel block of a 32-key tile
-  static constexpr int KV_STAGE = KB * KV_BLOCK;
-  static constexpr int OFF_KV = DO_BYTES;
-  static constexpr int OFF_BAR = OFF_KV + PB_STAGES * KV_STAGE;
-  static constexpr int SMEM = 1024 + OFF_BAR + 256;
-};
+template <int D, bool DS>
+constexpr int sp_smem() {
+  return 1024 + SP_STAGES * ((DS ? 512 : D) / 64) * (SP_N * 128) + 256;
+}
 
 constexpr int DQ_N = 64;          // slots per tile (MMA K per tile)
 constexpr int DQ_STAGES = 3;
@@ -68,23 +73,30 @@ __device__ __forceinline__ float ex2(float x) {
 
 }  // namespace
 
-template <int D>
-__global__ void __launch_bounds__(PB_THREADS, 1)
-    mla_bwd_pds_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ MlaBwdArgs a) {
-  using L = PbLayout<D>;
+// One launch of either pass over queries q0 .. q0+gridDim.x (one CTA each).
+// DS = false: S = q K^T (A = q rows in TMEM, KC = D channels), writes P.
+// DS = true:  dP = dO V^T (A = dO rows in TMEM, KC = 512 value channels),
+//             reads P, writes dS = scale P (dP - Dlt).
+template <int D, bool DS>
+__global__ void __launch_bounds__(SP_THREADS, 1)
+    mla_bwd_sp_tc_kernel(const __grid_constant__ MlaBwdArgs a) {
+  constexpr int KC = DS ? 512 : D;   // channels of the contraction
+  constexpr int KB = KC / 64;        // 64-channel blocks of a gathered row
+  constexpr int ACOLS = KC / 2;      // TMEM columns of the A operand (bf16 pairs)
+  constexpr int KV_BLOCK = SP_N * 128;
+  constexpr int KV_STAGE = KB * KV_BLOCK;
+  constexpr int OFF_BAR = SP_STAGES * KV_STAGE;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* gbase = smem_raw + (base - raw);
-  const uint32_t sDO = base, sKV = base + L::OFF_KV;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + L::OFF_BAR);
-  uint64_t* dofull = bars;                      // [1] dO landed (TMA)
-  uint64_t* qready = bars + 1;                  // [1] q stored into TMEM (4 warps)
-  uint64_t* kv_full = bars + 2;                 // [STAGES] 128 asynchronous producer arrivals
-  uint64_t* kv_empty = kv_full + PB_STAGES;     // [STAGES]
-  uint64_t* sd_full = kv_empty + PB_STAGES;     // [2] S and dP of a tile in TMEM
-  uint64_t* sd_empty = sd_full + 2;             // [2] (4 warps)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sd_empty + 2);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + OFF_BAR);
+  uint64_t* aready = bars;                      // [1] A rows stored into TMEM (4 warps)
+  uint64_t* kv_full = bars + 1;                 // [STAGES] asynchronous producer arrivals
+  uint64_t* kv_empty = kv_full + SP_STAGES;     // [STAGES]
+  uint64_t* acc_full = kv_empty + SP_STAGES;    // [2] a tile's S (or dP) in TMEM
+  uint64_t* acc_empty = acc_full + 2;           // [2] (4 warps)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int lq = blockIdx.x;
@@ -93,19 +105,18 @@ __global__ void __launch_bounds__(PB_THREADS, 1)
   const int s0 = a.st.cu[sq];
   const int n = a.st.cu[sq + 1] - s0;
   const int* idx_row = a.idx + (int64_t)t * a.topk;
-  const int ntiles = (a.topk + PB_N - 1) / PB_N;
+  const int ntiles = (a.topk + SP_N - 1) / SP_N;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    tc::mbar_init(dofull, 1);
-    tc::mbar_init(qready, 4);
-    for (int i = 0; i < PB_STAGES; ++i) {
-      tc::mbar_init(&kv_full[i], 128);
+    tc::mbar_init(aready, 4);
+    for (int i = 0; i < SP_STAGES; ++i) {
+      tc::mbar_init(&kv_full[i], SP_PRODUCERS);
       tc::mbar_init(&kv_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&sd_full[i], 1);
-      tc::mbar_init(&sd_empty[i], 4);
+      tc::mbar_init(&acc_full[i], 1);
+      tc::mbar_init(&acc_empty[i], 4);
     }
     *abort_flag = 0;
     tc::fence_barrier_init();
@@ -117,34 +128,40 @@ __global__ void __launch_bounds__(PB_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp >= 5) {
-    // ------------------------------------------------------------ gather producers (128 threads)
-    // 32 rows x 4 parts; each thread copies KB*2 16-byte chunks of one selected
-    // row into the 128-byte-swizzled K-major tile, arriving asynchronously on
-    // the stage's barrier when they land.
-    const int pt = tid - 160;
-    const int row = pt >> 2, part = pt & 3;
-    constexpr int per = L::KB * 2;
+    // ------------------------------------------------------------ gather producers (8 warps)
+    // Warp w copies rows 8w .. 8w+7 of each 64-row tile; lane l copies the
+    // 16-byte chunks l, l+32, ... of a row, so one instruction covers 512
+    // contiguous bytes of the row.  The chunks land in the 128-byte-swizzled
+    // K-major tile, and each thread's copies arrive asynchronously on the
+    // stage's barrier when they land.  The slot indices of the next tile are
+    // loaded one tile ahead (lane r < 8 holds row 8w + r).
+    const int w8 = (warp - 5) * 8;
+    constexpr int NCH = KC / 8;  // 16-byte chunks per row
     const char* kvb = reinterpret_cast<const char*>(a.kv);
     bool ok = true;
-    int id_next = row < a.topk ? __ldg(idx_row + row) : -1;
+    int id_next = (lane < 8 && w8 + lane < a.topk) ? __ldg(idx_row + w8 + lane) : -1;
     for (int j = 0; j < ntiles; ++j) {
-      const int st = j % PB_STAGES;
-      const int id = id_next;
-      const int slot_next = (j + 1) * PB_N + row;
-      id_next = slot_next < a.topk ? __ldg(idx_row + slot_next) : -1;
-      if (!__all_sync(0xffffffffu, tc::mbar_wait(&kv_empty[st], ((j / PB_STAGES) & 1) ^ 1u, abort_flag))) {
+      const int st = j % SP_STAGES;
+      const int id_mine = id_next;
+      const int slot_next = (j + 1) * SP_N + w8 + lane;
+      id_next = (lane < 8 && slot_next < a.topk) ? __ldg(idx_row + slot_next) : -1;
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&kv_empty[st], ((j / SP_STAGES) & 1) ^ 1u, abort_flag))) {
         ok = false;
         break;
       }
-      const bool valid = id >= 0 && id < n;
-      if (part == 0 && id >= n) raise_flag(a.flags, TSA_FLAG_INDEX_RANGE);
-      const char* src_row = kvb + (int64_t)(valid ? s0 + id : 0) * D * 2;
-      const uint32_t dst = sKV + st * L::KV_STAGE + row * 128;
+      if (!DS && lane < 8 && id_mine >= n) raise_flag(a.flags, TSA_FLAG_INDEX_RANGE);
 #pragma unroll
-      for (int q = 0; q < per; ++q) {
-        const int c16 = part * per + q;
-        const int cb = c16 >> 3, jj = c16 & 7;
-        cp_async16(dst + cb * L::KV_BLOCK + ((jj ^ (row & 7)) << 4), src_row + c16 * 16, valid ? 16u : 0u);
+      for (int r = 0; r < 8; ++r) {
+        const int id = __shfl_sync(0xffffffffu, id_mine, r);
+        const int row = w8 + r;
+        const bool valid = id >= 0 && id < n;
+        const char* src_row = kvb + (int64_t)(valid ? s0 + id : 0) * D * 2;
+        const uint32_t dst = base + st * KV_STAGE + row * 128;
+#pragma unroll
+        for (int c16 = lane; c16 < NCH; c16 += 32) {
+          const int cb = c16 >> 3, jj = c16 & 7;
+          cp_async16(dst + cb * KV_BLOCK + ((jj ^ (row & 7)) << 4), src_row + c16 * 16, valid ? 16u : 0u);
+        }
       }
       cp_async_commit();
       asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&kv_full[st]))
@@ -153,62 +170,51 @@ __global__ void __launch_bounds__(PB_THREADS, 1)
     cp_async_wait<0>();
     if (!ok) *abort_flag = 1;
   } else if (warp == 4) {
-    // ------------------------------------------------------------ dO (TMA) + MMA issuer
+    // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      tc::prefetch_tmap(&tm_do);
-      tc::mbar_arrive_expect_tx(dofull, L::DO_BYTES);
-      for (int c = 0; c < 8; ++c) tc::tma_load_2d(sDO + c * (PB_H * 128), &tm_do, dofull, c * 64, t * PB_H);
-      constexpr uint32_t idesc = tc::idesc_bf16_f32(PB_H, PB_N);
-      bool ok = tc::mbar_wait(dofull, 0, abort_flag) && tc::mbar_wait(qready, 0, abort_flag);
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(SP_H, SP_N);
+      bool ok = tc::mbar_wait(aready, 0, abort_flag);
       tc::fence_after_sync();
       for (int j = 0; ok && j < ntiles; ++j) {
-        const int st = j % PB_STAGES, b = j & 1;
-        if (!tc::mbar_wait(&kv_full[st], (j / PB_STAGES) & 1, abort_flag) ||
-            !tc::mbar_wait(&sd_empty[b], ((j >> 1) & 1) ^ 1u, abort_flag)) {
+        const int st = j % SP_STAGES, b = j & 1;
+        if (!tc::mbar_wait(&kv_full[st], (j / SP_STAGES) & 1, abort_flag) ||
+            !tc::mbar_wait(&acc_empty[b], ((j >> 1) & 1) ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
         tc::fence_proxy_async_smem();  // the gathered tile was written through the generic proxy
         tc::fence_after_sync();
-        const uint32_t dS_ = tmem + PB_QC + b * PB_N;
-        const uint32_t dP_ = tmem + PB_QC + 2 * PB_N + b * PB_N;
-        const uint32_t kv = sKV + st * L::KV_STAGE;
-        // S = q K^T: A = q from TMEM (8 columns per 16 channels)
-        for (int c = 0; c < L::KB; ++c) {
+        const uint32_t d = tmem + SP_ACC + b * SP_N;
+        const uint32_t kv = base + st * KV_STAGE;
+        for (int c = 0; c < KB; ++c) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            tc::mma_bf16_ts(dS_, tmem + (c * 4 + kk) * 8, tc::desc_sw128(kv + c * L::KV_BLOCK + kk * 32), idesc,
+            tc::mma_bf16_ts(d, tmem + (c * 4 + kk) * 8, tc::desc_sw128(kv + c * KV_BLOCK + kk * 32), idesc,
                             (c | kk) != 0 ? 1u : 0u);
         }
-        // dP = dO V^T over the 512 value channels
-        for (int c = 0; c < 8; ++c) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc::mma_bf16_ss(dP_, tc::desc_sw128(sDO + c * (PB_H * 128) + kk * 32),
-                            tc::desc_sw128(kv + c * L::KV_BLOCK + kk * 32), idesc, (c | kk) != 0 ? 1u : 0u);
-        }
         tc::mma_commit(&kv_empty[st]);
-        tc::mma_commit(&sd_full[b]);
+        tc::mma_commit(&acc_full[b]);
       }
       if (!ok) *abort_flag = 1;
     }
   } else {
-    // ------------------------------------------------------------ P / dS (warps 0-3, thread = head)
+    // ------------------------------------------------------------ epilogue (warps 0-3, thread = head)
     const int h = tid;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const float NEG_INF = __int_as_float(0xff800000);
-    const float Lh = a.lse[(int64_t)t * PB_H + h];
+    const float Lh = a.lse[(int64_t)t * SP_H + h];
     const float lse2 = Lh * kLog2e;
     const bool live = Lh != NEG_INF;  // a row without valid slots has P = dS = 0
-    const float dl = a.dlt[(int64_t)t * PB_H + h];
-    // q row h -> TMEM columns [0, D/2): 32 columns (64 channels) per store
+    const float dl = DS ? a.dlt[(int64_t)t * SP_H + h] : 0.f;
+    // A row h -> TMEM columns [0, KC/2): 32 columns (64 channels) per store
     {
-      const uint4* qrow = reinterpret_cast<const uint4*>(a.q + ((int64_t)t * PB_H + h) * D);
-      for (int c = 0; c < D / 64; ++c) {
+      const uint4* arow = DS ? reinterpret_cast<const uint4*>(a.dout + ((int64_t)t * SP_H + h) * 512)
+                             : reinterpret_cast<const uint4*>(a.q + ((int64_t)t * SP_H + h) * D);
+      for (int c = 0; c < KB; ++c) {
         uint32_t r[32];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const uint4 v = __ldg(qrow + c * 8 + i);
+          const uint4 v = __ldg(arow + c * 8 + i);
           r[4 * i] = v.x;
           r[4 * i + 1] = v.y;
           r[4 * i + 2] = v.z;
@@ -220,54 +226,72 @@ __global__ void __launch_bounds__(PB_THREADS, 1)
       tc::tmem_st_wait();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(qready);
+      if (lane == 0) tc::mbar_arrive(aready);
     }
-    __nv_bfloat16* prow = a.p_out + ((int64_t)lq * PB_H + h) * a.kp;
-    __nv_bfloat16* dsrow = a.ds_out + ((int64_t)lq * PB_H + h) * a.kp;
+    static_assert(ACOLS <= SP_ACC, "A operand overlaps the accumulators");
+    __nv_bfloat16* prow = a.p_out + ((int64_t)lq * SP_H + h) * a.kp;
+    __nv_bfloat16* dsrow = a.ds_out + ((int64_t)lq * SP_H + h) * a.kp;
     bool ok = true;
-    int idn = lane < a.topk ? __ldg(idx_row + lane) : -1;
+    int idn0 = lane < a.topk ? __ldg(idx_row + lane) : -1;
+    int idn1 = 32 + lane < a.topk ? __ldg(idx_row + 32 + lane) : -1;
+    uint4 pn[8];
+    if (DS) {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) pn[c] = reinterpret_cast<const uint4*>(prow)[c];
+    }
     for (int j = 0; j < ntiles; ++j) {
       const int b = j & 1;
-      const uint32_t mask = __ballot_sync(0xffffffffu, idn >= 0 && idn < n);
-      const int slot_next = (j + 1) * PB_N + lane;
-      idn = slot_next < a.topk ? __ldg(idx_row + slot_next) : -1;
-      if (!__all_sync(0xffffffffu, tc::mbar_wait(&sd_full[b], (j >> 1) & 1, abort_flag))) {
+      const uint32_t m0 = __ballot_sync(0xffffffffu, idn0 >= 0 && idn0 < n);
+      const uint32_t m1 = __ballot_sync(0xffffffffu, idn1 >= 0 && idn1 < n);
+      const uint64_t mask = static_cast<uint64_t>(m1) << 32 | m0;
+      if (!DS) {
+        const int sn = (j + 1) * SP_N + lane;
+        idn0 = sn < a.topk ? __ldg(idx_row + sn) : -1;
+        idn1 = sn + 32 < a.topk ? __ldg(idx_row + sn + 32) : -1;
+      }
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&acc_full[b], (j >> 1) & 1, abort_flag))) {
         ok = false;
         break;
       }
       tc::fence_after_sync();
-      uint32_t s[32], dp[32];
-      tc::tmem_ld32(tmem + lane_base + PB_QC + b * PB_N, s);
-      tc::tmem_ld32(tmem + lane_base + PB_QC + 2 * PB_N + b * PB_N, dp);
+      uint32_t x[64];
+      tc::tmem_ld32(tmem + lane_base + SP_ACC + b * SP_N, x);
+      tc::tmem_ld32(tmem + lane_base + SP_ACC + b * SP_N + 32, x + 32);
       tc::tmem_ld_wait();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&sd_empty[b]);
-      uint32_t pk[16], dk[16];
+      if (lane == 0) tc::mbar_arrive(&acc_empty[b]);
+      uint32_t pk[32];
+      if (!DS) {
 #pragma unroll
-      for (int i = 0; i < 32; i += 2) {
-        float p0 = 0.f, p1 = 0.f;
-        if (live && ((mask >> i) & 1u)) p0 = ex2(fmaf(__uint_as_float(s[i]), a.scale_log2, -lse2));
-        if (live && ((mask >> (i + 1)) & 1u)) p1 = ex2(fmaf(__uint_as_float(s[i + 1]), a.scale_log2, -lse2));
-        const float d0 = a.scale * p0 * (__uint_as_float(dp[i]) - dl);
-        const float d1 = a.scale * p1 * (__uint_as_float(dp[i + 1]) - dl);
-        pk[i / 2] = pack_bf16(p0, p1);
-        dk[i / 2] = pack_bf16(d0, d1);
+        for (int i = 0; i < 64; i += 2) {
+          float p0 = 0.f, p1 = 0.f;
+          if (live && ((mask >> i) & 1u)) p0 = ex2(fmaf(__uint_as_float(x[i]), a.scale_log2, -lse2));
+          if (live && ((mask >> (i + 1)) & 1u)) p1 = ex2(fmaf(__uint_as_float(x[i + 1]), a.scale_log2, -lse2));
+          pk[i / 2] = pack_bf16(p0, p1);
+        }
+      } else {
+        const uint32_t* pw = reinterpret_cast<const uint32_t*>(pn);
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) {
+          const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pw[i / 2]));
+          pk[i / 2] = pack_bf16(a.scale * p.x * (__uint_as_float(x[i]) - dl),
+                                a.scale * p.y * (__uint_as_float(x[i + 1]) - dl));
+        }
       }
-      uint4* pd = reinterpret_cast<uint4*>(prow + j * PB_N);
-      uint4* dd = reinterpret_cast<uint4*>(dsrow + j * PB_N);
+      uint4* dst = reinterpret_cast<uint4*>((DS ? dsrow : prow) + j * SP_N);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        pd[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        dd[c] = make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
+      for (int c = 0; c < 8; ++c) dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      if (DS && j + 1 < ntiles) {
+        // P of the next tile: in flight while that tile's dP is computed
+#pragma unroll
+        for (int c = 0; c < 8; ++c) pn[c] = reinterpret_cast<const uint4*>(prow + (j + 1) * SP_N)[c];
       }
     }
     if (!ok) *abort_flag = 1;
-    // zero the padding slots [ntiles * 32, kp)
-    for (int c = ntiles * PB_N; c < a.kp; c += 8) {
-      *reinterpret_cast<uint4*>(prow + c) = make_uint4(0u, 0u, 0u, 0u);
-      *reinterpret_cast<uint4*>(dsrow + c) = make_uint4(0u, 0u, 0u, 0u);
-    }
+    // zero the padding slots [ntiles * 64, kp)
+    __nv_bfloat16* orow = DS ? dsrow : prow;
+    for (int c = ntiles * SP_N; c < a.kp; c += 8) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0u, 0u, 0u, 0u);
   }
 
   tc::fence_before_sync();
@@ -354,35 +378,42 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       if (!ok) *abort_flag = 1;
     }
   } else {
-    // ------------------------------------------------------------ gather (256 threads): 64 rows x 4 parts
-    const int pt = warp < 4 ? tid : tid - 32;
-    const int row = pt >> 2, part = pt & 3;
-    if (pt == 0) tc::prefetch_tmap(&tm_ds);
-    const int per = nblk * 2;  // 16-byte chunks per part (8 or 10)
+    // ------------------------------------------------------------ gather (8 warps)
+    // Warp g (0..7 over warps 0-3, 5-8) copies rows 8g .. 8g+7 of each 64-row
+    // tile; lane l copies the 16-byte chunks l, l+32 of the row's channel
+    // slice, so one instruction covers up to 512 contiguous bytes.
+    const int g = warp < 4 ? warp : warp - 1;
+    const int w8 = g * 8;
+    const int nchunk = nch / 8;  // 32 or 40
     const char* kvb = reinterpret_cast<const char*>(a.kv);
     bool ok = true;
-    int id_next = row < a.topk ? __ldg(idx_row + row) : -1;
+    if (tid == 0) tc::prefetch_tmap(&tm_ds);
+    int id_next = (lane < 8 && w8 + lane < a.topk) ? __ldg(idx_row + w8 + lane) : -1;
     for (int j = 0; j < ntiles; ++j) {
       const int st = j % DQ_STAGES;
-      const int id = id_next;
-      const int slot_next = (j + 1) * DQ_N + row;
-      id_next = slot_next < a.topk ? __ldg(idx_row + slot_next) : -1;
+      const int id_mine = id_next;
+      const int slot_next = (j + 1) * DQ_N + w8 + lane;
+      id_next = (lane < 8 && slot_next < a.topk) ? __ldg(idx_row + slot_next) : -1;
       if (!__all_sync(0xffffffffu, tc::mbar_wait(&sempty[st], ((j / DQ_STAGES) & 1) ^ 1u, abort_flag))) {
         ok = false;
         break;
       }
-      if (pt == 0) {
+      if (tid == 0) {
         // the dS tile of this stage (A operand) by TMA
         tc::mbar_arrive_expect_tx(&afull[st], DQ_A);
         tc::tma_load_2d(base + st * DQ_STAGE, &tm_ds, &afull[st], j * DQ_N, lq * PB_H);
       }
-      const bool valid = id >= 0 && id < n;
-      const char* src_row = kvb + ((int64_t)(valid ? s0 + id : 0) * D + ch0) * 2;
-      const uint32_t dst = base + st * DQ_STAGE + DQ_A + row * 128;
-      for (int q = 0; q < per; ++q) {
-        const int c16 = part * per + q;
-        const int cb = c16 >> 3, jj = c16 & 7;
-        cp_async16(dst + cb * DQ_BBLK + ((jj ^ (row & 7)) << 4), src_row + c16 * 16, valid ? 16u : 0u);
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const int id = __shfl_sync(0xffffffffu, id_mine, r);
+        const int row = w8 + r;
+        const bool valid = id >= 0 && id < n;
+        const char* src_row = kvb + ((int64_t)(valid ? s0 + id : 0) * D + ch0) * 2;
+        const uint32_t dst = base + st * DQ_STAGE + DQ_A + row * 128;
+        for (int c16 = lane; c16 < nchunk; c16 += 32) {
+          const int cb = c16 >> 3, jj = c16 & 7;
+          cp_async16(dst + cb * DQ_BBLK + ((jj ^ (row & 7)) << 4), src_row + c16 * 16, valid ? 16u : 0u);
+        }
       }
       cp_async_commit();
       asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&bfull[st]))
@@ -426,17 +457,13 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   }
 }
 
-template <int D>
-static cudaError_t launch_pds_t(const MlaBwdArgs& a, int nq, cudaStream_t stream) {
-  CUtensorMap tdo;
-  cudaError_t e = make_tmap_bf16_2d(&tdo, a.dout, (uint64_t)a.T * PB_H, 512, PB_H, 64);
-  if (e != cudaSuccess) return e;
-  constexpr int smem = PbLayout<D>::SMEM;
+template <int D, bool DS>
+static cudaError_t launch_sp_t(const MlaBwdArgs& a, int nq, cudaStream_t stream) {
+  constexpr int smem = sp_smem<D, DS>();
   static_assert(smem <= 227 * 1024, "shared memory budget");
-  if ((e = cudaFuncSetAttribute(mla_bwd_pds_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
-      cudaSuccess)
-    return e;
-  mla_bwd_pds_tc_kernel<D><<<dim3(nq), PB_THREADS, smem, stream>>>(tdo, a);
+  cudaError_t e = cudaFuncSetAttribute(mla_bwd_sp_tc_kernel<D, DS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  mla_bwd_sp_tc_kernel<D, DS><<<dim3(nq), SP_THREADS, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -456,7 +483,9 @@ static cudaError_t launch_dq_t(const MlaBwdArgs& a, int nq, cudaStream_t stream)
 cudaError_t launch_mla_bwd_pds_tc(const MlaBwdArgs& a, int D, int nq, cudaStream_t stream) {
   if (nq <= 0) return cudaSuccess;
   if (a.H != PB_H || a.kp % 128 != 0 || a.p_out == nullptr || a.ds_out == nullptr) return cudaErrorInvalidValue;
-  return D == 576 ? launch_pds_t<576>(a, nq, stream) : launch_pds_t<512>(a, nq, stream);
+  cudaError_t e = D == 576 ? launch_sp_t<576, false>(a, nq, stream) : launch_sp_t<512, false>(a, nq, stream);
+  if (e != cudaSuccess) return e;
+  return D == 576 ? launch_sp_t<576, true>(a, nq, stream) : launch_sp_t<512, true>(a, nq, stream);
 }
 
 cudaError_t launch_mla_bwd_dq_tc(const MlaBwdArgs& a, int D, int nq, cudaStream_t stream) {

@@ -19,7 +19,8 @@
 // The q / dO blocks are the fixed A operand (MN-major, loaded once by TMA);
 // the dS / P tiles stream through a two-stage TMA pipeline as the MN-major B
 // operand; the accumulator is double-buffered in TMEM so that the drain of
-// tile j overlaps the MMAs of tile j+1.  All 128 heads are summed before the
+// tile j overlaps the MMAs of tile j+1.  Eight drain warps (two per TMEM lane
+// quadrant) keep enough reductions in flight.  All 128 heads are summed before the
 // scatter, so each selected row receives one reduction per query.
 #include "kernels.cuh"
 #include "tc.cuh"
@@ -34,7 +35,8 @@ namespace {
 constexpr int BH = 128;           // heads = MMA K of this GEMM
 constexpr int DK_NS = 128;        // slots per tile (MMA N)
 constexpr int DK_STAGES = 2;
-constexpr int DK_THREADS = 192;   // warps 0-3 drain, warp 4 TMA producer, warp 5 MMA
+constexpr int DK_THREADS = 320;   // warps 0-7 drain, warp 8 TMA producer, warp 9 MMA
+constexpr int DK_DRAIN = 8;       // drain warps: TMEM lane quadrant w % 4, slot half w / 4
 constexpr int DK_BOX = BH * 128;  // one 64-column box of 128 rows: 16 KB
 constexpr int DK_A = 2 * DK_BOX;  // one 128-channel A block (q or dO): 32 KB
 constexpr int DK_B = 2 * DK_BOX;  // one 128-slot B tile (dS or P): 32 KB
@@ -43,7 +45,7 @@ constexpr int DK_OFF_AQ = 0;
 constexpr int DK_OFF_AO = DK_OFF_AQ + DK_A;
 constexpr int DK_OFF_B = DK_OFF_AO + DK_A;
 constexpr int DK_OFF_X = DK_OFF_B + DK_STAGES * 2 * DK_B;
-constexpr int DK_OFF_BAR = DK_OFF_X + 4 * DK_XP;
+constexpr int DK_OFF_BAR = DK_OFF_X + DK_DRAIN * DK_XP;
 constexpr int DK_SMEM = 1024 + DK_OFF_BAR + 256;
 static_assert(DK_SMEM <= 227 * 1024, "dKV kernel shared memory");
 
@@ -89,7 +91,7 @@ __global__ void __launch_bounds__(DK_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&dfull[i], 1);
-      tc::mbar_init(&dempty[i], 4);
+      tc::mbar_init(&dempty[i], DK_DRAIN);
     }
     *abort_flag = 0;
     tc::fence_barrier_init();
@@ -100,13 +102,13 @@ __global__ void __launch_bounds__(DK_THREADS, 1)
     for (int i = tid; i < DK_BOX / 16; i += DK_THREADS) z[i] = make_uint4(0u, 0u, 0u, 0u);
     tc::fence_proxy_async_smem();
   }
-  if (warp == 5) tc::tmem_alloc(tmem_slot, 256);
+  if (warp == 9) tc::tmem_alloc(tmem_slot, 256);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == 8) {
     if (lane == 0) {
       const uint32_t sAq = base + DK_OFF_AQ, sAo = base + DK_OFF_AO;
       const int qboxes = nch / 64;
@@ -128,7 +130,7 @@ __global__ void __launch_bounds__(DK_THREADS, 1)
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     if (lane == 0) {
       // A (q / dO block, channels contiguous) and B (dS / P tile, slots contiguous) are both MN-major.
       const uint32_t idesc = tc::idesc_bf16_f32(128, DK_NS) | (1u << 15) | (1u << 16);
@@ -160,34 +162,44 @@ __global__ void __launch_bounds__(DK_THREADS, 1)
       if (!ok) *abort_flag = 1;
     }
   } else {
-    // ------------------------------------------------------------ drain: warp w = channels 32w..32w+31
+    // ------------------------------------------------------------ drain
+    // warp w: channels 32 (w % 4) .. +31 (its TMEM lane quadrant), slots
+    // 64 (w / 4) .. +63 of each tile, in two pieces of 32.  The slot rows of
+    // the next tile are loaded while this one drains.
+    const int qd = warp & 3, hf = warp >> 2;
     const int sq = seq_of(a.st, t);
     const int s0 = a.st.cu[sq];
     const int n = a.st.cu[sq + 1] - s0;
     const int* idx_row = a.idx + (int64_t)t * a.topk;
     float* xb = reinterpret_cast<float*>(gbase + DK_OFF_X + warp * DK_XP);  // [32 slots][32 channels]
-    const bool live = warp * 32 < nch;
+    const bool live = qd * 32 < nch;
     const int cq = (lane & 7) * 4;  // this lane's 4 channels within the warp's 32 in the scatter
-    float* dkv_base = a.dkv_acc + ch0 + warp * 32 + cq;
+    float* dkv_base = a.dkv_acc + ch0 + qd * 32 + cq;
+    auto rows_of = [&](int j, int pc) -> int {
+      const int slot = j * DK_NS + hf * 64 + pc * 32 + lane;
+      if (slot >= a.topk) return -1;
+      const int id = __ldg(idx_row + slot);
+      return (id >= 0 && id < n) ? s0 + id : -1;
+    };
+    int nx0 = live ? rows_of(0, 0) : -1, nx1 = live ? rows_of(0, 1) : -1;
     for (int j = 0; j < ntiles; ++j) {
       const int acc = j & 1;
+      const int my0 = nx0, my1 = nx1;
+      if (live && j + 1 < ntiles) {
+        nx0 = rows_of(j + 1, 0);
+        nx1 = rows_of(j + 1, 1);
+      }
       if (!__all_sync(0xffffffffu, tc::mbar_wait(&dfull[acc], (j >> 1) & 1, abort_flag))) {
         *abort_flag = 1;
         break;
       }
       tc::fence_after_sync();
       if (live) {
-#pragma unroll 1
-        for (int pc = 0; pc < DK_NS / 32; ++pc) {
-          const int sbase = j * DK_NS + pc * 32;
-          // this lane's slot row (for the shuffles below): local row of the slot sbase + lane
-          int my = -1;
-          if (sbase + lane < a.topk) {
-            const int id = __ldg(idx_row + sbase + lane);
-            if (id >= 0 && id < n) my = s0 + id;
-          }
+#pragma unroll
+        for (int pc = 0; pc < 2; ++pc) {
+          const int my = pc == 0 ? my0 : my1;
           uint32_t r[32];
-          tc::tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + acc * DK_NS + pc * 32, r);
+          tc::tmem_ld32(tmem + (static_cast<uint32_t>(qd * 32) << 16) + acc * DK_NS + hf * 64 + pc * 32, r);
           tc::tmem_ld_wait();
           // transpose through shared memory: xb[slot][channel]
 #pragma unroll
@@ -211,7 +223,7 @@ __global__ void __launch_bounds__(DK_THREADS, 1)
   tc::fence_before_sync();
   __syncthreads();
   if (*abort_flag && tid == 0) raise_flag(a.flags, TSA_FLAG_TIMEOUT);
-  if (warp == 5) {
+  if (warp == 9) {
     __syncwarp();
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, 256);

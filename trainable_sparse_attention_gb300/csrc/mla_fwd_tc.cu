@@ -134,47 +134,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp >= 5) {
-    // ------------------------------------------------------------ gather producers (128 threads)
-    // 32 rows x 4 parts: each thread copies kb*2 16-byte chunks of one selected
-    // row straight into the 128-byte-swizzled K-major tile (cp.async).  Each
-    // thread's copies arrive on the stage's barrier asynchronously when they
-    // land (cp.async.mbarrier.arrive.noinc), so the producers never wait on
-    // their own copies: every free stage holds a tile in flight.  The MMA
-    // thread orders the landed data for the tensor cores with a proxy fence.
-    // The index of the next tile is loaded one iteration ahead.
-    const int pt = tid - 160;
-    const int row = pt >> 2, part = pt & 3;
-    const int per = kb * 2;
+    // ------------------------------------------------------------ gather producers (4 warps)
+    // Warp w copies rows 8w .. 8w+7 of each 32-row tile; lane l copies the
+    // 16-byte chunks l, l+32 of the row's channel slice, so one instruction
+    // covers up to 512 contiguous bytes of the row.  The chunks land in the
+    // 128-byte-swizzled K-major tile; each thread's copies arrive on the
+    // stage's barrier asynchronously when they land
+    // (cp.async.mbarrier.arrive.noinc), so the producers never wait on their
+    // own copies: every free stage holds a tile in flight.  The MMA thread
+    // orders the landed data for the tensor cores with a proxy fence.  The
+    // slot indices of the next tile are loaded one tile ahead (lane r < 8
+    // holds row 8w + r).
+    const int w8 = (warp - 5) * 8;
+    const int nchunk = kb * 8;  // 32 or 40
     const char* kvb = reinterpret_cast<const char*>(a.kv);
     bool ok = true;
-    int id_next = row < a.topk ? __ldg(idx_row + row) : -1;
+    int id_next = (lane < 8 && w8 + lane < a.topk) ? __ldg(idx_row + w8 + lane) : -1;
     for (int j = 0; j < ntiles; ++j) {
       const int st = j % MT_STAGES;
-      const int id = id_next;
-      const int slot_next = (j + 1) * MT_N + row;
-      id_next = slot_next < a.topk ? __ldg(idx_row + slot_next) : -1;
+      const int id_mine = id_next;
+      const int slot_next = (j + 1) * MT_N + w8 + lane;
+      id_next = (lane < 8 && slot_next < a.topk) ? __ldg(idx_row + slot_next) : -1;
       if (!__all_sync(0xffffffffu, tc::mbar_wait(&kv_empty[st], ((j / MT_STAGES) & 1) ^ 1u, abort_flag))) {
         ok = false;
         break;
       }
-      const bool valid = id >= 0 && id < n;
-      if (part == 0 && id >= n) raise_flag(a.flags, TSA_FLAG_INDEX_RANGE);
-      const char* src_row = kvb + ((int64_t)(valid ? s0 + id : 0) * D + ch0) * 2;
-      const uint32_t dst = sKV + st * L::KV_STAGE + row * 128;
-      for (int q = 0; q < per; ++q) {
-        const int c16 = part * per + q;
-        const int cb = c16 >> 3, jj = c16 & 7;
-        cp_async16(dst + cb * L::KV_BLOCK + ((jj ^ (row & 7)) << 4), src_row + c16 * 16, valid ? 16u : 0u);
+      if (lane < 8 && id_mine >= n) raise_flag(a.flags, TSA_FLAG_INDEX_RANGE);
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const int id = __shfl_sync(0xffffffffu, id_mine, r);
+        const int row = w8 + r;
+        const bool valid = id >= 0 && id < n;
+        const char* src_row = kvb + ((int64_t)(valid ? s0 + id : 0) * D + ch0) * 2;
+        const uint32_t dst = sKV + st * L::KV_STAGE + row * 128;
+        for (int c16 = lane; c16 < nchunk; c16 += 32) {
+          const int cb = c16 >> 3, jj = c16 & 7;
+          cp_async16(dst + cb * L::KV_BLOCK + ((jj ^ (row & 7)) << 4), src_row + c16 * 16, valid ? 16u : 0u);
+        }
       }
       cp_async_commit();
       asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&kv_full[st]))
                    : "memory");
-      // valid-slot bits: lanes with part == 0 hold rows 8*(warp-5) + lane/4
-      const uint32_t bal = __ballot_sync(0xffffffffu, part == 0 && valid);
+      // valid-slot bits of this warp's 8 rows: byte w of the stage's mask word
+      const uint32_t bal = __ballot_sync(0xffffffffu, lane < 8 && id_mine >= 0 && id_mine < n);
       if (lane == 0) {
-        uint32_t byte = 0;
-        for (int r8 = 0; r8 < 8; ++r8) byte |= ((bal >> (4 * r8)) & 1u) << r8;
-        reinterpret_cast<volatile unsigned char*>(&masks[st])[warp - 5] = static_cast<unsigned char>(byte);
+        reinterpret_cast<volatile unsigned char*>(&masks[st])[warp - 5] = static_cast<unsigned char>(bal & 0xffu);
         tc::mbar_arrive(&mask_full[st]);
       }
     }
