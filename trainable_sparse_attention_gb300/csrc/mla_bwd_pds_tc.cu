@@ -50,13 +50,15 @@ constexpr int SP_PRODUCERS = 256;
 constexpr int SP_THREADS = 160 + SP_PRODUCERS;  // warps 0-3 epilogue, warp 4 MMA, warps 5-12 gather
 constexpr int SP_ACC = 288;      // first TMEM column of the two accumulators (after the A operand)
 
+constexpr int SP_PTILE = SP_H * 128;  // one P tile of the dS pass: 128 heads x 64 slots bf16
+
 template <int D, bool DS>
 constexpr int sp_smem() {
-  return 1024 + SP_STAGES * ((DS ? 512 : D) / 64) * (SP_N * 128) + 256;
+  return 1024 + SP_STAGES * ((DS ? 512 : D) / 64) * (SP_N * 128) + (DS ? 2 * SP_PTILE : 0) + 256;
 }
 
 constexpr int DQ_N = 64;          // slots per tile (MMA K per tile)
-constexpr int DQ_STAGES = 3;
+constexpr int DQ_STAGES = 4;
 constexpr int DQ_THREADS = 288;   // warps 0-3 and 5-8 gather (thread 0 also loads the dS tiles, 0-3 drain dQ), warp 4 MMA
 constexpr int DQ_A = PB_H * 128;  // dS tile: 128 rows x 64 slots bf16 = 16 KB
 constexpr int DQ_BBLK = DQ_N * 128;  // 64 channels x 64 slots = 8 KB
@@ -79,24 +81,27 @@ __device__ __forceinline__ float ex2(float x) {
 //             reads P, writes dS = scale P (dP - Dlt).
 template <int D, bool DS>
 __global__ void __launch_bounds__(SP_THREADS, 1)
-    mla_bwd_sp_tc_kernel(const __grid_constant__ MlaBwdArgs a) {
+    mla_bwd_sp_tc_kernel(const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ MlaBwdArgs a) {
   constexpr int KC = DS ? 512 : D;   // channels of the contraction
   constexpr int KB = KC / 64;        // 64-channel blocks of a gathered row
   constexpr int ACOLS = KC / 2;      // TMEM columns of the A operand (bf16 pairs)
   constexpr int KV_BLOCK = SP_N * 128;
   constexpr int KV_STAGE = KB * KV_BLOCK;
-  constexpr int OFF_BAR = SP_STAGES * KV_STAGE;
+  constexpr int OFF_P = SP_STAGES * KV_STAGE;            // dS pass: two P tiles (TMA, 128-byte swizzle)
+  constexpr int OFF_BAR = OFF_P + (DS ? 2 * SP_PTILE : 0);
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* gbase = smem_raw + (base - raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + OFF_BAR);
-  uint64_t* aready = bars;                      // [1] A rows stored into TMEM (4 warps)
+  uint64_t* aready = bars;                      // [1] A rows stored into TMEM (12 warps)
   uint64_t* kv_full = bars + 1;                 // [STAGES] asynchronous producer arrivals
   uint64_t* kv_empty = kv_full + SP_STAGES;     // [STAGES]
   uint64_t* acc_full = kv_empty + SP_STAGES;    // [2] a tile's S (or dP) in TMEM
   uint64_t* acc_empty = acc_full + 2;           // [2] (4 warps)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint64_t* pfull = acc_empty + 2;              // [2] dS pass: P tile landed (TMA)
+  uint64_t* pempty = pfull + 2;                 // [2] dS pass: P tile read (4 warps)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int lq = blockIdx.x;
@@ -109,7 +114,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    tc::mbar_init(aready, 4);
+    tc::mbar_init(aready, 12);
     for (int i = 0; i < SP_STAGES; ++i) {
       tc::mbar_init(&kv_full[i], SP_PRODUCERS);
       tc::mbar_init(&kv_empty[i], 1);
@@ -117,6 +122,8 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&acc_full[i], 1);
       tc::mbar_init(&acc_empty[i], 4);
+      tc::mbar_init(&pfull[i], 1);
+      tc::mbar_init(&pempty[i], 4);
     }
     *abort_flag = 0;
     tc::fence_barrier_init();
@@ -126,6 +133,33 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+
+  // A rows -> TMEM columns [0, KC/2), 32 columns (64 channels) per store.  The
+  // three warps that share a TMEM lane quadrant (epilogue warp w, producer
+  // warps w+4 / w+8 with w+4 taken mod 4) split the KB blocks of their 32 rows.
+  auto load_a_rows = [&](int share) {
+    const int h = (warp & 3) * 32 + lane;
+    const uint4* arow = DS ? reinterpret_cast<const uint4*>(a.dout + ((int64_t)t * SP_H + h) * 512)
+                           : reinterpret_cast<const uint4*>(a.q + ((int64_t)t * SP_H + h) * D);
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    for (int c = share; c < KB; c += 3) {
+      uint32_t r[32];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 v = __ldg(arow + c * 8 + i);
+        r[4 * i] = v.x;
+        r[4 * i + 1] = v.y;
+        r[4 * i + 2] = v.z;
+        r[4 * i + 3] = v.w;
+      }
+      __syncwarp();
+      tc::tmem_st32(tmem + lane_base + c * 32, r);
+    }
+    tc::tmem_st_wait();
+    tc::fence_before_sync();
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(aready);
+  };
 
   if (warp >= 5) {
     // ------------------------------------------------------------ gather producers (8 warps)
@@ -139,6 +173,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
     constexpr int NCH = KC / 8;  // 16-byte chunks per row
     const char* kvb = reinterpret_cast<const char*>(a.kv);
     bool ok = true;
+    const int npre = ntiles < SP_STAGES ? ntiles : SP_STAGES;
     int id_next = (lane < 8 && w8 + lane < a.topk) ? __ldg(idx_row + w8 + lane) : -1;
     for (int j = 0; j < ntiles; ++j) {
       const int st = j % SP_STAGES;
@@ -166,6 +201,8 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
       cp_async_commit();
       asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&kv_full[st]))
                    : "memory");
+      // the first tiles are in flight: help load the A rows
+      if (j == npre - 1) load_a_rows(warp < 9 ? 1 : 2);
     }
     cp_async_wait<0>();
     if (!ok) *abort_flag = 1;
@@ -206,38 +243,21 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
     const float lse2 = Lh * kLog2e;
     const bool live = Lh != NEG_INF;  // a row without valid slots has P = dS = 0
     const float dl = DS ? a.dlt[(int64_t)t * SP_H + h] : 0.f;
-    // A row h -> TMEM columns [0, KC/2): 32 columns (64 channels) per store
-    {
-      const uint4* arow = DS ? reinterpret_cast<const uint4*>(a.dout + ((int64_t)t * SP_H + h) * 512)
-                             : reinterpret_cast<const uint4*>(a.q + ((int64_t)t * SP_H + h) * D);
-      for (int c = 0; c < KB; ++c) {
-        uint32_t r[32];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 v = __ldg(arow + c * 8 + i);
-          r[4 * i] = v.x;
-          r[4 * i + 1] = v.y;
-          r[4 * i + 2] = v.z;
-          r[4 * i + 3] = v.w;
-        }
-        __syncwarp();
-        tc::tmem_st32(tmem + lane_base + c * 32, r);
-      }
-      tc::tmem_st_wait();
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(aready);
-    }
+    load_a_rows(0);
     static_assert(ACOLS <= SP_ACC, "A operand overlaps the accumulators");
     __nv_bfloat16* prow = a.p_out + ((int64_t)lq * SP_H + h) * a.kp;
     __nv_bfloat16* dsrow = a.ds_out + ((int64_t)lq * SP_H + h) * a.kp;
     bool ok = true;
     int idn0 = lane < a.topk ? __ldg(idx_row + lane) : -1;
     int idn1 = 32 + lane < a.topk ? __ldg(idx_row + 32 + lane) : -1;
-    uint4 pn[8];
-    if (DS) {
-#pragma unroll
-      for (int c = 0; c < 8; ++c) pn[c] = reinterpret_cast<const uint4*>(prow)[c];
+    if (DS && tid == 0) {
+      // P tiles 0 and 1 (TMA); later tiles are issued as the ring frees up
+      tc::prefetch_tmap(&tm_p);
+      for (int jj = 0; jj < 2 && jj < ntiles; ++jj) {
+        tc::mbar_arrive_expect_tx(&pfull[jj], SP_PTILE);
+        tc::tma_load_2d_hint(base + OFF_P + jj * SP_PTILE, &tm_p, &pfull[jj], jj * SP_N, lq * SP_H,
+                             tc::policy_evict_first());
+      }
     }
     for (int j = 0; j < ntiles; ++j) {
       const int b = j & 1;
@@ -271,6 +291,27 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
           pk[i / 2] = pack_bf16(p0, p1);
         }
       } else {
+        // P row h of this tile from the TMA ring (128-byte swizzled rows)
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(&pfull[b], (j >> 1) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        uint4 pn[8];
+        const unsigned char* ps = gbase + OFF_P + b * SP_PTILE + h * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) pn[c] = *reinterpret_cast<const uint4*>(ps + ((c ^ (h & 7)) << 4));
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&pempty[b]);
+        if (tid == 0 && j + 2 < ntiles) {
+          // refill this slot with tile j+2 once all four warps have read tile j
+          if (tc::mbar_wait(&pempty[b], (j >> 1) & 1, abort_flag)) {
+            tc::mbar_arrive_expect_tx(&pfull[b], SP_PTILE);
+            tc::tma_load_2d_hint(base + OFF_P + b * SP_PTILE, &tm_p, &pfull[b], (j + 2) * SP_N, lq * SP_H,
+                                 tc::policy_evict_first());
+          } else {
+            *abort_flag = 1;
+          }
+        }
         const uint32_t* pw = reinterpret_cast<const uint32_t*>(pn);
 #pragma unroll
         for (int i = 0; i < 64; i += 2) {
@@ -279,14 +320,10 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
                                 a.scale * p.y * (__uint_as_float(x[i + 1]) - dl));
         }
       }
+      // streaming stores (evict-first in L2): read back once per consumer
       uint4* dst = reinterpret_cast<uint4*>((DS ? dsrow : prow) + j * SP_N);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      if (DS && j + 1 < ntiles) {
-        // P of the next tile: in flight while that tile's dP is computed
-#pragma unroll
-        for (int c = 0; c < 8; ++c) pn[c] = reinterpret_cast<const uint4*>(prow + (j + 1) * SP_N)[c];
-      }
+      for (int c = 0; c < 8; ++c) __stcs(dst + c, make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
     }
     if (!ok) *abort_flag = 1;
     // zero the padding slots [ntiles * 64, kp)
@@ -401,7 +438,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       if (tid == 0) {
         // the dS tile of this stage (A operand) by TMA
         tc::mbar_arrive_expect_tx(&afull[st], DQ_A);
-        tc::tma_load_2d(base + st * DQ_STAGE, &tm_ds, &afull[st], j * DQ_N, lq * PB_H);
+        tc::tma_load_2d_hint(base + st * DQ_STAGE, &tm_ds, &afull[st], j * DQ_N, lq * PB_H, tc::policy_evict_first());
       }
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
@@ -461,9 +498,12 @@ template <int D, bool DS>
 static cudaError_t launch_sp_t(const MlaBwdArgs& a, int nq, cudaStream_t stream) {
   constexpr int smem = sp_smem<D, DS>();
   static_assert(smem <= 227 * 1024, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(mla_bwd_sp_tc_kernel<D, DS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  CUtensorMap tp;
+  cudaError_t e = make_tmap_bf16_2d(&tp, a.p_out, (uint64_t)nq * SP_H, a.kp, SP_H, 64);
   if (e != cudaSuccess) return e;
-  mla_bwd_sp_tc_kernel<D, DS><<<dim3(nq), SP_THREADS, smem, stream>>>(a);
+  e = cudaFuncSetAttribute(mla_bwd_sp_tc_kernel<D, DS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  mla_bwd_sp_tc_kernel<D, DS><<<dim3(nq), SP_THREADS, smem, stream>>>(tp, a);
   return cudaGetLastError();
 }
 

@@ -124,9 +124,11 @@ __global__ void __launch_bounds__(DK_THREADS, 1)
         }
         tc::mbar_arrive_expect_tx(&bfull[st], (has_v ? 2 : 1) * DK_B);
         const uint32_t dst = base + DK_OFF_B + st * 2 * DK_B;
+        const uint64_t pol = tc::policy_evict_first();  // P / dS tiles: read by this query's CTAs only
         for (int c = 0; c < 2; ++c) {
-          tc::tma_load_2d(dst + c * DK_BOX, &tm_ds, &bfull[st], j * DK_NS + c * 64, lq * BH);
-          if (has_v) tc::tma_load_2d(dst + DK_B + c * DK_BOX, &tm_p, &bfull[st], j * DK_NS + c * 64, lq * BH);
+          tc::tma_load_2d_hint(dst + c * DK_BOX, &tm_ds, &bfull[st], j * DK_NS + c * 64, lq * BH, pol);
+          if (has_v)
+            tc::tma_load_2d_hint(dst + DK_B + c * DK_BOX, &tm_p, &bfull[st], j * DK_NS + c * 64, lq * BH, pol);
         }
       }
     }

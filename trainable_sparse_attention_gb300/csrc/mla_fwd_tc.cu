@@ -78,7 +78,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* gbase = smem_raw + (base - raw);
   const uint32_t sQ = base, sKV = base + L::OFF_KV, sP = base + L::OFF_P;
-  float* X = reinterpret_cast<float*>(gbase + L::OFF_X);  // [2][128][32] partial logits written by the peer
+  // [2][128][32] partial logits written by the peer; chunk q (4 floats) of row h
+  // sits at chunk q ^ (h & 7), so the 16-byte stores and loads of a warp spread
+  // over all banks
+  float* X = reinterpret_cast<float*>(gbase + L::OFF_X);
   uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + L::OFF_BAR);
   uint64_t* qfull = bars;
   uint64_t* kv_full = bars + 1;                       // [STAGES]
@@ -267,7 +270,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
         const float4* xr = reinterpret_cast<const float4*>(X + bb * (MT_H * MT_N) + h * MT_N);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          const float4 v = xr[q];
+          const float4 v = xr[q ^ (h & 7)];  // 16-byte chunks of a row are swizzled by the row
           x2[4 * q] = __uint_as_float(cur[4 * q]) + v.x;
           x2[4 * q + 1] = __uint_as_float(cur[4 * q + 1]) + v.y;
           x2[4 * q + 2] = __uint_as_float(cur[4 * q + 2]) + v.z;
@@ -285,7 +288,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
         const uint32_t rbar = peer_xfull + b * 8;
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-          tc::st_async_v4(dst + q * 16, rbar, __uint_as_float(nxt[4 * q]), __uint_as_float(nxt[4 * q + 1]),
+          tc::st_async_v4(dst + ((q ^ (h & 7)) << 4), rbar, __uint_as_float(nxt[4 * q]), __uint_as_float(nxt[4 * q + 1]),
                           __uint_as_float(nxt[4 * q + 2]), __uint_as_float(nxt[4 * q + 3]));
       }
       if (j > 0) {
