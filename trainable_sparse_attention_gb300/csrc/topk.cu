@@ -13,8 +13,8 @@
 //  * rows of <= 4096 entries: bitonic sort of all composite keys in shared memory;
 //  * longer rows: three histogram passes (11+11+10 bits) find the k-th largest
 //    u = tau; one ordered pass then keeps every u > tau and the lowest-index
-//    (k - count(u > tau)) entries with u == tau, using warp ballots and a block
-//    prefix sum in index order; the k survivors are bitonic-sorted.
+//    (k - count(u > tau)) entries with u == tau, ranked by a block prefix sum
+//    in index order; the k survivors are bitonic-sorted.
 #include "kernels.cuh"
 
 namespace tsa {
@@ -24,6 +24,7 @@ constexpr int TK_WARPS = TK_THREADS / 32;
 constexpr int TK_SMALL = 4096;  // rows with at most this many entries are fully sorted
 constexpr int TK_MAXK = 4096;   // largest supported k
 constexpr int TK_BINS = 2048;
+constexpr int TK_PER = 8;       // consecutive entries per thread in the sweeps over long rows
 
 
 __device__ __forceinline__ uint32_t order_key(float s) {
@@ -122,7 +123,9 @@ __global__ void __launch_bounds__(TK_THREADS) topk_rows_kernel(TopkRows a) {
     return;
   }
 
-  // ---- radix select of the k-th largest u (three passes over the row)
+  // ---- radix select of the k-th largest u (three passes over the row).  Each
+  // thread takes TK_PER consecutive entries per sweep, so their loads are in
+  // flight together.
   const int shifts[3] = {21, 10, 0};
   const int nbits[3] = {11, 11, 10};
   uint32_t prefix = 0, above_total = 0, kk = static_cast<uint32_t>(k);
@@ -132,11 +135,17 @@ __global__ void __launch_bounds__(TK_THREADS) topk_rows_kernel(TopkRows a) {
     for (int i = threadIdx.x; i < TK_BINS; i += blockDim.x) hist[i] = 0;
     __syncthreads();
     const int sh_pref = shifts[pass] + nbits[pass];  // bits above this pass
-    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
-      float s = row[i];
-      if (s == NEG_INF) continue;
-      uint32_t u = order_key(s);
-      if (pass == 0 || (u >> sh_pref) == prefix) atomicAdd(&hist[(u >> shifts[pass]) & (nb - 1)], 1u);
+    for (int64_t base = 0; base < n; base += TK_PER * TK_THREADS) {
+      const int64_t i0 = base + static_cast<int64_t>(threadIdx.x) * TK_PER;
+      float v[TK_PER];
+#pragma unroll
+      for (int e = 0; e < TK_PER; ++e) v[e] = (i0 + e < n) ? row[i0 + e] : NEG_INF;
+#pragma unroll
+      for (int e = 0; e < TK_PER; ++e) {
+        if (v[e] == NEG_INF) continue;
+        const uint32_t u = order_key(v[e]);
+        if (pass == 0 || (u >> sh_pref) == prefix) atomicAdd(&hist[(u >> shifts[pass]) & (nb - 1)], 1u);
+      }
     }
     __syncthreads();
     find_bin(hist, nb == TK_BINS ? TK_BINS : nb, kk, warp_tot[0], sh);
@@ -154,37 +163,51 @@ __global__ void __launch_bounds__(TK_THREADS) topk_rows_kernel(TopkRows a) {
   const uint32_t c_gt = take_all ? 0u : above_total;
   const uint32_t need = take_all ? 0u : kk;  // how many u == tau to keep (lowest indices)
 
-  // ---- ordered selection pass
+  // ---- ordered selection pass: thread t holds entries [base + TK_PER t, +TK_PER),
+  // so thread order is index order; one block-wide exclusive scan of the
+  // per-thread counts ranks every kept entry.
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint32_t lt_mask = (1u << lane) - 1u;
   uint32_t base_gt = 0, base_eq = 0;
-  for (int64_t base = 0; base < n; base += blockDim.x) {
-    int64_t i = base + threadIdx.x;
-    uint32_t u = 0;
-    bool cand = false;
-    if (i < n) {
-      float s = row[i];
-      cand = s != NEG_INF;
-      if (cand) u = order_key(s);
+  for (int64_t base = 0; base < n; base += TK_PER * TK_THREADS) {
+    const int64_t i0 = base + static_cast<int64_t>(threadIdx.x) * TK_PER;
+    uint32_t uu[TK_PER];
+    uint32_t mgt = 0, meq = 0;
+#pragma unroll
+    for (int e = 0; e < TK_PER; ++e) {
+      const float s = (i0 + e < n) ? row[i0 + e] : NEG_INF;
+      const bool cand = s != NEG_INF;
+      const uint32_t u = cand ? order_key(s) : 0u;
+      uu[e] = u;
+      if (cand && u > tau) mgt |= 1u << e;
+      if (cand && !take_all && u == tau) meq |= 1u << e;
     }
-    bool gt = cand && u > tau;
-    bool eq = cand && !take_all && u == tau;
-    uint32_t bg = __ballot_sync(0xffffffffu, gt), be = __ballot_sync(0xffffffffu, eq);
-    if (lane == 0) { warp_tot[0][warp] = __popc(bg); warp_tot[1][warp] = __popc(be); }
+    // inclusive warp scans of the two counts, packed 16 + 16 bits (each <= 32 * TK_PER)
+    const uint32_t mine = (static_cast<uint32_t>(__popc(mgt)) << 16) | static_cast<uint32_t>(__popc(meq));
+    uint32_t x = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[0][warp] = x;
     __syncthreads();
-    uint32_t og = 0, oe = 0, tg = 0, te = 0;
+    uint32_t off = x - mine, tot = 0;
     for (int w = 0; w < TK_WARPS; ++w) {
-      uint32_t g = warp_tot[0][w], e = warp_tot[1][w];
-      if (w < warp) { og += g; oe += e; }
-      tg += g; te += e;
+      const uint32_t wt = warp_tot[0][w];
+      if (w < warp) off += wt;
+      tot += wt;
     }
-    if (gt) keys[base_gt + og + __popc(bg & lt_mask)] = comp_key(u, static_cast<uint32_t>(i));
-    if (eq) {
-      uint32_t rk = base_eq + oe + __popc(be & lt_mask);
-      if (rk < need) keys[c_gt + rk] = comp_key(u, static_cast<uint32_t>(i));
+    uint32_t og = base_gt + (off >> 16), oe = base_eq + (off & 0xffffu);
+#pragma unroll
+    for (int e = 0; e < TK_PER; ++e) {
+      if ((mgt >> e) & 1u) keys[og++] = comp_key(uu[e], static_cast<uint32_t>(i0 + e));
+      if ((meq >> e) & 1u) {
+        if (oe < need) keys[c_gt + oe] = comp_key(uu[e], static_cast<uint32_t>(i0 + e));
+        ++oe;
+      }
     }
-    base_gt += tg;
-    base_eq += te;
+    base_gt += tot >> 16;
+    base_eq += tot & 0xffffu;
     __syncthreads();
   }
   const int nsel = take_all ? static_cast<int>(base_gt) : k;
