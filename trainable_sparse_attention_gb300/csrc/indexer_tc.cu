@@ -7,19 +7,28 @@
 // scores, streaming bounded-memory runner) and Megatron-LM PR #3674 (fused
 // indexer forward + logits cleaning).
 //
-// One CTA owns QB = 256 / H_I consecutive queries (their q_I rows form the
-// MMA's B operand, N = 256 columns = (query, head)) and streams key tiles of
-// 128 keys (the A operand, M = 128) through a 4-stage TMA ring.  Keys sit on
-// TMEM lanes, so each epilogue thread owns one key and reduces the heads of a
-// group inside its own registers: ReLU, head weight and group sum never leave
-// the thread, and only causal scores are written ("cleaned" logits are never
+// A query block is QB = 256 / H_I consecutive queries: their q_I rows form the
+// MMA's B operand (N = 256 columns = (query, head)); key tiles of 128 keys (the
+// A operand, M = 128) stream through a 4-stage TMA ring.  Keys sit on TMEM
+// lanes, so each epilogue thread owns one key and reduces the heads of a group
+// inside its own registers: ReLU, head weight and group sum never leave the
+// thread, and only causal scores are written ("cleaned" logits are never
 // produced).  The 2 x 256-column TMEM accumulator is double-buffered so the
 // epilogue of tile i overlaps the MMAs of tile i+1.
+//
+// The kernel is persistent: one CTA per SM walks a contiguous share of the
+// launch's (query block, causal key tile) pairs, so TMEM allocation and
+// pipeline fill are paid once per SM rather than once per short work item.
+// When its share moves to the next query block, the new q_I block is loaded
+// as soon as the MMAs of the previous one are done, and the head weights go
+// to the other half of a double buffer.
 //
 // Warp roles (192 threads): warps 0-3 epilogue (TMEM lanes 0-127), warp 4 TMA
 // producer, warp 5 TMEM allocator + MMA issuer (one elected thread).  Every
 // wait is bounded; a timeout raises TSA_FLAG_TIMEOUT and the CTA winds down,
 // releasing its TMEM.
+#include <algorithm>
+
 #include "kernels.cuh"
 #include "tc.cuh"
 
@@ -30,7 +39,6 @@ namespace {
 constexpr int IT_M = 128;
 constexpr int IT_N = 256;
 constexpr int IT_STAGES = 4;
-constexpr int IT_KT_PER_CTA = 16;
 constexpr int IT_THREADS = 192;
 
 template <int DI>
@@ -38,17 +46,31 @@ struct ItLayout {
   static constexpr int KB = DI / 64;                    // 128-byte column blocks along d_I
   static constexpr int B_BYTES = KB * IT_N * 128;       // q_I block
   static constexpr int A_BYTES = KB * IT_M * 128;       // one key tile
-  static constexpr int USED = 1024 + B_BYTES + IT_STAGES * A_BYTES + IT_N * 4 + 256;
+  static constexpr int USED = 1024 + B_BYTES + IT_STAGES * A_BYTES + 2 * IT_N * 4 + 256;
   // at least 120 KB so that a single CTA (the only TMEM owner) fits on an SM
   static constexpr int SMEM = USED > 120 * 1024 ? USED : 120 * 1024;
 };
 
 }  // namespace
 
+// The work of one launch is the list of (query block, key tile) pairs, query
+// blocks of QB queries in order and, inside a block, its causal key tiles
+// 0 .. nkt(qb)-1.  CTA c of G takes the contiguous share [c W / G, (c+1) W / G)
+// of the W pairs; every role walks the same share with this iterator.
+struct ItWalk {
+  int qb, kt, nkt, tr;  // query block, key tile, key tiles of the block, block changes so far
+  bool first, last;     // first / last pair of its query block in this share
+};
+
+__device__ __forceinline__ int it_nkt(const IndexerArgs& a, int QB, int qb) {
+  const int qn = min(QB, a.nq - qb * QB);
+  return (a.p_begin + qb * QB + qn - 1) / IT_M + 1;
+}
+
 template <int DI, int HG>
 __global__ void __launch_bounds__(IT_THREADS, 1)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ IndexerArgs a) {
+                      const __grid_constant__ IndexerArgs a, int total) {
   using L = ItLayout<DI>;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -56,73 +78,140 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
   unsigned char* gbase = smem_raw + (base - raw);
   const uint32_t sB = base;
   const uint32_t sA = base + L::B_BYTES;
-  float* Ws = reinterpret_cast<float*>(gbase + L::B_BYTES + IT_STAGES * L::A_BYTES);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(Ws + IT_N);
-  uint64_t* full = bars;                       // [IT_STAGES]
+  float* Ws = reinterpret_cast<float*>(gbase + L::B_BYTES + IT_STAGES * L::A_BYTES);  // [2][IT_N]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(Ws + 2 * IT_N);
+  uint64_t* full = bars;                       // [IT_STAGES] key tile landed
   uint64_t* empty = bars + IT_STAGES;          // [IT_STAGES]
-  uint64_t* bfull = bars + 2 * IT_STAGES;      // [1]
-  uint64_t* accf = bars + 2 * IT_STAGES + 1;   // [2]
-  uint64_t* acce = bars + 2 * IT_STAGES + 3;   // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * IT_STAGES + 5);
+  uint64_t* bfull = empty + IT_STAGES;         // [1] q_I block landed (one phase per block change)
+  uint64_t* bempty = bfull + 1;                // [1] MMAs of the previous block done
+  uint64_t* accf = bempty + 1;                 // [2]
+  uint64_t* acce = accf + 2;                   // [2]
+  uint64_t* wsfull = acce + 2;                 // [2] head weights of a block written (32 lanes)
+  uint64_t* wsempty = wsfull + 2;              // [2] epilogue done with a weight buffer (4 warps)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wsempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int H_I = a.H_I;
   const int QB = IT_N / H_I;
-  const int q0 = blockIdx.y * QB;
-  const int qn = min(QB, a.nq - q0);
-  const int p_first = a.p_begin + q0;
-  const int p_last = p_first + qn - 1;
-  const int kt0 = blockIdx.x * IT_KT_PER_CTA;
-  if (kt0 * IT_M > p_last) return;  // uniform: nothing causal for this CTA
-  const int ntiles = min(kt0 + IT_KT_PER_CTA, p_last / IT_M + 1) - kt0;
-
+  const int nqb = (a.nq + QB - 1) / QB;
+  const int w0 = static_cast<int>((static_cast<int64_t>(total) * blockIdx.x) / gridDim.x);
+  const int w1 = static_cast<int>((static_cast<int64_t>(total) * (blockIdx.x + 1)) / gridDim.x);
+  const int nitems = w1 - w0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (nitems <= 0) return;  // uniform
+
+  // start of the share: (qb, kt) of pair w0
+  ItWalk start;
+  {
+    int qb = 0, acc = 0, nk = it_nkt(a, QB, 0);
+    while (qb + 1 < nqb && acc + nk <= w0) {
+      acc += nk;
+      ++qb;
+      nk = it_nkt(a, QB, qb);
+    }
+    start.qb = qb;
+    start.kt = w0 - acc;
+    start.nkt = nk;
+    start.tr = 0;
+    start.first = true;
+    start.last = (start.kt + 1 == nk) || nitems == 1;
+  }
+  auto advance = [&](ItWalk& w, int i) {  // w describes item i; move to item i+1
+    if (++w.kt == w.nkt) {
+      ++w.qb;
+      w.kt = 0;
+      w.nkt = it_nkt(a, QB, w.qb);
+      ++w.tr;
+      w.first = true;
+    } else {
+      w.first = false;
+    }
+    w.last = (w.kt + 1 == w.nkt) || (i + 2 == nitems);
+  };
+
   if (tid == 0) {
     for (int i = 0; i < IT_STAGES; ++i) { tc::mbar_init(&full[i], 1); tc::mbar_init(&empty[i], 1); }
     tc::mbar_init(bfull, 1);
-    for (int i = 0; i < 2; ++i) { tc::mbar_init(&accf[i], 1); tc::mbar_init(&acce[i], 4); }
+    tc::mbar_init(bempty, 1);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&accf[i], 1);
+      tc::mbar_init(&acce[i], 4);
+      tc::mbar_init(&wsfull[i], 32);
+      tc::mbar_init(&wsempty[i], 4);
+    }
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
   if (warp == 5) tc::tmem_alloc(tmem_slot, 512);
-  for (int c = tid; c < IT_N; c += IT_THREADS) {
-    int qq = c / H_I, h = c % H_I;
-    Ws[c] = (qq < qn) ? a.w[(int64_t)(a.seq_start + p_first + qq) * H_I + h] : 0.f;
-  }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 4) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ producer: head weights (all lanes), TMA (lane 0)
     if (lane == 0) {
       tc::prefetch_tmap(&tm_q);
       tc::prefetch_tmap(&tm_k);
-      tc::mbar_arrive_expect_tx(bfull, L::B_BYTES);
-      for (int c = 0; c < L::KB; ++c)
-        tc::tma_load_2d(sB + c * (IT_N * 128), &tm_q, bfull, c * 64, (a.seq_start + p_first) * H_I);
-      for (int it = 0; it < ntiles; ++it) {
+    }
+    bool ok = true;
+    ItWalk w = start;
+    for (int it = 0; ok && it < nitems; ++it) {
+      if (w.first) {
+        const int q0 = w.qb * QB, qn = min(QB, a.nq - q0);
+        const int p_first = a.p_begin + q0;
+        // head weights of this block (buffer tr & 1, free once the block two changes back is done)
+        const int wb = w.tr & 1;
+        if (w.tr >= 2 && !__all_sync(0xffffffffu, tc::mbar_wait(&wsempty[wb], ((w.tr - 2) >> 1) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        for (int c = lane; c < IT_N; c += 32) {
+          const int qq = c / H_I, h = c % H_I;
+          Ws[wb * IT_N + c] = (qq < qn) ? a.w[(int64_t)(a.seq_start + p_first + qq) * H_I + h] : 0.f;
+        }
+        tc::mbar_arrive(&wsfull[wb]);
+        if (lane == 0) {
+          // q_I block (B operand) once the MMAs of the previous block are done
+          if (w.tr >= 1 && !tc::mbar_wait(bempty, (w.tr - 1) & 1, abort_flag)) ok = false;
+          if (ok) {
+            tc::mbar_arrive_expect_tx(bfull, L::B_BYTES);
+            for (int c = 0; c < L::KB; ++c)
+              tc::tma_load_2d(sB + c * (IT_N * 128), &tm_q, bfull, c * 64, (a.seq_start + p_first) * H_I);
+          }
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+      }
+      if (lane == 0) {
         const int st = it % IT_STAGES;
         const uint32_t ph = (it / IT_STAGES) & 1;
-        if (!tc::mbar_wait(&empty[st], ph ^ 1u, abort_flag)) { *abort_flag = 1; break; }
-        tc::mbar_arrive_expect_tx(&full[st], L::A_BYTES);
-        const int row = a.seq_start + (kt0 + it) * IT_M;
-        for (int c = 0; c < L::KB; ++c)
-          tc::tma_load_2d(sA + st * L::A_BYTES + c * (IT_M * 128), &tm_k, &full[st], c * 64, row);
+        if (!tc::mbar_wait(&empty[st], ph ^ 1u, abort_flag)) {
+          ok = false;
+        } else {
+          tc::mbar_arrive_expect_tx(&full[st], L::A_BYTES);
+          const int row = a.seq_start + w.kt * IT_M;
+          for (int c = 0; c < L::KB; ++c)
+            tc::tma_load_2d(sA + st * L::A_BYTES + c * (IT_M * 128), &tm_k, &full[st], c * 64, row);
+        }
       }
+      ok = __all_sync(0xffffffffu, ok);
+      advance(w, it);
     }
+    if (!ok) *abort_flag = 1;
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16_f32(IT_M, IT_N);
-      bool ok = tc::mbar_wait(bfull, 0, abort_flag);
-      for (int it = 0; ok && it < ntiles; ++it) {
+      bool ok = true;
+      ItWalk w = start;
+      for (int it = 0; ok && it < nitems; ++it) {
         const int st = it % IT_STAGES;
         const uint32_t ph = (it / IT_STAGES) & 1;
         const int acc = it & 1;
         const uint32_t aph = (it >> 1) & 1;
-        if (!tc::mbar_wait(&full[st], ph, abort_flag) || !tc::mbar_wait(&acce[acc], aph ^ 1u, abort_flag)) {
+        if ((w.first && !tc::mbar_wait(bfull, w.tr & 1, abort_flag)) || !tc::mbar_wait(&full[st], ph, abort_flag) ||
+            !tc::mbar_wait(&acce[acc], aph ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
@@ -137,45 +226,71 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
         }
         tc::mma_commit(&empty[st]);
         tc::mma_commit(&accf[acc]);
+        if (w.last) tc::mma_commit(bempty);  // the q_I block may be replaced once these MMAs are done
+        advance(w, it);
       }
       if (!ok) *abort_flag = 1;
     }
   } else {
     // ------------------------------------------------------------ epilogue (warps 0-3)
     const int key_in_tile = warp * 32 + lane;
-    for (int it = 0; it < ntiles; ++it) {
+    ItWalk w = start;
+    for (int it = 0; it < nitems; ++it) {
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
-      if (!tc::mbar_wait(&accf[acc], aph, abort_flag)) { *abort_flag = 1; break; }
+      const int wb = w.tr & 1;
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&accf[acc], aph, abort_flag)) ||
+          (w.first && !__all_sync(0xffffffffu, tc::mbar_wait(&wsfull[wb], (w.tr >> 1) & 1, abort_flag)))) {
+        *abort_flag = 1;
+        break;
+      }
       tc::fence_after_sync();
+      const int q0 = w.qb * QB, qn = min(QB, a.nq - q0);
+      const int p_first = a.p_begin + q0;
+      const float* W = Ws + wb * IT_N;
       const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + acc * IT_N;
-      const int s = (kt0 + it) * IT_M + key_in_tile;
-      float run = 0.f;  // running sum of the current (query, group) segment
-#pragma unroll 1
+      const int s = w.kt * IT_M + key_in_tile;
+      // four partial sums of the current (query, group) segment break the FMA
+      // dependency chain; the TMEM load of block cb+1 is in flight while block
+      // cb is reduced
+      float run[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t rbuf[2][32];
+      __syncwarp();
+      tc::tmem_ld32(taddr, rbuf[0]);
+#pragma unroll
       for (int cb = 0; cb < IT_N / 32; ++cb) {
-        uint32_t r[32];
-        __syncwarp();
-        tc::tmem_ld32(taddr + cb * 32, r);
+        uint32_t* r = rbuf[cb & 1];
         tc::tmem_ld_wait();
+        tc::reg_dep32(r);
+        if (cb + 1 < IT_N / 32) {
+          __syncwarp();  // converged for the .sync.aligned load
+          tc::tmem_ld32(taddr + (cb + 1) * 32, rbuf[(cb + 1) & 1]);
+        }
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          run = fmaf(Ws[cb * 32 + j], fmaxf(__uint_as_float(r[j]), 0.f), run);
+          run[j & 3] = fmaf(W[cb * 32 + j], fmaxf(__uint_as_float(r[j]), 0.f), run[j & 3]);
           const bool seg_done = (HG <= 32) ? ((j + 1) % HG == 0) : (j == 31 && ((cb + 1) * 32) % HG == 0);
           if (seg_done) {
+            const float tot = (run[0] + run[1]) + (run[2] + run[3]);
             const int sg = (cb * 32 + j) / HG;
             const int qq = sg / a.groups, gg = sg % a.groups;
             if (qq < qn && s <= p_first + qq)
-              a.out[((int64_t)(q0 + qq) * a.groups + gg) * a.width + s] = run * a.score_scale + 0.f;
-            run = 0.f;
+              a.out[((int64_t)(q0 + qq) * a.groups + gg) * a.width + s] = tot * a.score_scale + 0.f;
+            run[0] = run[1] = run[2] = run[3] = 0.f;
           }
         }
       }
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&acce[acc]);
+      if (lane == 0) {
+        tc::mbar_arrive(&acce[acc]);
+        if (w.last) tc::mbar_arrive(&wsempty[wb]);
+      }
+      advance(w, it);
     }
   }
 
+  tc::fence_before_sync();
   __syncthreads();
   if (*abort_flag && tid == 0) raise_flag(a.flags, TSA_FLAG_TIMEOUT);
   if (warp == 5) {
@@ -240,11 +355,23 @@ static cudaError_t launch_tc_t(const IndexerArgs& a, cudaStream_t stream) {
   constexpr int smem = ItLayout<DI>::SMEM;
   e = cudaFuncSetAttribute(indexer_tc_kernel<DI, HG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  // total (query block, key tile) pairs of the launch; one persistent CTA per SM
   const int QB = IT_N / a.H_I;
-  const int p_last = a.p_begin + a.nq - 1;
-  const int ktiles = p_last / IT_M + 1;
-  dim3 grid((ktiles + IT_KT_PER_CTA - 1) / IT_KT_PER_CTA, (a.nq + QB - 1) / QB);
-  indexer_tc_kernel<DI, HG><<<grid, IT_THREADS, smem, stream>>>(tq, tk, a);
+  const int nqb = (a.nq + QB - 1) / QB;
+  int64_t total = 0;
+  for (int qb = 0; qb < nqb; ++qb) {
+    const int qn = std::min(QB, a.nq - qb * QB);
+    total += (a.p_begin + qb * QB + qn - 1) / IT_M + 1;
+  }
+  if (total > 0x7fffffffLL) return cudaErrorInvalidValue;
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  }
+  const int grid = static_cast<int>(std::min<int64_t>(total, sms));
+  indexer_tc_kernel<DI, HG><<<grid, IT_THREADS, smem, stream>>>(tq, tk, a, static_cast<int>(total));
   return cudaGetLastError();
 }
 
