@@ -17,11 +17,15 @@
 // logits and take identical softmax decisions.  No MMA is repeated and every
 // selected row is read once.
 //
-// Per CTA: TMEM columns [0,256) = O slice, [256,320) = two 32-key S buffers.
-// Warps 0-3: softmax (thread h = head h = TMEM lane h); warp 4: TMEM owner,
-// TMA load of the q slice and single-thread MMA issuer (QK^T of tile j+2 is
-// issued before PV of tile j); warps 5-8: cp.async gather of the selected rows
-// into a 4-stage ring of 32-key tiles.
+// Per CTA, TMEM columns [0,256) = O slice, [256,320) = two 32-key S buffers,
+// [320, 320 + 32 kb) = the q slice (the A operand of QK^T, loaded once).
+// Warps 0-7: softmax, two warps per TMEM lane quadrant (thread = head = TMEM
+// lane), each owning 16 of the 32 key columns of a tile: the two halves of a
+// row agree on the tile maximum through shared memory and keep partial row
+// sums; each rescales and writes half of the O slice.  Warp 8: TMEM owner and
+// QK^T issuer; warp 9: PV issuer (two issuing threads, so that QK^T waiting
+// for a gather never delays a ready PV); warps 10-13: cp.async gather of the
+// selected rows into a 6-stage ring of 32-key tiles.
 //
 // The softmax is software-pipelined: while tile j is normalised, the partial
 // logits of tile j+1 are already on their way to the peer (two exchange
@@ -38,10 +42,13 @@ namespace {
 
 constexpr int MT_H = 128;        // heads = MMA M
 constexpr int MT_N = 32;         // keys per tile
-constexpr int MT_STAGES = 4;
-constexpr int MT_THREADS = 288;  // warps 0-3 softmax, 4 MMA, 5-8 gather producers
+constexpr int MT_STAGES = 6;
+constexpr int MT_SOFTMAX = 8;    // softmax warps
+constexpr int MT_THREADS = 448;  // warps 0-7 softmax, 8 QK^T issuer, 9 PV issuer, 10-13 gather producers
 constexpr int MT_DV = 512;
-constexpr int MT_OCOLS = 256;    // value channels per CTA
+constexpr int MT_OCOLS = 256;    // value channels per CTA (TMEM columns [0, 256))
+constexpr int MT_SCOL = 256;     // TMEM column of the two S buffers
+constexpr int MT_QCOL = 320;     // TMEM column of the q slice (up to 160 columns)
 constexpr float kRescaleLog2 = 8.f;
 
 template <int D>
@@ -49,16 +56,17 @@ struct MtLayout {
   static constexpr int KB0 = 4;                      // CTA 0: channels [0, 256)
   static constexpr int KB1 = (D - 256) / 64;         // CTA 1: channels [256, D)
   static constexpr int KBMAX = KB1 > KB0 ? KB1 : KB0;
-  static constexpr int Q_BYTES = KBMAX * MT_H * 128;
   static constexpr int KV_BLOCK = MT_N * 128;        // one 64-channel column block of a tile
   static constexpr int KV_STAGE = KBMAX * KV_BLOCK;
   static constexpr int P_BYTES = MT_H * 128;         // one P buffer (keys 0..31 of 128-byte rows)
   static constexpr int X_BYTES = MT_H * MT_N * 4;    // one exchange buffer
-  static constexpr int OFF_KV = Q_BYTES;
+  static constexpr int OFF_KV = 0;
   static constexpr int OFF_P = OFF_KV + MT_STAGES * KV_STAGE;
   static constexpr int OFF_X = OFF_P + 2 * P_BYTES;
-  static constexpr int OFF_BAR = OFF_X + 2 * X_BYTES;
+  static constexpr int OFF_M = OFF_X + 2 * X_BYTES;  // [2 parity][2 halves][128] row maxima / sums
+  static constexpr int OFF_BAR = OFF_M + 2 * 2 * MT_H * 4;
   static constexpr int SMEM = 1024 + OFF_BAR + 512;
+  static_assert(MT_QCOL + 32 * KBMAX <= 512, "TMEM columns");
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -71,27 +79,29 @@ __device__ __forceinline__ float ex2(float x) {
 
 template <int D>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
-    mla_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ MlaFwdArgs a) {
+    mla_fwd_tc_kernel(const __grid_constant__ MlaFwdArgs a) {
   using L = MtLayout<D>;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* gbase = smem_raw + (base - raw);
-  const uint32_t sQ = base, sKV = base + L::OFF_KV, sP = base + L::OFF_P;
+  const uint32_t sKV = base + L::OFF_KV, sP = base + L::OFF_P;
   // [2][128][32] partial logits written by the peer; chunk q (4 floats) of row h
   // sits at chunk q ^ (h & 7), so the 16-byte stores and loads of a warp spread
   // over all banks
   float* X = reinterpret_cast<float*>(gbase + L::OFF_X);
+  float* Mx = reinterpret_cast<float*>(gbase + L::OFF_M);  // [2][2][128] half-row maxima (and final sums)
   uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + L::OFF_BAR);
-  uint64_t* qfull = bars;
+  uint64_t* qready = bars;                            // q slice stored into TMEM (8 warps)
   uint64_t* kv_full = bars + 1;                       // [STAGES]
   uint64_t* kv_empty = kv_full + MT_STAGES;           // [STAGES]
   uint64_t* s_full = kv_empty + MT_STAGES;            // [2]
-  uint64_t* s_empty = s_full + 2;                     // [2]
-  uint64_t* p_full = s_empty + 2;                     // [2]
+  uint64_t* s_empty = s_full + 2;                     // [2] (256 softmax threads)
+  uint64_t* p_full = s_empty + 2;                     // [2] (256 softmax threads)
   uint64_t* p_empty = p_full + 2;                     // [2] (PV of that buffer completed)
   uint64_t* xfull = p_empty + 2;                      // [2] the peer's half of a tile landed in my X[b]
-  uint64_t* mask_full = xfull + 2;                    // [STAGES] valid-slot bits of the stage written
+  uint64_t* mx_full = xfull + 2;                      // [2 parity][4 quadrants] both halves wrote (64 threads)
+  uint64_t* mask_full = mx_full + 8;                  // [STAGES] valid-slot bits of the stage written
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mask_full + MT_STAGES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   uint32_t* masks = tmem_slot + 2;                    // [STAGES] valid-slot bits of each staged tile
@@ -110,7 +120,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
   const float NEG_INF = __int_as_float(0xff800000);
 
   if (tid == 0) {
-    tc::mbar_init(qfull, 1);
+    tc::mbar_init(qready, MT_SOFTMAX);
     for (int i = 0; i < MT_STAGES; ++i) {
       tc::mbar_init(&kv_full[i], 128);  // one asynchronous arrival per producer thread when its copies land
       tc::mbar_init(&kv_empty[i], 1);
@@ -118,17 +128,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&s_full[i], 1);
-      tc::mbar_init(&s_empty[i], MT_H);
-      tc::mbar_init(&p_full[i], MT_H);
+      tc::mbar_init(&s_empty[i], 32 * MT_SOFTMAX);
+      tc::mbar_init(&p_full[i], 32 * MT_SOFTMAX);
       tc::mbar_init(&p_empty[i], 1);
       tc::mbar_init(&xfull[i], 1);  // own expect_tx arrival + the peer's st.async bytes
     }
+    for (int i = 0; i < 8; ++i) tc::mbar_init(&mx_full[i], 64);
     *abort_flag = 0;
     tc::fence_barrier_init();
     tc::mbar_arrive_expect_tx(&xfull[0], L::X_BYTES);  // tiles 0 and 1
     tc::mbar_arrive_expect_tx(&xfull[1], L::X_BYTES);
   }
-  if (warp == 4) tc::tmem_alloc(tmem_slot, 512);
+  if (warp == 8) tc::tmem_alloc(tmem_slot, 512);
   tc::fence_before_sync();
   __syncthreads();
   __syncwarp();
@@ -136,7 +147,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp >= 5) {
+  if (warp >= 10) {
     // ------------------------------------------------------------ gather producers (4 warps)
     // Warp w copies rows 8w .. 8w+7 of each 32-row tile; lane l copies the
     // 16-byte chunks l, l+32 of the row's channel slice, so one instruction
@@ -148,7 +159,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
     // orders the landed data for the tensor cores with a proxy fence.  The
     // slot indices of the next tile are loaded one tile ahead (lane r < 8
     // holds row 8w + r).
-    const int w8 = (warp - 5) * 8;
+    const int w8 = (warp - 10) * 8;
     const int nchunk = kb * 8;  // 32 or 40
     const char* kvb = reinterpret_cast<const char*>(a.kv);
     bool ok = true;
@@ -181,45 +192,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
       // valid-slot bits of this warp's 8 rows: byte w of the stage's mask word
       const uint32_t bal = __ballot_sync(0xffffffffu, lane < 8 && id_mine >= 0 && id_mine < n);
       if (lane == 0) {
-        reinterpret_cast<volatile unsigned char*>(&masks[st])[warp - 5] = static_cast<unsigned char>(bal & 0xffu);
+        reinterpret_cast<volatile unsigned char*>(&masks[st])[warp - 10] = static_cast<unsigned char>(bal & 0xffu);
         tc::mbar_arrive(&mask_full[st]);
       }
     }
     cp_async_wait<0>();
     if (!ok) *abort_flag = 1;
-  } else if (warp == 4) {
-    // ------------------------------------------------------------ q slice (TMA) + MMA issuer
+  } else if (warp == 8) {
+    // ------------------------------------------------------------ QK^T issuer (A = q slice in TMEM)
     if (lane == 0) {
-      tc::prefetch_tmap(&tm_q);
-      tc::mbar_arrive_expect_tx(qfull, kb * MT_H * 128);
-      for (int c = 0; c < kb; ++c) tc::tma_load_2d(sQ + c * (MT_H * 128), &tm_q, qfull, ch0 + c * 64, t * MT_H);
       constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(MT_H, MT_N);
-      constexpr uint32_t idesc_pv = tc::idesc_bf16_f32_bmn(MT_H, MT_OCOLS);
-      bool ok = tc::mbar_wait(qfull, 0, abort_flag);
-      auto issue_qk = [&](int j) -> bool {
+      bool ok = tc::mbar_wait(qready, 0, abort_flag);
+      tc::fence_after_sync();
+      // QK^T of every tile, as soon as its rows have landed and an S buffer is
+      // free (the softmax frees one as soon as it has read it).
+      for (int j = 0; ok && j < ntiles; ++j) {
         const int st = j % MT_STAGES, b = j & 1;
-        if (!tc::mbar_wait(&kv_full[st], (j / MT_STAGES) & 1, abort_flag)) return false;
-        if (!tc::mbar_wait(&s_empty[b], ((j >> 1) & 1) ^ 1u, abort_flag)) return false;
+        if (!tc::mbar_wait(&kv_full[st], (j / MT_STAGES) & 1, abort_flag) ||
+            !tc::mbar_wait(&s_empty[b], ((j >> 1) & 1) ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
         tc::fence_proxy_async_smem();  // the gathered tile was written through the generic proxy
         tc::fence_after_sync();
-        const uint32_t d = tmem + MT_OCOLS + b * MT_N;
+        const uint32_t d = tmem + MT_SCOL + b * MT_N;
         for (int c = 0; c < kb; ++c) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = tc::desc_sw128(sQ + c * (MT_H * 128) + kk * 32);
-            const uint64_t bd = tc::desc_sw128(sKV + st * L::KV_STAGE + c * L::KV_BLOCK + kk * 32);
-            tc::mma_bf16_ss(d, ad, bd, idesc_qk, (c | kk) != 0 ? 1u : 0u);
-          }
+          for (int kk = 0; kk < 4; ++kk)
+            tc::mma_bf16_ts(d, tmem + MT_QCOL + (c * 4 + kk) * 8,
+                            tc::desc_sw128(sKV + st * L::KV_STAGE + c * L::KV_BLOCK + kk * 32), idesc_qk,
+                            (c | kk) != 0 ? 1u : 0u);
         }
         tc::mma_commit(&s_full[b]);
-        return true;
-      };
-      // QK^T runs two tiles ahead of PV: the softmax frees an S buffer as soon
-      // as it has read it, long before it produces that tile's P.
-      if (ok && ntiles > 0) ok = issue_qk(0);
-      if (ok && ntiles > 1) ok = issue_qk(1);
+      }
+      if (!ok) *abort_flag = 1;
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ PV issuer
+    // QK^T(j) completed before the softmax published P(j), so the commits of
+    // this thread (kv_empty after PV(j)) also cover every MMA that read stage j.
+    if (lane == 0) {
+      constexpr uint32_t idesc_pv = tc::idesc_bf16_f32_bmn(MT_H, MT_OCOLS);
+      bool ok = true;
       for (int j = 0; ok && j < ntiles; ++j) {
-        if (j + 2 < ntiles && !issue_qk(j + 2)) { ok = false; break; }
         const int pb = j & 1;
         if (!tc::mbar_wait(&p_full[pb], (j >> 1) & 1, abort_flag)) { ok = false; break; }
         tc::fence_after_sync();
@@ -236,31 +251,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
       if (!ok) *abort_flag = 1;
     }
   } else {
-    // ------------------------------------------------------------ softmax (warps 0-3)
-    // Iteration j: fetch tile j's partial logits from TMEM, receive the peer's
-    // half of tile j-1, send this CTA's half of tile j (st.async, completing
-    // on the peer's barrier), then normalise tile j-1 while it travels.
-    const int h = tid;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // ------------------------------------------------------------ softmax (warps 0-7)
+    // Thread (h, hf): head h = 32 (warp % 4) + lane, key columns 16 hf .. +15
+    // of every tile, hf = warp / 4.  Iteration j: fetch tile j's partial
+    // logits from TMEM, receive the peer's half of tile j-1, send this CTA's
+    // half of tile j (st.async, completing on the peer's barrier), then
+    // normalise tile j-1 while it travels.
+    const int qd = warp & 3, hf = warp >> 2;
+    const int h = qd * 32 + lane;
+    const int cofs = hf * 16;
+    const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
+    // q slice row h -> TMEM columns [MT_QCOL, MT_QCOL + 32 kb): blocks hf, hf + 2, ...
+    {
+      const uint4* qrow = reinterpret_cast<const uint4*>(a.q + ((int64_t)t * MT_H + h) * D + ch0);
+      for (int c = hf; c < kb; c += 2) {
+        uint32_t r[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 v = __ldg(qrow + c * 8 + i);
+          r[4 * i] = v.x;
+          r[4 * i + 1] = v.y;
+          r[4 * i + 2] = v.z;
+          r[4 * i + 3] = v.w;
+        }
+        __syncwarp();
+        tc::tmem_st32(tmem + lane_base + MT_QCOL + c * 32, r);
+      }
+      tc::tmem_st_wait();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(qready);
+    }
     const uint32_t x_peer_row = tc::mapa(smem_u32(X + h * MT_N), peer);
     const uint32_t peer_xfull = tc::mapa(smem_u32(xfull), peer);
-    float m_use = NEG_INF, l = 0.f;
+    float m_use = NEG_INF, l = 0.f;  // running max (shared by both halves) and this half's row sum
     bool ok = true;
-    uint32_t cur[32];
+    uint32_t cur[16];
     for (int j = 0; j <= ntiles; ++j) {
-      uint32_t nxt[32];
+      uint32_t nxt[16];
       if (j < ntiles) {
         const int b = j & 1;
         if (!__all_sync(0xffffffffu, tc::mbar_wait(&s_full[b], (j >> 1) & 1, abort_flag))) { ok = false; break; }
         tc::fence_after_sync();
         __syncwarp();
-        tc::tmem_ld32(tmem + lane_base + MT_OCOLS + b * MT_N, nxt);
+        tc::tmem_ld16(tmem + lane_base + MT_SCOL + b * MT_N + cofs, nxt);
         tc::tmem_ld_wait();
         tc::fence_before_sync();
         tc::mbar_arrive(&s_empty[b]);
       }
       // receive the peer's half of tile j-1 (published at the end of its previous iteration)
-      float x2[32];
+      float x2[16];
       if (j > 0) {
         const int jj = j - 1, bb = jj & 1;
         if (!__all_sync(0xffffffffu, tc::mbar_wait_cluster(&xfull[bb], (jj >> 1) & 1, abort_flag))) {
@@ -269,8 +309,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
         }
         const float4* xr = reinterpret_cast<const float4*>(X + bb * (MT_H * MT_N) + h * MT_N);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float4 v = xr[q ^ (h & 7)];  // 16-byte chunks of a row are swizzled by the row
+        for (int q = 0; q < 4; ++q) {
+          const float4 v = xr[(hf * 4 + q) ^ (h & 7)];  // 16-byte chunks of a row are swizzled by the row
           x2[4 * q] = __uint_as_float(cur[4 * q]) + v.x;
           x2[4 * q + 1] = __uint_as_float(cur[4 * q + 1]) + v.y;
           x2[4 * q + 2] = __uint_as_float(cur[4 * q + 2]) + v.z;
@@ -278,18 +318,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
         }
         // the next use of X[bb] is tile jj+2; the peer can send it only after
         // all of this CTA's threads sent tile jj+1, i.e. after they read X[bb]
-        if (h == 0 && jj + 2 < ntiles) tc::mbar_arrive_expect_tx(&xfull[bb], L::X_BYTES);
+        if (h == 0 && hf == 0 && jj + 2 < ntiles) tc::mbar_arrive_expect_tx(&xfull[bb], L::X_BYTES);
       }
-      // send this CTA's half of tile j: asynchronous stores that complete on
-      // the peer's barrier when they land (no fence, no remote arrival)
+      // send this thread's 16 columns of tile j: asynchronous stores that
+      // complete on the peer's barrier when they land (no fence, no remote arrival)
       if (j < ntiles) {
         const int b = j & 1;
         const uint32_t dst = x_peer_row + b * L::X_BYTES;
         const uint32_t rbar = peer_xfull + b * 8;
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          tc::st_async_v4(dst + ((q ^ (h & 7)) << 4), rbar, __uint_as_float(nxt[4 * q]), __uint_as_float(nxt[4 * q + 1]),
-                          __uint_as_float(nxt[4 * q + 2]), __uint_as_float(nxt[4 * q + 3]));
+        for (int q = 0; q < 4; ++q)
+          tc::st_async_v4(dst + (((hf * 4 + q) ^ (h & 7)) << 4), rbar, __uint_as_float(nxt[4 * q]),
+                          __uint_as_float(nxt[4 * q + 1]), __uint_as_float(nxt[4 * q + 2]),
+                          __uint_as_float(nxt[4 * q + 3]));
       }
       if (j > 0) {
         const int jj = j - 1, bb = jj & 1;
@@ -299,21 +340,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
           ok = false;
           break;
         }
-        const uint32_t mask = masks[st];
-        float tmax = NEG_INF;
-        if (mask == 0xffffffffu) {
+        const uint32_t mask = (masks[st] >> cofs) & 0xffffu;
+        if (mask == 0xffffu) {
 #pragma unroll
-          for (int i = 0; i < MT_N; ++i) {
-            x2[i] *= a.scale_log2;
-            tmax = fmaxf(tmax, x2[i]);
-          }
+          for (int i = 0; i < 16; ++i) x2[i] *= a.scale_log2;
         } else {
 #pragma unroll
-          for (int i = 0; i < MT_N; ++i) {
-            x2[i] = ((mask >> i) & 1u) ? x2[i] * a.scale_log2 : NEG_INF;
-            tmax = fmaxf(tmax, x2[i]);
-          }
+          for (int i = 0; i < 16; ++i) x2[i] = ((mask >> i) & 1u) ? x2[i] * a.scale_log2 : NEG_INF;
         }
+        float mx[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mx[i] = fmaxf(fmaxf(x2[i], x2[i + 4]), fmaxf(x2[i + 8], x2[i + 12]));
+        const float hmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        // the tile maximum of row h: both halves publish theirs and wait for each other
+        float* mrow = Mx + bb * (2 * MT_H);
+        mrow[hf * MT_H + h] = hmax;
+        tc::mbar_arrive(&mx_full[bb * 4 + qd]);
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(&mx_full[bb * 4 + qd], (jj >> 1) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        const float tmax = fmaxf(hmax, mrow[(hf ^ 1) * MT_H + h]);
         float alpha = 1.f;
         const bool resc = tmax > m_use + kRescaleLog2;
         if (resc) {
@@ -322,21 +369,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
           l *= alpha;
         }
         const float mu = (m_use == NEG_INF) ? 0.f : m_use;
-        uint32_t pk[MT_N / 2];
-        float psum = 0.f;
+        uint32_t pk[8];
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < MT_N; i += 2) {
+        for (int i = 0; i < 16; i += 2) {
           const float p0 = ex2(x2[i] - mu), p1 = ex2(x2[i + 1] - mu);
-          psum += p0 + p1;
+          ps[(i >> 1) & 3] += p0 + p1;
           pk[i / 2] = pack_bf16(p0, p1);
         }
-        l += psum;
+        l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
         // P buffer bb is free once PV(jj-2) completed
         if (!__all_sync(0xffffffffu, tc::mbar_wait(&p_empty[bb], ((jj >> 1) & 1) ^ 1u, abort_flag))) {
           ok = false;
           break;
         }
-        // a raised running max rescales the O slice, which PV(jj-1) must have finished
+        // a raised running max rescales this half of the O slice, which PV(jj-1) must have finished
         if (jj > 0 && __any_sync(0xffffffffu, resc)) {
           const int pb = (jj - 1) & 1;
           if (!__all_sync(0xffffffffu, tc::mbar_wait(&p_empty[pb], ((jj - 1) >> 1) & 1, abort_flag))) {
@@ -344,42 +391,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
             break;
           }
           tc::fence_after_sync();
-          for (int cb = 0; cb < MT_OCOLS / 32; ++cb) {
+          for (int cb = 0; cb < MT_OCOLS / 64; ++cb) {
             uint32_t o[32];
-            tc::tmem_ld32(tmem + lane_base + cb * 32, o);
+            const uint32_t oc = tmem + lane_base + hf * (MT_OCOLS / 2) + cb * 32;
+            tc::tmem_ld32(oc, o);
             tc::tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tc::tmem_st32(tmem + lane_base + cb * 32, o);
+            tc::tmem_st32(oc, o);
           }
           tc::tmem_st_wait();
         }
-        // P row h: 32 bf16 = 4 x 16 B chunks in a 128-byte-swizzled K-major row
+        // P row h: this half's 16 bf16 = chunks 2 hf, 2 hf + 1 of a 128-byte-swizzled K-major row
         unsigned char* prow = gbase + L::OFF_P + bb * L::P_BYTES + h * 128;
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          *reinterpret_cast<uint4*>(prow + ((c ^ (h & 7)) << 4)) =
+        for (int c = 0; c < 2; ++c)
+          *reinterpret_cast<uint4*>(prow + (((2 * hf + c) ^ (h & 7)) << 4)) =
               make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
         tc::fence_proxy_async_smem();
         tc::fence_before_sync();
         tc::mbar_arrive(&p_full[bb]);
       }
 #pragma unroll
-      for (int i = 0; i < 32; ++i) cur[i] = nxt[i];
+      for (int i = 0; i < 16; ++i) cur[i] = nxt[i];
     }
     if (!ok) *abort_flag = 1;
-    // epilogue: O slice / l -> bf16, lse
+    // epilogue: the row sum of both halves, O half / l -> bf16, lse
     const int lb = (ntiles - 1) & 1;
-    const bool last_ok =
-        ok && __all_sync(0xffffffffu, tc::mbar_wait(&p_empty[lb], ((ntiles - 1) >> 1) & 1, abort_flag));
+    bool last_ok = ok && __all_sync(0xffffffffu, tc::mbar_wait(&p_empty[lb], ((ntiles - 1) >> 1) & 1, abort_flag));
+    float lt = 0.f;
+    if (last_ok) {
+      const int pe = ntiles & 1;  // next use of the max exchange slots: tile ntiles
+      float* mrow = Mx + pe * (2 * MT_H);
+      mrow[hf * MT_H + h] = l;
+      tc::mbar_arrive(&mx_full[pe * 4 + qd]);
+      last_ok = __all_sync(0xffffffffu, tc::mbar_wait(&mx_full[pe * 4 + qd], (ntiles >> 1) & 1, abort_flag));
+      if (last_ok) lt = l + mrow[(hf ^ 1) * MT_H + h];
+    }
+    __nv_bfloat16* orow = a.out + ((int64_t)t * MT_H + h) * MT_DV + ch0 + hf * (MT_OCOLS / 2);
     if (last_ok) {
       tc::fence_after_sync();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* orow = a.out + ((int64_t)t * MT_H + h) * MT_DV + ch0;
-      for (int cb = 0; cb < MT_OCOLS / 32; ++cb) {
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      for (int cb = 0; cb < MT_OCOLS / 64; ++cb) {
         uint32_t o[32];
         __syncwarp();
-        tc::tmem_ld32(tmem + lane_base + cb * 32, o);
+        tc::tmem_ld32(tmem + lane_base + hf * (MT_OCOLS / 2) + cb * 32, o);
         tc::tmem_ld_wait();
         uint4* dst = reinterpret_cast<uint4*>(orow + cb * 32);
 #pragma unroll
@@ -389,12 +445,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
                               pack_bf16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv),
                               pack_bf16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv));
       }
-      if (rank == 0) a.lse[(int64_t)t * MT_H + h] = l > 0.f ? (m_use + log2f(l)) * kLn2 : NEG_INF;
+      if (rank == 0 && hf == 0) a.lse[(int64_t)t * MT_H + h] = lt > 0.f ? (m_use + log2f(lt)) * kLn2 : NEG_INF;
     } else {
-      // wound down after a timeout: zero output slice, -inf lse
-      __nv_bfloat16* orow = a.out + ((int64_t)t * MT_H + h) * MT_DV + ch0;
-      for (int c = 0; c < MT_OCOLS; c += 8) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
-      if (rank == 0) a.lse[(int64_t)t * MT_H + h] = NEG_INF;
+      // wound down after a timeout: zero output half, -inf lse
+      *abort_flag = 1;
+      for (int c = 0; c < MT_OCOLS / 2; c += 8) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
+      if (rank == 0 && hf == 0) a.lse[(int64_t)t * MT_H + h] = NEG_INF;
     }
   }
 
@@ -403,26 +459,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
   if (*abort_flag && tid == 0) raise_flag(a.flags, TSA_FLAG_TIMEOUT);
   __syncwarp();
   tc::cluster_sync();  // the peer no longer writes into this CTA's shared memory
-  if (warp == 4) {
+  if (warp == 8) {
     __syncwarp();
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, 512);
   }
 }
 
-cudaError_t make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
-                              uint32_t box_cols);
-
 template <int D>
 static cudaError_t launch_tc_t(const MlaFwdArgs& a, cudaStream_t stream) {
-  CUtensorMap tq;
-  cudaError_t e = make_tmap_bf16_2d(&tq, a.q, (uint64_t)a.T * MT_H, D, MT_H, 64);
-  if (e != cudaSuccess) return e;
   constexpr int smem = MtLayout<D>::SMEM;
   static_assert(smem <= 227 * 1024, "shared memory budget");
-  e = cudaFuncSetAttribute(mla_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(mla_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  mla_fwd_tc_kernel<D><<<dim3(2 * a.T), MT_THREADS, smem, stream>>>(tq, a);
+  mla_fwd_tc_kernel<D><<<dim3(2 * a.T), MT_THREADS, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
