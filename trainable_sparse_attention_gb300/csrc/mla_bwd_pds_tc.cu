@@ -19,9 +19,9 @@
 //   pass 2: dP = dO V^T with the dO rows in TMEM, dS = scale P (dP - Dlt)
 //           from the bf16 P of pass 1, written in bf16.
 // Each pass streams its gathered 64-row tiles through a three-stage ring
-// (cp.async, 8 producer warps) and double-buffers the accumulator in TMEM;
-// warps 0-3 (thread = head = TMEM lane) write [query][head][slot] rows, slots
-// padded to kp with zeros.  No softmax state is carried between tiles: L is
+// (cp.async, 4 producer warps) and double-buffers the accumulator in TMEM;
+// warps 0-7 (two per TMEM lane quadrant, thread = head, 32 of the 64 key
+// columns each) write [query][head][slot] rows, slots padded to kp with zeros.  No softmax state is carried between tiles: L is
 // known, so every tile is final when it is computed.
 //
 // mla_bwd_dq_tc_kernel: dQ = dS K over the gathered rows.  The 128 x D fp32
@@ -46,8 +46,8 @@ constexpr int PB_H = 128;        // heads = MMA M
 constexpr int SP_H = PB_H;
 constexpr int SP_N = 64;         // keys per tile (MMA N)
 constexpr int SP_STAGES = 3;
-constexpr int SP_PRODUCERS = 256;
-constexpr int SP_THREADS = 160 + SP_PRODUCERS;  // warps 0-3 epilogue, warp 4 MMA, warps 5-12 gather
+constexpr int SP_PRODUCERS = 128;
+constexpr int SP_THREADS = 288 + SP_PRODUCERS;  // warps 0-7 epilogue, warp 8 MMA, warps 9-12 gather
 constexpr int SP_ACC = 288;      // first TMEM column of the two accumulators (after the A operand)
 
 constexpr int SP_PTILE = SP_H * 128;  // one P tile of the dS pass: 128 heads x 64 slots bf16
@@ -121,22 +121,22 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&acc_full[i], 1);
-      tc::mbar_init(&acc_empty[i], 4);
+      tc::mbar_init(&acc_empty[i], 8);
       tc::mbar_init(&pfull[i], 1);
-      tc::mbar_init(&pempty[i], 4);
+      tc::mbar_init(&pempty[i], 8);
     }
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
-  if (warp == 4) tc::tmem_alloc(tmem_slot, 512);
+  if (warp == 8) tc::tmem_alloc(tmem_slot, 512);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
   // A rows -> TMEM columns [0, KC/2), 32 columns (64 channels) per store.  The
-  // three warps that share a TMEM lane quadrant (epilogue warp w, producer
-  // warps w+4 / w+8 with w+4 taken mod 4) split the KB blocks of their 32 rows.
+  // three warps that share a TMEM lane quadrant (epilogue warps q and q+4, the
+  // producer warp of that quadrant) split the KB blocks of their 32 rows.
   auto load_a_rows = [&](int share) {
     const int h = (warp & 3) * 32 + lane;
     const uint4* arow = DS ? reinterpret_cast<const uint4*>(a.dout + ((int64_t)t * SP_H + h) * 512)
@@ -161,32 +161,32 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
     if (lane == 0) tc::mbar_arrive(aready);
   };
 
-  if (warp >= 5) {
-    // ------------------------------------------------------------ gather producers (8 warps)
-    // Warp w copies rows 8w .. 8w+7 of each 64-row tile; lane l copies the
+  if (warp >= 9) {
+    // ------------------------------------------------------------ gather producers (4 warps)
+    // Warp w copies rows 16w .. 16w+15 of each 64-row tile; lane l copies the
     // 16-byte chunks l, l+32, ... of a row, so one instruction covers 512
     // contiguous bytes of the row.  The chunks land in the 128-byte-swizzled
     // K-major tile, and each thread's copies arrive asynchronously on the
     // stage's barrier when they land.  The slot indices of the next tile are
-    // loaded one tile ahead (lane r < 8 holds row 8w + r).
-    const int w8 = (warp - 5) * 8;
+    // loaded one tile ahead (lane r < 16 holds row 16w + r).
+    const int w8 = (warp - 9) * 16;
     constexpr int NCH = KC / 8;  // 16-byte chunks per row
     const char* kvb = reinterpret_cast<const char*>(a.kv);
     bool ok = true;
     const int npre = ntiles < SP_STAGES ? ntiles : SP_STAGES;
-    int id_next = (lane < 8 && w8 + lane < a.topk) ? __ldg(idx_row + w8 + lane) : -1;
+    int id_next = (lane < 16 && w8 + lane < a.topk) ? __ldg(idx_row + w8 + lane) : -1;
     for (int j = 0; j < ntiles; ++j) {
       const int st = j % SP_STAGES;
       const int id_mine = id_next;
       const int slot_next = (j + 1) * SP_N + w8 + lane;
-      id_next = (lane < 8 && slot_next < a.topk) ? __ldg(idx_row + slot_next) : -1;
+      id_next = (lane < 16 && slot_next < a.topk) ? __ldg(idx_row + slot_next) : -1;
       if (!__all_sync(0xffffffffu, tc::mbar_wait(&kv_empty[st], ((j / SP_STAGES) & 1) ^ 1u, abort_flag))) {
         ok = false;
         break;
       }
-      if (!DS && lane < 8 && id_mine >= n) raise_flag(a.flags, TSA_FLAG_INDEX_RANGE);
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
+      if (!DS && lane < 16 && id_mine >= n) raise_flag(a.flags, TSA_FLAG_INDEX_RANGE);
+#pragma unroll 4
+      for (int r = 0; r < 16; ++r) {
         const int id = __shfl_sync(0xffffffffu, id_mine, r);
         const int row = w8 + r;
         const bool valid = id >= 0 && id < n;
@@ -202,11 +202,11 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
       asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&kv_full[st]))
                    : "memory");
       // the first tiles are in flight: help load the A rows
-      if (j == npre - 1) load_a_rows(warp < 9 ? 1 : 2);
+      if (j == npre - 1) load_a_rows(2);
     }
     cp_async_wait<0>();
     if (!ok) *abort_flag = 1;
-  } else if (warp == 4) {
+  } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16_f32(SP_H, SP_N);
@@ -235,21 +235,24 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
       if (!ok) *abort_flag = 1;
     }
   } else {
-    // ------------------------------------------------------------ epilogue (warps 0-3, thread = head)
-    const int h = tid;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // ------------------------------------------------------------ epilogue (warps 0-7)
+    // Thread (h, hf): head h = 32 (warp % 4) + lane (its TMEM lane), key
+    // columns 32 hf .. +31 of each 64-key tile, hf = warp / 4.
+    const int qd = warp & 3, hf = warp >> 2;
+    const int h = qd * 32 + lane;
+    const int cofs = hf * 32;
+    const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
     const float NEG_INF = __int_as_float(0xff800000);
     const float Lh = a.lse[(int64_t)t * SP_H + h];
     const float lse2 = Lh * kLog2e;
     const bool live = Lh != NEG_INF;  // a row without valid slots has P = dS = 0
     const float dl = DS ? a.dlt[(int64_t)t * SP_H + h] : 0.f;
-    load_a_rows(0);
+    load_a_rows(hf);
     static_assert(ACOLS <= SP_ACC, "A operand overlaps the accumulators");
     __nv_bfloat16* prow = a.p_out + ((int64_t)lq * SP_H + h) * a.kp;
     __nv_bfloat16* dsrow = a.ds_out + ((int64_t)lq * SP_H + h) * a.kp;
     bool ok = true;
-    int idn0 = lane < a.topk ? __ldg(idx_row + lane) : -1;
-    int idn1 = 32 + lane < a.topk ? __ldg(idx_row + 32 + lane) : -1;
+    int idn = cofs + lane < a.topk ? __ldg(idx_row + cofs + lane) : -1;
     if (DS && tid == 0) {
       // P tiles 0 and 1 (TMA); later tiles are issued as the ring frees up
       tc::prefetch_tmap(&tm_p);
@@ -261,49 +264,45 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
     }
     for (int j = 0; j < ntiles; ++j) {
       const int b = j & 1;
-      const uint32_t m0 = __ballot_sync(0xffffffffu, idn0 >= 0 && idn0 < n);
-      const uint32_t m1 = __ballot_sync(0xffffffffu, idn1 >= 0 && idn1 < n);
-      const uint64_t mask = static_cast<uint64_t>(m1) << 32 | m0;
+      const uint32_t mask = __ballot_sync(0xffffffffu, idn >= 0 && idn < n);
       if (!DS) {
-        const int sn = (j + 1) * SP_N + lane;
-        idn0 = sn < a.topk ? __ldg(idx_row + sn) : -1;
-        idn1 = sn + 32 < a.topk ? __ldg(idx_row + sn + 32) : -1;
+        const int sn = (j + 1) * SP_N + cofs + lane;
+        idn = sn < a.topk ? __ldg(idx_row + sn) : -1;
       }
       if (!__all_sync(0xffffffffu, tc::mbar_wait(&acc_full[b], (j >> 1) & 1, abort_flag))) {
         ok = false;
         break;
       }
       tc::fence_after_sync();
-      uint32_t x[64];
-      tc::tmem_ld32(tmem + lane_base + SP_ACC + b * SP_N, x);
-      tc::tmem_ld32(tmem + lane_base + SP_ACC + b * SP_N + 32, x + 32);
+      uint32_t x[32];
+      tc::tmem_ld32(tmem + lane_base + SP_ACC + b * SP_N + cofs, x);
       tc::tmem_ld_wait();
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&acc_empty[b]);
-      uint32_t pk[32];
+      uint32_t pk[16];
       if (!DS) {
 #pragma unroll
-        for (int i = 0; i < 64; i += 2) {
+        for (int i = 0; i < 32; i += 2) {
           float p0 = 0.f, p1 = 0.f;
           if (live && ((mask >> i) & 1u)) p0 = ex2(fmaf(__uint_as_float(x[i]), a.scale_log2, -lse2));
           if (live && ((mask >> (i + 1)) & 1u)) p1 = ex2(fmaf(__uint_as_float(x[i + 1]), a.scale_log2, -lse2));
           pk[i / 2] = pack_bf16(p0, p1);
         }
       } else {
-        // P row h of this tile from the TMA ring (128-byte swizzled rows)
+        // this thread's 32 P values of tile j from the TMA ring (128-byte swizzled rows)
         if (!__all_sync(0xffffffffu, tc::mbar_wait(&pfull[b], (j >> 1) & 1, abort_flag))) {
           ok = false;
           break;
         }
-        uint4 pn[8];
+        uint4 pn[4];
         const unsigned char* ps = gbase + OFF_P + b * SP_PTILE + h * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) pn[c] = *reinterpret_cast<const uint4*>(ps + ((c ^ (h & 7)) << 4));
+        for (int c = 0; c < 4; ++c) pn[c] = *reinterpret_cast<const uint4*>(ps + (((4 * hf + c) ^ (h & 7)) << 4));
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&pempty[b]);
         if (tid == 0 && j + 2 < ntiles) {
-          // refill this slot with tile j+2 once all four warps have read tile j
+          // refill this slot with tile j+2 once all eight warps have read tile j
           if (tc::mbar_wait(&pempty[b], (j >> 1) & 1, abort_flag)) {
             tc::mbar_arrive_expect_tx(&pfull[b], SP_PTILE);
             tc::tma_load_2d_hint(base + OFF_P + b * SP_PTILE, &tm_p, &pfull[b], (j + 2) * SP_N, lq * SP_H,
@@ -314,27 +313,28 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
         }
         const uint32_t* pw = reinterpret_cast<const uint32_t*>(pn);
 #pragma unroll
-        for (int i = 0; i < 64; i += 2) {
+        for (int i = 0; i < 32; i += 2) {
           const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pw[i / 2]));
           pk[i / 2] = pack_bf16(a.scale * p.x * (__uint_as_float(x[i]) - dl),
                                 a.scale * p.y * (__uint_as_float(x[i + 1]) - dl));
         }
       }
       // streaming stores (evict-first in L2): read back once per consumer
-      uint4* dst = reinterpret_cast<uint4*>((DS ? dsrow : prow) + j * SP_N);
+      uint4* dst = reinterpret_cast<uint4*>((DS ? dsrow : prow) + j * SP_N + cofs);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) __stcs(dst + c, make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
+      for (int c = 0; c < 4; ++c) __stcs(dst + c, make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
     }
     if (!ok) *abort_flag = 1;
-    // zero the padding slots [ntiles * 64, kp)
+    // zero the padding slots [ntiles * 64, kp) (each half its own 32-column runs)
     __nv_bfloat16* orow = DS ? dsrow : prow;
-    for (int c = ntiles * SP_N; c < a.kp; c += 8) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0u, 0u, 0u, 0u);
+    for (int c = ntiles * SP_N + cofs; c < a.kp; c += SP_N)
+      for (int e = 0; e < 32; e += 8) *reinterpret_cast<uint4*>(orow + c + e) = make_uint4(0u, 0u, 0u, 0u);
   }
 
   tc::fence_before_sync();
   __syncthreads();
   if (*abort_flag && tid == 0) raise_flag(a.flags, TSA_FLAG_TIMEOUT);
-  if (warp == 4) {
+  if (warp == 8) {
     __syncwarp();
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, 512);
