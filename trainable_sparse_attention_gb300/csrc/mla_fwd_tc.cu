@@ -25,7 +25,10 @@
 // sums; each rescales and writes half of the O slice.  Warp 8: TMEM owner and
 // QK^T issuer; warp 9: PV issuer (two issuing threads, so that QK^T waiting
 // for a gather never delays a ready PV); warps 10-13: cp.async gather of the
-// selected rows into a 6-stage ring of 32-key tiles.
+// selected rows into a 6-stage ring of 32-key tiles; warp 14: sender, one
+// bulk copy per tile of the staged partial logits into the peer's exchange
+// buffer (per-thread stores into the peer's shared memory held up the softmax
+// warps' next shared-memory accesses by ~0.5 us per tile).
 //
 // The softmax is software-pipelined: while tile j is normalised, the partial
 // logits of tile j+1 are already on their way to the peer (two exchange
@@ -44,7 +47,7 @@ constexpr int MT_H = 128;        // heads = MMA M
 constexpr int MT_N = 32;         // keys per tile
 constexpr int MT_STAGES = 6;
 constexpr int MT_SOFTMAX = 8;    // softmax warps
-constexpr int MT_THREADS = 448;  // warps 0-7 softmax, 8 QK^T issuer, 9 PV issuer, 10-13 gather producers
+constexpr int MT_THREADS = 480;  // warps 0-7 softmax, 8 QK^T issuer, 9 PV issuer, 10-13 gather producers, 14 sender
 constexpr int MT_DV = 512;
 constexpr int MT_OCOLS = 256;    // value channels per CTA (TMEM columns [0, 256))
 constexpr int MT_SCOL = 256;     // TMEM column of the two S buffers
@@ -63,7 +66,8 @@ struct MtLayout {
   static constexpr int OFF_KV = 0;
   static constexpr int OFF_P = OFF_KV + MT_STAGES * KV_STAGE;
   static constexpr int OFF_X = OFF_P + 2 * P_BYTES;
-  static constexpr int OFF_M = OFF_X + 2 * X_BYTES;  // [2 parity][2 halves][128] row maxima / sums
+  static constexpr int OFF_SB = OFF_X + 2 * X_BYTES;  // two staging buffers of this CTA's partials (same layout as X)
+  static constexpr int OFF_M = OFF_SB + 2 * X_BYTES;  // [2 parity][2 halves][128] row maxima / sums
   static constexpr int OFF_BAR = OFF_M + 2 * 2 * MT_H * 4;
   static constexpr int SMEM = 1024 + OFF_BAR + 512;
   static_assert(MT_QCOL + 32 * KBMAX <= 512, "TMEM columns");
@@ -101,7 +105,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
   uint64_t* p_empty = p_full + 2;                     // [2] (PV of that buffer completed)
   uint64_t* xfull = p_empty + 2;                      // [2] the peer's half of a tile landed in my X[b]
   uint64_t* mx_full = xfull + 2;                      // [2 parity][4 quadrants] both halves wrote (64 threads)
-  uint64_t* mask_full = mx_full + 8;                  // [STAGES] valid-slot bits of the stage written
+  uint64_t* sb_full = mx_full + 8;                    // [2] staging buffer written (256 softmax threads)
+  uint64_t* sb_empty = sb_full + 2;                   // [2] bulk copy of the staging buffer has read it
+  uint64_t* mask_full = sb_empty + 2;                 // [STAGES] valid-slot bits of the stage written
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mask_full + MT_STAGES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   uint32_t* masks = tmem_slot + 2;                    // [STAGES] valid-slot bits of each staged tile
@@ -134,6 +140,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
       tc::mbar_init(&xfull[i], 1);  // own expect_tx arrival + the peer's st.async bytes
     }
     for (int i = 0; i < 8; ++i) tc::mbar_init(&mx_full[i], 64);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&sb_full[i], 32 * MT_SOFTMAX);
+      tc::mbar_init(&sb_empty[i], 1);
+    }
     *abort_flag = 0;
     tc::fence_barrier_init();
     tc::mbar_arrive_expect_tx(&xfull[0], L::X_BYTES);  // tiles 0 and 1
@@ -147,7 +157,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp >= 10) {
+  if (warp >= 10 && warp <= 13) {
     // ------------------------------------------------------------ gather producers (4 warps)
     // Warp w copies rows 8w .. 8w+7 of each 32-row tile; lane l copies the
     // 16-byte chunks l, l+32 of the row's channel slice, so one instruction
@@ -227,6 +237,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
       }
       if (!ok) *abort_flag = 1;
     }
+  } else if (warp == 14) {
+    // ------------------------------------------------------------ sender
+    // One bulk copy per tile moves this CTA's staged partial logits into the
+    // peer's exchange buffer, completing on the peer's barrier; the staging
+    // buffer is handed back once the copy has read it.
+    if (lane == 0) {
+      const uint32_t x_peer = tc::mapa(smem_u32(X), peer);
+      const uint32_t peer_xfull = tc::mapa(smem_u32(xfull), peer);
+      bool ok = true;
+      for (int j = 0; ok && j < ntiles; ++j) {
+        const int b = j & 1;
+        if (!tc::mbar_wait(&sb_full[b], (j >> 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc::bulk_copy_to_peer(x_peer + b * L::X_BYTES, base + L::OFF_SB + b * L::X_BYTES, L::X_BYTES,
+                              peer_xfull + b * 8);
+        tc::bulk_commit();
+        tc::bulk_wait_read0();
+        tc::mbar_arrive(&sb_empty[b]);
+      }
+      if (!ok) *abort_flag = 1;
+    }
   } else if (warp == 9) {
     // ------------------------------------------------------------ PV issuer
     // QK^T(j) completed before the softmax published P(j), so the commits of
@@ -254,9 +287,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
     // ------------------------------------------------------------ softmax (warps 0-7)
     // Thread (h, hf): head h = 32 (warp % 4) + lane, key columns 16 hf .. +15
     // of every tile, hf = warp / 4.  Iteration j: fetch tile j's partial
-    // logits from TMEM, receive the peer's half of tile j-1, send this CTA's
-    // half of tile j (st.async, completing on the peer's barrier), then
-    // normalise tile j-1 while it travels.
+    // logits from TMEM, receive the peer's half of tile j-1, stage this CTA's
+    // half of tile j for the sender, then normalise tile j-1 while it travels.
     const int qd = warp & 3, hf = warp >> 2;
     const int h = qd * 32 + lane;
     const int cofs = hf * 16;
@@ -282,8 +314,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(qready);
     }
-    const uint32_t x_peer_row = tc::mapa(smem_u32(X + h * MT_N), peer);
-    const uint32_t peer_xfull = tc::mapa(smem_u32(xfull), peer);
     float m_use = NEG_INF, l = 0.f;  // running max (shared by both halves) and this half's row sum
     bool ok = true;
     uint32_t cur[16];
@@ -320,17 +350,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
         // all of this CTA's threads sent tile jj+1, i.e. after they read X[bb]
         if (h == 0 && hf == 0 && jj + 2 < ntiles) tc::mbar_arrive_expect_tx(&xfull[bb], L::X_BYTES);
       }
-      // send this thread's 16 columns of tile j: asynchronous stores that
-      // complete on the peer's barrier when they land (no fence, no remote arrival)
+      // stage this thread's 16 columns of tile j for the sender (same swizzled
+      // layout as the peer's exchange buffer); staging buffer b is free once
+      // the bulk copy of tile j-2 has read it
       if (j < ntiles) {
         const int b = j & 1;
-        const uint32_t dst = x_peer_row + b * L::X_BYTES;
-        const uint32_t rbar = peer_xfull + b * 8;
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(&sb_empty[b], ((j >> 1) & 1) ^ 1u, abort_flag))) {
+          ok = false;
+          break;
+        }
+        unsigned char* srow = gbase + L::OFF_SB + b * L::X_BYTES + h * (MT_N * 4);
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          tc::st_async_v4(dst + (((hf * 4 + q) ^ (h & 7)) << 4), rbar, __uint_as_float(nxt[4 * q]),
-                          __uint_as_float(nxt[4 * q + 1]), __uint_as_float(nxt[4 * q + 2]),
-                          __uint_as_float(nxt[4 * q + 3]));
+          *reinterpret_cast<uint4*>(srow + (((hf * 4 + q) ^ (h & 7)) << 4)) =
+              make_uint4(nxt[4 * q], nxt[4 * q + 1], nxt[4 * q + 2], nxt[4 * q + 3]);
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive(&sb_full[b]);
       }
       if (j > 0) {
         const int jj = j - 1, bb = jj & 1;

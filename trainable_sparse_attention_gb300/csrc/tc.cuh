@@ -246,6 +246,18 @@ __device__ __forceinline__ void st_async_v4(uint32_t raddr, uint32_t rbar, float
                "f"(a), "f"(b), "f"(c), "f"(d), "r"(rbar)
                : "memory");
 }
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory into the
+// shared memory of a CTA of the cluster (raddr, from mapa); the copied bytes
+// complete on that CTA's mbarrier rbar.  Both addresses 16-byte aligned.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t raddr, uint32_t src, uint32_t bytes, uint32_t rbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(raddr),
+      "r"(src), "r"(bytes), "r"(rbar)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until the source of every committed bulk copy of this thread has been read.
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // Arrive on an mbarrier of another CTA in the cluster, releasing prior writes.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t raddr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(raddr) : "memory");
