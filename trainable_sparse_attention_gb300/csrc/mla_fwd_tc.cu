@@ -18,7 +18,9 @@
 // selected row is read once.
 //
 // Per CTA, TMEM columns [0,256) = O slice, [256,320) = two 32-key S buffers,
-// [320, 320 + 32 kb) = the q slice (the A operand of QK^T, loaded once).
+// [320, 320 + 32 kb) = the q slice (the A operand of QK^T, loaded once),
+// [480,512) = two P buffers (the A operand of PV, written by the softmax with
+// tcgen05.st: no shared memory and no proxy fence between softmax and PV).
 // Warps 0-7: softmax, two warps per TMEM lane quadrant (thread = head = TMEM
 // lane), each owning 16 of the 32 key columns of a tile: the two halves of a
 // row agree on the tile maximum through shared memory and keep partial row
@@ -52,6 +54,7 @@ constexpr int MT_DV = 512;
 constexpr int MT_OCOLS = 256;    // value channels per CTA (TMEM columns [0, 256))
 constexpr int MT_SCOL = 256;     // TMEM column of the two S buffers
 constexpr int MT_QCOL = 320;     // TMEM column of the q slice (up to 160 columns)
+constexpr int MT_PCOL = 480;     // TMEM column of the two P buffers (32 keys of bf16 pairs = 16 columns each)
 constexpr float kRescaleLog2 = 8.f;
 
 template <int D>
@@ -61,16 +64,14 @@ struct MtLayout {
   static constexpr int KBMAX = KB1 > KB0 ? KB1 : KB0;
   static constexpr int KV_BLOCK = MT_N * 128;        // one 64-channel column block of a tile
   static constexpr int KV_STAGE = KBMAX * KV_BLOCK;
-  static constexpr int P_BYTES = MT_H * 128;         // one P buffer (keys 0..31 of 128-byte rows)
   static constexpr int X_BYTES = MT_H * MT_N * 4;    // one exchange buffer
   static constexpr int OFF_KV = 0;
-  static constexpr int OFF_P = OFF_KV + MT_STAGES * KV_STAGE;
-  static constexpr int OFF_X = OFF_P + 2 * P_BYTES;
+  static constexpr int OFF_X = OFF_KV + MT_STAGES * KV_STAGE;
   static constexpr int OFF_SB = OFF_X + 2 * X_BYTES;  // two staging buffers of this CTA's partials (same layout as X)
   static constexpr int OFF_M = OFF_SB + 2 * X_BYTES;  // [2 parity][2 halves][128] row maxima / sums
   static constexpr int OFF_BAR = OFF_M + 2 * 2 * MT_H * 4;
   static constexpr int SMEM = 1024 + OFF_BAR + 512;
-  static_assert(MT_QCOL + 32 * KBMAX <= 512, "TMEM columns");
+  static_assert(MT_QCOL + 32 * KBMAX <= MT_PCOL && MT_PCOL + 2 * 16 <= 512, "TMEM columns");
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -89,7 +90,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* gbase = smem_raw + (base - raw);
-  const uint32_t sKV = base + L::OFF_KV, sP = base + L::OFF_P;
+  const uint32_t sKV = base + L::OFF_KV;
   // [2][128][32] partial logits written by the peer; chunk q (4 floats) of row h
   // sits at chunk q ^ (h & 7), so the 16-byte stores and loads of a warp spread
   // over all banks
@@ -274,9 +275,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
         const int st = j % MT_STAGES;
 #pragma unroll
         for (int ks = 0; ks < MT_N / 16; ++ks) {
-          const uint64_t ad = tc::desc_sw128(sP + pb * L::P_BYTES + ks * 32);
           const uint64_t bd = tc::desc_sw128_mn(sKV + st * L::KV_STAGE + ks * 2048, L::KV_BLOCK);
-          tc::mma_bf16_ss(tmem, ad, bd, idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
+          tc::mma_bf16_ts(tmem, tmem + MT_PCOL + pb * 16 + ks * 8, bd, idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
         }
         tc::mma_commit(&kv_empty[st]);
         tc::mma_commit(&p_empty[pb]);
@@ -437,13 +437,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
           }
           tc::tmem_st_wait();
         }
-        // P row h: this half's 16 bf16 = chunks 2 hf, 2 hf + 1 of a 128-byte-swizzled K-major row
-        unsigned char* prow = gbase + L::OFF_P + bb * L::P_BYTES + h * 128;
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-          *reinterpret_cast<uint4*>(prow + (((2 * hf + c) ^ (h & 7)) << 4)) =
-              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        tc::fence_proxy_async_smem();
+        // P row h, this half's 16 keys = 8 columns of TMEM P buffer bb (the A operand of PV)
+        __syncwarp();
+        tc::tmem_st8(tmem + lane_base + MT_PCOL + bb * 16 + hf * 8, pk);
+        tc::tmem_st_wait();
         tc::fence_before_sync();
         tc::mbar_arrive(&p_full[bb]);
       }
