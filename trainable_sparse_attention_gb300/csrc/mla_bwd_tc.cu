@@ -19,7 +19,7 @@
 // The q / dO blocks are the fixed A operand (MN-major, loaded once by TMA);
 // the dS / P tiles stream through a two-stage TMA pipeline as the MN-major B
 // operand; the accumulator is double-buffered in TMEM so that the drain of
-// tile j overlaps the MMAs of tile j+1.  Eight drain warps (two per TMEM lane
+// tile j overlaps the MMAs of tile j+1.  Sixteen drain warps (four per TMEM lane
 // quadrant) keep enough reductions in flight.  All 128 heads are summed before the
 // scatter, so each selected row receives one reduction per query.
 #include "kernels.cuh"
@@ -35,12 +35,12 @@ namespace {
 constexpr int BH = 128;           // heads = MMA K of this GEMM
 constexpr int DK_NS = 128;        // slots per tile (MMA N)
 constexpr int DK_STAGES = 2;
-constexpr int DK_THREADS = 320;   // warps 0-7 drain, warp 8 TMA producer, warp 9 MMA
-constexpr int DK_DRAIN = 8;       // drain warps: TMEM lane quadrant w % 4, slot half w / 4
+constexpr int DK_THREADS = 576;   // warps 0-15 drain, warp 16 TMA producer, warp 17 MMA
+constexpr int DK_DRAIN = 16;      // drain warps: TMEM lane quadrant w % 4, 32-slot piece w / 4
 constexpr int DK_BOX = BH * 128;  // one 64-column box of 128 rows: 16 KB
 constexpr int DK_A = 2 * DK_BOX;  // one 128-channel A block (q or dO): 32 KB
 constexpr int DK_B = 2 * DK_BOX;  // one 128-slot B tile (dS or P): 32 KB
-constexpr int DK_XP = 32 * 32 * 4;  // per-warp transpose buffer: 4 KB
+constexpr int DK_XP = 16 * 32 * 4;  // per-warp transpose buffer (16 slots x 32 channels): 2 KB
 constexpr int DK_OFF_AQ = 0;
 constexpr int DK_OFF_AO = DK_OFF_AQ + DK_A;
 constexpr int DK_OFF_B = DK_OFF_AO + DK_A;
@@ -102,13 +102,13 @@ __global__ void __launch_bounds__(DK_THREADS, 1)
     for (int i = tid; i < DK_BOX / 16; i += DK_THREADS) z[i] = make_uint4(0u, 0u, 0u, 0u);
     tc::fence_proxy_async_smem();
   }
-  if (warp == 9) tc::tmem_alloc(tmem_slot, 256);
+  if (warp == 17) tc::tmem_alloc(tmem_slot, 256);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
+  if (warp == 16) {
     if (lane == 0) {
       const uint32_t sAq = base + DK_OFF_AQ, sAo = base + DK_OFF_AO;
       const int qboxes = nch / 64;
@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(DK_THREADS, 1)
         }
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == 17) {
     if (lane == 0) {
       // A (q / dO block, channels contiguous) and B (dS / P tile, slots contiguous) are both MN-major.
       const uint32_t idesc = tc::idesc_bf16_f32(128, DK_NS) | (1u << 15) | (1u << 16);
@@ -166,51 +166,48 @@ __global__ void __launch_bounds__(DK_THREADS, 1)
   } else {
     // ------------------------------------------------------------ drain
     // warp w: channels 32 (w % 4) .. +31 (its TMEM lane quadrant), slots
-    // 64 (w / 4) .. +63 of each tile, in two pieces of 32.  The slot rows of
-    // the next tile are loaded while this one drains.
-    const int qd = warp & 3, hf = warp >> 2;
+    // 32 (w / 4) .. +31 of each tile, transposed through shared memory in two
+    // halves of 16 slots.  The slot rows of the next tile are loaded while
+    // this one drains.
+    const int qd = warp & 3, pc = warp >> 2;
     const int sq = seq_of(a.st, t);
     const int s0 = a.st.cu[sq];
     const int n = a.st.cu[sq + 1] - s0;
     const int* idx_row = a.idx + (int64_t)t * a.topk;
-    float* xb = reinterpret_cast<float*>(gbase + DK_OFF_X + warp * DK_XP);  // [32 slots][32 channels]
+    float* xb = reinterpret_cast<float*>(gbase + DK_OFF_X + warp * DK_XP);  // [16 slots][32 channels]
     const bool live = qd * 32 < nch;
     const int cq = (lane & 7) * 4;  // this lane's 4 channels within the warp's 32 in the scatter
     float* dkv_base = a.dkv_acc + ch0 + qd * 32 + cq;
-    auto rows_of = [&](int j, int pc) -> int {
-      const int slot = j * DK_NS + hf * 64 + pc * 32 + lane;
+    auto rows_of = [&](int j) -> int {
+      const int slot = j * DK_NS + pc * 32 + lane;
       if (slot >= a.topk) return -1;
       const int id = __ldg(idx_row + slot);
       return (id >= 0 && id < n) ? s0 + id : -1;
     };
-    int nx0 = live ? rows_of(0, 0) : -1, nx1 = live ? rows_of(0, 1) : -1;
+    int nx = live ? rows_of(0) : -1;
     for (int j = 0; j < ntiles; ++j) {
       const int acc = j & 1;
-      const int my0 = nx0, my1 = nx1;
-      if (live && j + 1 < ntiles) {
-        nx0 = rows_of(j + 1, 0);
-        nx1 = rows_of(j + 1, 1);
-      }
+      const int my = nx;
+      if (live && j + 1 < ntiles) nx = rows_of(j + 1);
       if (!__all_sync(0xffffffffu, tc::mbar_wait(&dfull[acc], (j >> 1) & 1, abort_flag))) {
         *abort_flag = 1;
         break;
       }
       tc::fence_after_sync();
       if (live) {
+        uint32_t r[32];
+        tc::tmem_ld32(tmem + (static_cast<uint32_t>(qd * 32) << 16) + acc * DK_NS + pc * 32, r);
+        tc::tmem_ld_wait();
 #pragma unroll
-        for (int pc = 0; pc < 2; ++pc) {
-          const int my = pc == 0 ? my0 : my1;
-          uint32_t r[32];
-          tc::tmem_ld32(tmem + (static_cast<uint32_t>(qd * 32) << 16) + acc * DK_NS + hf * 64 + pc * 32, r);
-          tc::tmem_ld_wait();
+        for (int hh = 0; hh < 2; ++hh) {
           // transpose through shared memory: xb[slot][channel]
 #pragma unroll
-          for (int i = 0; i < 32; ++i) xb[i * 32 + lane] = __uint_as_float(r[i]);
+          for (int i = 0; i < 16; ++i) xb[i * 32 + lane] = __uint_as_float(r[16 * hh + i]);
           __syncwarp();
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
+          for (int k = 0; k < 4; ++k) {
             const int sl = 4 * k + (lane >> 3);
-            const int row = __shfl_sync(0xffffffffu, my, sl);
+            const int row = __shfl_sync(0xffffffffu, my, 16 * hh + sl);
             const float4 v = *reinterpret_cast<const float4*>(xb + sl * 32 + cq);
             if (row >= 0) red_v4(dkv_base + (int64_t)row * a.D, v.x, v.y, v.z, v.w);
           }
@@ -225,7 +222,7 @@ __global__ void __launch_bounds__(DK_THREADS, 1)
   tc::fence_before_sync();
   __syncthreads();
   if (*abort_flag && tid == 0) raise_flag(a.flags, TSA_FLAG_TIMEOUT);
-  if (warp == 9) {
+  if (warp == 17) {
     __syncwarp();
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, 256);
