@@ -59,7 +59,7 @@ constexpr int sp_smem() {
 
 constexpr int DQ_N = 64;          // slots per tile (MMA K per tile)
 constexpr int DQ_STAGES = 4;
-constexpr int DQ_THREADS = 288;   // warps 0-3 and 5-8 gather (thread 0 also loads the dS tiles, 0-3 drain dQ), warp 4 MMA
+constexpr int DQ_THREADS = 544;   // warps 0-3 and 5-16 gather (thread 0 also loads the dS tiles, 0-3 drain dQ), warp 4 MMA
 constexpr int DQ_A = PB_H * 128;  // dS tile: 128 rows x 64 slots bf16 = 16 KB
 constexpr int DQ_BBLK = DQ_N * 128;  // 64 channels x 64 slots = 8 KB
 constexpr int DQ_B = 5 * DQ_BBLK;    // up to 320 channels
@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   if (tid == 0) {
     for (int i = 0; i < DQ_STAGES; ++i) {
       tc::mbar_init(&afull[i], 1);
-      tc::mbar_init(&bfull[i], 256);
+      tc::mbar_init(&bfull[i], 512);
       tc::mbar_init(&sempty[i], 1);
     }
     tc::mbar_init(dfull, 1);
@@ -415,22 +415,23 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       if (!ok) *abort_flag = 1;
     }
   } else {
-    // ------------------------------------------------------------ gather (8 warps)
-    // Warp g (0..7 over warps 0-3, 5-8) copies rows 8g .. 8g+7 of each 64-row
-    // tile; lane l copies the 16-byte chunks l, l+32 of the row's channel
-    // slice, so one instruction covers up to 512 contiguous bytes.
+    // ------------------------------------------------------------ gather (16 warps)
+    // Warp g (0..15 over warps 0-3, 5-16) copies rows 4g .. 4g+3 of each
+    // 64-row tile (more warps keep more copies in flight); lane l copies the
+    // 16-byte chunks l, l+32 of the row's channel slice, so one instruction
+    // covers up to 512 contiguous bytes.
     const int g = warp < 4 ? warp : warp - 1;
-    const int w8 = g * 8;
+    const int w8 = g * 4;
     const int nchunk = nch / 8;  // 32 or 40
     const char* kvb = reinterpret_cast<const char*>(a.kv);
     bool ok = true;
     if (tid == 0) tc::prefetch_tmap(&tm_ds);
-    int id_next = (lane < 8 && w8 + lane < a.topk) ? __ldg(idx_row + w8 + lane) : -1;
+    int id_next = (lane < 4 && w8 + lane < a.topk) ? __ldg(idx_row + w8 + lane) : -1;
     for (int j = 0; j < ntiles; ++j) {
       const int st = j % DQ_STAGES;
       const int id_mine = id_next;
       const int slot_next = (j + 1) * DQ_N + w8 + lane;
-      id_next = (lane < 8 && slot_next < a.topk) ? __ldg(idx_row + slot_next) : -1;
+      id_next = (lane < 4 && slot_next < a.topk) ? __ldg(idx_row + slot_next) : -1;
       if (!__all_sync(0xffffffffu, tc::mbar_wait(&sempty[st], ((j / DQ_STAGES) & 1) ^ 1u, abort_flag))) {
         ok = false;
         break;
@@ -441,7 +442,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         tc::tma_load_2d_hint(base + st * DQ_STAGE, &tm_ds, &afull[st], j * DQ_N, lq * PB_H, tc::policy_evict_first());
       }
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
+      for (int r = 0; r < 4; ++r) {
         const int id = __shfl_sync(0xffffffffu, id_mine, r);
         const int row = w8 + r;
         const bool valid = id >= 0 && id < n;
