@@ -19,7 +19,7 @@
 //   pass 2: dP = dO V^T with the dO rows in TMEM, dS = scale P (dP - Dlt)
 //           from the bf16 P of pass 1, written in bf16.
 // Each pass streams its gathered 64-row tiles through a three-stage ring
-// (cp.async, 4 producer warps) and double-buffers the accumulator in TMEM;
+// (cp.async, 8 producer warps) and double-buffers the accumulator in TMEM;
 // warps 0-7 (two per TMEM lane quadrant, thread = head, 32 of the 64 key
 // columns each) write [query][head][slot] rows, slots padded to kp with zeros.  No softmax state is carried between tiles: L is
 // known, so every tile is final when it is computed.
@@ -46,8 +46,8 @@ constexpr int PB_H = 128;        // heads = MMA M
 constexpr int SP_H = PB_H;
 constexpr int SP_N = 64;         // keys per tile (MMA N)
 constexpr int SP_STAGES = 3;
-constexpr int SP_PRODUCERS = 128;
-constexpr int SP_THREADS = 288 + SP_PRODUCERS;  // warps 0-7 epilogue, warp 8 MMA, warps 9-12 gather
+constexpr int SP_PRODUCERS = 256;
+constexpr int SP_THREADS = 288 + SP_PRODUCERS;  // warps 0-7 epilogue, warp 8 MMA, warps 9-16 gather
 constexpr int SP_ACC = 288;      // first TMEM column of the two accumulators (after the A operand)
 
 constexpr int SP_PTILE = SP_H * 128;  // one P tile of the dS pass: 128 heads x 64 slots bf16
@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    tc::mbar_init(aready, 12);
+    tc::mbar_init(aready, 16);
     for (int i = 0; i < SP_STAGES; ++i) {
       tc::mbar_init(&kv_full[i], SP_PRODUCERS);
       tc::mbar_init(&kv_empty[i], 1);
@@ -135,14 +135,14 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   // A rows -> TMEM columns [0, KC/2), 32 columns (64 channels) per store.  The
-  // three warps that share a TMEM lane quadrant (epilogue warps q and q+4, the
-  // producer warp of that quadrant) split the KB blocks of their 32 rows.
+  // four warps that share a TMEM lane quadrant (epilogue warps q and q+4, the
+  // two producer warps of that quadrant) split the KB blocks of their 32 rows.
   auto load_a_rows = [&](int share) {
     const int h = (warp & 3) * 32 + lane;
     const uint4* arow = DS ? reinterpret_cast<const uint4*>(a.dout + ((int64_t)t * SP_H + h) * 512)
                            : reinterpret_cast<const uint4*>(a.q + ((int64_t)t * SP_H + h) * D);
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    for (int c = share; c < KB; c += 3) {
+    for (int c = share; c < KB; c += 4) {
       uint32_t r[32];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -162,31 +162,31 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
   };
 
   if (warp >= 9) {
-    // ------------------------------------------------------------ gather producers (4 warps)
-    // Warp w copies rows 16w .. 16w+15 of each 64-row tile; lane l copies the
+    // ------------------------------------------------------------ gather producers (8 warps)
+    // Warp w copies rows 8w .. 8w+7 of each 64-row tile; lane l copies the
     // 16-byte chunks l, l+32, ... of a row, so one instruction covers 512
     // contiguous bytes of the row.  The chunks land in the 128-byte-swizzled
     // K-major tile, and each thread's copies arrive asynchronously on the
     // stage's barrier when they land.  The slot indices of the next tile are
-    // loaded one tile ahead (lane r < 16 holds row 16w + r).
-    const int w8 = (warp - 9) * 16;
+    // loaded one tile ahead (lane r < 8 holds row 8w + r).
+    const int w8 = (warp - 9) * 8;
     constexpr int NCH = KC / 8;  // 16-byte chunks per row
     const char* kvb = reinterpret_cast<const char*>(a.kv);
     bool ok = true;
     const int npre = ntiles < SP_STAGES ? ntiles : SP_STAGES;
-    int id_next = (lane < 16 && w8 + lane < a.topk) ? __ldg(idx_row + w8 + lane) : -1;
+    int id_next = (lane < 8 && w8 + lane < a.topk) ? __ldg(idx_row + w8 + lane) : -1;
     for (int j = 0; j < ntiles; ++j) {
       const int st = j % SP_STAGES;
       const int id_mine = id_next;
       const int slot_next = (j + 1) * SP_N + w8 + lane;
-      id_next = (lane < 16 && slot_next < a.topk) ? __ldg(idx_row + slot_next) : -1;
+      id_next = (lane < 8 && slot_next < a.topk) ? __ldg(idx_row + slot_next) : -1;
       if (!__all_sync(0xffffffffu, tc::mbar_wait(&kv_empty[st], ((j / SP_STAGES) & 1) ^ 1u, abort_flag))) {
         ok = false;
         break;
       }
-      if (!DS && lane < 16 && id_mine >= n) raise_flag(a.flags, TSA_FLAG_INDEX_RANGE);
-#pragma unroll 4
-      for (int r = 0; r < 16; ++r) {
+      if (!DS && lane < 8 && id_mine >= n) raise_flag(a.flags, TSA_FLAG_INDEX_RANGE);
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
         const int id = __shfl_sync(0xffffffffu, id_mine, r);
         const int row = w8 + r;
         const bool valid = id >= 0 && id < n;
@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
       asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&kv_full[st]))
                    : "memory");
       // the first tiles are in flight: help load the A rows
-      if (j == npre - 1) load_a_rows(2);
+      if (j == npre - 1) load_a_rows(warp < 13 ? 2 : 3);
     }
     cp_async_wait<0>();
     if (!ok) *abort_flag = 1;
