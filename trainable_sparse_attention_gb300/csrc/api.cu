@@ -97,11 +97,16 @@ int64_t score_width(int max_len, int block_size) {
   return block_size == 1 ? max_len : (max_len + block_size - 1) / block_size;
 }
 
-// Query rows per streamed chunk: the chunk's scores stay within ~64 MB (L2-sized).
+// Score scratch of one query chunk of the streaming indexer + top-k.  Large
+// enough that a chunk's top-k launch has thousands of rows (one CTA each) in
+// flight; far below the T x T scores it replaces.
+static constexpr int64_t kScoreChunkBytes = int64_t(512) << 20;
+
+// Query rows per streamed chunk: the chunk's scores stay within kScoreChunkBytes.
 int64_t chunk_rows(int max_len, int groups, int block_size) {
   int64_t w = score_width(max_len, block_size);
   if (w < 1) w = 1;
-  int64_t c = (int64_t(64) << 20) / (4 * w * groups);
+  int64_t c = kScoreChunkBytes / (4 * w * groups);
   c = (c / 128) * 128;
   if (c < 128) c = 128;
   if (c > max_len) c = max_len;
