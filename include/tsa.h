@@ -182,7 +182,7 @@ int sparse_mla_fwd(const void* q_dev, const void* kv_dev, const int32_t* indices
  *   dq_dev bf16 [T, H, d_qk], dkv_dev bf16 [T, d_qk] (fully overwritten).
  *   workspace: sparse_mla_bwd_workspace_size(T, H, d_qk, topk) bytes: fp32
  *   dkv and Dlt, and for H = 128 a bf16 staging area for P and dS of one
- *   chunk of queries (at most 1 GiB; the chunk shrinks as topk grows).
+ *   chunk of queries (at most 4 GiB; the chunk shrinks as topk grows).
  *   Returns 0 for T < 0, H < 1, d_qk < 1 or topk < 1.
  * Same support as sparse_mla_fwd.  dkv summation order is not fixed.
  * ------------------------------------------------------------------------- */

@@ -312,7 +312,7 @@ int sparse_mla_fwd(const void* q, const void* kv, const int32_t* indices, const 
 // The 128-head backward stages P and dS of one chunk of queries in bf16
 // ([query][head][slot], slots rounded up to 128) for the dKV GEMM; the chunk
 // is sized so that the staging stays within kMlaStageBytes.
-static constexpr int64_t kMlaStageBytes = int64_t(1) << 30;
+static constexpr int64_t kMlaStageBytes = int64_t(4) << 30;
 
 static int64_t mla_kp(int topk) { return (static_cast<int64_t>(topk) + 127) / 128 * 128; }
 
