@@ -40,7 +40,7 @@ TOPK = 2048
 # DRAM bytes (read + write) of one forward launch per query, from an ncu capture
 # of the current forward kernel on the same workload at T=4096 (scaled by the
 # number of queries); None when the kernel changed since the capture.
-FWD_TRAFFIC_BYTES_PER_QUERY = None
+FWD_TRAFFIC_BYTES_PER_QUERY = 277695
 SCALE = 1.0 / math.sqrt(192)
 H_I = 64
 D_I = 128
