@@ -365,8 +365,11 @@ def run_gpu(args):
 
 
 def run_e2e(args, tsa, dev, cu, dev_inputs, f_step, world):
-    """Same step through the public API from pinned host buffers: H2D of every
-    input and D2H of every output inside the timed region."""
+    """Same step through the public API from pinned host buffers: every step
+    copies its inputs host -> device and reads its results device -> host
+    inside the timed region.  The copies are pipelined with the compute: the
+    inputs of step i+1 are copied (H2D stream, second device buffer set) and
+    the results of step i read back (D2H stream) while step i+1 computes."""
     import torch
     host_in = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in dev_inputs.items()}
     for k, v in dev_inputs.items():
@@ -374,41 +377,76 @@ def run_e2e(args, tsa, dev, cu, dev_inputs, f_step, world):
     outs_shape = {"idx": ((T_TOK, 1, TOPK), torch.int32), "out": ((T_TOK, H, DV), torch.bfloat16),
                   "lse": ((T_TOK, H), torch.float32), "dq": ((T_TOK, H, D), torch.bfloat16),
                   "dkv": ((T_TOK, D), torch.bfloat16)}
-    host_out = {k: torch.empty(s, dtype=d, pin_memory=True) for k, (s, d) in outs_shape.items()}
+    host_out = [{k: torch.empty(s, dtype=d, pin_memory=True) for k, (s, d) in outs_shape.items()} for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
-    stream = torch.cuda.current_stream()
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
+    comp = torch.cuda.current_stream()
+    s_in = torch.cuda.Stream()
+    s_out = torch.cuda.Stream()
     ws_topk = torch.empty(tsa.qsa_topk_workspace_size(cu), dtype=torch.uint8, device=dev)
     ws_bwd = torch.empty(tsa.sparse_mla_bwd_workspace_size(T_TOK, H, D, TOPK), dtype=torch.uint8, device=dev)
-    d_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+    d_in = [dict(dev_inputs), {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}]
 
-    def e2e_step():
-        for k in host_in:
-            d_in[k].copy_(host_in[k], non_blocking=True)
-        idx = tsa.qsa_topk(d_in["q_idx"], d_in["k_idx"], d_in["w"], cu, TOPK, workspace=ws_topk)
+    def copy_in(i, after):
+        # inputs of step i into buffer set i % 2, once the step that last read it has finished
+        with torch.cuda.stream(s_in):
+            if after is not None:
+                s_in.wait_event(after)
+            for k in host_in:
+                d_in[i % 2][k].copy_(host_in[k], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(s_in)
+        return ev
+
+    def compute(i, ready):
+        comp.wait_event(ready)
+        x = d_in[i % 2]
+        idx = tsa.qsa_topk(x["q_idx"], x["k_idx"], x["w"], cu, TOPK, workspace=ws_topk)
         i2 = idx.view(T_TOK, TOPK)
-        out, lse = tsa.sparse_mla_fwd(d_in["q"], d_in["kv"], i2, cu, SCALE)
-        dq, dkv = tsa.sparse_mla_bwd(d_in["q"], d_in["kv"], i2, out, lse, d_in["dout"], cu, SCALE, workspace=ws_bwd)
-        for k, t in (("idx", idx), ("out", out), ("lse", lse), ("dq", dq), ("dkv", dkv)):
-            host_out[k].copy_(t, non_blocking=True)
+        out, lse = tsa.sparse_mla_fwd(x["q"], x["kv"], i2, cu, SCALE)
+        dq, dkv = tsa.sparse_mla_bwd(x["q"], x["kv"], i2, out, lse, x["dout"], cu, SCALE, workspace=ws_bwd)
+        done = torch.cuda.Event()
+        done.record(comp)
+        return {"idx": idx, "out": out, "lse": lse, "dq": dq, "dkv": dkv}, done
 
-    e2e_step()
+    def copy_out(i, res, done):
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(done)
+            for k, t in res.items():
+                host_out[i % 2][k].copy_(t, non_blocking=True)
+                t.record_stream(s_out)
+
+    def run(nsteps, start=None):
+        ready = copy_in(0, start)  # the first copy belongs to the timed region
+        prev_done = None
+        for i in range(nsteps):
+            res, done = compute(i, ready)
+            if i + 1 < nsteps:
+                ready = copy_in(i + 1, prev_done)  # buffer set (i+1) % 2 was last read by step i-1
+            copy_out(i, res, done)
+            prev_done = done
+            del res
+
+    run(1)
     torch.cuda.synchronize()
-    steps = max(1, min(args.steps, 3))
+    steps = max(1, min(args.steps, 5))
     barrier(world)
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        e2e_step()
-    b.record(stream)
+    a.record(comp)
+    run(steps, a)
+    s_out_done = torch.cuda.Event()
+    s_out_done.record(s_out)
+    comp.wait_event(s_out_done)
+    b.record(comp)
     torch.cuda.synchronize()
     ms = allmax(a.elapsed_time(b) / steps, world)
     del d_in, host_in, host_out
     torch.cuda.empty_cache()
     return {"value": world * f_step / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "pipelined": "H2D of step i+1 and D2H of step i overlap the compute of step i+1"}
 
 
 def main():
