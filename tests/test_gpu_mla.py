@@ -241,7 +241,8 @@ def test_mla_h128_large_logits_rescale(tsa):
     (576, 65, [130, 200]),       # THD; slots padded from 65 to 128 for the dKV GEMM
     (576, 1000, [700]),          # -1 tails
     (512, 96, [257]),            # NoPE layout: four 128-channel dKV blocks
-    (576, 2048, [2100]),         # three query chunks of the P/dS staging
+    (576, 2048, [2100]),         # 33 tiles of 64 slots
+    (576, 4000, [2100, 300]),    # kp = 4096: 2048-query P/dS chunks, a boundary inside sequence 0
 ])
 def test_mla_h128_backward(tsa, D, topk, lengths):
     """H = 128 backward (recompute of P/dS + tcgen05 dKV GEMM): dO is kept on
