@@ -53,6 +53,26 @@ def test_topk_from_scores_distinct_random(tsa):
     np.testing.assert_array_equal(got, O.topk_rows(s.numpy(), 1000))
 
 
+@pytest.mark.parametrize("L,k", [(20000, 2048), (9000, 1), (12000, 300), (15000, 700), (70000, 4096),
+                                 (5000, 4096), (65536, 2048)])
+def test_topk_from_scores_selection_branches(tsa, L, k):
+    """Long rows through each branch of the selection: distinct values (the
+    threshold bin fits the key buffer), a tie level of 5000 equal scores at the
+    threshold (it does not: the exact three-digit search), and rows with fewer
+    finite entries than k (all kept)."""
+    g = torch.Generator().manual_seed(L + k)
+    distinct = torch.randn((2, L), generator=g)
+    ties = torch.randn((2, L), generator=g) * 0.1
+    ties[:, torch.randperm(L, generator=g)[:5000]] = 1.0    # 5000 exact ties just below the top
+    ties[:, torch.randperm(L, generator=g)[:k // 2]] = 5.0   # k/2 clear winners (also tied)
+    sparse = torch.full((2, L), -math.inf)
+    keep = torch.randperm(L, generator=g)[:max(1, k - 7)]
+    sparse[:, keep] = torch.randn((2, keep.numel()), generator=g).abs().round()  # few distinct values, +0.0 ties
+    s = torch.cat([distinct, ties, sparse]).contiguous()
+    got = tsa.qsa_topk_from_scores(s.to(DEV), k).cpu().numpy()
+    np.testing.assert_array_equal(got, O.topk_rows(s.numpy(), k))
+
+
 def test_topk_deterministic_replay_under_contention(tsa):
     s = synth.tie_stress_scores(256, 12000, seed=9).to(DEV)
     a = tsa.qsa_topk_from_scores(s, 2048)
