@@ -23,8 +23,10 @@
 // as soon as the MMAs of the previous one are done, and the head weights go
 // to the other half of a double buffer.
 //
-// Warp roles (192 threads): warps 0-3 epilogue (TMEM lanes 0-127), warp 4 TMA
-// producer, warp 5 TMEM allocator + MMA issuer (one elected thread).  Every
+// Warp roles (320 threads): warps 0-7 epilogue (warp w: TMEM lanes 32 (w % 4)
+// .. +31, accumulator columns 128 (w / 4) .. +127, so two warps share each
+// sub-partition and hide each other's latencies), warp 8 TMA producer, warp 9
+// TMEM allocator + MMA issuer (one elected thread).  Every
 // wait is bounded; a timeout raises TSA_FLAG_TIMEOUT and the CTA winds down,
 // releasing its TMEM.
 #include <algorithm>
@@ -39,7 +41,7 @@ namespace {
 constexpr int IT_M = 128;
 constexpr int IT_N = 256;
 constexpr int IT_STAGES = 4;
-constexpr int IT_THREADS = 192;
+constexpr int IT_THREADS = 320;
 
 template <int DI>
 struct ItLayout {
@@ -87,7 +89,7 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
   uint64_t* accf = bempty + 1;                 // [2]
   uint64_t* acce = accf + 2;                   // [2]
   uint64_t* wsfull = acce + 2;                 // [2] head weights of a block written (32 lanes)
-  uint64_t* wsempty = wsfull + 2;              // [2] epilogue done with a weight buffer (4 warps)
+  uint64_t* wsempty = wsfull + 2;              // [2] epilogue done with a weight buffer (8 warps)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wsempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -135,20 +137,20 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
     tc::mbar_init(bempty, 1);
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&accf[i], 1);
-      tc::mbar_init(&acce[i], 4);
+      tc::mbar_init(&acce[i], 8);
       tc::mbar_init(&wsfull[i], 32);
-      tc::mbar_init(&wsempty[i], 4);
+      tc::mbar_init(&wsempty[i], 8);
     }
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
-  if (warp == 5) tc::tmem_alloc(tmem_slot, 512);
+  if (warp == 9) tc::tmem_alloc(tmem_slot, 512);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer: head weights (all lanes), TMA (lane 0)
     if (lane == 0) {
       tc::prefetch_tmap(&tm_q);
@@ -199,7 +201,7 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
       advance(w, it);
     }
     if (!ok) *abort_flag = 1;
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16_f32(IT_M, IT_N);
@@ -232,8 +234,9 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
       if (!ok) *abort_flag = 1;
     }
   } else {
-    // ------------------------------------------------------------ epilogue (warps 0-3)
-    const int key_in_tile = warp * 32 + lane;
+    // ------------------------------------------------------------ epilogue (warps 0-7)
+    const int qd = warp & 3, ch = warp >> 2;  // lane quadrant, column half
+    const int key_in_tile = qd * 32 + lane;
     ItWalk w = start;
     for (int it = 0; it < nitems; ++it) {
       const int acc = it & 1;
@@ -247,32 +250,37 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
       tc::fence_after_sync();
       const int q0 = w.qb * QB, qn = min(QB, a.nq - q0);
       const int p_first = a.p_begin + q0;
-      const float* W = Ws + wb * IT_N;
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + acc * IT_N;
+      const float4* W4 = reinterpret_cast<const float4*>(Ws + wb * IT_N + ch * (IT_N / 2));  // 16-byte aligned
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(qd * 32) << 16) + acc * IT_N + ch * (IT_N / 2);
       const int s = w.kt * IT_M + key_in_tile;
       // four partial sums of the current (query, group) segment break the FMA
       // dependency chain; the TMEM load of block cb+1 is in flight while block
-      // cb is reduced
+      // cb is reduced; the head weights come four at a time
       float run[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t rbuf[2][32];
+      constexpr int NCB = IT_N / 64;  // 32-column blocks of this warp's half
       __syncwarp();
       tc::tmem_ld32(taddr, rbuf[0]);
 #pragma unroll
-      for (int cb = 0; cb < IT_N / 32; ++cb) {
+      for (int cb = 0; cb < NCB; ++cb) {
         uint32_t* r = rbuf[cb & 1];
         tc::tmem_ld_wait();
         tc::reg_dep32(r);
-        if (cb + 1 < IT_N / 32) {
+        if (cb + 1 < NCB) {
           __syncwarp();  // converged for the .sync.aligned load
           tc::tmem_ld32(taddr + (cb + 1) * 32, rbuf[(cb + 1) & 1]);
         }
+        float4 wv;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          run[j & 3] = fmaf(W[cb * 32 + j], fmaxf(__uint_as_float(r[j]), 0.f), run[j & 3]);
+          if ((j & 3) == 0) wv = W4[cb * 8 + (j >> 2)];
+          const float wj = (j & 3) == 0 ? wv.x : (j & 3) == 1 ? wv.y : (j & 3) == 2 ? wv.z : wv.w;
+          run[j & 3] = fmaf(wj, fmaxf(__uint_as_float(r[j]), 0.f), run[j & 3]);
+          const int col = ch * (IT_N / 2) + cb * 32 + j;  // accumulator column = (query, head)
           const bool seg_done = (HG <= 32) ? ((j + 1) % HG == 0) : (j == 31 && ((cb + 1) * 32) % HG == 0);
           if (seg_done) {
             const float tot = (run[0] + run[1]) + (run[2] + run[3]);
-            const int sg = (cb * 32 + j) / HG;
+            const int sg = col / HG;
             const int qq = sg / a.groups, gg = sg % a.groups;
             if (qq < qn && s <= p_first + qq)
               a.out[((int64_t)(q0 + qq) * a.groups + gg) * a.width + s] = tot * a.score_scale + 0.f;

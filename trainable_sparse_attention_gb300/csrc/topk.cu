@@ -347,26 +347,57 @@ __global__ void __launch_bounds__(TK_THREADS, 3) topk_rows_kernel(TopkRows a) {
   __syncthreads();
   const int64_t sample = static_cast<int64_t>(TK_PER) * TK_THREADS;
   const int64_t target = static_cast<int64_t>(k) + (k >> 2);
-  find_bin(hist, TK_BINS, static_cast<uint32_t>((target * sample + n - 1) / n), warp_tot, sh);
+  const uint32_t tq = static_cast<uint32_t>((target * sample + n - 1) / n);  // the target rank in the sample
+  find_bin(hist, TK_BINS, tq, warp_tot, sh);
   const int gbin = sh[0];
 
   if (gbin >= 0) {
-    // ---- guided sweep: gather every candidate >= g (float order; -0.0 == +0.0)
-    const float g = bin_floor(gbin);
+    // ---- guided sweep: gather every candidate >= g (float order; -0.0 ==
+    // +0.0).  g interpolates inside the sample's bin, assuming its entries
+    // spread evenly over the bin's score range.  Warp w appends to its own
+    // region of WCAP keys: ballots rank the lanes and the warp's count stays
+    // in a register, so the sweep has no atomics and no shuffles.
+    float g = bin_floor(gbin);
+    if (gbin + 1 < TK_BINS) {
+      const float top = bin_floor(gbin + 1);
+      const float f = static_cast<float>(tq - static_cast<uint32_t>(sh[1])) / static_cast<float>(hist[gbin]);
+      g = top - f * (top - g);
+    }
+    constexpr int WCAP = TK_MAXK / TK_WARPS;
+    uint64_t* wk = keys + warp * WCAP;
+    const uint32_t lt = (1u << lane) - 1u;
+    uint32_t wcnt = 0;  // warp-uniform
     for_runs(row, n, vec, [&](const float (&v)[TK_PER], int64_t i0) {
-      uint32_t msk = 0;
 #pragma unroll
-      for (int e = 0; e < TK_PER; ++e)
-        if (v[e] >= g && v[e] != NEG_INF) msk |= 1u << e;
-      append_keys(v, i0, msk, keys, &slots[0]);
+      for (int e = 0; e < TK_PER; ++e) {
+        const bool hit = v[e] >= g && v[e] != NEG_INF;
+        const uint32_t bal = __ballot_sync(0xffffffffu, hit);
+        if (hit) {
+          const uint32_t pos = wcnt + static_cast<uint32_t>(__popc(bal & lt));
+          if (pos < static_cast<uint32_t>(WCAP)) wk[pos] = comp_key(order_key(v[e]), static_cast<uint32_t>(i0 + e));
+        }
+        wcnt += static_cast<uint32_t>(__popc(bal));
+      }
     });
+    if (lane == 0) warp_tot[warp] = wcnt;
     __syncthreads();
-    const uint32_t cnt = slots[0];
-    if (cnt >= static_cast<uint32_t>(k) && cnt <= static_cast<uint32_t>(TK_MAXK)) {
-      finish_row(keys, static_cast<int>(cnt), k, out);
+    uint32_t cnt = 0, before = 0;
+    bool over = false;
+    for (int w = 0; w < TK_WARPS; ++w) {
+      const uint32_t t = warp_tot[w];
+      if (w < warp) before += t;
+      cnt += t;
+      over = over || t > static_cast<uint32_t>(WCAP);
+    }
+    if (!over && cnt >= static_cast<uint32_t>(k)) {
+      // the k largest are among the gathered keys: pack the regions into the
+      // (now free) histogram area and sort there
+      uint64_t* packed = reinterpret_cast<uint64_t*>(hist);
+      for (uint32_t i = lane; i < wcnt; i += 32) packed[before + i] = wk[i];
+      finish_row(packed, static_cast<int>(cnt), k, out);
       return;
     }
-    __syncthreads();  // every thread has read slots[0]
+    __syncthreads();  // every thread has read warp_tot
   }
 
   // ---- sweep 1: histogram of the first digit (top TK_BITS1 bits of u)
