@@ -69,6 +69,14 @@ __device__ __forceinline__ int it_nkt(const IndexerArgs& a, int QB, int qb) {
   return (a.p_begin + qb * QB + qn - 1) / IT_M + 1;
 }
 
+// (c0, c1) += (a0 * b0, a1 * b1), one packed fp32 FMA (each lane rounds as fmaf).
+__device__ __forceinline__ void fma2(float& c0, float& c1, float a0, float a1, float b0, float b1) {
+  asm("{\n .reg .b64 ra, rb, rc;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rc, {%0, %1};\n"
+      " fma.rn.f32x2 rc, ra, rb, rc;\n mov.b64 {%0, %1}, rc;\n}"
+      : "+f"(c0), "+f"(c1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 template <int DI, int HG>
 __global__ void __launch_bounds__(IT_THREADS, 1)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -274,8 +282,11 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           if ((j & 3) == 0) wv = W4[cb * 8 + (j >> 2)];
-          const float wj = (j & 3) == 0 ? wv.x : (j & 3) == 1 ? wv.y : (j & 3) == 2 ? wv.z : wv.w;
-          run[j & 3] = fmaf(wj, fmaxf(__uint_as_float(r[j]), 0.f), run[j & 3]);
+          if ((j & 1) == 0) {  // columns j, j+1: one packed FMA into the partial sums (j & 3), (j & 3) + 1
+            const float w0 = (j & 3) == 0 ? wv.x : wv.z, w1 = (j & 3) == 0 ? wv.y : wv.w;
+            fma2(run[j & 3], run[(j & 3) + 1], w0, w1, fmaxf(__uint_as_float(r[j]), 0.f),
+                 fmaxf(__uint_as_float(r[j + 1]), 0.f));
+          }
           const int col = ch * (IT_N / 2) + cb * 32 + j;  // accumulator column = (query, head)
           const bool seg_done = (HG <= 32) ? ((j + 1) % HG == 0) : (j == 31 && ((cb + 1) * 32) % HG == 0);
           if (seg_done) {

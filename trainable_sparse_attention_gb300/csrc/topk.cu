@@ -133,6 +133,50 @@ __device__ void bitonic_desc_reg(uint64_t* s) {
   __syncthreads();
 }
 
+// Bitonic merge of the bitonic sequence s[0..P) into descending order, P = 512 E.
+template <int E>
+__device__ void bitonic_merge_reg(uint64_t* s) {
+  constexpr int P = TK_THREADS * E;
+  constexpr int W = 32 * E;
+  for (int stride = P >> 1; stride >= W; stride >>= 1) {
+    for (int i = threadIdx.x; i < (P >> 1); i += TK_THREADS) {
+      const int pos = 2 * i - (i & (stride - 1));
+      const int par = pos + stride;
+      const uint64_t a = s[pos], b = s[par];
+      if (a < b) { s[pos] = b; s[par] = a; }
+    }
+    __syncthreads();
+  }
+  const int lane = threadIdx.x & 31;
+  const int wbase = (threadIdx.x >> 5) * W;
+  uint64_t v[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) v[e] = s[wbase + 32 * e + lane];
+  bitonic_reg_steps<E>(v, wbase, 2 * P, W >> 1);  // block length 2P: every pair descending
+#pragma unroll
+  for (int e = 0; e < E; ++e) s[wbase + 32 * e + lane] = v[e];
+  __syncthreads();
+}
+
+// Merge of a bitonic s[0..P) into descending order, P a power of two <= TK_MAXK.
+__device__ void merge_desc(uint64_t* s, int P) {
+  if (P >= 4096) bitonic_merge_reg<8>(s);
+  else if (P == 2048) bitonic_merge_reg<4>(s);
+  else if (P == 1024) bitonic_merge_reg<2>(s);
+  else if (P == 512) bitonic_merge_reg<1>(s);
+  else {
+    for (int stride = P >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < (P >> 1); i += blockDim.x) {
+        const int pos = 2 * i - (i & (stride - 1));
+        const int par = pos + stride;
+        const uint64_t a = s[pos], b = s[par];
+        if (a < b) { s[pos] = b; s[par] = a; }
+      }
+      __syncthreads();
+    }
+  }
+}
+
 // Sort s[0..P) descending, P a power of two <= TK_MAXK.
 __device__ void sort_desc(uint64_t* s, int P) {
   if (P >= 4096) bitonic_desc_reg<8>(s);
@@ -205,12 +249,11 @@ __device__ __forceinline__ void load_run(const float* row, int64_t i0, int64_t n
 // each run of TK_PER x TK_THREADS; the next run's loads are issued before f
 // processes the current one.  f(v, i0) is called by every thread for every
 // run (block-uniform trip count, so f may hold block barriers).
+// for_runs_from takes the first run already loaded (into v).
 template <class F>
-__device__ __forceinline__ void for_runs(const float* row, int64_t n, bool vec, F f) {
+__device__ __forceinline__ void for_runs_from(const float* row, int64_t n, bool vec, float (&v)[TK_PER], F f) {
   const int64_t me = static_cast<int64_t>(threadIdx.x) * TK_PER;
   const int64_t step = static_cast<int64_t>(TK_PER) * TK_THREADS;
-  float v[TK_PER];
-  load_run(row, me, n, vec, v);
   for (int64_t base = 0; base < n; base += step) {
     float nv[TK_PER];
     const bool more = base + step < n;
@@ -221,6 +264,12 @@ __device__ __forceinline__ void for_runs(const float* row, int64_t n, bool vec, 
       for (int e = 0; e < TK_PER; ++e) v[e] = nv[e];
     }
   }
+}
+template <class F>
+__device__ __forceinline__ void for_runs(const float* row, int64_t n, bool vec, F f) {
+  float v[TK_PER];
+  load_run(row, static_cast<int64_t>(threadIdx.x) * TK_PER, n, vec, v);
+  for_runs_from(row, n, vec, v, f);
 }
 
 // Appends the keys of the run entries flagged in msk (thread-local bits) to
@@ -266,9 +315,32 @@ __device__ __forceinline__ float key_score(uint64_t key) {
   return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
 }
 
-// Sorts the m keys of keys[0..m) (zero-padded to a power of two) and writes
-// the row's first k.
+// Orders the m keys of keys[0..m) and writes the row's first k.  When m is
+// between Pk = 2^ceil(log2 k) and 2 Pk, the first Pk keys (A) and the other
+// m - Pk (B, zero-padded to PB) are sorted on their own; A[i] = max(A[i],
+// B[Pk - 1 - i]) then holds the Pk largest of both as a bitonic sequence (B
+// read backwards, zeros past PB), and one merge orders them.  Otherwise all m
+// keys are sorted, zero-padded to a power of two.
 __device__ __forceinline__ void finish_row(uint64_t* keys, int m, int k, int32_t* out) {
+  int Pk = 1;
+  while (Pk < k) Pk <<= 1;
+  if (Pk >= 512 && m > Pk && m - Pk <= Pk) {
+    int PB = 1;
+    while (PB < m - Pk) PB <<= 1;
+    for (int i = m + threadIdx.x; i < Pk + PB; i += TK_THREADS) keys[i] = 0ull;
+    __syncthreads();
+    sort_desc(keys, Pk);
+    sort_desc(keys + Pk, PB);
+    for (int t = threadIdx.x; t < PB; t += TK_THREADS) {
+      const int i = Pk - PB + t;
+      const uint64_t a = keys[i], b = keys[Pk + PB - 1 - t];
+      keys[i] = a > b ? a : b;
+    }
+    __syncthreads();
+    merge_desc(keys, Pk);
+    emit(keys, Pk, k, out);
+    return;
+  }
   int P = 1;
   while (P < m) P <<= 1;
   for (int i = m + threadIdx.x; i < P; i += TK_THREADS) keys[i] = 0ull;
@@ -332,14 +404,18 @@ __global__ void __launch_bounds__(TK_THREADS, 3) topk_rows_kernel(TopkRows a) {
 
   const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
 
-  // ---- sample: thread t counts the TK_PER entries at about t n / TK_THREADS
-  for (int i = threadIdx.x; i < TK_BINS; i += TK_THREADS) hist[i] = 0;
-  if (threadIdx.x < 2) slots[threadIdx.x] = 0;
-  __syncthreads();
+  // ---- sample: thread t counts the TK_PER entries at about t n / TK_THREADS.
+  // Its loads and those of the guided sweep's first run are issued together,
+  // and the histogram is cleared while they are in flight.
+  float v0[TK_PER];
   {
     const int64_t i0 = ((static_cast<int64_t>(threadIdx.x) * n / TK_THREADS) & ~static_cast<int64_t>(TK_PER - 1));
     float v[TK_PER];
     load_run(row, i0, n, vec, v);
+    load_run(row, static_cast<int64_t>(threadIdx.x) * TK_PER, n, vec, v0);
+    for (int i = threadIdx.x; i < TK_BINS; i += TK_THREADS) hist[i] = 0;
+    if (threadIdx.x < 2) slots[threadIdx.x] = 0;
+    __syncthreads();
 #pragma unroll
     for (int e = 0; e < TK_PER; ++e)
       if (v[e] != NEG_INF) atomicAdd(&hist[order_key(v[e]) >> TK_SH1], 1u);
@@ -367,7 +443,7 @@ __global__ void __launch_bounds__(TK_THREADS, 3) topk_rows_kernel(TopkRows a) {
     uint64_t* wk = keys + warp * WCAP;
     const uint32_t lt = (1u << lane) - 1u;
     uint32_t wcnt = 0;  // warp-uniform
-    for_runs(row, n, vec, [&](const float (&v)[TK_PER], int64_t i0) {
+    for_runs_from(row, n, vec, v0, [&](const float (&v)[TK_PER], int64_t i0) {
 #pragma unroll
       for (int e = 0; e < TK_PER; ++e) {
         const bool hit = v[e] >= g && v[e] != NEG_INF;
