@@ -21,16 +21,17 @@
 // [320, 320 + 32 kb) = the q slice (the A operand of QK^T, loaded once),
 // [480,512) = two P buffers (the A operand of PV, written by the softmax with
 // tcgen05.st: no shared memory and no proxy fence between softmax and PV).
-// Warps 0-7: softmax, two warps per TMEM lane quadrant (thread = head = TMEM
-// lane), each owning 16 of the 32 key columns of a tile: the two halves of a
-// row agree on the tile maximum through shared memory and keep partial row
-// sums; each rescales and writes half of the O slice.  Warp 8: TMEM owner and
-// QK^T issuer; warp 9: PV issuer (two issuing threads, so that QK^T waiting
-// for a gather never delays a ready PV); warps 10-13: cp.async gather of the
-// selected rows into a 6-stage ring of 32-key tiles; warp 14: sender, one
-// bulk copy per tile of the staged partial logits into the peer's exchange
-// buffer (per-thread stores into the peer's shared memory held up the softmax
-// warps' next shared-memory accesses by ~0.5 us per tile).
+// Warps 0-3: softmax, one warp per TMEM lane quadrant (thread = head = TMEM
+// lane) owning all 32 key columns of a tile, so a row's maximum and sum stay
+// in one thread (two warps per quadrant, agreeing on each tile's maximum
+// through shared memory, were slower); each rescales and writes its row of
+// the O slice.  Warp 4: TMEM owner and QK^T issuer; warp 5: PV issuer (two
+// issuing threads, so that QK^T waiting for a gather never delays a ready
+// PV); warps 6-9: cp.async gather of the selected rows into a 6-stage ring of
+// 32-key tiles; warp 10: sender, one bulk copy per tile of the staged partial
+// logits into the peer's exchange buffer (per-thread stores into the peer's
+// shared memory held up the softmax warps' next shared-memory accesses by
+// ~0.5 us per tile).
 //
 // The softmax is software-pipelined: while tile j is normalised, the partial
 // logits of tile j+1 are already on their way to the peer (two exchange
@@ -48,8 +49,12 @@ namespace {
 constexpr int MT_H = 128;        // heads = MMA M
 constexpr int MT_N = 32;         // keys per tile
 constexpr int MT_STAGES = 6;
-constexpr int MT_SOFTMAX = 8;    // softmax warps
-constexpr int MT_THREADS = 480;  // warps 0-7 softmax, 8 QK^T issuer, 9 PV issuer, 10-13 gather producers, 14 sender
+constexpr int MT_SOFTMAX = 4;    // softmax warps, one per TMEM lane quadrant
+constexpr int MT_W_QK = 4;       // QK^T issuer and TMEM owner
+constexpr int MT_W_PV = 5;       // PV issuer
+constexpr int MT_W_PROD = 6;     // first of the four gather producer warps
+constexpr int MT_W_SEND = 10;    // sender of the staged partial logits
+constexpr int MT_THREADS = 352;
 constexpr int MT_DV = 512;
 constexpr int MT_OCOLS = 256;    // value channels per CTA (TMEM columns [0, 256))
 constexpr int MT_SCOL = 256;     // TMEM column of the two S buffers
@@ -68,8 +73,7 @@ struct MtLayout {
   static constexpr int OFF_KV = 0;
   static constexpr int OFF_X = OFF_KV + MT_STAGES * KV_STAGE;
   static constexpr int OFF_SB = OFF_X + 2 * X_BYTES;  // two staging buffers of this CTA's partials (same layout as X)
-  static constexpr int OFF_M = OFF_SB + 2 * X_BYTES;  // [2 parity][2 halves][128] row maxima / sums
-  static constexpr int OFF_BAR = OFF_M + 2 * 2 * MT_H * 4;
+  static constexpr int OFF_BAR = OFF_SB + 2 * X_BYTES;
   static constexpr int SMEM = 1024 + OFF_BAR + 512;
   static_assert(MT_QCOL + 32 * KBMAX <= MT_PCOL && MT_PCOL + 2 * 16 <= 512, "TMEM columns");
 };
@@ -95,18 +99,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
   // sits at chunk q ^ (h & 7), so the 16-byte stores and loads of a warp spread
   // over all banks
   float* X = reinterpret_cast<float*>(gbase + L::OFF_X);
-  float* Mx = reinterpret_cast<float*>(gbase + L::OFF_M);  // [2][2][128] half-row maxima (and final sums)
   uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + L::OFF_BAR);
   uint64_t* qready = bars;                            // q slice stored into TMEM (8 warps)
   uint64_t* kv_full = bars + 1;                       // [STAGES]
   uint64_t* kv_empty = kv_full + MT_STAGES;           // [STAGES]
   uint64_t* s_full = kv_empty + MT_STAGES;            // [2]
-  uint64_t* s_empty = s_full + 2;                     // [2] (256 softmax threads)
-  uint64_t* p_full = s_empty + 2;                     // [2] (256 softmax threads)
+  uint64_t* s_empty = s_full + 2;                     // [2] (128 softmax threads)
+  uint64_t* p_full = s_empty + 2;                     // [2] (128 softmax threads)
   uint64_t* p_empty = p_full + 2;                     // [2] (PV of that buffer completed)
   uint64_t* xfull = p_empty + 2;                      // [2] the peer's half of a tile landed in my X[b]
-  uint64_t* mx_full = xfull + 2;                      // [2 parity][4 quadrants] both halves wrote (64 threads)
-  uint64_t* sb_full = mx_full + 8;                    // [2] staging buffer written (256 softmax threads)
+  uint64_t* sb_full = xfull + 2;                      // [2] staging buffer written (128 softmax threads)
   uint64_t* sb_empty = sb_full + 2;                   // [2] bulk copy of the staging buffer has read it
   uint64_t* mask_full = sb_empty + 2;                 // [STAGES] valid-slot bits of the stage written
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mask_full + MT_STAGES);
@@ -140,7 +142,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
       tc::mbar_init(&p_empty[i], 1);
       tc::mbar_init(&xfull[i], 1);  // own expect_tx arrival + the peer's st.async bytes
     }
-    for (int i = 0; i < 8; ++i) tc::mbar_init(&mx_full[i], 64);
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&sb_full[i], 32 * MT_SOFTMAX);
       tc::mbar_init(&sb_empty[i], 1);
@@ -150,7 +151,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
     tc::mbar_arrive_expect_tx(&xfull[0], L::X_BYTES);  // tiles 0 and 1
     tc::mbar_arrive_expect_tx(&xfull[1], L::X_BYTES);
   }
-  if (warp == 8) tc::tmem_alloc(tmem_slot, 512);
+  if (warp == MT_W_QK) tc::tmem_alloc(tmem_slot, 512);
   tc::fence_before_sync();
   __syncthreads();
   __syncwarp();
@@ -158,7 +159,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp >= 10 && warp <= 13) {
+  if (warp >= MT_W_PROD && warp < MT_W_PROD + 4) {
     // ------------------------------------------------------------ gather producers (4 warps)
     // Warp w copies rows 8w .. 8w+7 of each 32-row tile; lane l copies the
     // 16-byte chunks l, l+32 of the row's channel slice, so one instruction
@@ -170,7 +171,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
     // orders the landed data for the tensor cores with a proxy fence.  The
     // slot indices of the next tile are loaded one tile ahead (lane r < 8
     // holds row 8w + r).
-    const int w8 = (warp - 10) * 8;
+    const int w8 = (warp - MT_W_PROD) * 8;
     const int nchunk = kb * 8;  // 32 or 40
     const char* kvb = reinterpret_cast<const char*>(a.kv);
     bool ok = true;
@@ -203,13 +204,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
       // valid-slot bits of this warp's 8 rows: byte w of the stage's mask word
       const uint32_t bal = __ballot_sync(0xffffffffu, lane < 8 && id_mine >= 0 && id_mine < n);
       if (lane == 0) {
-        reinterpret_cast<volatile unsigned char*>(&masks[st])[warp - 10] = static_cast<unsigned char>(bal & 0xffu);
+        reinterpret_cast<volatile unsigned char*>(&masks[st])[warp - MT_W_PROD] = static_cast<unsigned char>(bal & 0xffu);
         tc::mbar_arrive(&mask_full[st]);
       }
     }
     cp_async_wait<0>();
     if (!ok) *abort_flag = 1;
-  } else if (warp == 8) {
+  } else if (warp == MT_W_QK) {
     // ------------------------------------------------------------ QK^T issuer (A = q slice in TMEM)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(MT_H, MT_N);
@@ -238,7 +239,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
       }
       if (!ok) *abort_flag = 1;
     }
-  } else if (warp == 14) {
+  } else if (warp == MT_W_SEND) {
     // ------------------------------------------------------------ sender
     // One bulk copy per tile moves this CTA's staged partial logits into the
     // peer's exchange buffer, completing on the peer's barrier; the staging
@@ -261,7 +262,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
       }
       if (!ok) *abort_flag = 1;
     }
-  } else if (warp == 9) {
+  } else if (warp == MT_W_PV) {
     // ------------------------------------------------------------ PV issuer
     // QK^T(j) completed before the softmax published P(j), so the commits of
     // this thread (kv_empty after PV(j)) also cover every MMA that read stage j.
@@ -284,19 +285,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
       if (!ok) *abort_flag = 1;
     }
   } else {
-    // ------------------------------------------------------------ softmax (warps 0-7)
-    // Thread (h, hf): head h = 32 (warp % 4) + lane, key columns 16 hf .. +15
-    // of every tile, hf = warp / 4.  Iteration j: fetch tile j's partial
-    // logits from TMEM, receive the peer's half of tile j-1, stage this CTA's
-    // half of tile j for the sender, then normalise tile j-1 while it travels.
-    const int qd = warp & 3, hf = warp >> 2;
-    const int h = qd * 32 + lane;
-    const int cofs = hf * 16;
-    const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
-    // q slice row h -> TMEM columns [MT_QCOL, MT_QCOL + 32 kb): blocks hf, hf + 2, ...
+    // ------------------------------------------------------------ softmax (warps 0-3)
+    // Thread h (warp h / 32 reads its TMEM lane quadrant) owns row h: all 32
+    // key columns of every tile, so a row's maximum and sum never leave the
+    // thread.  Iteration j: fetch tile j's partial logits from TMEM, receive
+    // the peer's half of tile j-1, stage this CTA's half of tile j for the
+    // sender, then normalise tile j-1 while it travels.
+    const int h = warp * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // q slice row h -> TMEM columns [MT_QCOL, MT_QCOL + 32 kb)
     {
       const uint4* qrow = reinterpret_cast<const uint4*>(a.q + ((int64_t)t * MT_H + h) * D + ch0);
-      for (int c = hf; c < kb; c += 2) {
+      for (int c = 0; c < kb; ++c) {
         uint32_t r[32];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -314,23 +314,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(qready);
     }
-    float m_use = NEG_INF, l = 0.f;  // running max (shared by both halves) and this half's row sum
+    float m_use = NEG_INF, l = 0.f;  // running max and row sum
     bool ok = true;
-    uint32_t cur[16];
+    uint32_t cur[32];
     for (int j = 0; j <= ntiles; ++j) {
-      uint32_t nxt[16];
+      uint32_t nxt[32];
       if (j < ntiles) {
         const int b = j & 1;
         if (!__all_sync(0xffffffffu, tc::mbar_wait(&s_full[b], (j >> 1) & 1, abort_flag))) { ok = false; break; }
         tc::fence_after_sync();
         __syncwarp();
-        tc::tmem_ld16(tmem + lane_base + MT_SCOL + b * MT_N + cofs, nxt);
+        tc::tmem_ld32(tmem + lane_base + MT_SCOL + b * MT_N, nxt);
         tc::tmem_ld_wait();
         tc::fence_before_sync();
         tc::mbar_arrive(&s_empty[b]);
       }
       // receive the peer's half of tile j-1 (published at the end of its previous iteration)
-      float x2[16];
+      float x2[32];
       if (j > 0) {
         const int jj = j - 1, bb = jj & 1;
         if (!__all_sync(0xffffffffu, tc::mbar_wait_cluster(&xfull[bb], (jj >> 1) & 1, abort_flag))) {
@@ -339,8 +339,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
         }
         const float4* xr = reinterpret_cast<const float4*>(X + bb * (MT_H * MT_N) + h * MT_N);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 v = xr[(hf * 4 + q) ^ (h & 7)];  // 16-byte chunks of a row are swizzled by the row
+        for (int q = 0; q < 8; ++q) {
+          const float4 v = xr[q ^ (h & 7)];  // 16-byte chunks of a row are swizzled by the row
           x2[4 * q] = __uint_as_float(cur[4 * q]) + v.x;
           x2[4 * q + 1] = __uint_as_float(cur[4 * q + 1]) + v.y;
           x2[4 * q + 2] = __uint_as_float(cur[4 * q + 2]) + v.z;
@@ -348,11 +348,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
         }
         // the next use of X[bb] is tile jj+2; the peer can send it only after
         // all of this CTA's threads sent tile jj+1, i.e. after they read X[bb]
-        if (h == 0 && hf == 0 && jj + 2 < ntiles) tc::mbar_arrive_expect_tx(&xfull[bb], L::X_BYTES);
+        if (h == 0 && jj + 2 < ntiles) tc::mbar_arrive_expect_tx(&xfull[bb], L::X_BYTES);
       }
-      // stage this thread's 16 columns of tile j for the sender (same swizzled
-      // layout as the peer's exchange buffer); staging buffer b is free once
-      // the bulk copy of tile j-2 has read it
+      // stage this thread's row of tile j for the sender (same swizzled layout
+      // as the peer's exchange buffer); staging buffer b is free once the bulk
+      // copy of tile j-2 has read it
       if (j < ntiles) {
         const int b = j & 1;
         if (!__all_sync(0xffffffffu, tc::mbar_wait(&sb_empty[b], ((j >> 1) & 1) ^ 1u, abort_flag))) {
@@ -361,41 +361,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
         }
         unsigned char* srow = gbase + L::OFF_SB + b * L::X_BYTES + h * (MT_N * 4);
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          *reinterpret_cast<uint4*>(srow + (((hf * 4 + q) ^ (h & 7)) << 4)) =
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<uint4*>(srow + ((q ^ (h & 7)) << 4)) =
               make_uint4(nxt[4 * q], nxt[4 * q + 1], nxt[4 * q + 2], nxt[4 * q + 3]);
         tc::fence_proxy_async_smem();
         tc::mbar_arrive(&sb_full[b]);
       }
       if (j > 0) {
         const int jj = j - 1, bb = jj & 1;
-        // valid-slot bits published by the producer with this stage
+        // valid-slot bits published by the producers with this stage
         const int st = jj % MT_STAGES;
         if (!__all_sync(0xffffffffu, tc::mbar_wait(&mask_full[st], (jj / MT_STAGES) & 1, abort_flag))) {
           ok = false;
           break;
         }
-        const uint32_t mask = (masks[st] >> cofs) & 0xffffu;
-        if (mask == 0xffffu) {
+        const uint32_t mask = masks[st];
+        if (mask == 0xffffffffu) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) x2[i] *= a.scale_log2;
+          for (int i = 0; i < 32; ++i) x2[i] *= a.scale_log2;
         } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) x2[i] = ((mask >> i) & 1u) ? x2[i] * a.scale_log2 : NEG_INF;
+          for (int i = 0; i < 32; ++i) x2[i] = ((mask >> i) & 1u) ? x2[i] * a.scale_log2 : NEG_INF;
         }
-        float mx[4];
+        float mx[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) mx[i] = fmaxf(fmaxf(x2[i], x2[i + 4]), fmaxf(x2[i + 8], x2[i + 12]));
-        const float hmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-        // the tile maximum of row h: both halves publish theirs and wait for each other
-        float* mrow = Mx + bb * (2 * MT_H);
-        mrow[hf * MT_H + h] = hmax;
-        tc::mbar_arrive(&mx_full[bb * 4 + qd]);
-        if (!__all_sync(0xffffffffu, tc::mbar_wait(&mx_full[bb * 4 + qd], (jj >> 1) & 1, abort_flag))) {
-          ok = false;
-          break;
-        }
-        const float tmax = fmaxf(hmax, mrow[(hf ^ 1) * MT_H + h]);
+        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(fmaxf(x2[i], x2[i + 8]), fmaxf(x2[i + 16], x2[i + 24]));
+        const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         float alpha = 1.f;
         const bool resc = tmax > m_use + kRescaleLog2;
         if (resc) {
@@ -404,10 +396,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
           l *= alpha;
         }
         const float mu = (m_use == NEG_INF) ? 0.f : m_use;
-        uint32_t pk[8];
+        uint32_t pk[16];
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < 16; i += 2) {
+        for (int i = 0; i < 32; i += 2) {
           const float p0 = ex2(x2[i] - mu), p1 = ex2(x2[i + 1] - mu);
           ps[(i >> 1) & 3] += p0 + p1;
           pk[i / 2] = pack_bf16(p0, p1);
@@ -418,7 +410,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
           ok = false;
           break;
         }
-        // a raised running max rescales this half of the O slice, which PV(jj-1) must have finished
+        // a raised running max rescales this row of the O slice, which PV(jj-1) must have finished
         if (jj > 0 && __any_sync(0xffffffffu, resc)) {
           const int pb = (jj - 1) & 1;
           if (!__all_sync(0xffffffffu, tc::mbar_wait(&p_empty[pb], ((jj - 1) >> 1) & 1, abort_flag))) {
@@ -426,9 +418,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
             break;
           }
           tc::fence_after_sync();
-          for (int cb = 0; cb < MT_OCOLS / 64; ++cb) {
+          for (int cb = 0; cb < MT_OCOLS / 32; ++cb) {
             uint32_t o[32];
-            const uint32_t oc = tmem + lane_base + hf * (MT_OCOLS / 2) + cb * 32;
+            const uint32_t oc = tmem + lane_base + cb * 32;
             tc::tmem_ld32(oc, o);
             tc::tmem_ld_wait();
 #pragma unroll
@@ -437,37 +429,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
           }
           tc::tmem_st_wait();
         }
-        // P row h, this half's 16 keys = 8 columns of TMEM P buffer bb (the A operand of PV)
+        // P row h, 32 keys = 16 columns of TMEM P buffer bb (the A operand of PV)
         __syncwarp();
-        tc::tmem_st8(tmem + lane_base + MT_PCOL + bb * 16 + hf * 8, pk);
+        tc::tmem_st16(tmem + lane_base + MT_PCOL + bb * 16, pk);
         tc::tmem_st_wait();
         tc::fence_before_sync();
         tc::mbar_arrive(&p_full[bb]);
       }
 #pragma unroll
-      for (int i = 0; i < 16; ++i) cur[i] = nxt[i];
+      for (int i = 0; i < 32; ++i) cur[i] = nxt[i];
     }
     if (!ok) *abort_flag = 1;
-    // epilogue: the row sum of both halves, O half / l -> bf16, lse
+    // epilogue: O row / l -> bf16, lse
     const int lb = (ntiles - 1) & 1;
-    bool last_ok = ok && __all_sync(0xffffffffu, tc::mbar_wait(&p_empty[lb], ((ntiles - 1) >> 1) & 1, abort_flag));
-    float lt = 0.f;
-    if (last_ok) {
-      const int pe = ntiles & 1;  // next use of the max exchange slots: tile ntiles
-      float* mrow = Mx + pe * (2 * MT_H);
-      mrow[hf * MT_H + h] = l;
-      tc::mbar_arrive(&mx_full[pe * 4 + qd]);
-      last_ok = __all_sync(0xffffffffu, tc::mbar_wait(&mx_full[pe * 4 + qd], (ntiles >> 1) & 1, abort_flag));
-      if (last_ok) lt = l + mrow[(hf ^ 1) * MT_H + h];
-    }
-    __nv_bfloat16* orow = a.out + ((int64_t)t * MT_H + h) * MT_DV + ch0 + hf * (MT_OCOLS / 2);
+    const bool last_ok = ok && __all_sync(0xffffffffu, tc::mbar_wait(&p_empty[lb], ((ntiles - 1) >> 1) & 1, abort_flag));
+    __nv_bfloat16* orow = a.out + ((int64_t)t * MT_H + h) * MT_DV + ch0;
     if (last_ok) {
       tc::fence_after_sync();
-      const float inv = lt > 0.f ? 1.f / lt : 0.f;
-      for (int cb = 0; cb < MT_OCOLS / 64; ++cb) {
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      for (int cb = 0; cb < MT_OCOLS / 32; ++cb) {
         uint32_t o[32];
         __syncwarp();
-        tc::tmem_ld32(tmem + lane_base + hf * (MT_OCOLS / 2) + cb * 32, o);
+        tc::tmem_ld32(tmem + lane_base + cb * 32, o);
         tc::tmem_ld_wait();
         uint4* dst = reinterpret_cast<uint4*>(orow + cb * 32);
 #pragma unroll
@@ -477,12 +460,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
                               pack_bf16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv),
                               pack_bf16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv));
       }
-      if (rank == 0 && hf == 0) a.lse[(int64_t)t * MT_H + h] = lt > 0.f ? (m_use + log2f(lt)) * kLn2 : NEG_INF;
+      if (rank == 0) a.lse[(int64_t)t * MT_H + h] = l > 0.f ? (m_use + log2f(l)) * kLn2 : NEG_INF;
     } else {
-      // wound down after a timeout: zero output half, -inf lse
+      // wound down after a timeout: zero output row, -inf lse
       *abort_flag = 1;
-      for (int c = 0; c < MT_OCOLS / 2; c += 8) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
-      if (rank == 0 && hf == 0) a.lse[(int64_t)t * MT_H + h] = NEG_INF;
+      for (int c = 0; c < MT_OCOLS; c += 8) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
+      if (rank == 0) a.lse[(int64_t)t * MT_H + h] = NEG_INF;
     }
   }
 
@@ -491,7 +474,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
   if (*abort_flag && tid == 0) raise_flag(a.flags, TSA_FLAG_TIMEOUT);
   __syncwarp();
   tc::cluster_sync();  // the peer no longer writes into this CTA's shared memory
-  if (warp == 8) {
+  if (warp == MT_W_QK) {
     __syncwarp();
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, 512);
