@@ -13,6 +13,12 @@ counted from the actual indices) with inputs resident in HBM; per-stage times,
 indexer queries/s and roofline fractions are reported alongside.  Inputs
 (~20 GB) exceed the 129 MB L2, so no flush is needed between steps.
 
+`secondary.qsa_gqa` times the block Sparse-GQA workload on its own after the
+main step (packed THD of four sequences 4096/8192/12288/8192, Hq = 32,
+Hkv = 4, d = 128, block 64, top-32 blocks per query and kv group, indexer with
+8 heads in 4 groups): block indexer + top-k, GQA forward and backward.  It is
+not part of `value`.
+
 `--impl reference` times the CPU oracle on a bounded sample of the same
 workload on the host cores (the reference arm: the pages ship no runnable
 reference implementation).
@@ -40,7 +46,7 @@ TOPK = 2048
 # DRAM bytes (read + write) of one forward launch per query, from an ncu capture
 # of the current forward kernel on the same workload at T=4096 (scaled by the
 # number of queries); None when the kernel changed since the capture.
-FWD_TRAFFIC_BYTES_PER_QUERY = 277695
+FWD_TRAFFIC_BYTES_PER_QUERY = 277545
 SCALE = 1.0 / math.sqrt(192)
 H_I = 64
 D_I = 128
@@ -332,6 +338,8 @@ def run_gpu(args):
         e2e = run_e2e(args, tsa, dev, cu, {"q_idx": q_i, "k_idx": k_i, "w": w, "q": q, "kv": kv, "dout": dout},
                       f_step, world)
 
+    gqa = None if args.no_gqa else run_gqa(args, tsa, dev, world)
+
     cpu = None
     if rank == 0 and world >= 1 and not args.no_cpu_baseline:
         dt, f, _ = oracle_sample(args.ref_rows)
@@ -356,12 +364,89 @@ def run_gpu(args):
             "gpu_launches": int(launches),
             "clocks": clk,
             "flops_per_step": {"indexer": f_idx, "fwd": f_fwd, "bwd": f_bwd, "valid_pairs": valid},
+            "secondary": {"qsa_gqa": gqa},
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+GQA_LENGTHS = [4096, 8192, 12288, 8192]  # packed THD of four sequences
+GQA_HQ, GQA_HKV, GQA_D, GQA_BS, GQA_NSEL = 32, 4, 128, 64, 32
+GQA_HI, GQA_DI = 8, 128
+
+
+def run_gqa(args, tsa, dev, world):
+    """QSA block Sparse-GQA workload, timed on its own after the main step:
+    block indexer + exact top-32 blocks per (query, kv group), GQA forward and
+    backward.  Algorithmic FLOPs per attended (query, group, token) triple:
+    forward 4 d G (QK^T and PV for the G = Hq / Hkv heads of the group),
+    backward 10 d G (S recompute, dP, dQ, dK, dV); gathered K + V rows
+    2 d bf16 per triple."""
+    import torch
+    import synth
+    cu = synth.cu_seqlens_thd(GQA_LENGTHS)
+    T = cu[-1]
+    g = synth.gqa_inputs(T, GQA_HQ, GQA_HKV, GQA_D, seed=8, device=dev, with_grad_out=True)
+    x = synth.indexer_inputs(T, GQA_HI, GQA_DI, seed=6, device=dev)
+    scale = 1.0 / math.sqrt(GQA_D)
+    ws = torch.empty(max(1, tsa.qsa_topk_workspace_size(cu, GQA_HKV, GQA_BS)), dtype=torch.uint8, device=dev)
+    blk = torch.empty((T, GQA_HKV, GQA_NSEL), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        tsa.qsa_topk(x["q_idx"], x["k_idx"], x["w"], cu, GQA_NSEL, groups=GQA_HKV, block_size=GQA_BS,
+                     workspace=ws, out=blk)
+        if ev:
+            ev[1].record(stream)
+        out, lse = tsa.sparse_gqa_fwd(g["q"], g["k"], g["v"], blk, cu, GQA_BS, scale)
+        if ev:
+            ev[2].record(stream)
+        tsa.sparse_gqa_bwd(g["q"], g["k"], g["v"], blk, out, lse, g["dout"], cu, GQA_BS, scale)
+        if ev:
+            ev[3].record(stream)
+
+    for _ in range(max(3, min(args.warmup, 3))):
+        step()
+    torch.cuda.synchronize()
+    # attended (query, group, token) triples: the causal tokens s <= t of each selected block
+    cuT = torch.tensor(cu, device=dev)
+    t = torch.arange(T, device=dev)
+    p = t - cuT[torch.searchsorted(cuT, t, right=True) - 1]
+    b = blk.long()
+    ntok = torch.where(b >= 0, torch.clamp(p[:, None, None] - b * GQA_BS + 1, 0, GQA_BS), torch.zeros_like(b))
+    triples = int(ntok.sum().item())
+    pairs = sum(n * (n + 1) // 2 for n in GQA_LENGTHS)
+    G = GQA_HQ // GQA_HKV
+    f_idx = pairs * GQA_HI * GQA_DI * 2
+    f_fwd = triples * 4 * GQA_D * G
+    f_bwd = triples * 10 * GQA_D * G
+    steps = max(1, min(args.steps, 5))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        step(evs[i])
+    torch.cuda.synchronize()
+    ms = [sum(e[k].elapsed_time(e[k + 1]) for e in evs) / steps for k in range(3)]
+    ms = [allmax(v, world) for v in ms]
+    del g, x, ws, blk
+    torch.cuda.empty_cache()
+    return {
+        "workload": "qsa_gqa_thd32768_hq32_hkv4_bs64_top32",
+        "lengths": GQA_LENGTHS, "Hq": GQA_HQ, "Hkv": GQA_HKV, "d": GQA_D, "block_size": GQA_BS,
+        "blocks_selected": GQA_NSEL, "indexer_heads": GQA_HI, "d_I": GQA_DI, "steps": steps,
+        "note": "timed separately after the main step; not part of value",
+        "block_indexer_topk": {"ms": ms[0], "tflops": world * f_idx / (ms[0] * 1e-3) / 1e12,
+                               "queries_per_s": world * T / (ms[0] * 1e-3)},
+        "gqa_fwd": {"ms": ms[1], "tflops": world * f_fwd / (ms[1] * 1e-3) / 1e12,
+                    "gather_gbs": world * triples * 2 * GQA_D * 2 / (ms[1] * 1e-3) / 1e9},
+        "gqa_bwd": {"ms": ms[2], "tflops": world * f_bwd / (ms[2] * 1e-3) / 1e12},
+        "attended_triples": triples,
+    }
 
 
 def run_e2e(args, tsa, dev, cu, dev_inputs, f_step, world):
@@ -459,6 +544,7 @@ def main():
     ap.add_argument("--T", type=int, default=T_TOK, help="sequence length (smaller only for profiling captures)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-gqa", action="store_true", help="skip the separately timed block Sparse-GQA workload")
     args = ap.parse_args()
     if args.T != T_TOK:
         set_T(args.T)

@@ -104,11 +104,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
   uint64_t* kv_full = bars + 1;                       // [STAGES]
   uint64_t* kv_empty = kv_full + MT_STAGES;           // [STAGES]
   uint64_t* s_full = kv_empty + MT_STAGES;            // [2]
-  uint64_t* s_empty = s_full + 2;                     // [2] (128 softmax threads)
-  uint64_t* p_full = s_empty + 2;                     // [2] (128 softmax threads)
+  uint64_t* s_empty = s_full + 2;                     // [2] (one arrival per softmax warp)
+  uint64_t* p_full = s_empty + 2;                     // [2] (one arrival per softmax warp)
   uint64_t* p_empty = p_full + 2;                     // [2] (PV of that buffer completed)
   uint64_t* xfull = p_empty + 2;                      // [2] the peer's half of a tile landed in my X[b]
-  uint64_t* sb_full = xfull + 2;                      // [2] staging buffer written (128 softmax threads)
+  uint64_t* sb_full = xfull + 2;                      // [2] staging buffer written (one arrival per softmax warp)
   uint64_t* sb_empty = sb_full + 2;                   // [2] bulk copy of the staging buffer has read it
   uint64_t* mask_full = sb_empty + 2;                 // [STAGES] valid-slot bits of the stage written
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mask_full + MT_STAGES);
@@ -137,13 +137,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&s_full[i], 1);
-      tc::mbar_init(&s_empty[i], 32 * MT_SOFTMAX);
-      tc::mbar_init(&p_full[i], 32 * MT_SOFTMAX);
+      tc::mbar_init(&s_empty[i], MT_SOFTMAX);
+      tc::mbar_init(&p_full[i], MT_SOFTMAX);
       tc::mbar_init(&p_empty[i], 1);
       tc::mbar_init(&xfull[i], 1);  // own expect_tx arrival + the peer's st.async bytes
     }
     for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&sb_full[i], 32 * MT_SOFTMAX);
+      tc::mbar_init(&sb_full[i], MT_SOFTMAX);
       tc::mbar_init(&sb_empty[i], 1);
     }
     *abort_flag = 0;
@@ -327,7 +327,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
         tc::tmem_ld32(tmem + lane_base + MT_SCOL + b * MT_N, nxt);
         tc::tmem_ld_wait();
         tc::fence_before_sync();
-        tc::mbar_arrive(&s_empty[b]);
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&s_empty[b]);
       }
       // receive the peer's half of tile j-1 (published at the end of its previous iteration)
       float x2[32];
@@ -365,7 +366,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
           *reinterpret_cast<uint4*>(srow + ((q ^ (h & 7)) << 4)) =
               make_uint4(nxt[4 * q], nxt[4 * q + 1], nxt[4 * q + 2], nxt[4 * q + 3]);
         tc::fence_proxy_async_smem();
-        tc::mbar_arrive(&sb_full[b]);
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&sb_full[b]);
       }
       if (j > 0) {
         const int jj = j - 1, bb = jj & 1;
@@ -434,7 +436,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
         tc::tmem_st16(tmem + lane_base + MT_PCOL + bb * 16, pk);
         tc::tmem_st_wait();
         tc::fence_before_sync();
-        tc::mbar_arrive(&p_full[bb]);
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&p_full[bb]);
       }
 #pragma unroll
       for (int i = 0; i < 32; ++i) cur[i] = nxt[i];
