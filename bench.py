@@ -449,6 +449,29 @@ def run_gqa(args, tsa, dev, world):
     }
 
 
+def gpu_local_cpus(local: int):
+    """The allowed CPUs that sysfs lists as local to the GPU, or None.  Pinned
+    host pages are placed on the NUMA node of the allocating thread, so the
+    end-to-end leg allocates them from these CPUs: on a two-socket host, pages
+    on the far socket cross the inter-socket link on every copy."""
+    try:
+        import torch
+        p = torch.cuda.get_device_properties(local)
+        path = (f"/sys/bus/pci/devices/{p.pci_domain_id:04x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+                "/local_cpulist")
+        cpus = set()
+        for part in open(path).read().strip().split(","):
+            if "-" in part:
+                lo, hi = part.split("-")
+                cpus.update(range(int(lo), int(hi) + 1))
+            elif part:
+                cpus.add(int(part))
+        cpus &= os.sched_getaffinity(0)
+        return sorted(cpus) if cpus else None
+    except Exception:
+        return None
+
+
 def run_e2e(args, tsa, dev, cu, dev_inputs, f_step, world):
     """Same step through the public API from pinned host buffers: every step
     copies its inputs host -> device and reads its results device -> host
@@ -456,6 +479,10 @@ def run_e2e(args, tsa, dev, cu, dev_inputs, f_step, world):
     inputs of step i+1 are copied (H2D stream, second device buffer set) and
     the results of step i read back (D2H stream) while step i+1 computes."""
     import torch
+    saved_affinity = os.sched_getaffinity(0)
+    local_cpus = gpu_local_cpus(dev.index if dev.index is not None else 0)
+    if local_cpus:
+        os.sched_setaffinity(0, local_cpus)
     host_in = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in dev_inputs.items()}
     for k, v in dev_inputs.items():
         host_in[k].copy_(v)
@@ -529,9 +556,11 @@ def run_e2e(args, tsa, dev, cu, dev_inputs, f_step, world):
     ms = allmax(a.elapsed_time(b) / steps, world)
     del d_in, host_in, host_out
     torch.cuda.empty_cache()
+    os.sched_setaffinity(0, saved_affinity)
     return {"value": world * f_step / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
-            "pipelined": "H2D of step i+1 and D2H of step i overlap the compute of step i+1"}
+            "pipelined": "H2D of step i+1 and D2H of step i overlap the compute of step i+1",
+            "host_cpus": f"{len(local_cpus)} GPU-local CPUs" if local_cpus else "unrestricted (no sysfs locality)"}
 
 
 def main():
