@@ -206,16 +206,19 @@ int sparse_mla_bwd(const void* q_dev, const void* kv_dev, const int32_t* indices
  *   q_dev bf16 [T, Hq, d], k_dev/v_dev bf16 [T, Hkv, d],
  *   block_indices_dev int32 [T, Hkv, nsel], out_dev bf16 [T, Hq, d],
  *   lse_dev fp32 [T, Hq].  Backward: dq [T,Hq,d], dk/dv [T,Hkv,d] bf16
- *   (overwritten), workspace sparse_gqa_bwd_workspace_size bytes.
+ *   (overwritten), workspace sparse_gqa_bwd_workspace_size(T, Hq, Hkv, d,
+ *   nsel) bytes: fp32 dq/dk/dv accumulators, rowsum(dO * O) and the selections
+ *   inverted per (block, kv group), so that the backward visits each selected
+ *   block once per chunk of the queries that chose it.
  * Supported: Hq/Hkv in {1..16}, d in {64, 128}, block_size in {32, 64}.
- * Forward deterministic; backward dk/dv summation order not fixed.
+ * Forward deterministic; backward dq/dk/dv summation order not fixed.
  * ------------------------------------------------------------------------- */
 int sparse_gqa_fwd(const void* q_dev, const void* k_dev, const void* v_dev,
                    const int32_t* block_indices_dev, const int32_t* cu_seqlens, int num_seqs,
                    int Hq, int Hkv, int d, int block_size, int nsel, float softmax_scale,
                    void* out_dev, float* lse_dev, void* stream);
 
-size_t sparse_gqa_bwd_workspace_size(int64_t T, int Hq, int Hkv, int d);
+size_t sparse_gqa_bwd_workspace_size(int64_t T, int Hq, int Hkv, int d, int nsel);
 int sparse_gqa_bwd(const void* q_dev, const void* k_dev, const void* v_dev,
                    const int32_t* block_indices_dev, const void* out_dev, const float* lse_dev,
                    const void* dout_dev, const int32_t* cu_seqlens, int num_seqs, int Hq, int Hkv,

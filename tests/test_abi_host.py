@@ -101,7 +101,9 @@ def test_workspace_sizes_are_bounded(lib):
     big = lib.sparse_mla_bwd_workspace_size(65536, 128, 576, 2048)
     assert big <= 65536 * 576 * 4 + 65536 * 128 * 4 + 4 * 2 ** 30 + 1024
     assert lib.sparse_mla_bwd_workspace_size(64, 128, 576, 100) >= 64 * 128 * 128 * 4
-    assert lib.sparse_gqa_bwd_workspace_size(1000, 32, 4, 128) >= 2 * 1000 * 4 * 128 * 4
+    # fp32 dQ, dK, dV accumulators and the inverted selections (1000 x 4 x 32 entries)
+    assert lib.sparse_gqa_bwd_workspace_size(1000, 32, 4, 128, 32) >= (1000 * 32 * 128 + 2 * 1000 * 4 * 128) * 4 \
+        + 1000 * 4 * 32 * 4
 
 
 def test_binding_refuses_cpu_tensors():

@@ -45,7 +45,7 @@ SIGNATURES = {
                                c_int, c_int, c_int, c_float, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "sparse_gqa_fwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_i32p, c_int, c_int, c_int, c_int,
                                c_int, c_int, c_float, c_void_p, c_void_p, c_void_p]),
-    "sparse_gqa_bwd_workspace_size": (c_size_t, [c_int64, c_int, c_int, c_int]),
+    "sparse_gqa_bwd_workspace_size": (c_size_t, [c_int64, c_int, c_int, c_int, c_int]),
     "sparse_gqa_bwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_i32p,
                                c_int, c_int, c_int, c_int, c_int, c_int, c_float, c_void_p, c_void_p, c_void_p,
                                c_void_p, c_size_t, c_void_p]),
@@ -252,8 +252,8 @@ def sparse_gqa_fwd(q, k, v, block_indices, cu_seqlens, block_size: int, softmax_
     return out, lse
 
 
-def sparse_gqa_bwd_workspace_size(T: int, Hq: int, Hkv: int, d: int) -> int:
-    return int(load_library().sparse_gqa_bwd_workspace_size(T, Hq, Hkv, d))
+def sparse_gqa_bwd_workspace_size(T: int, Hq: int, Hkv: int, d: int, nsel: int) -> int:
+    return int(load_library().sparse_gqa_bwd_workspace_size(T, Hq, Hkv, d, nsel))
 
 
 def sparse_gqa_bwd(q, k, v, block_indices, out, lse, dout, cu_seqlens, block_size: int, softmax_scale: float,
@@ -268,7 +268,7 @@ def sparse_gqa_bwd(q, k, v, block_indices, out, lse, dout, cu_seqlens, block_siz
     nsel = block_indices.shape[2]
     cu, nseq = _cu(cu_seqlens)
     lib = load_library()
-    need = int(lib.sparse_gqa_bwd_workspace_size(T, Hq, Hkv, d))
+    need = int(lib.sparse_gqa_bwd_workspace_size(T, Hq, Hkv, d, nsel))
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)

@@ -432,22 +432,30 @@ int sparse_gqa_fwd(const void* q, const void* k, const void* v, const int32_t* b
   a.out = static_cast<__nv_bfloat16*>(out);
   a.lse = lse;
   a.flags = flags_ptr();
-  TSA_LAUNCH(launch_gqa(a, block_size, d, false, static_cast<cudaStream_t>(stream)), "gqa fwd launch");
+  TSA_LAUNCH(launch_gqa(a, block_size, d, static_cast<cudaStream_t>(stream)), "gqa fwd launch");
   return TSA_OK;
 }
 
-size_t sparse_gqa_bwd_workspace_size(int64_t T, int Hq, int Hkv, int d) {
-  if (T < 0 || Hq < 1 || Hkv < 1 || d < 1) return 0;
-  size_t one = (static_cast<size_t>(T) * Hkv * d * sizeof(float) + 255) & ~size_t(255);
-  return 2 * one + static_cast<size_t>(T) * Hq * sizeof(float);
+// Workspace of the key-centric backward: fp32 dQ, dK, dV accumulators, Delta,
+// the inverted selections and their offsets.  At most one block per token, so
+// T * Hkv bounds the number of (block, group) lists.
+static size_t gqa_ws_align(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t sparse_gqa_bwd_workspace_size(int64_t T, int Hq, int Hkv, int d, int nsel) {
+  if (T < 0 || Hq < 1 || Hkv < 1 || d < 1 || nsel < 1) return 0;
+  const size_t t = static_cast<size_t>(T);
+  const size_t nb = t * Hkv + 1;
+  return gqa_ws_align(t * Hq * d * sizeof(float)) + 2 * gqa_ws_align(t * Hkv * d * sizeof(float)) +
+         gqa_ws_align(t * Hq * sizeof(float)) + gqa_ws_align(t * Hkv * nsel * sizeof(int)) +
+         4 * gqa_ws_align((nb + 1) * sizeof(int));
 }
 
 int sparse_gqa_bwd(const void* q, const void* k, const void* v, const int32_t* block_indices, const void* out,
                    const float* lse, const void* dout, const int32_t* cu_seqlens, int num_seqs, int Hq, int Hkv,
                    int d, int block_size, int nsel, float softmax_scale, void* dq, void* dk, void* dv,
                    void* workspace, size_t workspace_bytes, void* stream) {
-  GqaArgs a;
-  memset(static_cast<void*>(&a), 0, sizeof(a) - sizeof(SeqTable));
+  GqaKvArgs a;
+  memset(static_cast<void*>(&a), 0, sizeof(a));
   int64_t T;
   int rc = make_seqs(cu_seqlens, num_seqs, &a.st, &T);
   if (rc) return rc;
@@ -455,35 +463,54 @@ int sparse_gqa_bwd(const void* q, const void* k, const void* v, const int32_t* b
   if (T == 0) return TSA_OK;
   if (!q || !k || !v || !block_indices || !out || !lse || !dout || !dq || !dk || !dv)
     return fail(TSA_ERR_INVALID_ARG, "null tensor pointer");
-  size_t need = sparse_gqa_bwd_workspace_size(T, Hq, Hkv, d);
+  size_t need = sparse_gqa_bwd_workspace_size(T, Hq, Hkv, d, nsel);
   if (workspace == nullptr || workspace_bytes < need)
     return fail(TSA_ERR_WORKSPACE, "workspace %zu bytes < %zu", workspace_bytes, need);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  size_t one_elems = static_cast<size_t>(T) * Hkv * d;
-  size_t one = (one_elems * sizeof(float) + 255) & ~size_t(255);
-  float* dk_acc = static_cast<float*>(workspace);
-  float* dv_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + one);
-  float* dlt = reinterpret_cast<float*>(static_cast<char*>(workspace) + 2 * one);
-  TSA_CHECK_CUDA(cudaMemsetAsync(workspace, 0, 2 * one, s), "memset");
+  // first global block of every sequence
+  int nblk = 0;
+  for (int i = 0; i < a.st.num_seqs; ++i) {
+    a.blk_base[i] = nblk;
+    nblk += (a.st.cu[i + 1] - a.st.cu[i] + block_size - 1) / block_size;
+  }
+  a.blk_base[a.st.num_seqs] = nblk;
+  const size_t t = static_cast<size_t>(T);
+  const size_t nb = t * Hkv + 1;
+  char* w = static_cast<char*>(workspace);
+  auto take = [&](size_t bytes) { char* p = w; w += gqa_ws_align(bytes); return p; };
+  float* dq_acc = reinterpret_cast<float*>(take(t * Hq * d * sizeof(float)));
+  float* dk_acc = reinterpret_cast<float*>(take(t * Hkv * d * sizeof(float)));
+  float* dv_acc = reinterpret_cast<float*>(take(t * Hkv * d * sizeof(float)));
+  float* dlt = reinterpret_cast<float*>(take(t * Hq * sizeof(float)));
+  a.list = reinterpret_cast<int*>(take(t * Hkv * nsel * sizeof(int)));
+  a.cnt = reinterpret_cast<int*>(take((nb + 1) * sizeof(int)));
+  a.off = reinterpret_cast<int*>(take((nb + 1) * sizeof(int)));
+  a.cur = reinterpret_cast<int*>(take((nb + 1) * sizeof(int)));
+  a.choff = reinterpret_cast<int*>(take((nb + 1) * sizeof(int)));
+  TSA_CHECK_CUDA(cudaMemsetAsync(dq_acc, 0, t * Hq * d * sizeof(float), s), "memset");
+  TSA_CHECK_CUDA(cudaMemsetAsync(dk_acc, 0, t * Hkv * d * sizeof(float), s), "memset");
+  TSA_CHECK_CUDA(cudaMemsetAsync(dv_acc, 0, t * Hkv * d * sizeof(float), s), "memset");
   TSA_LAUNCH(launch_bwd_delta(static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout),
-                                  dlt, T * Hq, d, s), "delta launch");
+                              dlt, T * Hq, d, s), "delta launch");
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.k = static_cast<const __nv_bfloat16*>(k);
   a.v = static_cast<const __nv_bfloat16*>(v);
+  a.dout = static_cast<const __nv_bfloat16*>(dout);
   a.blk = block_indices;
   a.lse_in = lse;
   a.dlt = dlt;
-  a.dout = static_cast<const __nv_bfloat16*>(dout);
-  a.T = static_cast<int>(T); a.Hq = Hq; a.Hkv = Hkv; a.G = Hq / Hkv; a.nsel = nsel;
+  a.T = static_cast<int>(T); a.Hq = Hq; a.Hkv = Hkv; a.G = Hq / Hkv; a.nsel = nsel; a.bs = block_size;
   a.scale = softmax_scale;
   a.scale_log2 = softmax_scale * kLog2e;
-  a.dq = static_cast<__nv_bfloat16*>(dq);
+  a.nblk = nblk;
+  a.dq_acc = dq_acc;
   a.dk_acc = dk_acc;
   a.dv_acc = dv_acc;
   a.flags = flags_ptr();
-  TSA_LAUNCH(launch_gqa(a, block_size, d, true, s), "gqa bwd launch");
-  TSA_LAUNCH(launch_f32_to_bf16(dk_acc, static_cast<__nv_bfloat16*>(dk), (int64_t)one_elems, s), "convert");
-  TSA_LAUNCH(launch_f32_to_bf16(dv_acc, static_cast<__nv_bfloat16*>(dv), (int64_t)one_elems, s), "convert");
+  TSA_LAUNCH(launch_gqa_bwd_kv(a, d, s), "gqa bwd launch");
+  TSA_LAUNCH(launch_f32_to_bf16(dq_acc, static_cast<__nv_bfloat16*>(dq), (int64_t)(t * Hq * d), s), "convert");
+  TSA_LAUNCH(launch_f32_to_bf16(dk_acc, static_cast<__nv_bfloat16*>(dk), (int64_t)(t * Hkv * d), s), "convert");
+  TSA_LAUNCH(launch_f32_to_bf16(dv_acc, static_cast<__nv_bfloat16*>(dv), (int64_t)(t * Hkv * d), s), "convert");
   return TSA_OK;
 }
 

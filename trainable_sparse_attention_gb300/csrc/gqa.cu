@@ -4,12 +4,11 @@
 // backend" ("Describe the solution you'd like": Sparse-GQA forward and
 // backward kernels over exact block top-k selections, BSHD and packed THD).
 //
-// One CTA per (query t, kv group g) holds the group's Hq/Hkv query heads in a
-// 16-row MMA tile; each selected block (block_size tokens of the group's k and
-// v, causal inside the query's own block) streams through a double-buffered
-// cp.async pipeline.  Forward: online softmax, natural-log LSE.  Backward:
-// recompute P from the LSE, dQ in registers, dK/dV tile contributions
-// scattered with red.global.add.v2.f32 into fp32 workspaces, then converted.
+// Forward.  One CTA per (query t, kv group g) holds the group's Hq/Hkv query
+// heads in a 16-row MMA tile; each selected block (block_size tokens of the
+// group's k and v, causal inside the query's own block) streams through a
+// double-buffered cp.async pipeline; online softmax, natural-log LSE.  The
+// backward is key-centric (gqa_bwd_kv.cu).
 #include "kernels.cuh"
 
 namespace tsa {
@@ -190,194 +189,23 @@ __global__ void __launch_bounds__(128) gqa_fwd_mma_kernel(const __grid_constant_
 }
 
 template <int BS, int DH>
-__global__ void __launch_bounds__(128) gqa_bwd_mma_kernel(const __grid_constant__ GqaArgs a) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  constexpr int RS = DH + 8, PRS = BS + 8;
-  constexpr int KPW = BS / 4;
-  constexpr int NKT = KPW / 8;
-  constexpr int CPW = DH / 4;
-  constexpr int NTV = CPW / 8;
-  __nv_bfloat16* Qs = reinterpret_cast<__nv_bfloat16*>(smem_raw);  // [16][RS]
-  __nv_bfloat16* dOs = Qs + 16 * RS;                                // [16][RS]
-  __nv_bfloat16* Ks = dOs + 16 * RS;                                // [2][BS][RS]
-  __nv_bfloat16* Vs = Ks + 2 * BS * RS;
-  __nv_bfloat16* Ps = Vs + 2 * BS * RS;                             // [16][PRS]
-  __nv_bfloat16* dSs = Ps + 16 * PRS;
-  int* s_blk = reinterpret_cast<int*>(dSs + 16 * PRS);
-
-  const int t = blockIdx.x, gk = blockIdx.y;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int gq = lane >> 2, c4 = lane & 3;
-  const int sq = seq_of(a.st, t);
-  const int s0 = a.st.cu[sq];
-  const int n = a.st.cu[sq + 1] - s0;
-  const int p = t - s0;
-  const int h0 = gk * a.G;
-  const int* blk_row = a.blk + ((int64_t)t * a.Hkv + gk) * a.nsel;
-  constexpr int CPR = DH / 8;
-  const float NEG_INF = __int_as_float(0xff800000);
-
-  for (int i = tid; i < 16 * CPR; i += 128) {
-    int r = i / CPR, ch = i % CPR;
-    bool ok = r < a.G;
-    int64_t off = ((int64_t)t * a.Hq + h0 + (ok ? r : 0)) * DH + ch * 8;
-    cp_async16(smem_u32(Qs + r * RS + ch * 8), a.q + off, ok ? 16u : 0u);
-    cp_async16(smem_u32(dOs + r * RS + ch * 8), a.dout + off, ok ? 16u : 0u);
-  }
-  auto gather = [&](int j, int buf) {
-    int b = __ldg(blk_row + j);
-    bool bok = b >= 0 && b * BS < n;
-    for (int i = tid; i < BS * CPR; i += 128) {
-      int r = i / CPR, ch = i % CPR;
-      int pos = b * BS + r;
-      bool ok = bok && pos <= p;
-      int64_t row = ((int64_t)(s0 + (ok ? pos : 0)) * a.Hkv + gk) * DH + ch * 8;
-      cp_async16(smem_u32(Ks + (buf * BS + r) * RS + ch * 8), a.k + row, ok ? 16u : 0u);
-      cp_async16(smem_u32(Vs + (buf * BS + r) * RS + ch * 8), a.v + row, ok ? 16u : 0u);
-    }
-    if (tid == 0) s_blk[buf] = bok ? b : -1;
-  };
-  gather(0, 0);
-  cp_async_commit();
-
-  float lse2[2], dl[2];
-#pragma unroll
-  for (int rr = 0; rr < 2; ++rr) {
-    int r = gq + rr * 8;
-    float L = r < a.G ? a.lse_in[(int64_t)t * a.Hq + h0 + r] : NEG_INF;
-    lse2[rr] = L * kLog2e;
-    dl[rr] = r < a.G ? a.dlt[(int64_t)t * a.Hq + h0 + r] : 0.f;
-  }
-  float dq[NTV][4];
-#pragma unroll
-  for (int i = 0; i < NTV; ++i) dq[i][0] = dq[i][1] = dq[i][2] = dq[i][3] = 0.f;
-
-  for (int j = 0; j < a.nsel; ++j) {
-    const int buf = j & 1;
-    if (j + 1 < a.nsel) { gather(j + 1, buf ^ 1); cp_async_commit(); cp_async_wait<1>(); }
-    else { cp_async_wait<0>(); }
-    __syncthreads();
-    const int b = s_blk[buf];
-    const __nv_bfloat16* Kb = Ks + buf * BS * RS;
-    const __nv_bfloat16* Vb = Vs + buf * BS * RS;
-    if (b >= 0) {  // uniform across the CTA
-      float s[NKT][4], dp[NKT][4];
-#pragma unroll
-      for (int i = 0; i < NKT; ++i)
-        for (int e = 0; e < 4; ++e) s[i][e] = dp[i][e] = 0.f;
-#pragma unroll
-      for (int ks = 0; ks < DH / 16; ks += 2) {
-        uint32_t a0, a1, a2, a3, a4, a5, a6, a7, e0, e1, e2, e3, e4, e5, e6, e7;
-        ldsm_x4(smem_u32(Qs + (lane & 15) * RS + ks * 16 + (lane >> 4) * 8), a0, a1, a2, a3);
-        ldsm_x4(smem_u32(Qs + (lane & 15) * RS + (ks + 1) * 16 + (lane >> 4) * 8), a4, a5, a6, a7);
-        ldsm_x4(smem_u32(dOs + (lane & 15) * RS + ks * 16 + (lane >> 4) * 8), e0, e1, e2, e3);
-        ldsm_x4(smem_u32(dOs + (lane & 15) * RS + (ks + 1) * 16 + (lane >> 4) * 8), e4, e5, e6, e7);
-#pragma unroll
-        for (int nk = 0; nk < NKT; ++nk) {
-          uint32_t b0, b1, b2, b3;
-          int krow = warp * KPW + nk * 8 + (lane & 7);
-          ldsm_x4(smem_u32(Kb + krow * RS + ks * 16 + (lane >> 3) * 8), b0, b1, b2, b3);
-          mma_bf16(s[nk], a0, a1, a2, a3, b0, b1);
-          mma_bf16(s[nk], a4, a5, a6, a7, b2, b3);
-          ldsm_x4(smem_u32(Vb + krow * RS + ks * 16 + (lane >> 3) * 8), b0, b1, b2, b3);
-          mma_bf16(dp[nk], e0, e1, e2, e3, b0, b1);
-          mma_bf16(dp[nk], e4, e5, e6, e7, b2, b3);
-        }
-      }
-#pragma unroll
-      for (int nk = 0; nk < NKT; ++nk) {
-        int key = warp * KPW + nk * 8 + 2 * c4;
-        bool v0 = b * BS + key <= p, v1 = b * BS + key + 1 <= p;
-        float P[4], dS[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          int rr = i >> 1;
-          bool v = (i & 1) ? v1 : v0;
-          P[i] = (v && lse2[rr] != NEG_INF) ? exp2f(s[nk][i] * a.scale_log2 - lse2[rr]) : 0.f;
-          dS[i] = a.scale * P[i] * (dp[nk][i] - dl[rr]);
-        }
-        *reinterpret_cast<uint32_t*>(Ps + gq * PRS + key) = pack_bf16(P[0], P[1]);
-        *reinterpret_cast<uint32_t*>(Ps + (gq + 8) * PRS + key) = pack_bf16(P[2], P[3]);
-        *reinterpret_cast<uint32_t*>(dSs + gq * PRS + key) = pack_bf16(dS[0], dS[1]);
-        *reinterpret_cast<uint32_t*>(dSs + (gq + 8) * PRS + key) = pack_bf16(dS[2], dS[3]);
-      }
-      __syncthreads();
-      // dQ[:, warp channels] += dS K
-#pragma unroll
-      for (int ks = 0; ks < BS / 16; ++ks) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4(smem_u32(dSs + (lane & 15) * PRS + ks * 16 + (lane >> 4) * 8), a0, a1, a2, a3);
-#pragma unroll
-        for (int nt = 0; nt < NTV; nt += 2) {
-          uint32_t b0, b1, b2, b3;
-          int key = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-          int ch = warp * CPW + nt * 8 + (lane >> 4) * 8;
-          ldsm_x4_t(smem_u32(Kb + key * RS + ch), b0, b1, b2, b3);
-          mma_bf16(dq[nt], a0, a1, a2, a3, b0, b1);
-          mma_bf16(dq[nt + 1], a0, a1, a2, a3, b2, b3);
-        }
-      }
-      // dK tile = dS^T Q, dV tile = P^T dO  ([BS keys x DH], K = 16 heads); warp owns CPW channels
-#pragma unroll 1
-      for (int nt = 0; nt < NTV; ++nt) {
-        const int ch0 = warp * CPW + nt * 8;
-        uint32_t bq0, bq1, bo0, bo1;
-        ldsm_x2_t(smem_u32(Qs + (lane & 15) * RS + ch0), bq0, bq1);
-        ldsm_x2_t(smem_u32(dOs + (lane & 15) * RS + ch0), bo0, bo1);
-#pragma unroll
-        for (int m2 = 0; m2 < BS / 16; ++m2) {
-          float ak[4] = {0.f, 0.f, 0.f, 0.f}, av[4] = {0.f, 0.f, 0.f, 0.f};
-          uint32_t a0, a1, a2, a3;
-          int hrow = (lane & 7) + (lane >> 4) * 8;
-          int kcol = m2 * 16 + ((lane >> 3) & 1) * 8;
-          ldsm_x4_t(smem_u32(dSs + hrow * PRS + kcol), a0, a1, a2, a3);
-          mma_bf16(ak, a0, a1, a2, a3, bq0, bq1);
-          ldsm_x4_t(smem_u32(Ps + hrow * PRS + kcol), a0, a1, a2, a3);
-          mma_bf16(av, a0, a1, a2, a3, bo0, bo1);
-          const int pos0 = b * BS + m2 * 16 + gq, pos1 = pos0 + 8;
-          const int64_t off0 = ((int64_t)(s0 + pos0) * a.Hkv + gk) * DH + ch0;
-          const int64_t off1 = ((int64_t)(s0 + pos1) * a.Hkv + gk) * DH + ch0;
-          red_frag_v4(pos0 <= p ? a.dk_acc + off0 : nullptr, pos1 <= p ? a.dk_acc + off1 : nullptr, ak, c4);
-          red_frag_v4(pos0 <= p ? a.dv_acc + off0 : nullptr, pos1 <= p ? a.dv_acc + off1 : nullptr, av, c4);
-        }
-      }
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int rr = 0; rr < 2; ++rr) {
-    int r = gq + rr * 8;
-    if (r < a.G) {
-      __nv_bfloat16* drow = a.dq + ((int64_t)t * a.Hq + h0 + r) * DH + warp * CPW + 2 * c4;
-#pragma unroll
-      for (int nt = 0; nt < NTV; ++nt)
-        *reinterpret_cast<uint32_t*>(drow + nt * 8) = pack_bf16(dq[nt][2 * rr], dq[nt][2 * rr + 1]);
-    }
-  }
-}
-
-template <int BS, int DH>
-static cudaError_t launch_gqa_t(const GqaArgs& a, bool bwd, cudaStream_t stream) {
+static cudaError_t launch_gqa_t(const GqaArgs& a, cudaStream_t stream) {
   constexpr int RS = DH + 8, PRS = BS + 8;
   dim3 grid(a.T, a.Hkv);
-  if (!bwd) {
-    size_t smem = sizeof(__nv_bfloat16) * (16 * RS + 4 * BS * RS + 16 * PRS) + sizeof(float) * 128 + 16;
-    cudaFuncSetAttribute(gqa_fwd_mma_kernel<BS, DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    gqa_fwd_mma_kernel<BS, DH><<<grid, 128, smem, stream>>>(a);
-  } else {
-    size_t smem = sizeof(__nv_bfloat16) * (32 * RS + 4 * BS * RS + 32 * PRS) + 16;
-    cudaFuncSetAttribute(gqa_bwd_mma_kernel<BS, DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    gqa_bwd_mma_kernel<BS, DH><<<grid, 128, smem, stream>>>(a);
-  }
+  size_t smem = sizeof(__nv_bfloat16) * (16 * RS + 4 * BS * RS + 16 * PRS) + sizeof(float) * 128 + 16;
+  cudaError_t e = cudaFuncSetAttribute(gqa_fwd_mma_kernel<BS, DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  gqa_fwd_mma_kernel<BS, DH><<<grid, 128, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
-cudaError_t launch_gqa(const GqaArgs& a, int bs, int d, bool bwd, cudaStream_t stream) {
+cudaError_t launch_gqa(const GqaArgs& a, int bs, int d, cudaStream_t stream) {
   if (a.T <= 0) return cudaSuccess;
-  if (bs == 64 && d == 128) return launch_gqa_t<64, 128>(a, bwd, stream);
-  if (bs == 64 && d == 64) return launch_gqa_t<64, 64>(a, bwd, stream);
-  if (bs == 32 && d == 128) return launch_gqa_t<32, 128>(a, bwd, stream);
-  return launch_gqa_t<32, 64>(a, bwd, stream);
+  if (bs == 64 && d == 128) return launch_gqa_t<64, 128>(a, stream);
+  if (bs == 64 && d == 64) return launch_gqa_t<64, 64>(a, stream);
+  if (bs == 32 && d == 128) return launch_gqa_t<32, 128>(a, stream);
+  return launch_gqa_t<32, 64>(a, stream);
 }
 
 }  // namespace tsa

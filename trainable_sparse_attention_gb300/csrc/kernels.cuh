@@ -81,24 +81,45 @@ struct MlaBwdTcArgs {
   SeqTable st;
 };
 
-struct GqaArgs {
+struct GqaArgs {            // Sparse-GQA forward (gqa.cu)
   const __nv_bfloat16* q;   // [T, Hq, d]
   const __nv_bfloat16* k;   // [T, Hkv, d]
   const __nv_bfloat16* v;   // [T, Hkv, d]
   const int32_t* blk;       // [T, Hkv, nsel]
-  const float* lse_in;      // bwd: [T, Hq]
-  const float* dlt;         // bwd: [T, Hq]
-  const __nv_bfloat16* dout;// bwd: [T, Hq, d]
   int T, Hq, Hkv, G, nsel;
   float scale, scale_log2;
-  __nv_bfloat16* out;       // fwd: [T, Hq, d]
-  float* lse;               // fwd: [T, Hq]
-  __nv_bfloat16* dq;        // bwd
-  float* dk_acc;            // bwd: [T, Hkv, d] fp32
-  float* dv_acc;
+  __nv_bfloat16* out;       // [T, Hq, d]
+  float* lse;               // [T, Hq]
   unsigned int* flags;      // device error flags
   SeqTable st;
 };
+
+// Key-centric Sparse-GQA backward (gqa_bwd_kv.cu): inverted selections and
+// fp32 gradient accumulators, all in the caller's workspace.
+struct GqaKvArgs {
+  const __nv_bfloat16* q;     // [T, Hq, d]
+  const __nv_bfloat16* k;     // [T, Hkv, d]
+  const __nv_bfloat16* v;     // [T, Hkv, d]
+  const __nv_bfloat16* dout;  // [T, Hq, d]
+  const int32_t* blk;         // [T, Hkv, nsel] local block ids, -1 = none
+  const float* lse_in;        // [T, Hq] natural log
+  const float* dlt;           // [T, Hq] rowsum(dO * O)
+  int T, Hq, Hkv, G, nsel, bs;
+  float scale, scale_log2;
+  int nblk;                   // blocks over all sequences
+  int* cnt;                   // [nblk * Hkv] queries per (block, group)
+  int* off;                   // [nblk * Hkv + 1] list offsets
+  int* cur;                   // [nblk * Hkv] fill cursors
+  int* choff;                 // [nblk * Hkv + 1] chunk offsets
+  int* list;                  // [T * Hkv * nsel] query tokens per (block, group)
+  float* dq_acc;              // [T, Hq, d] fp32
+  float* dk_acc;              // [T, Hkv, d] fp32
+  float* dv_acc;
+  unsigned int* flags;
+  SeqTable st;
+  int blk_base[TSA_MAX_SEQS + 1];  // first global block of each sequence
+};
+cudaError_t launch_gqa_bwd_kv(const GqaKvArgs& a, int d, cudaStream_t stream);
 
 cudaError_t launch_topk_rows(const TopkRows& a, int64_t rows, cudaStream_t stream);
 cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t stream);
@@ -116,7 +137,7 @@ cudaError_t launch_mla_bwd_dq_tc(const MlaBwdArgs& a, int D, int nq, cudaStream_
 cudaError_t launch_bwd_delta(const __nv_bfloat16* o, const __nv_bfloat16* dout, float* dlt, int64_t rows, int dv,
                              cudaStream_t stream);
 cudaError_t launch_f32_to_bf16(const float* src, __nv_bfloat16* dst, int64_t n, cudaStream_t stream);
-cudaError_t launch_gqa(const GqaArgs& a, int bs, int d, bool bwd, cudaStream_t stream);
+cudaError_t launch_gqa(const GqaArgs& a, int bs, int d, cudaStream_t stream);
 
 constexpr int kIndexerKTile = 128;  // keys per indexer tile (block sizes must divide it)
 constexpr int kTopkMaxK = 4096;
