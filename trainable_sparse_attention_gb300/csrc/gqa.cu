@@ -21,7 +21,8 @@ struct GqaSmem {
   static constexpr int PRS = BS + 8;
 };
 
-template <int BS, int DH>
+// NST-stage cp.async ring of selected blocks (K and V tiles).
+template <int BS, int DH, int NST>
 __global__ void __launch_bounds__(128) gqa_fwd_mma_kernel(const __grid_constant__ GqaArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   constexpr int RS = DH + 8, PRS = BS + 8;
@@ -30,12 +31,12 @@ __global__ void __launch_bounds__(128) gqa_fwd_mma_kernel(const __grid_constant_
   constexpr int CPW = DH / 4;        // channels per warp in PV
   constexpr int NTV = CPW / 8;
   __nv_bfloat16* Qs = reinterpret_cast<__nv_bfloat16*>(smem_raw);  // [16][RS]
-  __nv_bfloat16* Ks = Qs + 16 * RS;                                 // [2][BS][RS]
-  __nv_bfloat16* Vs = Ks + 2 * BS * RS;                             // [2][BS][RS]
-  __nv_bfloat16* Ps = Vs + 2 * BS * RS;                             // [16][PRS]
+  __nv_bfloat16* Ks = Qs + 16 * RS;                                 // [NST][BS][RS]
+  __nv_bfloat16* Vs = Ks + NST * BS * RS;                           // [NST][BS][RS]
+  __nv_bfloat16* Ps = Vs + NST * BS * RS;                           // [16][PRS]
   float* red_max = reinterpret_cast<float*>(Ps + 16 * PRS);         // [4][16]
   float* red_sum = red_max + 64;
-  int* s_blk = reinterpret_cast<int*>(red_sum + 64);                // [2]
+  int* s_blk = reinterpret_cast<int*>(red_sum + 64);                // [NST]
 
   const int t = blockIdx.x, gk = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -68,8 +69,13 @@ __global__ void __launch_bounds__(128) gqa_fwd_mma_kernel(const __grid_constant_
     }
     if (tid == 0) s_blk[buf] = bok ? b : -1;
   };
-  gather(0, 0);
-  cp_async_commit();
+  // the q rows and the first NST - 1 blocks; one cp.async group per block
+  // (empty groups past the last block keep the group count uniform)
+#pragma unroll
+  for (int j = 0; j < NST - 1; ++j) {
+    if (j < a.nsel) gather(j, j);
+    cp_async_commit();
+  }
 
   const float NEG_INF = __int_as_float(0xff800000);
   float m_r[2] = {NEG_INF, NEG_INF}, l_r[2] = {0.f, 0.f};
@@ -78,9 +84,11 @@ __global__ void __launch_bounds__(128) gqa_fwd_mma_kernel(const __grid_constant_
   for (int i = 0; i < NTV; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
   for (int j = 0; j < a.nsel; ++j) {
-    const int buf = j & 1;
-    if (j + 1 < a.nsel) { gather(j + 1, buf ^ 1); cp_async_commit(); cp_async_wait<1>(); }
-    else { cp_async_wait<0>(); }
+    const int buf = j % NST;
+    // buffer (j + NST - 1) % NST was consumed in iteration j - 1 (closing barrier)
+    if (j + NST - 1 < a.nsel) gather(j + NST - 1, (j + NST - 1) % NST);
+    cp_async_commit();
+    cp_async_wait<NST - 1>();  // block j has landed
     __syncthreads();
     const int b = s_blk[buf];
     const __nv_bfloat16* Kb = Ks + buf * BS * RS;
@@ -191,12 +199,13 @@ __global__ void __launch_bounds__(128) gqa_fwd_mma_kernel(const __grid_constant_
 template <int BS, int DH>
 static cudaError_t launch_gqa_t(const GqaArgs& a, cudaStream_t stream) {
   constexpr int RS = DH + 8, PRS = BS + 8;
+  constexpr int NST = 3;  // two blocks in flight per CTA, two CTAs per SM at BS = 64, DH = 128
   dim3 grid(a.T, a.Hkv);
-  size_t smem = sizeof(__nv_bfloat16) * (16 * RS + 4 * BS * RS + 16 * PRS) + sizeof(float) * 128 + 16;
-  cudaError_t e = cudaFuncSetAttribute(gqa_fwd_mma_kernel<BS, DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  size_t smem = sizeof(__nv_bfloat16) * (16 * RS + 2 * NST * BS * RS + 16 * PRS) + sizeof(float) * 128 + 4 * NST;
+  cudaError_t e = cudaFuncSetAttribute(gqa_fwd_mma_kernel<BS, DH, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  gqa_fwd_mma_kernel<BS, DH><<<grid, 128, smem, stream>>>(a);
+  gqa_fwd_mma_kernel<BS, DH, NST><<<grid, 128, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
