@@ -47,6 +47,27 @@ def test_gqa_fwd_bwd(tsa, Hq, Hkv, d, bs, nsel, lengths):
     assert torch.all(out[min(5, T - 1)] == 0)
 
 
+def test_gqa_bwd_lists_longer_than_a_chunk(tsa):
+    """Every query selects block 0 (plus two others), so the inverted list of
+    block 0 holds all 1300 queries of the sequence: the backward splits it over
+    several CTAs whose dK/dV partial sums meet in the fp32 workspace."""
+    cu = [0, 1300]
+    T, Hq, Hkv, d, bs, nsel = 1300, 8, 1, 64, 64, 3
+    g = synth.gqa_inputs(T, Hq, Hkv, d, seed=31, with_grad_out=True)
+    blk = synth.random_block_indices(cu, Hkv, nsel, bs, seed=31)
+    has0 = (blk == 0).any(dim=2, keepdim=True)
+    blk[:, :, :1] = torch.where(has0, blk[:, :, :1], torch.zeros_like(blk[:, :, :1]))
+    assert bool((blk == 0).any(dim=2).all())
+    scale = 1 / math.sqrt(d)
+    q, k, v, dO = (g[n].to(DEV) for n in ("q", "k", "v", "dout"))
+    out, lse = tsa.sparse_gqa_fwd(q, k, v, blk.to(DEV), cu, bs, scale)
+    dq, dk, dv = tsa.sparse_gqa_bwd(q, k, v, blk.to(DEV), out, lse, dO, cu, bs, scale)
+    torch.cuda.synchronize()
+    dq_r, dk_r, dv_r = O.sparse_gqa_bwd(g["q"], g["k"], g["v"], blk, cu, bs, scale, g["dout"])
+    for got, ref in ((dq, dq_r), (dk, dk_r), (dv, dv_r)):
+        assert rel_l2(got, ref) <= TOL_GRAD
+
+
 def test_gqa_forward_deterministic(tsa):
     cu = [0, 900]
     g = synth.gqa_inputs(900, 16, 2, 128, seed=3)
