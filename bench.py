@@ -574,11 +574,20 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-gqa", action="store_true", help="skip the separately timed block Sparse-GQA workload")
+    ap.add_argument("--gqa-only", action="store_true",
+                    help="profiling aid: time only the block Sparse-GQA workload and print its object")
     args = ap.parse_args()
     if args.T != T_TOK:
         set_T(args.T)
     if args.impl == "reference":
         return run_reference(args)
+    if args.gqa_only:
+        import torch
+        import trainable_sparse_attention_gb300 as tsa
+        tsa.build()
+        tsa.load_library()
+        print(json.dumps(run_gqa(args, tsa, torch.device("cuda", 0), 1)), flush=True)
+        return 0
     return run_gpu(args)
 
 
