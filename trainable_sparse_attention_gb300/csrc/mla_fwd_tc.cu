@@ -27,8 +27,9 @@
 // through shared memory, were slower); each rescales and writes its row of
 // the O slice.  Warp 4: TMEM owner and QK^T issuer; warp 5: PV issuer (two
 // issuing threads, so that QK^T waiting for a gather never delays a ready
-// PV); warps 6-9: cp.async gather of the selected rows into a 6-stage ring of
-// 32-key tiles; warp 10: sender, one bulk copy per tile of the staged partial
+// PV); warps 6-9: TMA gathers (tile::gather4, issued from several lanes at
+// once) of the selected rows into a 6-stage ring of 32-key tiles; warp 10:
+// sender, one bulk copy per tile of the staged partial
 // logits into the peer's exchange buffer (per-thread stores into the peer's
 // shared memory held up the softmax warps' next shared-memory accesses by
 // ~0.5 us per tile).
@@ -43,6 +44,9 @@
 #include "tc.cuh"
 
 namespace tsa {
+
+cudaError_t make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                              uint32_t box_cols);
 
 namespace {
 
@@ -88,7 +92,7 @@ __device__ __forceinline__ float ex2(float x) {
 
 template <int D>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
-    mla_fwd_tc_kernel(const __grid_constant__ MlaFwdArgs a) {
+    mla_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ MlaFwdArgs a) {
   using L = MtLayout<D>;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -131,7 +135,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
   if (tid == 0) {
     tc::mbar_init(qready, MT_SOFTMAX);
     for (int i = 0; i < MT_STAGES; ++i) {
-      tc::mbar_init(&kv_full[i], 128);  // one asynchronous arrival per producer thread when its copies land
+      tc::mbar_init(&kv_full[i], 4);  // one expect-tx arrival per producer warp; its gathers complete the bytes
       tc::mbar_init(&kv_empty[i], 1);
       tc::mbar_init(&mask_full[i], 4);
     }
@@ -161,20 +165,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
 
   if (warp >= MT_W_PROD && warp < MT_W_PROD + 4) {
     // ------------------------------------------------------------ gather producers (4 warps)
-    // Warp w copies rows 8w .. 8w+7 of each 32-row tile; lane l copies the
-    // 16-byte chunks l, l+32 of the row's channel slice, so one instruction
-    // covers up to 512 contiguous bytes of the row.  The chunks land in the
-    // 128-byte-swizzled K-major tile; each thread's copies arrive on the
-    // stage's barrier asynchronously when they land
-    // (cp.async.mbarrier.arrive.noinc), so the producers never wait on their
-    // own copies: every free stage holds a tile in flight.  The MMA thread
-    // orders the landed data for the tensor cores with a proxy fence.  The
-    // slot indices of the next tile are loaded one tile ahead (lane r < 8
-    // holds row 8w + r).
+    // Warp w fetches rows 8w .. 8w+7 of each 32-row tile with TMA gathers of
+    // 4 rows x one 64-channel block (tile::gather4, 128-byte swizzle, the
+    // K-major layout the MMA reads): lane l < 2 kb issues the gather of row
+    // group l / kb and channel block l % kb, so the warp's 8 or 10 gathers are
+    // in flight together and no copy goes through the load/store pipe.  A slot
+    // that is -1 (or outside its sequence) fetches the sequence's first row
+    // instead; the softmax masks it (P = 0), so nothing of it reaches the
+    // output.  The slot indices of the next tile are loaded one tile ahead
+    // (lane r < 8 holds row 8w + r).
     const int w8 = (warp - MT_W_PROD) * 8;
-    const int nchunk = kb * 8;  // 32 or 40
-    const char* kvb = reinterpret_cast<const char*>(a.kv);
     bool ok = true;
+    int issued = 0;  // tiles whose gathers this warp has issued
     int id_next = (lane < 8 && w8 + lane < a.topk) ? __ldg(idx_row + w8 + lane) : -1;
     for (int j = 0; j < ntiles; ++j) {
       const int st = j % MT_STAGES;
@@ -186,30 +188,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
         break;
       }
       if (lane < 8 && id_mine >= n) raise_flag(a.flags, TSA_FLAG_INDEX_RANGE);
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const int id = __shfl_sync(0xffffffffu, id_mine, r);
-        const int row = w8 + r;
-        const bool valid = id >= 0 && id < n;
-        const char* src_row = kvb + ((int64_t)(valid ? s0 + id : 0) * D + ch0) * 2;
-        const uint32_t dst = sKV + st * L::KV_STAGE + row * 128;
-        for (int c16 = lane; c16 < nchunk; c16 += 32) {
-          const int cb = c16 >> 3, jj = c16 & 7;
-          cp_async16(dst + cb * L::KV_BLOCK + ((jj ^ (row & 7)) << 4), src_row + c16 * 16, valid ? 16u : 0u);
-        }
-      }
-      cp_async_commit();
-      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&kv_full[st]))
-                   : "memory");
+      const bool valid = id_mine >= 0 && id_mine < n;
+      const int row_mine = s0 + (valid ? id_mine : 0);
+      // this warp's bytes (8 rows x kb blocks of 128 bytes) are expected before its gathers are issued
+      if (lane == 0) tc::mbar_arrive_expect_tx(&kv_full[st], kb * 8 * 128);
+      __syncwarp();
+      const int grp = lane / kb, c = lane - grp * kb;  // row group (4 rows) and channel block of this lane
+      const int r0 = __shfl_sync(0xffffffffu, row_mine, (4 * grp) & 31);
+      const int r1 = __shfl_sync(0xffffffffu, row_mine, (4 * grp + 1) & 31);
+      const int r2 = __shfl_sync(0xffffffffu, row_mine, (4 * grp + 2) & 31);
+      const int r3 = __shfl_sync(0xffffffffu, row_mine, (4 * grp + 3) & 31);
+      if (lane < 2 * kb)
+        tc::tma_gather4(sKV + st * L::KV_STAGE + c * L::KV_BLOCK + (w8 + 4 * grp) * 128, &tm_kv, &kv_full[st],
+                        ch0 + c * 64, r0, r1, r2, r3);
+      issued = j + 1;
       // valid-slot bits of this warp's 8 rows: byte w of the stage's mask word
-      const uint32_t bal = __ballot_sync(0xffffffffu, lane < 8 && id_mine >= 0 && id_mine < n);
+      const uint32_t bal = __ballot_sync(0xffffffffu, lane < 8 && valid);
       if (lane == 0) {
         reinterpret_cast<volatile unsigned char*>(&masks[st])[warp - MT_W_PROD] = static_cast<unsigned char>(bal & 0xffu);
         tc::mbar_arrive(&mask_full[st]);
       }
     }
-    cp_async_wait<0>();
     if (!ok) *abort_flag = 1;
+    // the gathers still in flight land before the CTA can exit (bounded by
+    // time only, so this also runs after an abort)
+    volatile int keep_waiting = 0;
+    for (int g = issued > MT_STAGES ? issued - MT_STAGES : 0; g < issued; ++g)
+      (void)tc::mbar_wait(&kv_full[g % MT_STAGES], (g / MT_STAGES) & 1, &keep_waiting);
   } else if (warp == MT_W_QK) {
     // ------------------------------------------------------------ QK^T issuer (A = q slice in TMEM)
     if (lane == 0) {
@@ -488,9 +493,13 @@ template <int D>
 static cudaError_t launch_tc_t(const MlaFwdArgs& a, cudaStream_t stream) {
   constexpr int smem = MtLayout<D>::SMEM;
   static_assert(smem <= 227 * 1024, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(mla_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // kv [T, D] bf16, boxes of one row x 64 channels (128 bytes) for tile::gather4
+  CUtensorMap tm_kv;
+  cudaError_t e = make_tmap_bf16_2d(&tm_kv, a.kv, static_cast<uint64_t>(a.T), D, 1, 64);
   if (e != cudaSuccess) return e;
-  mla_fwd_tc_kernel<D><<<dim3(2 * a.T), MT_THREADS, smem, stream>>>(a);
+  e = cudaFuncSetAttribute(mla_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  mla_fwd_tc_kernel<D><<<dim3(2 * a.T), MT_THREADS, smem, stream>>>(tm_kv, a);
   return cudaGetLastError();
 }
 
