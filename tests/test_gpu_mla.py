@@ -258,6 +258,10 @@ def test_mla_h128_backward(tsa, D, topk, lengths):
     mask[rows] = True
     m["dout"] = torch.where(mask[:, None, None], m["dout"], torch.zeros_like(m["dout"]))
     r = _run_fwd_bwd(tsa, m, idx, cu, scale)
+    # dq has no atomics: a second call on the same inputs is bit-identical
+    dq2, _ = tsa.sparse_mla_bwd(m["q"].to(DEV), m["kv"].to(DEV), idx.to(DEV), r["out"], r["lse"],
+                                m["dout"].to(DEV), cu, scale)
+    assert torch.equal(dq2, r["dq"])
     dq_ref, dkv_ref = O.sparse_mla_bwd(m["q"], m["kv"], idx, cu, scale, m["dout"], rows=rows)
     dq = r["dq"].cpu()
     assert rel_l2(dq[rows], dq_ref) <= TOL_GRAD

@@ -81,7 +81,8 @@ __device__ __forceinline__ float ex2(float x) {
 //             reads P, writes dS = scale P (dP - Dlt).
 template <int D, bool DS>
 __global__ void __launch_bounds__(SP_THREADS, 1)
-    mla_bwd_sp_tc_kernel(const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ MlaBwdArgs a) {
+    mla_bwd_sp_tc_kernel(const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_kv,
+                         const __grid_constant__ MlaBwdArgs a) {
   constexpr int KC = DS ? 512 : D;   // channels of the contraction
   constexpr int KB = KC / 64;        // 64-channel blocks of a gathered row
   constexpr int ACOLS = KC / 2;      // TMEM columns of the A operand (bf16 pairs)
@@ -116,7 +117,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
   if (tid == 0) {
     tc::mbar_init(aready, 16);
     for (int i = 0; i < SP_STAGES; ++i) {
-      tc::mbar_init(&kv_full[i], SP_PRODUCERS);
+      tc::mbar_init(&kv_full[i], SP_PRODUCERS / 32);  // one expect-tx arrival per producer warp
       tc::mbar_init(&kv_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -163,16 +164,17 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
 
   if (warp >= 9) {
     // ------------------------------------------------------------ gather producers (8 warps)
-    // Warp w copies rows 8w .. 8w+7 of each 64-row tile; lane l copies the
-    // 16-byte chunks l, l+32, ... of a row, so one instruction covers 512
-    // contiguous bytes of the row.  The chunks land in the 128-byte-swizzled
-    // K-major tile, and each thread's copies arrive asynchronously on the
-    // stage's barrier when they land.  The slot indices of the next tile are
-    // loaded one tile ahead (lane r < 8 holds row 8w + r).
+    // Warp w fetches rows 8w .. 8w+7 of each 64-row tile with TMA gathers of
+    // 4 rows x one 64-channel block (tile::gather4, 128-byte swizzle, the
+    // K-major layout the MMA reads): lane l < 2 KB issues the gather of row
+    // group l / KB and channel block l % KB, so the warp's gathers are in
+    // flight together and no copy goes through the load/store pipe.  A slot
+    // that is -1 (or outside its sequence) fetches the sequence's first row;
+    // the epilogue zeroes its P (and so its dS).  The slot indices of the next
+    // tile are loaded one tile ahead (lane r < 8 holds row 8w + r).
     const int w8 = (warp - 9) * 8;
-    constexpr int NCH = KC / 8;  // 16-byte chunks per row
-    const char* kvb = reinterpret_cast<const char*>(a.kv);
     bool ok = true;
+    int issued = 0;
     const int npre = ntiles < SP_STAGES ? ntiles : SP_STAGES;
     int id_next = (lane < 8 && w8 + lane < a.topk) ? __ldg(idx_row + w8 + lane) : -1;
     for (int j = 0; j < ntiles; ++j) {
@@ -185,27 +187,28 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
         break;
       }
       if (!DS && lane < 8 && id_mine >= n) raise_flag(a.flags, TSA_FLAG_INDEX_RANGE);
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const int id = __shfl_sync(0xffffffffu, id_mine, r);
-        const int row = w8 + r;
-        const bool valid = id >= 0 && id < n;
-        const char* src_row = kvb + (int64_t)(valid ? s0 + id : 0) * D * 2;
-        const uint32_t dst = base + st * KV_STAGE + row * 128;
-#pragma unroll
-        for (int c16 = lane; c16 < NCH; c16 += 32) {
-          const int cb = c16 >> 3, jj = c16 & 7;
-          cp_async16(dst + cb * KV_BLOCK + ((jj ^ (row & 7)) << 4), src_row + c16 * 16, valid ? 16u : 0u);
-        }
-      }
-      cp_async_commit();
-      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&kv_full[st]))
-                   : "memory");
+      const int row_mine = s0 + ((id_mine >= 0 && id_mine < n) ? id_mine : 0);
+      // this warp's bytes (8 rows x KB blocks of 128 bytes) are expected before its gathers are issued
+      if (lane == 0) tc::mbar_arrive_expect_tx(&kv_full[st], KB * 8 * 128);
+      __syncwarp();
+      const int grp = lane / KB, c = lane - grp * KB;
+      const int r0 = __shfl_sync(0xffffffffu, row_mine, (4 * grp) & 31);
+      const int r1 = __shfl_sync(0xffffffffu, row_mine, (4 * grp + 1) & 31);
+      const int r2 = __shfl_sync(0xffffffffu, row_mine, (4 * grp + 2) & 31);
+      const int r3 = __shfl_sync(0xffffffffu, row_mine, (4 * grp + 3) & 31);
+      if (lane < 2 * KB)
+        tc::tma_gather4(base + st * KV_STAGE + c * KV_BLOCK + (w8 + 4 * grp) * 128, &tm_kv, &kv_full[st], c * 64,
+                        r0, r1, r2, r3);
+      issued = j + 1;
       // the first tiles are in flight: help load the A rows
       if (j == npre - 1) load_a_rows(warp < 13 ? 2 : 3);
     }
-    cp_async_wait<0>();
     if (!ok) *abort_flag = 1;
+    // the gathers still in flight land before the CTA can exit (bounded by
+    // time only, so this also runs after an abort)
+    volatile int keep_waiting = 0;
+    for (int g = issued > SP_STAGES ? issued - SP_STAGES : 0; g < issued; ++g)
+      (void)tc::mbar_wait(&kv_full[g % SP_STAGES], (g / SP_STAGES) & 1, &keep_waiting);
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -299,6 +302,18 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
         const unsigned char* ps = gbase + OFF_P + b * SP_PTILE + h * 128;
 #pragma unroll
         for (int c = 0; c < 4; ++c) pn[c] = *reinterpret_cast<const uint4*>(ps + (((4 * hf + c) ^ (h & 7)) << 4));
+        const uint32_t* pw = reinterpret_cast<const uint32_t*>(pn);
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pw[i / 2]));
+          pk[i / 2] = pack_bf16(a.scale * p.x * (__uint_as_float(x[i]) - dl),
+                                a.scale * p.y * (__uint_as_float(x[i + 1]) - dl));
+        }
+        // The slot is released only after its values have been consumed, and
+        // the generic-proxy reads are ordered before the TMA (async-proxy)
+        // refill that the release allows: without both, a refill could land
+        // before a read and hand this thread tile j+2's P.
+        tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&pempty[b]);
         if (tid == 0 && j + 2 < ntiles) {
@@ -310,13 +325,6 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
           } else {
             *abort_flag = 1;
           }
-        }
-        const uint32_t* pw = reinterpret_cast<const uint32_t*>(pn);
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pw[i / 2]));
-          pk[i / 2] = pack_bf16(a.scale * p.x * (__uint_as_float(x[i]) - dl),
-                                a.scale * p.y * (__uint_as_float(x[i + 1]) - dl));
         }
       }
       // streaming stores (evict-first in L2): read back once per consumer
@@ -344,14 +352,15 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
 // grid.x = 2 * nq: query q0 + blockIdx.x / 2, channel half blockIdx.x % 2.
 template <int D>
 __global__ void __launch_bounds__(DQ_THREADS, 1)
-    mla_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_ds, const __grid_constant__ MlaBwdArgs a) {
+    mla_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_ds, const __grid_constant__ CUtensorMap tm_kv,
+                         const __grid_constant__ MlaBwdArgs a) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* gbase = smem_raw + (base - raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + DQ_OFF_BAR);
   uint64_t* afull = bars;                     // [STAGES] dS tile (TMA)
-  uint64_t* bfull = afull + DQ_STAGES;        // [STAGES] 256 asynchronous gather arrivals
+  uint64_t* bfull = afull + DQ_STAGES;        // [STAGES] one expect-tx arrival per gather warp
   uint64_t* sempty = bfull + DQ_STAGES;       // [STAGES]
   uint64_t* dfull = sempty + DQ_STAGES;       // [1] all MMAs done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dfull + 1);
@@ -373,7 +382,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   if (tid == 0) {
     for (int i = 0; i < DQ_STAGES; ++i) {
       tc::mbar_init(&afull[i], 1);
-      tc::mbar_init(&bfull[i], 512);
+      tc::mbar_init(&bfull[i], 16);
       tc::mbar_init(&sempty[i], 1);
     }
     tc::mbar_init(dfull, 1);
@@ -416,15 +425,15 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ gather (16 warps)
-    // Warp g (0..15 over warps 0-3, 5-16) copies rows 4g .. 4g+3 of each
-    // 64-row tile (more warps keep more copies in flight); lane l copies the
-    // 16-byte chunks l, l+32 of the row's channel slice, so one instruction
-    // covers up to 512 contiguous bytes.
+    // Warp g (0..15 over warps 0-3, 5-16) fetches rows 4g .. 4g+3 of each
+    // 64-row tile with TMA gathers of 4 rows x one 64-channel block of its
+    // channel slice (tile::gather4, 128-byte swizzle, the MN-major B layout),
+    // lane c < nblk issuing block c.  A slot that is -1 (or outside its
+    // sequence) fetches the sequence's first row; its dS is zero.
     const int g = warp < 4 ? warp : warp - 1;
     const int w8 = g * 4;
-    const int nchunk = nch / 8;  // 32 or 40
-    const char* kvb = reinterpret_cast<const char*>(a.kv);
     bool ok = true;
+    int issued = 0;
     if (tid == 0) tc::prefetch_tmap(&tm_ds);
     int id_next = (lane < 4 && w8 + lane < a.topk) ? __ldg(idx_row + w8 + lane) : -1;
     for (int j = 0; j < ntiles; ++j) {
@@ -441,24 +450,27 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         tc::mbar_arrive_expect_tx(&afull[st], DQ_A);
         tc::tma_load_2d_hint(base + st * DQ_STAGE, &tm_ds, &afull[st], j * DQ_N, lq * PB_H, tc::policy_evict_first());
       }
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int id = __shfl_sync(0xffffffffu, id_mine, r);
-        const int row = w8 + r;
-        const bool valid = id >= 0 && id < n;
-        const char* src_row = kvb + ((int64_t)(valid ? s0 + id : 0) * D + ch0) * 2;
-        const uint32_t dst = base + st * DQ_STAGE + DQ_A + row * 128;
-        for (int c16 = lane; c16 < nchunk; c16 += 32) {
-          const int cb = c16 >> 3, jj = c16 & 7;
-          cp_async16(dst + cb * DQ_BBLK + ((jj ^ (row & 7)) << 4), src_row + c16 * 16, valid ? 16u : 0u);
-        }
-      }
-      cp_async_commit();
-      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&bfull[st]))
-                   : "memory");
+      const int row_mine = s0 + ((id_mine >= 0 && id_mine < n) ? id_mine : 0);
+      // this warp's bytes (4 rows x nblk blocks of 128 bytes) are expected before its gathers are issued
+      if (lane == 0) tc::mbar_arrive_expect_tx(&bfull[st], nblk * 4 * 128);
+      __syncwarp();
+      const int r0 = __shfl_sync(0xffffffffu, row_mine, 0);
+      const int r1 = __shfl_sync(0xffffffffu, row_mine, 1);
+      const int r2 = __shfl_sync(0xffffffffu, row_mine, 2);
+      const int r3 = __shfl_sync(0xffffffffu, row_mine, 3);
+      if (lane < nblk)
+        tc::tma_gather4(base + st * DQ_STAGE + DQ_A + lane * DQ_BBLK + w8 * 128, &tm_kv, &bfull[st], ch0 + lane * 64,
+                        r0, r1, r2, r3);
+      issued = j + 1;
     }
-    cp_async_wait<0>();
     if (!ok) *abort_flag = 1;
+    // the gathers still in flight land before the CTA can exit (bounded by
+    // time only, so this also runs after an abort)
+    {
+      volatile int keep_waiting = 0;
+      for (int gg = issued > DQ_STAGES ? issued - DQ_STAGES : 0; gg < issued; ++gg)
+        (void)tc::mbar_wait(&bfull[gg % DQ_STAGES], (gg / DQ_STAGES) & 1, &keep_waiting);
+    }
     if (warp < 4) {
       // ---------------------------------------------------------- drain dQ (thread = head)
       const int h = tid;
@@ -499,25 +511,29 @@ template <int D, bool DS>
 static cudaError_t launch_sp_t(const MlaBwdArgs& a, int nq, cudaStream_t stream) {
   constexpr int smem = sp_smem<D, DS>();
   static_assert(smem <= 227 * 1024, "shared memory budget");
-  CUtensorMap tp;
+  CUtensorMap tp, tkv;
   cudaError_t e = make_tmap_bf16_2d(&tp, a.p_out, (uint64_t)nq * SP_H, a.kp, SP_H, 64);
   if (e != cudaSuccess) return e;
+  // kv [T, D] bf16, boxes of one row x 64 channels for tile::gather4
+  if ((e = make_tmap_bf16_2d(&tkv, a.kv, static_cast<uint64_t>(a.T), D, 1, 64)) != cudaSuccess) return e;
   e = cudaFuncSetAttribute(mla_bwd_sp_tc_kernel<D, DS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  mla_bwd_sp_tc_kernel<D, DS><<<dim3(nq), SP_THREADS, smem, stream>>>(tp, a);
+  mla_bwd_sp_tc_kernel<D, DS><<<dim3(nq), SP_THREADS, smem, stream>>>(tp, tkv, a);
   return cudaGetLastError();
 }
 
 template <int D>
 static cudaError_t launch_dq_t(const MlaBwdArgs& a, int nq, cudaStream_t stream) {
-  CUtensorMap tds;
+  CUtensorMap tds, tkv;
   cudaError_t e = make_tmap_bf16_2d(&tds, a.ds_out, (uint64_t)nq * PB_H, a.kp, PB_H, 64);
   if (e != cudaSuccess) return e;
+  // kv [T, D] bf16, boxes of one row x 64 channels for tile::gather4
+  if ((e = make_tmap_bf16_2d(&tkv, a.kv, static_cast<uint64_t>(a.T), D, 1, 64)) != cudaSuccess) return e;
   static_assert(DQ_SMEM <= 227 * 1024, "shared memory budget");
   if ((e = cudaFuncSetAttribute(mla_bwd_dq_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, DQ_SMEM)) !=
       cudaSuccess)
     return e;
-  mla_bwd_dq_tc_kernel<D><<<dim3(2 * nq), DQ_THREADS, DQ_SMEM, stream>>>(tds, a);
+  mla_bwd_dq_tc_kernel<D><<<dim3(2 * nq), DQ_THREADS, DQ_SMEM, stream>>>(tds, tkv, a);
   return cudaGetLastError();
 }
 

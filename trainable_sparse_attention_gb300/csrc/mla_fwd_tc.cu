@@ -1,5 +1,5 @@
 // Sparse MLA forward for H = 128 heads on tcgen05 (TMEM accumulators, 2-CTA
-// cluster, cp.async gather into swizzled tiles).
+// cluster, TMA gathers into swizzled tiles).
 //
 // Megatron-LM PR #3674 "Enable DSA CP/absorbed/THD paths with TileLang fused
 // ops" (sparse MLA forward over the absorbed latent) and Megatron-LM PR #7617
