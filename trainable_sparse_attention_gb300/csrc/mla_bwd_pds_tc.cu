@@ -21,8 +21,9 @@
 // Each pass streams its gathered 64-row tiles through a three-stage ring
 // (cp.async, 8 producer warps) and double-buffers the accumulator in TMEM;
 // warps 0-7 (two per TMEM lane quadrant, thread = head, 32 of the 64 key
-// columns each) write [query][head][slot] rows, slots padded to kp with zeros.  No softmax state is carried between tiles: L is
-// known, so every tile is final when it is computed.
+// columns each) write [query][head][slot] rows, slots padded to kp with
+// zeros.  No softmax state is carried between tiles: L is known, so every
+// tile is final when it is computed.
 //
 // mla_bwd_dq_tc_kernel: dQ = dS K over the gathered rows.  The 128 x D fp32
 // accumulator does not fit one SM's 512 TMEM columns for D = 576, so two CTAs
@@ -30,8 +31,13 @@
 // gathers only its slice of the selected rows as the MN-major B operand and
 // streams the dS tiles (A, K-major) by TMA.
 //
-// All gathers copy a selected row with consecutive lanes on consecutive
-// 16-byte chunks, so the cp.async of a warp coalesce into whole lines.
+// The recompute passes copy a selected row with consecutive lanes on
+// consecutive 16-byte chunks, so the cp.async of a warp coalesce into whole
+// lines; the dQ kernel fetches its rows with TMA gathers of 4 rows x 64
+// channels (tile::gather4).  Each kernel uses the copy path that measured
+// faster for it: TMA gathers in the recompute passes, or split half and half
+// with cp.async, made the backward 1-2 % slower, while in the dQ kernel they
+// took a quarter off its time.
 #include "kernels.cuh"
 #include "tc.cuh"
 
@@ -81,8 +87,7 @@ __device__ __forceinline__ float ex2(float x) {
 //             reads P, writes dS = scale P (dP - Dlt).
 template <int D, bool DS>
 __global__ void __launch_bounds__(SP_THREADS, 1)
-    mla_bwd_sp_tc_kernel(const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_kv,
-                         const __grid_constant__ MlaBwdArgs a) {
+    mla_bwd_sp_tc_kernel(const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ MlaBwdArgs a) {
   constexpr int KC = DS ? 512 : D;   // channels of the contraction
   constexpr int KB = KC / 64;        // 64-channel blocks of a gathered row
   constexpr int ACOLS = KC / 2;      // TMEM columns of the A operand (bf16 pairs)
@@ -117,7 +122,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
   if (tid == 0) {
     tc::mbar_init(aready, 16);
     for (int i = 0; i < SP_STAGES; ++i) {
-      tc::mbar_init(&kv_full[i], SP_PRODUCERS / 32);  // one expect-tx arrival per producer warp
+      tc::mbar_init(&kv_full[i], SP_PRODUCERS);
       tc::mbar_init(&kv_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -164,17 +169,16 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
 
   if (warp >= 9) {
     // ------------------------------------------------------------ gather producers (8 warps)
-    // Warp w fetches rows 8w .. 8w+7 of each 64-row tile with TMA gathers of
-    // 4 rows x one 64-channel block (tile::gather4, 128-byte swizzle, the
-    // K-major layout the MMA reads): lane l < 2 KB issues the gather of row
-    // group l / KB and channel block l % KB, so the warp's gathers are in
-    // flight together and no copy goes through the load/store pipe.  A slot
-    // that is -1 (or outside its sequence) fetches the sequence's first row;
-    // the epilogue zeroes its P (and so its dS).  The slot indices of the next
-    // tile are loaded one tile ahead (lane r < 8 holds row 8w + r).
+    // Warp w copies rows 8w .. 8w+7 of each 64-row tile; lane l copies the
+    // 16-byte chunks l, l+32, ... of a row, so one instruction covers 512
+    // contiguous bytes of the row.  The chunks land in the 128-byte-swizzled
+    // K-major tile, and each thread's copies arrive asynchronously on the
+    // stage's barrier when they land.  The slot indices of the next tile are
+    // loaded one tile ahead (lane r < 8 holds row 8w + r).
     const int w8 = (warp - 9) * 8;
+    constexpr int NCH = KC / 8;  // 16-byte chunks per row
+    const char* kvb = reinterpret_cast<const char*>(a.kv);
     bool ok = true;
-    int issued = 0;
     const int npre = ntiles < SP_STAGES ? ntiles : SP_STAGES;
     int id_next = (lane < 8 && w8 + lane < a.topk) ? __ldg(idx_row + w8 + lane) : -1;
     for (int j = 0; j < ntiles; ++j) {
@@ -187,28 +191,27 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
         break;
       }
       if (!DS && lane < 8 && id_mine >= n) raise_flag(a.flags, TSA_FLAG_INDEX_RANGE);
-      const int row_mine = s0 + ((id_mine >= 0 && id_mine < n) ? id_mine : 0);
-      // this warp's bytes (8 rows x KB blocks of 128 bytes) are expected before its gathers are issued
-      if (lane == 0) tc::mbar_arrive_expect_tx(&kv_full[st], KB * 8 * 128);
-      __syncwarp();
-      const int grp = lane / KB, c = lane - grp * KB;
-      const int r0 = __shfl_sync(0xffffffffu, row_mine, (4 * grp) & 31);
-      const int r1 = __shfl_sync(0xffffffffu, row_mine, (4 * grp + 1) & 31);
-      const int r2 = __shfl_sync(0xffffffffu, row_mine, (4 * grp + 2) & 31);
-      const int r3 = __shfl_sync(0xffffffffu, row_mine, (4 * grp + 3) & 31);
-      if (lane < 2 * KB)
-        tc::tma_gather4(base + st * KV_STAGE + c * KV_BLOCK + (w8 + 4 * grp) * 128, &tm_kv, &kv_full[st], c * 64,
-                        r0, r1, r2, r3);
-      issued = j + 1;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const int id = __shfl_sync(0xffffffffu, id_mine, r);
+        const int row = w8 + r;
+        const bool valid = id >= 0 && id < n;
+        const char* src_row = kvb + (int64_t)(valid ? s0 + id : 0) * D * 2;
+        const uint32_t dst = base + st * KV_STAGE + row * 128;
+#pragma unroll
+        for (int c16 = lane; c16 < NCH; c16 += 32) {
+          const int cb = c16 >> 3, jj = c16 & 7;
+          cp_async16(dst + cb * KV_BLOCK + ((jj ^ (row & 7)) << 4), src_row + c16 * 16, valid ? 16u : 0u);
+        }
+      }
+      cp_async_commit();
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&kv_full[st]))
+                   : "memory");
       // the first tiles are in flight: help load the A rows
       if (j == npre - 1) load_a_rows(warp < 13 ? 2 : 3);
     }
+    cp_async_wait<0>();
     if (!ok) *abort_flag = 1;
-    // the gathers still in flight land before the CTA can exit (bounded by
-    // time only, so this also runs after an abort)
-    volatile int keep_waiting = 0;
-    for (int g = issued > SP_STAGES ? issued - SP_STAGES : 0; g < issued; ++g)
-      (void)tc::mbar_wait(&kv_full[g % SP_STAGES], (g / SP_STAGES) & 1, &keep_waiting);
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -429,7 +432,9 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     // 64-row tile with TMA gathers of 4 rows x one 64-channel block of its
     // channel slice (tile::gather4, 128-byte swizzle, the MN-major B layout),
     // lane c < nblk issuing block c.  A slot that is -1 (or outside its
-    // sequence) fetches the sequence's first row; its dS is zero.
+    // sequence) has dS = 0 and fetches some row of its sequence, picked by
+    // slot number so that the padding of short rows does not send every CTA
+    // to the same row (a hot spot in L2).
     const int g = warp < 4 ? warp : warp - 1;
     const int w8 = g * 4;
     bool ok = true;
@@ -450,7 +455,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         tc::mbar_arrive_expect_tx(&afull[st], DQ_A);
         tc::tma_load_2d_hint(base + st * DQ_STAGE, &tm_ds, &afull[st], j * DQ_N, lq * PB_H, tc::policy_evict_first());
       }
-      const int row_mine = s0 + ((id_mine >= 0 && id_mine < n) ? id_mine : 0);
+      const int row_mine = s0 + ((id_mine >= 0 && id_mine < n) ? id_mine : (j * DQ_N + w8 + lane) % n);
       // this warp's bytes (4 rows x nblk blocks of 128 bytes) are expected before its gathers are issued
       if (lane == 0) tc::mbar_arrive_expect_tx(&bfull[st], nblk * 4 * 128);
       __syncwarp();
@@ -511,14 +516,12 @@ template <int D, bool DS>
 static cudaError_t launch_sp_t(const MlaBwdArgs& a, int nq, cudaStream_t stream) {
   constexpr int smem = sp_smem<D, DS>();
   static_assert(smem <= 227 * 1024, "shared memory budget");
-  CUtensorMap tp, tkv;
+  CUtensorMap tp;
   cudaError_t e = make_tmap_bf16_2d(&tp, a.p_out, (uint64_t)nq * SP_H, a.kp, SP_H, 64);
   if (e != cudaSuccess) return e;
-  // kv [T, D] bf16, boxes of one row x 64 channels for tile::gather4
-  if ((e = make_tmap_bf16_2d(&tkv, a.kv, static_cast<uint64_t>(a.T), D, 1, 64)) != cudaSuccess) return e;
   e = cudaFuncSetAttribute(mla_bwd_sp_tc_kernel<D, DS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  mla_bwd_sp_tc_kernel<D, DS><<<dim3(nq), SP_THREADS, smem, stream>>>(tp, tkv, a);
+  mla_bwd_sp_tc_kernel<D, DS><<<dim3(nq), SP_THREADS, smem, stream>>>(tp, a);
   return cudaGetLastError();
 }
 
