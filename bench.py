@@ -129,16 +129,24 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def dist_setup(n_gpus: int):
+def dist_setup(n_gpus: int, backend: str = "nccl"):
+    """Rank, world size and local rank from the torchrun environment; with more
+    than one rank, joins the process group (NCCL on GPUs, one rank per GPU;
+    gloo for the host-side logic on CPU, where no device is selected)."""
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != n_gpus:
+        raise SystemExit(f"--gpus {n_gpus} but WORLD_SIZE={world}: launch one process per GPU with torchrun")
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group(backend)
+    elif backend == "nccl":
         torch.cuda.set_device(0)
     return rank, world, local
 
@@ -150,13 +158,21 @@ def barrier(world):
 
 
 def allmax(x: float, world) -> float:
+    """Maximum of x over the ranks (the timed region of the slowest rank)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_tflops(world: int, flops_per_rank: float, ms: float) -> float:
+    """Whole-job rate: every rank runs the same work on its own replica, and the
+    job takes as long as its slowest rank (ms, already the max over ranks)."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
 
 
 # ---------------------------------------------------------------- oracle timing
@@ -311,7 +327,7 @@ def run_gpu(args):
     st_idx = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
     st_fwd = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
     st_bwd = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps
-    value = world * f_step / (ms_step * 1e-3) / 1e12
+    value = job_tflops(world, f_step, ms_step)
     psus = peaks["bf16_tflops_sustained"]
     stages = {
         "indexer_topk": {"ms": st_idx, "tflops": f_idx / (st_idx * 1e-3) / 1e12,
@@ -440,11 +456,11 @@ def run_gqa(args, tsa, dev, world):
         "lengths": GQA_LENGTHS, "Hq": GQA_HQ, "Hkv": GQA_HKV, "d": GQA_D, "block_size": GQA_BS,
         "blocks_selected": GQA_NSEL, "indexer_heads": GQA_HI, "d_I": GQA_DI, "steps": steps,
         "note": "timed separately after the main step; not part of value",
-        "block_indexer_topk": {"ms": ms[0], "tflops": world * f_idx / (ms[0] * 1e-3) / 1e12,
+        "block_indexer_topk": {"ms": ms[0], "tflops": job_tflops(world, f_idx, ms[0]),
                                "queries_per_s": world * T / (ms[0] * 1e-3)},
-        "gqa_fwd": {"ms": ms[1], "tflops": world * f_fwd / (ms[1] * 1e-3) / 1e12,
+        "gqa_fwd": {"ms": ms[1], "tflops": job_tflops(world, f_fwd, ms[1]),
                     "gather_gbs": world * triples * 2 * GQA_D * 2 / (ms[1] * 1e-3) / 1e9},
-        "gqa_bwd": {"ms": ms[2], "tflops": world * f_bwd / (ms[2] * 1e-3) / 1e12},
+        "gqa_bwd": {"ms": ms[2], "tflops": job_tflops(world, f_bwd, ms[2])},
         "attended_triples": triples,
     }
 
@@ -557,7 +573,7 @@ def run_e2e(args, tsa, dev, cu, dev_inputs, f_step, world):
     del d_in, host_in, host_out
     torch.cuda.empty_cache()
     os.sched_setaffinity(0, saved_affinity)
-    return {"value": world * f_step / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+    return {"value": job_tflops(world, f_step, ms), "unit": "TFLOP/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "pipelined": "H2D of step i+1 and D2H of step i overlap the compute of step i+1",
             "host_cpus": f"{len(local_cpus)} GPU-local CPUs" if local_cpus else "unrestricted (no sysfs locality)"}

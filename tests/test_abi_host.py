@@ -114,3 +114,14 @@ def test_binding_refuses_cpu_tensors():
     idx = torch.zeros(4, 64, dtype=torch.int32)
     with pytest.raises(ValueError, match="CUDA"):
         tsa.sparse_mla_fwd(q, kv, idx, [0, 4], 0.1)
+
+
+def test_explicit_library_path_serves_later_calls(lib):
+    """A build loaded from an explicit path is the one every later call uses."""
+    import trainable_sparse_attention_gb300 as tsa
+    from trainable_sparse_attention_gb300 import _binding
+    try:
+        other = tsa.load_library(_binding.LIB_PATH)
+        assert tsa.load_library() is other
+    finally:
+        _binding._lib = lib

@@ -62,7 +62,8 @@ class TsaError(RuntimeError):
 
 
 def load_library(path: Optional[str] = None):
-    """Load libtsa.so (built in-tree by ``build()``); raises if it is absent."""
+    """Load libtsa.so (built in-tree by ``build()``; or the build at ``path``,
+    which then serves every later call of this module); raises if it is absent."""
     global _lib
     if _lib is not None and path is None:
         return _lib
@@ -75,8 +76,7 @@ def load_library(path: Optional[str] = None):
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
-    if path is None:
-        _lib = lib
+    _lib = lib
     return lib
 
 
