@@ -188,7 +188,11 @@ def test_mla_t65536_h128_sampled(tsa):
     scale = 1 / math.sqrt(192)
     out, lse = tsa.sparse_mla_fwd(m["q"], m["kv"], idx, cu, scale)
     dq, dkv = tsa.sparse_mla_bwd(m["q"], m["kv"], idx, out, lse, m["dout"], cu, scale)
+    # the bench's launch configuration replays bit-identically (dq has no atomics)
+    dq2, _ = tsa.sparse_mla_bwd(m["q"], m["kv"], idx, out, lse, m["dout"], cu, scale)
     torch.cuda.synchronize()
+    assert torch.equal(dq, dq2)
+    del dq2
     o_ref, l_ref = O.sparse_mla_fwd(m["q"], m["kv"], idx, cu, scale, rows=rows)
     check_out_lse(out, lse, o_ref, l_ref, rows=rows)
     dq_ref, dkv_ref = O.sparse_mla_bwd(m["q"], m["kv"], idx, cu, scale, m["dout"], rows=rows)
