@@ -184,7 +184,9 @@ int sparse_mla_fwd(const void* q_dev, const void* kv_dev, const int32_t* indices
  *   dkv and Dlt, and for H = 128 a bf16 staging area for P and dS of one
  *   chunk of queries (at most 4 GiB; the chunk shrinks as topk grows).
  *   Returns 0 for T < 0, H < 1, d_qk < 1 or topk < 1.
- * Same support as sparse_mla_fwd.  dkv summation order is not fixed.
+ * Same support as sparse_mla_fwd.  dq is bit-identical across runs (no
+ * atomics: every element accumulates its slots in a fixed order); the dkv
+ * summation order is not fixed.
  * ------------------------------------------------------------------------- */
 size_t sparse_mla_bwd_workspace_size(int64_t T, int H, int d_qk, int topk);
 int sparse_mla_bwd(const void* q_dev, const void* kv_dev, const int32_t* indices_dev,
