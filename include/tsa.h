@@ -70,6 +70,14 @@ unsigned long long tsa_kernel_launches(void);
  * synchronising `stream`; clear them when clear != 0. */
 int tsa_read_flags(uint32_t* flags, int clear, void* stream);
 
+/* Self-test of the failure path of the kernels' bounded waits, with no fault:
+ * launches one CTA on `stream` that waits on a shared-memory barrier no thread
+ * arrives on, using the same bounded wait as every pipeline of the library.
+ * After the wait limit (2 s) the CTA raises TSA_FLAG_TIMEOUT and returns
+ * normally; the CUDA context stays usable.  Asynchronous: read the flag with
+ * tsa_read_flags.  Returns TSA_ERR_CUDA if the launch fails. */
+int tsa_selftest_bounded_wait(void* stream);
+
 /* ---------------------------------------------------------------------------
  * qsa_indexer_scores -- materialised indexer scores for a range of queries.
  * [QSA "Describe the solution": trainable indexer with ReLU scores, exact

@@ -7,12 +7,12 @@ The compute lives in ``libtsa.so`` (hand-written CUDA, C ABI in
 """
 from ._binding import (FLAG_INDEX_RANGE, FLAG_TIMEOUT, LIB_PATH, SIGNATURES, TsaError, load_library,
                        max_seqlen, qsa_indexer_scores, qsa_topk, qsa_topk_from_scores, qsa_topk_workspace_size,
-                       kernel_launches, read_flags, sparse_gqa_bwd, sparse_gqa_bwd_workspace_size, sparse_gqa_fwd, sparse_mla_bwd,
+                       kernel_launches, read_flags, selftest_bounded_wait, sparse_gqa_bwd, sparse_gqa_bwd_workspace_size, sparse_gqa_fwd, sparse_mla_bwd,
                        sparse_mla_bwd_workspace_size, sparse_mla_fwd)
 
 __all__ = ["qsa_indexer_scores", "qsa_topk", "qsa_topk_from_scores", "qsa_topk_workspace_size",
            "sparse_mla_fwd", "sparse_mla_bwd", "sparse_mla_bwd_workspace_size", "sparse_gqa_fwd",
-           "sparse_gqa_bwd", "sparse_gqa_bwd_workspace_size", "read_flags", "kernel_launches", "load_library", "TsaError",
+           "sparse_gqa_bwd", "sparse_gqa_bwd_workspace_size", "read_flags", "selftest_bounded_wait", "kernel_launches", "load_library", "TsaError",
            "FLAG_INDEX_RANGE", "FLAG_TIMEOUT", "max_seqlen", "build"]
 
 

@@ -30,6 +30,7 @@ SIGNATURES = {
     "tsa_version": (c_int, []),
     "tsa_kernel_launches": (ctypes.c_ulonglong, []),
     "tsa_read_flags": (c_int, [ctypes.POINTER(ctypes.c_uint32), c_int, c_void_p]),
+    "tsa_selftest_bounded_wait": (c_int, [c_void_p]),
     "qsa_indexer_scores": (c_int, [c_void_p, c_void_p, c_void_p, c_i32p, c_int, c_int, c_int, c_int, c_int,
                                    c_float, c_int64, c_int64, c_void_p, c_int64, c_void_p]),
     "qsa_topk_from_scores": (c_int, [c_void_p, c_int64, c_int64, c_int64, c_int, c_void_p, c_void_p]),
@@ -289,6 +290,13 @@ def read_flags(clear: bool = True, stream=None) -> int:
     v = ctypes.c_uint32(0)
     _check("tsa_read_flags", load_library().tsa_read_flags(ctypes.byref(v), int(clear), _stream(stream)))
     return int(v.value)
+
+
+def selftest_bounded_wait(stream=None) -> None:
+    """Launch the library's bounded-wait self-test (a wait that nothing
+    satisfies gives up after 2 s and raises FLAG_TIMEOUT); read the flag with
+    read_flags()."""
+    _check("tsa_selftest_bounded_wait", load_library().tsa_selftest_bounded_wait(_stream(stream)))
 
 
 FLAG_INDEX_RANGE = 0x1

@@ -162,6 +162,13 @@ int tsa_read_flags(uint32_t* flags, int clear, void* stream) {
   return TSA_OK;
 }
 
+int tsa_selftest_bounded_wait(void* stream) {
+  unsigned int* f = flags_ptr();
+  if (f == nullptr) return fail(TSA_ERR_CUDA, "device flag word unavailable");
+  TSA_LAUNCH(launch_bounded_wait_selftest(f, static_cast<cudaStream_t>(stream)), "self-test launch");
+  return TSA_OK;
+}
+
 // ---------------------------------------------------------------- indexer
 
 int qsa_indexer_scores(const void* q_idx, const void* k_idx, const float* w, const int32_t* cu_seqlens,

@@ -127,6 +127,7 @@ cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t stream);
 bool indexer_tc_supported(int H_I, int d_I, int groups, int bs);
 cudaError_t launch_indexer_tc(const IndexerArgs& a, cudaStream_t stream);
 cudaError_t launch_fill(float* p, int64_t n, float v, cudaStream_t stream);
+cudaError_t launch_bounded_wait_selftest(unsigned int* flags, cudaStream_t stream);
 cudaError_t launch_mla_fwd(const MlaFwdArgs& a, int D, cudaStream_t stream);
 cudaError_t launch_mla_fwd_tc(const MlaFwdArgs& a, int D, cudaStream_t stream);
 cudaError_t launch_mla_bwd(const MlaBwdArgs& a, int D, cudaStream_t stream);
