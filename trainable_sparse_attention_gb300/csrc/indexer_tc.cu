@@ -108,6 +108,8 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
   const int w1 = static_cast<int>((static_cast<int64_t>(total) * (blockIdx.x + 1)) / gridDim.x);
   const int nitems = w1 - w0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // producer lane: key tiles issued, and the walk index of the last q_I block issued (-1: none)
+  int a_issued = 0, b_last_tr = -1;
   if (nitems <= 0) return;  // uniform
 
   // start of the share: (qb, kt) of pair w0
@@ -188,6 +190,7 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
             tc::mbar_arrive_expect_tx(bfull, L::B_BYTES);
             for (int c = 0; c < L::KB; ++c)
               tc::tma_load_2d(sB + c * (IT_N * 128), &tm_q, bfull, c * 64, (a.seq_start + p_first) * H_I);
+            b_last_tr = w.tr;
           }
         }
         ok = __all_sync(0xffffffffu, ok);
@@ -203,6 +206,7 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
           const int row = a.seq_start + w.kt * IT_M;
           for (int c = 0; c < L::KB; ++c)
             tc::tma_load_2d(sA + st * L::A_BYTES + c * (IT_M * 128), &tm_k, &full[st], c * 64, row);
+          a_issued = it + 1;
         }
       }
       ok = __all_sync(0xffffffffu, ok);
@@ -312,6 +316,14 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
   tc::fence_before_sync();
   __syncthreads();
   if (*abort_flag && tid == 0) raise_flag(a.flags, TSA_FLAG_TIMEOUT);
+  if (*abort_flag && warp == 8 && lane == 0) {
+    // after an abort a q_I block or a key tile may still be landing: wait
+    // (bounded by time only) for the last loads issued before the CTA exits
+    volatile int keep_waiting = 0;
+    if (b_last_tr >= 0) (void)tc::mbar_wait(bfull, b_last_tr & 1, &keep_waiting);
+    for (int g = a_issued > IT_STAGES ? a_issued - IT_STAGES : 0; g < a_issued; ++g)
+      (void)tc::mbar_wait(&full[g % IT_STAGES], (g / IT_STAGES) & 1, &keep_waiting);
+  }
   if (warp == 5) {
     __syncwarp();
     tc::fence_after_sync();

@@ -118,6 +118,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
   const int* idx_row = a.idx + (int64_t)t * a.topk;
   const int ntiles = (a.topk + SP_N - 1) / SP_N;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int p_issued = 0;  // dS pass: P tiles whose TMA loads thread 0 issued
 
   if (tid == 0) {
     tc::mbar_init(aready, 16);
@@ -266,6 +267,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
         tc::mbar_arrive_expect_tx(&pfull[jj], SP_PTILE);
         tc::tma_load_2d_hint(base + OFF_P + jj * SP_PTILE, &tm_p, &pfull[jj], jj * SP_N, lq * SP_H,
                              tc::policy_evict_first());
+        ++p_issued;
       }
     }
     for (int j = 0; j < ntiles; ++j) {
@@ -325,6 +327,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
             tc::mbar_arrive_expect_tx(&pfull[b], SP_PTILE);
             tc::tma_load_2d_hint(base + OFF_P + b * SP_PTILE, &tm_p, &pfull[b], (j + 2) * SP_N, lq * SP_H,
                                  tc::policy_evict_first());
+            ++p_issued;
           } else {
             *abort_flag = 1;
           }
@@ -344,7 +347,14 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
 
   tc::fence_before_sync();
   __syncthreads();
-  if (*abort_flag && tid == 0) raise_flag(a.flags, TSA_FLAG_TIMEOUT);
+  if (*abort_flag && tid == 0) {
+    raise_flag(a.flags, TSA_FLAG_TIMEOUT);
+    // after an abort a P tile may still be landing: wait (bounded by time
+    // only) for the last tile issued into each slot before the CTA exits
+    volatile int keep_waiting = 0;
+    for (int g = p_issued > 2 ? p_issued - 2 : 0; g < p_issued; ++g)
+      (void)tc::mbar_wait(&pfull[g & 1], (g >> 1) & 1, &keep_waiting);
+  }
   if (warp == 8) {
     __syncwarp();
     tc::fence_after_sync();
@@ -381,6 +391,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   const int* idx_row = a.idx + (int64_t)t * a.topk;
   const int ntiles = a.kp / DQ_N;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int a_issued = 0;  // dS tiles whose TMA loads thread 0 issued
 
   if (tid == 0) {
     for (int i = 0; i < DQ_STAGES; ++i) {
@@ -454,6 +465,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         // the dS tile of this stage (A operand) by TMA
         tc::mbar_arrive_expect_tx(&afull[st], DQ_A);
         tc::tma_load_2d_hint(base + st * DQ_STAGE, &tm_ds, &afull[st], j * DQ_N, lq * PB_H, tc::policy_evict_first());
+        ++a_issued;
       }
       const int row_mine = s0 + ((id_mine >= 0 && id_mine < n) ? id_mine : (j * DQ_N + w8 + lane) % n);
       // this warp's bytes (4 rows x nblk blocks of 128 bytes) are expected before its gathers are issued
@@ -504,7 +516,14 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (*abort_flag && tid == 0) raise_flag(a.flags, TSA_FLAG_TIMEOUT);
+  if (*abort_flag && tid == 0) {
+    raise_flag(a.flags, TSA_FLAG_TIMEOUT);
+    // after an abort a dS tile may still be landing: wait (bounded by time
+    // only) for the last tile issued into each stage before the CTA exits
+    volatile int keep_waiting = 0;
+    for (int g = a_issued > DQ_STAGES ? a_issued - DQ_STAGES : 0; g < a_issued; ++g)
+      (void)tc::mbar_wait(&afull[g % DQ_STAGES], (g / DQ_STAGES) & 1, &keep_waiting);
+  }
   if (warp == 4) {
     __syncwarp();
     tc::fence_after_sync();

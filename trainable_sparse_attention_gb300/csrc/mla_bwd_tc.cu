@@ -82,6 +82,7 @@ __global__ void __launch_bounds__(DK_THREADS, 1)
   const bool has_v = ch0 < 512;         // the block holds value channels (the dO term applies)
   const int ntiles = a.kp / DK_NS;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int b_issued = 0;  // P / dS tiles whose TMA loads the producer issued
 
   if (tid == 0) {
     tc::mbar_init(afull, 1);
@@ -130,6 +131,7 @@ __global__ void __launch_bounds__(DK_THREADS, 1)
           if (has_v)
             tc::tma_load_2d_hint(dst + DK_B + c * DK_BOX, &tm_p, &bfull[st], j * DK_NS + c * 64, lq * BH, pol);
         }
+        ++b_issued;
       }
     }
   } else if (warp == 17) {
@@ -222,6 +224,14 @@ __global__ void __launch_bounds__(DK_THREADS, 1)
   tc::fence_before_sync();
   __syncthreads();
   if (*abort_flag && tid == 0) raise_flag(a.flags, TSA_FLAG_TIMEOUT);
+  if (*abort_flag && warp == 16 && lane == 0) {
+    // after an abort the q / dO boxes or a P / dS tile may still be landing:
+    // wait (bounded by time only) for them before the CTA exits
+    volatile int keep_waiting = 0;
+    (void)tc::mbar_wait(afull, 0, &keep_waiting);
+    for (int g = b_issued > DK_STAGES ? b_issued - DK_STAGES : 0; g < b_issued; ++g)
+      (void)tc::mbar_wait(&bfull[g % DK_STAGES], (g / DK_STAGES) & 1, &keep_waiting);
+  }
   if (warp == 17) {
     __syncwarp();
     tc::fence_after_sync();
