@@ -125,3 +125,26 @@ def test_explicit_library_path_serves_later_calls(lib):
         assert tsa.load_library() is other
     finally:
         _binding._lib = lib
+
+
+def test_backward_and_sequence_table_validation(lib):
+    """More refusals decided on the host before any launch: the backward entry
+    points, the sequence table's size limit and the GQA selection width."""
+    cu = _cu([0, 8])
+    fake = ctypes.c_void_p(16)
+    # MLA backward: a null gradient pointer, an unsupported width
+    assert lib.sparse_mla_bwd(fake, fake, fake, fake, fake, None, cu, 1, 8, 576, 64, 0.1, fake, fake,
+                              fake, 1 << 30, None) == 1
+    assert lib.sparse_mla_bwd(fake, fake, fake, fake, fake, fake, cu, 1, 8, 320, 64, 0.1, fake, fake,
+                              fake, 1 << 30, None) == 2
+    # GQA backward: group size above 16, zero selected blocks, workspace too small, null dq
+    args = lambda Hq, Hkv, nsel, dq, ws_bytes: (fake, fake, fake, fake, fake, fake, fake, cu, 1, Hq, Hkv, 128,
+                                               64, nsel, 0.1, dq, fake, fake, fake, ws_bytes, None)
+    assert lib.sparse_gqa_bwd(*args(64, 2, 4, fake, 1 << 30)) == 2
+    assert lib.sparse_gqa_bwd(*args(32, 4, 0, fake, 1 << 30)) == 1
+    assert lib.sparse_gqa_bwd(*args(32, 4, 4, fake, 16)) == 3
+    assert lib.sparse_gqa_bwd(*args(32, 4, 4, None, 1 << 30)) == 1
+    # more sequences than the kernels' sequence table holds
+    n = 1025
+    many = _cu(list(range(n + 1)))
+    assert lib.sparse_mla_fwd(fake, fake, fake, many, n, 8, 576, 64, 0.1, fake, fake, None) == 1
