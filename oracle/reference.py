@@ -33,7 +33,10 @@ Readings where the pages are silent (each is also listed in the design notes):
   * indices are positions local to their sequence;
   * LSE is the natural log; an all-invalid row gives o = 0 and lse = -inf;
   * sparse MLA does not re-mask the indices it is given (no causal test);
-    sparse GQA keeps only tokens s <= t of the selected blocks.
+    sparse GQA keeps only tokens s <= t of the selected blocks;
+  * the indexer's sparse KL: teacher = the attention probabilities averaged
+    over heads on the selected slots, student = softmax of the indexer scores
+    on the same slots, loss = KL(teacher || student) per query row.
 
 Parity pins: every function here is checked in ``tests/test_oracle_pins.py``
 against closed forms, textbook dense attention, brute force, hand-derived
@@ -292,6 +295,116 @@ def sparse_mla_bwd(q, kv, idx, cu_seqlens, scale: float, dout, d_v: int = 512,
 def mla_bwd_delta(o, dout) -> np.ndarray:
     """Dlt[t,h] = sum_c dO[t,h,c] * o[t,h,c] (the backward's preprocess)."""
     return (as_f64(o) * as_f64(dout)).sum(axis=-1)
+
+
+# --------------------------------------------------------------------------
+# indexer training: sparse KL against the attention teacher, and the indexer
+# backward ([QSA] "Describe the problem": sparse KL supervision for training
+# the indexer; "Describe the solution you'd like": sparse Stage-2 teacher/KL
+# loss for indexer training; [DSA] "Changes": sparse-KL streaming for the
+# indexer loss; file table: fused indexer backward kernel).  The pages print
+# no formula; the reading taken here:
+#   teacher a[t, j]  = the sparse attention probabilities of query t averaged
+#                      over its heads, on t's selected slots j (a distribution,
+#                      since every head's probabilities sum to 1 over them);
+#   student p[t, j]  = softmax over the same slots of the indexer scores;
+#   loss_t           = KL(a_t || p_t) = sum_j a log(a / p), 0 log 0 = 0;
+#   d loss_t / d I   = p - a on the selected slots (the teacher is a target).
+# --------------------------------------------------------------------------
+
+def _selected(idx_t: np.ndarray, n: int) -> np.ndarray:
+    """Mask of the slots of one index row that name a key of the sequence."""
+    return (idx_t >= 0) & (idx_t < n)
+
+
+def indexer_scores_at(q_idx, k_idx, w, cu_seqlens, idx, groups: int = 1,
+                      score_scale: float = 1.0) -> np.ndarray:
+    """The indexer score of every selected slot, in fp64 (not rounded to fp32):
+    S[t, g, j] = score_scale * sum_{h in g} w[t,h] * max(q_I[t,h] . k_I[s0 + idx[t,g,j]], 0),
+    -inf at slots that are -1 or outside t's sequence.  idx: int [T, groups, k]."""
+    Q, K, W, I = as_f64(q_idx), as_f64(k_idx), as_f64(w), as_i64(idx)
+    T, H_I, _ = Q.shape
+    hg = H_I // groups
+    out = np.full(I.shape, -np.inf)
+    for t in range(T):
+        s0, n = seq_bounds(cu_seqlens, t)
+        for g in range(groups):
+            hs = slice(g * hg, (g + 1) * hg)
+            for j, s in enumerate(I[t, g]):
+                if 0 <= s < n:
+                    dots = Q[t, hs] @ K[s0 + s]                 # [hg]
+                    out[t, g, j] = score_scale * float(W[t, hs] @ np.maximum(dots, 0.0))
+    return out
+
+
+def mla_teacher(q, kv, idx, cu_seqlens, scale: float, rows: Optional[Iterable[int]] = None) -> np.ndarray:
+    """The indexer's teacher on the selected slots of each query row: the sparse
+    MLA attention probabilities exp(scale q[t,h] . kv[s] - lse[t,h]) averaged over
+    the heads.  0 at -1 slots; all 0 for a row without a valid slot.
+    Returns float64 [len(rows), topk]."""
+    Q, KV, I = as_f64(q), as_f64(kv), as_i64(idx)
+    T, H = Q.shape[0], Q.shape[1]
+    rr = range(T) if rows is None else list(rows)
+    out = np.zeros((len(rr), I.shape[1]))
+    for i, t in enumerate(rr):
+        s0, n = seq_bounds(cu_seqlens, t)
+        ok = _selected(I[t], n)
+        if not ok.any():
+            continue
+        S = scale * (Q[t] @ KV[s0 + I[t][ok]].T)           # [H, valid slots]
+        P = np.exp(S - S.max(axis=1, keepdims=True))
+        P /= P.sum(axis=1, keepdims=True)
+        out[i, ok] = P.mean(axis=0)
+    return out
+
+
+def sparse_kl(scores, teacher):
+    """KL(teacher || softmax(scores)) per row over the slots whose score is
+    finite, and its gradient with respect to the scores, softmax(scores) -
+    teacher (0 at the other slots).  A row without a finite score gives 0, 0.
+    scores, teacher: [R, k]; returns (loss float64 [R], grad float64 [R, k])."""
+    S, A = as_f64(scores), as_f64(teacher)
+    loss = np.zeros(S.shape[0])
+    grad = np.zeros_like(S)
+    for r in range(S.shape[0]):
+        ok = np.isfinite(S[r])
+        if not ok.any():
+            continue
+        z = S[r, ok]
+        log_p = z - z.max() - math.log(np.exp(z - z.max()).sum())
+        a = A[r, ok]
+        pos = a > 0
+        loss[r] = float((a[pos] * (np.log(a[pos]) - log_p[pos])).sum())
+        grad[r, ok] = np.exp(log_p) - a
+    return loss, grad
+
+
+def indexer_bwd(q_idx, k_idx, w, cu_seqlens, idx, dscore, groups: int = 1, score_scale: float = 1.0):
+    """Gradient of sum_{t,g,j} dscore[t,g,j] * I_g[t, s0 + idx[t,g,j]] (the indexer
+    score definition above, taken in fp64) with respect to q_I, k_I and w:
+      dw[t,h]   = score_scale * sum_j dscore * max(d, 0)
+      dq_I[t,h] = score_scale * sum_j dscore * w[t,h] * [d > 0] * k_I[s]
+      dk_I[s]   = score_scale * sum_{t,j} dscore * sum_h w[t,h] * [d > 0] * q_I[t,h]
+    with d = q_I[t,h] . k_I[s]; slots that are -1 or outside the sequence carry
+    no gradient.  Returns float64 (dq_I [T,H_I,d_I], dk_I [T,d_I], dw [T,H_I])."""
+    Q, K, W, I, G = as_f64(q_idx), as_f64(k_idx), as_f64(w), as_i64(idx), as_f64(dscore)
+    T, H_I, _ = Q.shape
+    hg = H_I // groups
+    dq, dk, dw = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(W)
+    for t in range(T):
+        s0, n = seq_bounds(cu_seqlens, t)
+        for g in range(groups):
+            hs = slice(g * hg, (g + 1) * hg)
+            for j, s in enumerate(I[t, g]):
+                if not (0 <= s < n) or G[t, g, j] == 0.0:
+                    continue
+                c = score_scale * G[t, g, j]
+                d = Q[t, hs] @ K[s0 + s]                       # [hg]
+                on = (d > 0).astype(np.float64)
+                dw[t, hs] += c * np.maximum(d, 0.0)
+                dq[t, hs] += c * (W[t, hs] * on)[:, None] * K[s0 + s][None, :]
+                dk[s0 + s] += c * ((W[t, hs] * on) @ Q[t, hs])
+    return dq, dk, dw
 
 
 # --------------------------------------------------------------------------

@@ -369,3 +369,174 @@ def test_synth_is_seeded():
     a = synth.mla_inputs(8, 2, 576, seed=1)
     b = synth.mla_inputs(8, 2, 576, seed=1)
     assert torch.equal(a["q"], b["q"]) and torch.equal(a["kv"], b["kv"])
+
+
+# ---------------------------------------------------------------- indexer training (sparse KL, indexer backward)
+
+def test_sparse_kl_closed_form():
+    # student softmax(0, ln 3) = (1/4, 3/4) against teacher (1/2, 1/2):
+    # KL = 1/2 ln(2) + 1/2 ln(2/3) = 1/2 ln(4/3); gradient p - a = (-1/4, 1/4)
+    loss, grad = O.sparse_kl([[0.0, math.log(3.0)]], [[0.5, 0.5]])
+    assert loss[0] == pytest.approx(0.5 * math.log(4.0 / 3.0), rel=1e-14)
+    np.testing.assert_allclose(grad[0], [-0.25, 0.25], atol=1e-15)
+    # a -inf slot (not a candidate) takes no part; a row without candidates gives 0
+    loss, grad = O.sparse_kl([[0.0, -np.inf, math.log(3.0)], [-np.inf] * 3], [[0.5, 0.0, 0.5], [0.0] * 3])
+    assert loss[0] == pytest.approx(0.5 * math.log(4.0 / 3.0), rel=1e-14) and loss[1] == 0.0
+    np.testing.assert_allclose(grad, [[-0.25, 0.0, 0.25], [0.0, 0.0, 0.0]], atol=1e-15)
+
+
+def test_sparse_kl_properties():
+    rng = np.random.default_rng(30)
+    S = rng.standard_normal((6, 9)) * 3
+    S[2, 4:] = -np.inf
+    A = rng.random((6, 9)) ** 3
+    A[~np.isfinite(S)] = 0.0
+    A /= A.sum(axis=1, keepdims=True)
+    loss, grad = O.sparse_kl(S, A)
+    assert np.all(loss >= 0)                                        # Gibbs' inequality
+    np.testing.assert_allclose(grad.sum(axis=1), 0.0, atol=1e-12)   # both sides are distributions
+    l2, g2 = O.sparse_kl(S + 7.25, A)                               # a softmax ignores a shift
+    np.testing.assert_allclose(l2, loss, rtol=1e-12)
+    np.testing.assert_allclose(g2, grad, atol=1e-13)
+    # a teacher equal to the student's own softmax costs nothing
+    P = np.zeros_like(S)
+    for r in range(S.shape[0]):
+        ok = np.isfinite(S[r])
+        P[r, ok] = sp_softmax(S[r, ok])
+    l0, g0 = O.sparse_kl(S, P)
+    np.testing.assert_allclose(l0, 0.0, atol=1e-12)
+    np.testing.assert_allclose(g0, 0.0, atol=1e-12)
+
+
+def test_sparse_kl_gradient_finite_differences():
+    rng = np.random.default_rng(31)
+    S = rng.standard_normal((3, 7))
+    S[1, 5:] = -np.inf
+    A = rng.random((3, 7))
+    A[~np.isfinite(S)] = 0.0
+    A /= A.sum(axis=1, keepdims=True)
+    _, grad = O.sparse_kl(S, A)
+    fin = np.isfinite(S)
+    x = np.where(fin, S, 0.0)
+
+    def loss():
+        return float(O.sparse_kl(np.where(fin, x, -np.inf), A)[0].sum())
+
+    _fd_check(loss, x, np.where(fin, grad, 0.0), n_probe=21)
+
+
+def test_mla_teacher_single_head_is_the_attention_row():
+    # H = 1: the teacher is the attention probability exp(scale q.k - lse), with lse
+    # from the dense-masked forward definition
+    cu = [0, 6, 11]
+    q, kv, _ = _mla(11, 1, 576, 32)
+    idx = synth.random_topk_indices(cu, 4, seed=6, invalid_rows=[7]).numpy()
+    scale = 0.06
+    _, lse = O.sparse_mla_fwd_dense(q, kv, idx, cu, scale)
+    a = O.mla_teacher(q, kv, idx, cu, scale)
+    for t in range(11):
+        s0, n = O.seq_bounds(cu, t)
+        for j, s in enumerate(idx[t]):
+            want = 0.0 if s < 0 else math.exp(scale * float(q[t, 0] @ kv[s0 + s]) - lse[t, 0])
+            assert a[t, j] == pytest.approx(want, rel=1e-12, abs=1e-300)
+    assert np.all(a[7] == 0)
+    valid = (idx >= 0).any(axis=1)
+    np.testing.assert_allclose(a[valid].sum(axis=1), 1.0, rtol=1e-12)
+
+
+def test_mla_teacher_two_heads_closed_form():
+    # head 0 has q = 0 (uniform over the two slots); head 1 puts sigma(delta) on the
+    # second slot with delta = scale q1 . (k1 - k0); the teacher is their average
+    rng = np.random.default_rng(33)
+    kv = rng.standard_normal((3, 576))
+    q = np.zeros((3, 2, 576))
+    q[2, 1] = rng.standard_normal(576) * 0.1
+    idx = np.array([[0, -1], [1, 0], [0, 1]])
+    scale = 0.3
+    a = O.mla_teacher(q, kv, idx, [0, 3], scale, rows=[2])
+    delta = scale * float(q[2, 1] @ (kv[1] - kv[0]))
+    p1 = 1.0 / (1.0 + math.exp(-delta))
+    np.testing.assert_allclose(a[0], [0.5 * (0.5 + 1 - p1), 0.5 * (0.5 + p1)], rtol=1e-12)
+    np.testing.assert_allclose(O.mla_teacher(q, kv, idx, [0, 3], scale, rows=[0])[0], [1.0, 0.0])
+
+
+def _indexer_case(seed, T_cu=(0, 5, 9), H_I=4, d_I=6, groups=2, k=3):
+    cu = list(T_cu)
+    rng = np.random.default_rng(seed)
+    T = cu[-1]
+    qI = rng.standard_normal((T, H_I, d_I))
+    kI = rng.standard_normal((T, d_I))
+    w = rng.random((T, H_I)) + 0.1
+    idx = np.stack([synth.random_topk_indices(cu, k, seed=seed + g).numpy() for g in range(groups)], axis=1)
+    return cu, qI, kI, w, idx
+
+
+def test_indexer_scores_at_gathers_the_token_scores():
+    cu, qI, kI, w, idx = _indexer_case(34)
+    S = O.indexer_scores_at(qI, kI, w, cu, idx, groups=2, score_scale=0.5)
+    full = O.indexer_token_scores(qI, kI, w, cu, range(cu[-1]), groups=2, score_scale=0.5)
+    for t in range(cu[-1]):
+        for g in range(2):
+            for j, s in enumerate(idx[t, g]):
+                if s < 0:
+                    assert S[t, g, j] == -np.inf
+                else:   # the token scores are the same values rounded once to fp32
+                    assert np.float32(S[t, g, j]) == full[t, g, s] or (S[t, g, j] == 0 and full[t, g, s] == 0)
+
+
+def test_indexer_bwd_one_pair_closed_form():
+    q = np.array([[[1.0, 2.0]]])
+    k = np.array([[0.5, 0.25]])        # q . k = 1 > 0
+    w = np.array([[3.0]])
+    idx = np.array([[[0]]])
+    dq, dk, dw = O.indexer_bwd(q, k, w, [0, 1], idx, np.array([[[2.0]]]), score_scale=0.5)
+    c = 0.5 * 2.0
+    np.testing.assert_allclose(dw, [[c * 1.0]])
+    np.testing.assert_allclose(dq, [[[c * 3.0 * 0.5, c * 3.0 * 0.25]]])
+    np.testing.assert_allclose(dk, [[c * 3.0 * 1.0, c * 3.0 * 2.0]])
+    # a negative dot is cut by the ReLU: no gradient anywhere
+    dq, dk, dw = O.indexer_bwd(-q, k, w, [0, 1], idx, np.array([[[2.0]]]), score_scale=0.5)
+    assert not dq.any() and not dk.any() and not dw.any()
+
+
+def test_indexer_bwd_finite_differences():
+    cu, qI, kI, w, idx = _indexer_case(35)
+    rng = np.random.default_rng(36)
+    G = rng.standard_normal(idx.shape)
+    valid = idx >= 0
+    # away from the ReLU kink, so that central differences see one branch
+    for t in range(cu[-1]):
+        s0, _ = O.seq_bounds(cu, t)
+        for g in range(2):
+            for s in idx[t, g][idx[t, g] >= 0]:
+                assert np.all(np.abs(qI[t, 2 * g:2 * g + 2] @ kI[s0 + s]) > 1e-4)
+
+    def loss():
+        S = O.indexer_scores_at(qI, kI, w, cu, idx, groups=2, score_scale=0.7)
+        return float((G * np.where(valid, S, 0.0)).sum())
+
+    dq, dk, dw = O.indexer_bwd(qI, kI, w, cu, idx, G, groups=2, score_scale=0.7)
+    _fd_check(loss, qI, dq, seed=3)
+    _fd_check(loss, kI, dk, seed=4)
+    _fd_check(loss, w, dw, seed=5)
+
+
+def test_indexer_kl_chain_finite_differences():
+    """The sparse KL of the indexer against a fixed teacher, differentiated
+    through the indexer backward, matches central differences of the loss."""
+    cu, qI, kI, w, idx = _indexer_case(37, groups=1, k=4)
+    rng = np.random.default_rng(38)
+    A = rng.random(idx.shape)
+    A[idx < 0] = 0.0
+    A /= np.maximum(A.sum(axis=2, keepdims=True), 1e-300)
+
+    def loss():
+        S = O.indexer_scores_at(qI, kI, w, cu, idx, groups=1, score_scale=0.4)
+        return float(O.sparse_kl(S[:, 0], A[:, 0])[0].sum())
+
+    S = O.indexer_scores_at(qI, kI, w, cu, idx, groups=1, score_scale=0.4)
+    _, gS = O.sparse_kl(S[:, 0], A[:, 0])
+    dq, dk, dw = O.indexer_bwd(qI, kI, w, cu, idx, gS[:, None, :], groups=1, score_scale=0.4)
+    _fd_check(loss, qI, dq, seed=6)
+    _fd_check(loss, kI, dk, seed=7)
+    _fd_check(loss, w, dw, seed=8)
