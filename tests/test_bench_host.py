@@ -27,3 +27,25 @@ def test_step_flops_match_closed_forms():
 def test_job_rate_is_ranks_times_work_over_slowest_time():
     assert bench.job_tflops(1, 1e12, 1000.0) == 1.0
     assert bench.job_tflops(8, 2e12, 500.0) == 32.0
+
+
+def test_reference_arm_prints_one_contract_line():
+    """`bench.py --impl reference` (the CPU oracle on a bounded row sample of the
+    same workload) prints one JSON line with the GPU arm's metric and unit."""
+    import json
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0", "--ref-rows", "2"], capture_output=True, text=True, timeout=600,
+                       env={**os.environ, "RANK": "0", "WORLD_SIZE": "1"})
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference"
+    assert line["metric"] == bench.METRIC
+    assert line["unit"] == "TFLOP/s" and line["higher_is_better"] is True and line["value"] > 0
+    assert line["config"]["workload"] == bench.WORKLOAD
+    cpu = line["cpu_baseline"]
+    assert cpu["kind"] == "oracle" and cpu["value"] == line["value"] and cpu["cores"] >= 1
+    e2e = line["e2e"]
+    assert e2e["value"] == line["value"] and e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
