@@ -421,7 +421,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           ok = false;
           break;
         }
-        tc::fence_proxy_async_smem();  // the gathered rows were written through the generic proxy
+        tc::fence_proxy_async_smem();  // kept from the cp.async version: the rows now arrive by TMA (async proxy) and need no proxy fence
         tc::fence_after_sync();
         const uint32_t sa = base + st * DQ_STAGE, sb = sa + DQ_A;
 #pragma unroll

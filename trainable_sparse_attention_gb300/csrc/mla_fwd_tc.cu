@@ -230,7 +230,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
           ok = false;
           break;
         }
-        tc::fence_proxy_async_smem();  // the gathered tile was written through the generic proxy
+        tc::fence_proxy_async_smem();  // kept from the cp.async version: the rows now arrive by TMA (async proxy) and need no proxy fence
         tc::fence_after_sync();
         const uint32_t d = tmem + MT_SCOL + b * MT_N;
         for (int c = 0; c < kb; ++c) {
