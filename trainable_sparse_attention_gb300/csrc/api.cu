@@ -51,14 +51,14 @@ int cuda_status(cudaError_t e, const char* where) {
     if (_e != cudaSuccess) return cuda_status(_e, where); \
   } while (0)
 
-// Kernels launched by this library since load (every launch_* starts one kernel).
+// Kernels launched by this library since load (counted at every launch site).
 std::atomic<unsigned long long> g_launches{0};
 
+// A launcher call; its kernels count themselves (note_launch at each launch site).
 #define TSA_LAUNCH(expr, where)                \
   do {                                         \
     cudaError_t _e = (expr);                   \
     if (_e != cudaSuccess) return cuda_status(_e, where); \
-    g_launches.fetch_add(1, std::memory_order_relaxed); \
   } while (0)
 
 // Validate cu_seqlens and fill the kernel-side table.
@@ -117,8 +117,8 @@ int64_t chunk_rows(int max_len, int groups, int block_size) {
 }  // namespace
 
 namespace tsa {
-// For entry points defined in other translation units: record a detail
-// message for tsa_last_error() and account for a kernel launch.
+// Record a detail message for tsa_last_error() (entry points of other
+// translation units), and account for a kernel launch (every launch site).
 int note_error(int code, const char* msg) {
   g_last_error = msg;
   return code;

@@ -206,6 +206,7 @@ static cudaError_t launch_gqa_t(const GqaArgs& a, cudaStream_t stream) {
                                        (int)smem);
   if (e != cudaSuccess) return e;
   gqa_fwd_mma_kernel<BS, DH, NST><<<grid, 128, smem, stream>>>(a);
+  note_launch();
   return cudaGetLastError();
 }
 

@@ -320,6 +320,7 @@ static cudaError_t launch_kv_t(const GqaKvArgs& a, int64_t grid, cudaStream_t st
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   gqa_bwd_kv_kernel<BS, DH><<<static_cast<unsigned>(grid), GK_THREADS, smem, stream>>>(a);
+  note_launch();
   return cudaGetLastError();
 }
 
@@ -331,10 +332,13 @@ cudaError_t launch_gqa_bwd_kv(const GqaKvArgs& a, int d, cudaStream_t stream) {
   const unsigned ig = static_cast<unsigned>(std::min<int64_t>((entries + 255) / 256, 4096));
   if ((e = cudaMemsetAsync(a.cnt, 0, sizeof(int) * nB, stream)) != cudaSuccess) return e;
   gqa_inv_kernel<false><<<ig, 256, 0, stream>>>(a);
+  note_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   gqa_inv_scan_kernel<<<1, 1024, 0, stream>>>(a, nB);
+  note_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   gqa_inv_kernel<true><<<ig, 256, 0, stream>>>(a);
+  note_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // chunks: at most one partial chunk per list plus entries / GK_CHUNK full ones
   const int64_t grid = nB + (entries + GK_CHUNK - 1) / GK_CHUNK;

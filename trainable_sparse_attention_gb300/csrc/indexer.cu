@@ -195,6 +195,7 @@ cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t stream) {
   int ktiles = p_last / IX_KTILE + 1;
   dim3 grid((ktiles + IX_KT_PER_CTA - 1) / IX_KT_PER_CTA, (a.nq + QB - 1) / QB);
   indexer_mma_kernel<<<grid, IX_THREADS, smem, stream>>>(a);
+  note_launch();
   return cudaGetLastError();
 }
 
@@ -208,6 +209,7 @@ cudaError_t launch_fill(float* p, int64_t n, float v, cudaStream_t stream) {
   int64_t blocks = (n + 255) / 256;
   if (blocks > 152 * 32) blocks = 152 * 32;
   fill_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p, n, v);
+  note_launch();
   return cudaGetLastError();
 }
 

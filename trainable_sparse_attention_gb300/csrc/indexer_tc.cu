@@ -403,6 +403,7 @@ static cudaError_t launch_tc_t(const IndexerArgs& a, cudaStream_t stream) {
   }
   const int grid = static_cast<int>(std::min<int64_t>(total, sms));
   indexer_tc_kernel<DI, HG><<<grid, IT_THREADS, smem, stream>>>(tq, tk, a, static_cast<int>(total));
+  note_launch();
   return cudaGetLastError();
 }
 

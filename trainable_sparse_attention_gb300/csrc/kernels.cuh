@@ -126,6 +126,9 @@ cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t stream);
 // tcgen05 indexer (token-level scores); launch_indexer routes to it when it applies.
 bool indexer_tc_supported(int H_I, int d_I, int groups, int bs);
 cudaError_t launch_indexer_tc(const IndexerArgs& a, cudaStream_t stream);
+// Account for one kernel launch of this library (the count tsa_kernel_launches reports);
+// every launch site calls it right after its <<<...>>> statement.
+void note_launch();
 cudaError_t launch_fill(float* p, int64_t n, float v, cudaStream_t stream);
 cudaError_t launch_bounded_wait_selftest(unsigned int* flags, cudaStream_t stream);
 cudaError_t launch_mla_fwd(const MlaFwdArgs& a, int D, cudaStream_t stream);

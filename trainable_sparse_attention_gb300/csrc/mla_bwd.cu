@@ -270,6 +270,7 @@ static cudaError_t launch_bwd_main(const MlaBwdArgs& a, cudaStream_t stream) {
   cudaFuncSetAttribute(mla_bwd_mma_kernel<D, MW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   dim3 grid(a.T, (a.H + 16 * MW - 1) / (16 * MW));
   mla_bwd_mma_kernel<D, MW><<<grid, 128 * MW, smem, stream>>>(a);
+  note_launch();
   return cudaGetLastError();
 }
 
@@ -278,6 +279,7 @@ cudaError_t launch_bwd_delta(const __nv_bfloat16* o, const __nv_bfloat16* dout, 
   if (rows <= 0) return cudaSuccess;
   int64_t blocks = (rows + 7) / 8;
   bwd_delta_kernel<<<(unsigned)blocks, 256, 0, stream>>>(o, dout, dlt, rows, dv);
+  note_launch();
   return cudaGetLastError();
 }
 
@@ -287,6 +289,7 @@ cudaError_t launch_f32_to_bf16(const float* src, __nv_bfloat16* dst, int64_t n, 
   if (blocks > 152 * 16) blocks = 152 * 16;
   if (blocks < 1) blocks = 1;
   f32_to_bf16_kernel<<<(unsigned)blocks, 256, 0, stream>>>(src, dst, n);
+  note_launch();
   return cudaGetLastError();
 }
 

@@ -541,6 +541,7 @@ static cudaError_t launch_sp_t(const MlaBwdArgs& a, int nq, cudaStream_t stream)
   e = cudaFuncSetAttribute(mla_bwd_sp_tc_kernel<D, DS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   mla_bwd_sp_tc_kernel<D, DS><<<dim3(nq), SP_THREADS, smem, stream>>>(tp, a);
+  note_launch();
   return cudaGetLastError();
 }
 
@@ -556,6 +557,7 @@ static cudaError_t launch_dq_t(const MlaBwdArgs& a, int nq, cudaStream_t stream)
       cudaSuccess)
     return e;
   mla_bwd_dq_tc_kernel<D><<<dim3(2 * nq), DQ_THREADS, DQ_SMEM, stream>>>(tds, tkv, a);
+  note_launch();
   return cudaGetLastError();
 }
 

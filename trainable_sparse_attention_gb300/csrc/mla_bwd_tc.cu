@@ -252,6 +252,7 @@ cudaError_t launch_mla_bwd_dkv_tc(const MlaBwdTcArgs& a, int nq, cudaStream_t st
     return e;
   const int nblk = (a.D + 127) / 128;
   mla_bwd_dkv_tc_kernel<<<dim3(nq * nblk), DK_THREADS, DK_SMEM, stream>>>(tds, tp, tq, tdo, a);
+  note_launch();
   return cudaGetLastError();
 }
 

@@ -195,10 +195,12 @@ cudaError_t launch_mla_fwd(const MlaFwdArgs& a, int D, cudaStream_t stream) {
     size_t smem = mla_fwd_smem<576>();
     cudaFuncSetAttribute(mla_fwd_mma_kernel<576>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     mla_fwd_mma_kernel<576><<<grid, MF_THREADS, smem, stream>>>(a);
+    note_launch();
   } else {
     size_t smem = mla_fwd_smem<512>();
     cudaFuncSetAttribute(mla_fwd_mma_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     mla_fwd_mma_kernel<512><<<grid, MF_THREADS, smem, stream>>>(a);
+    note_launch();
   }
   return cudaGetLastError();
 }

@@ -500,6 +500,7 @@ static cudaError_t launch_tc_t(const MlaFwdArgs& a, cudaStream_t stream) {
   e = cudaFuncSetAttribute(mla_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   mla_fwd_tc_kernel<D><<<dim3(2 * a.T), MT_THREADS, smem, stream>>>(tm_kv, a);
+  note_launch();
   return cudaGetLastError();
 }
 

@@ -128,7 +128,6 @@ extern "C" int qsa_topk_no_alloc(const void* q_idx, const void* k_idx, const flo
       a.T_total = cu_seqlens[num_seqs];
       cudaError_t e = launch_indexer(a, s);
       if (e != cudaSuccess) return note_error(TSA_ERR_CUDA, cudaGetErrorString(e));
-      note_launch();
       TopkRows r;
       r.scores = static_cast<const float*>(scratch); r.ld = width; r.width = width;
       r.mode = block_size == 1 ? 1 : 2;
@@ -138,7 +137,6 @@ extern "C" int qsa_topk_no_alloc(const void* q_idx, const void* k_idx, const flo
       r.k = topk;
       e = launch_topk_rows(r, static_cast<int64_t>(nq) * groups, s);
       if (e != cudaSuccess) return note_error(TSA_ERR_CUDA, cudaGetErrorString(e));
-      note_launch();
     }
   }
   return TSA_OK;

@@ -31,6 +31,7 @@ __global__ void __launch_bounds__(32, 1) bounded_wait_selftest_kernel(unsigned i
 cudaError_t launch_bounded_wait_selftest(unsigned int* flags, cudaStream_t stream) {
   if (flags == nullptr) return cudaErrorInvalidValue;
   bounded_wait_selftest_kernel<<<1, 32, 0, stream>>>(flags);
+  note_launch();
   return cudaGetLastError();
 }
 

@@ -594,6 +594,7 @@ cudaError_t launch_topk_rows(const TopkRows& a, int64_t rows, cudaStream_t strea
   cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TK_SMEM);
   if (e != cudaSuccess) return e;
   topk_rows_kernel<<<static_cast<unsigned>(rows), TK_THREADS, TK_SMEM, stream>>>(a);
+  note_launch();
   return cudaGetLastError();
 }
 
