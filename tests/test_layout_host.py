@@ -44,3 +44,19 @@ def test_no_committed_file_reads_the_working_folder():
     for f in _tracked((".py", ".cu", ".cuh", ".h", ".sh")):
         src = open(os.path.join(ROOT, f), encoding="utf-8").read()
         assert marker not in src, f
+
+
+def test_every_kernel_launch_is_counted():
+    """Each <<<...>>> statement of the library is followed by note_launch(), so the
+    launch count (tsa_kernel_launches, the bench's gpu_launches) is exact."""
+    csrc = os.path.join(PKG, "csrc")
+    sites = 0
+    for f in sorted(os.listdir(csrc)):
+        if not f.endswith(".cu"):
+            continue
+        lines = open(os.path.join(csrc, f), encoding="utf-8").read().split("\n")
+        for i, ln in enumerate(lines):
+            if "<<<" in ln and not ln.lstrip().startswith("//"):
+                sites += 1
+                assert lines[i + 1].strip() == "note_launch();", f"{f}:{i + 1} launch not counted"
+    assert sites >= 19
