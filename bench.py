@@ -3,15 +3,19 @@
 Workload: long-context absorbed sparse MLA, one sequence of T = 65536 tokens,
 H = 128 heads, q/kv bf16 with 576 channels (values = first 512), top-2048,
 softmax scale 1/sqrt(192); streaming indexer with 64 heads, d_I = 128,
-w ~ U(0,1).  One step = the whole path over one batch:
+w ~ U(0,1).  One step = the whole trainable path over one batch:
 
     qsa_topk (indexer score + exact top-k, streamed)  ->  sparse_mla_fwd
-    ->  sparse_mla_bwd (Dlt preprocess, dQ/dKV, dKV conversion)
+    ->  sparse_mla_bwd (Dlt preprocess, dQ/dKV, dKV conversion, and the
+        indexer's teacher: the head mean of P at the selected slots)
+    ->  qsa_indexer_kl (student scores at the slots, KL loss, dI = p - a)
+    ->  qsa_indexer_bwd (dq_I, dk_I, dw)
 
-value = algorithmic TFLOP/s of the step (indexer GEMM + attention fwd + bwd,
-counted from the actual indices) with inputs resident in HBM; per-stage times,
-indexer queries/s and roofline fractions are reported alongside.  Inputs
-(~20 GB) exceed the 129 MB L2, so no flush is needed between steps.
+value = algorithmic TFLOP/s of the step (indexer GEMM, attention fwd + bwd,
+the indexer's KL and backward GEMMs over the selected slots, all counted from
+the actual indices) with inputs resident in HBM; per-stage times, indexer
+queries/s and roofline fractions are reported alongside.  Inputs (~20 GB)
+exceed the 129 MB L2, so no flush is needed between steps.
 
 `secondary.qsa_gqa` times the block Sparse-GQA workload on its own after the
 main step (packed THD of four sequences 4096/8192/12288/8192, Hq = 32,
@@ -75,11 +79,15 @@ def load_peaks():
 
 def flops_of(valid_per_row_total: int, causal_pairs: int):
     """Algorithmic FLOPs: indexer GEMM over causal pairs; attention per valid
-    (query, key) pair and head: fwd 2*(576+512), bwd 2*(3*576+2*512)."""
+    (query, key) pair and head: fwd 2*(576+512), bwd 2*(3*576+2*512); the
+    indexer's training per valid pair and indexer head: KL 2*d_I (the student
+    scores), backward 3*2*d_I (the scores again, dq_I, dk_I)."""
     f_idx = causal_pairs * H_I * D_I * 2
     f_fwd = valid_per_row_total * H * 2 * (D + DV)
     f_bwd = valid_per_row_total * H * 2 * (3 * D + 2 * DV)
-    return f_idx, f_fwd, f_bwd
+    f_kl = valid_per_row_total * H_I * D_I * 2
+    f_ibwd = valid_per_row_total * H_I * D_I * 2 * 3
+    return f_idx, f_fwd, f_bwd, f_kl, f_ibwd
 
 
 class ClockSampler:
@@ -216,6 +224,12 @@ def oracle_sample(n_rows: int, seed: int = 123):
     I = Rows(torch.from_numpy(idx_rows), (T_TOK, TOPK))
     O.sparse_mla_fwd(Q, kv, I, cu, SCALE, rows=rows)
     O.sparse_mla_bwd(Q, kv, I, cu, SCALE, dO, rows=rows)
+    tea = O.mla_teacher(Q, kv, I, cu, SCALE, rows=rows)
+    I3 = Rows(torch.from_numpy(idx_rows[:, None, :]), (T_TOK, 1, TOPK))
+    sc_sel = O.indexer_scores_at(qI, k_idx, W, cu, I3, rows=rows)[:, 0, :]
+    _, dI = O.sparse_kl(sc_sel, tea)
+    G3 = Rows(torch.from_numpy(dI[:, None, :]), (T_TOK, 1, TOPK))
+    O.indexer_bwd(qI, k_idx, W, cu, I3, G3, rows=rows)
     dt = time.perf_counter() - t0
     valid = int((idx_rows >= 0).sum())
     pairs = sum(t + 1 for t in rows)
@@ -246,7 +260,7 @@ def run_reference(args):
                    "sample_rows_per_step": n_rows},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": f"{n_rows} random query rows of the T=65536 workload per step "
-                                   "(indexer+top-k, fwd, bwd), numpy fp64"},
+                                   "(indexer+top-k, fwd, bwd, teacher, indexer KL and backward), numpy fp64"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -281,34 +295,45 @@ def run_gpu(args):
     lse = torch.empty((T_TOK, H), dtype=torch.float32, device=dev)
     dq = torch.empty_like(q)
     dkv = torch.empty_like(kv)
+    teacher = torch.empty((T_TOK, TOPK), dtype=torch.float32, device=dev)
+    loss = torch.empty((T_TOK,), dtype=torch.float32, device=dev)
+    dscore = torch.empty((T_TOK, TOPK), dtype=torch.float32, device=dev)
+    dq_i, dk_i, dw = torch.empty_like(q_i), torch.empty_like(k_i), torch.empty_like(w)
+    ws_ibwd = torch.empty(tsa.qsa_indexer_bwd_workspace_size(T_TOK, D_I), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def step(ev=None):
+        i2 = idx.view(T_TOK, TOPK)
         if ev:
             ev[0].record(stream)
         tsa.qsa_topk(q_i, k_i, w, cu, TOPK, workspace=ws_topk, out=idx)
         if ev:
             ev[1].record(stream)
-        tsa.sparse_mla_fwd(q, kv, idx.view(T_TOK, TOPK), cu, SCALE, out=out, lse=lse)
+        tsa.sparse_mla_fwd(q, kv, i2, cu, SCALE, out=out, lse=lse)
         if ev:
             ev[2].record(stream)
-        tsa.sparse_mla_bwd(q, kv, idx.view(T_TOK, TOPK), out, lse, dout, cu, SCALE, workspace=ws_bwd,
-                           dq=dq, dkv=dkv)
+        tsa.sparse_mla_bwd(q, kv, i2, out, lse, dout, cu, SCALE, workspace=ws_bwd, dq=dq, dkv=dkv, teacher=teacher)
         if ev:
             ev[3].record(stream)
+        tsa.qsa_indexer_kl(q_i, k_i, w, cu, i2, teacher, loss=loss, dscore=dscore)
+        if ev:
+            ev[4].record(stream)
+        tsa.qsa_indexer_bwd(q_i, k_i, w, cu, i2, dscore, workspace=ws_ibwd, dq=dq_i, dk=dk_i, dw=dw)
+        if ev:
+            ev[5].record(stream)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     valid = int((idx >= 0).sum().item())
     pairs = T_TOK * (T_TOK + 1) // 2
-    f_idx, f_fwd, f_bwd = flops_of(valid, pairs)
-    f_step = f_idx + f_fwd + f_bwd
+    f_idx, f_fwd, f_bwd, f_kl, f_ibwd = flops_of(valid, pairs)
+    f_step = f_idx + f_fwd + f_bwd + f_kl + f_ibwd
 
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
     launches0 = tsa.kernel_launches()
     barrier(world)
     torch.cuda.synchronize()
@@ -328,6 +353,8 @@ def run_gpu(args):
     st_idx = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
     st_fwd = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
     st_bwd = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps
+    st_kl = sum(e[3].elapsed_time(e[4]) for e in evs) / args.steps
+    st_ibwd = sum(e[4].elapsed_time(e[5]) for e in evs) / args.steps
     value = job_tflops(world, f_step, ms_step)
     psus = peaks["bf16_tflops_sustained"]
     stages = {
@@ -337,7 +364,13 @@ def run_gpu(args):
         "mla_fwd": {"ms": st_fwd, "tflops": f_fwd / (st_fwd * 1e-3) / 1e12,
                     "frac_of_measured_bf16_sustained": f_fwd / (st_fwd * 1e-3) / 1e12 / psus},
         "mla_bwd": {"ms": st_bwd, "tflops": f_bwd / (st_bwd * 1e-3) / 1e12,
-                    "frac_of_measured_bf16_sustained": f_bwd / (st_bwd * 1e-3) / 1e12 / psus},
+                    "frac_of_measured_bf16_sustained": f_bwd / (st_bwd * 1e-3) / 1e12 / psus,
+                    "note": "includes the indexer teacher (head mean of the staged P)"},
+        "indexer_kl": {"ms": st_kl, "tflops": f_kl / (st_kl * 1e-3) / 1e12,
+                       "frac_of_measured_bf16_sustained": f_kl / (st_kl * 1e-3) / 1e12 / psus},
+        "indexer_bwd": {"ms": st_ibwd, "tflops": f_ibwd / (st_ibwd * 1e-3) / 1e12,
+                        "frac_of_measured_bf16_sustained": f_ibwd / (st_ibwd * 1e-3) / 1e12 / psus,
+                        "dk_reduction_gbs": valid * D_I * 4 / (st_ibwd * 1e-3) / 1e9},
     }
     # Roofline of the dominant kernel: the forward is one launch (mla_fwd_tc_kernel)
     # whose stage events bracket exactly that launch, and it is the longest single
@@ -380,7 +413,8 @@ def run_gpu(args):
             "e2e": e2e,
             "gpu_launches": int(launches),
             "clocks": clk,
-            "flops_per_step": {"indexer": f_idx, "fwd": f_fwd, "bwd": f_bwd, "valid_pairs": valid},
+            "flops_per_step": {"indexer": f_idx, "fwd": f_fwd, "bwd": f_bwd, "indexer_kl": f_kl,
+                               "indexer_bwd": f_ibwd, "valid_pairs": valid},
             "secondary": {"qsa_gqa": gqa},
         }
         print(json.dumps(line), flush=True)
@@ -410,6 +444,10 @@ def run_gqa(args, tsa, dev, world):
     x = synth.indexer_inputs(T, GQA_HI, GQA_DI, seed=6, device=dev)
     scale = 1.0 / math.sqrt(GQA_D)
     ws = torch.empty(max(1, tsa.qsa_topk_workspace_size(cu, GQA_HKV, GQA_BS)), dtype=torch.uint8, device=dev)
+    ws_f = torch.empty(tsa.sparse_gqa_fwd_workspace_size(T, GQA_HQ, GQA_HKV, GQA_D, GQA_NSEL), dtype=torch.uint8,
+                       device=dev)
+    ws_b = torch.empty(tsa.sparse_gqa_bwd_workspace_size(T, GQA_HQ, GQA_HKV, GQA_D, GQA_NSEL), dtype=torch.uint8,
+                       device=dev)
     blk = torch.empty((T, GQA_HKV, GQA_NSEL), dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -420,10 +458,10 @@ def run_gqa(args, tsa, dev, world):
                      workspace=ws, out=blk)
         if ev:
             ev[1].record(stream)
-        out, lse = tsa.sparse_gqa_fwd(g["q"], g["k"], g["v"], blk, cu, GQA_BS, scale)
+        out, lse = tsa.sparse_gqa_fwd(g["q"], g["k"], g["v"], blk, cu, GQA_BS, scale, workspace=ws_f)
         if ev:
             ev[2].record(stream)
-        tsa.sparse_gqa_bwd(g["q"], g["k"], g["v"], blk, out, lse, g["dout"], cu, GQA_BS, scale)
+        tsa.sparse_gqa_bwd(g["q"], g["k"], g["v"], blk, out, lse, g["dout"], cu, GQA_BS, scale, workspace=ws_b)
         if ev:
             ev[3].record(stream)
 
@@ -450,7 +488,7 @@ def run_gqa(args, tsa, dev, world):
     torch.cuda.synchronize()
     ms = [sum(e[k].elapsed_time(e[k + 1]) for e in evs) / steps for k in range(3)]
     ms = [allmax(v, world) for v in ms]
-    del g, x, ws, blk
+    del g, x, ws, ws_f, ws_b, blk
     torch.cuda.empty_cache()
     return {
         "workload": "qsa_gqa_thd32768_hq32_hkv4_bs64_top32",
@@ -505,7 +543,9 @@ def run_e2e(args, tsa, dev, cu, dev_inputs, f_step, world):
         host_in[k].copy_(v)
     outs_shape = {"idx": ((T_TOK, 1, TOPK), torch.int32), "out": ((T_TOK, H, DV), torch.bfloat16),
                   "lse": ((T_TOK, H), torch.float32), "dq": ((T_TOK, H, D), torch.bfloat16),
-                  "dkv": ((T_TOK, D), torch.bfloat16)}
+                  "dkv": ((T_TOK, D), torch.bfloat16), "loss": ((T_TOK,), torch.float32),
+                  "dq_i": ((T_TOK, H_I, D_I), torch.bfloat16), "dk_i": ((T_TOK, D_I), torch.bfloat16),
+                  "dw": ((T_TOK, H_I), torch.float32)}
     host_out = [{k: torch.empty(s, dtype=d, pin_memory=True) for k, (s, d) in outs_shape.items()} for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
@@ -514,6 +554,7 @@ def run_e2e(args, tsa, dev, cu, dev_inputs, f_step, world):
     s_out = torch.cuda.Stream()
     ws_topk = torch.empty(tsa.qsa_topk_workspace_size(cu), dtype=torch.uint8, device=dev)
     ws_bwd = torch.empty(tsa.sparse_mla_bwd_workspace_size(T_TOK, H, D, TOPK), dtype=torch.uint8, device=dev)
+    ws_ibwd = torch.empty(tsa.qsa_indexer_bwd_workspace_size(T_TOK, D_I), dtype=torch.uint8, device=dev)
     d_in = [dict(dev_inputs), {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}]
 
     def copy_in(i, after):
@@ -533,10 +574,14 @@ def run_e2e(args, tsa, dev, cu, dev_inputs, f_step, world):
         idx = tsa.qsa_topk(x["q_idx"], x["k_idx"], x["w"], cu, TOPK, workspace=ws_topk)
         i2 = idx.view(T_TOK, TOPK)
         out, lse = tsa.sparse_mla_fwd(x["q"], x["kv"], i2, cu, SCALE)
-        dq, dkv = tsa.sparse_mla_bwd(x["q"], x["kv"], i2, out, lse, x["dout"], cu, SCALE, workspace=ws_bwd)
+        dq, dkv, tea = tsa.sparse_mla_bwd(x["q"], x["kv"], i2, out, lse, x["dout"], cu, SCALE, workspace=ws_bwd,
+                                          want_teacher=True)
+        loss, dscore = tsa.qsa_indexer_kl(x["q_idx"], x["k_idx"], x["w"], cu, i2, tea)
+        dq_i, dk_i, dw = tsa.qsa_indexer_bwd(x["q_idx"], x["k_idx"], x["w"], cu, i2, dscore, workspace=ws_ibwd)
         done = torch.cuda.Event()
         done.record(comp)
-        return {"idx": idx, "out": out, "lse": lse, "dq": dq, "dkv": dkv}, done
+        return {"idx": idx, "out": out, "lse": lse, "dq": dq, "dkv": dkv, "loss": loss, "dq_i": dq_i,
+                "dk_i": dk_i, "dw": dw}, done
 
     def copy_out(i, res, done):
         with torch.cuda.stream(s_out):
@@ -586,7 +631,7 @@ def main():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--ref-rows", type=int, default=384, help="oracle rows per CPU sample")
+    ap.add_argument("--ref-rows", type=int, default=48, help="oracle rows per CPU sample")
     ap.add_argument("--T", type=int, default=T_TOK, help="sequence length (smaller only for profiling captures)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -188,6 +188,13 @@ int sparse_mla_fwd(const void* q_dev, const void* kv_dev, const int32_t* indices
  *   dS = P*(dP - Dlt); dq = scale*dS.K;
  *   dkv[idx] += scale*dS^T.q (+ P^T.dO on the first 512 channels).
  *   dq_dev bf16 [T, H, d_qk], dkv_dev bf16 [T, d_qk] (fully overwritten).
+ *   teacher_dev: optional (NULL to skip) fp32 [T, topk], fully overwritten
+ *   with the indexer's KL teacher [QSA "Describe the solution": sparse
+ *   Stage-2 teacher]: the head mean (1/H) sum_h P[t,h,j] of the attention
+ *   probabilities at every slot j (0 at -1 slots), from the P this backward
+ *   recomputes anyway (bf16, as the dKV product uses it).  For H = 128 it is
+ *   bit-identical across runs; for H < 128 the head blocks add their shares
+ *   with fp32 atomics (order not fixed).
  *   workspace: sparse_mla_bwd_workspace_size(T, H, d_qk, topk) bytes: fp32
  *   dkv and Dlt, and for H = 128 a bf16 staging area for P and dS of one
  *   chunk of queries (at most 4 GiB; the chunk shrinks as topk grows).
@@ -200,8 +207,50 @@ size_t sparse_mla_bwd_workspace_size(int64_t T, int H, int d_qk, int topk);
 int sparse_mla_bwd(const void* q_dev, const void* kv_dev, const int32_t* indices_dev,
                    const void* out_dev, const float* lse_dev, const void* dout_dev,
                    const int32_t* cu_seqlens, int num_seqs, int H, int d_qk, int topk,
-                   float softmax_scale, void* dq_dev, void* dkv_dev, void* workspace_dev,
-                   size_t workspace_bytes, void* stream);
+                   float softmax_scale, void* dq_dev, void* dkv_dev, float* teacher_dev,
+                   void* workspace_dev, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * qsa_indexer_kl / qsa_indexer_bwd -- training the indexer on the selected
+ * slots.  [QSA "Describe the problem": sparse KL supervision for training the
+ * indexer; "Describe the solution you'd like": sparse Stage-2 teacher/KL loss
+ * for indexer training; DSA "Changes": sparse-KL streaming for the indexer
+ * loss, fused indexer backward kernel.]  The pages print no formula; the
+ * reading (also the reference implementation's):
+ *
+ *   student I[t,j] = score_scale * sum_h w[t,h] * ReLU(q_I[t,h].k_I[s0+idx[t,j]])
+ *   p[t,:] = softmax of I[t,:] over t's valid slots (idx in [0, length))
+ *   loss[t] = KL(teacher[t,:] || p[t,:]) = sum_j a log(a/p) over valid slots
+ *   with a > 0; dscore[t,j] = p - a on valid slots, 0 elsewhere.
+ *
+ * qsa_indexer_kl: indices_dev int32 [T, topk] (one group: the DSA token
+ *   selection, e.g. qsa_topk's output), teacher_dev fp32 [T, topk] (e.g.
+ *   sparse_mla_bwd's teacher_dev), loss_dev fp32 [T], dscore_dev fp32
+ *   [T, topk] (fully overwritten).  A row without a valid slot gives 0, 0.
+ * qsa_indexer_bwd: the gradient of sum_{t,j} dscore[t,j] * I[t,j] with
+ *   respect to q_I, k_I and w (D = q_I[t,h].k_I[s]):
+ *     dw[t,h]   = score_scale * sum_j dscore * ReLU(D)
+ *     dq_I[t,h] = score_scale * sum_j dscore * w[t,h] * [D > 0] * k_I[s]
+ *     dk_I[s]   = score_scale * sum_{t,j} dscore * sum_h w[t,h] [D > 0] q_I[t,h]
+ *   dq_idx_dev bf16 [T, H_I, d_I], dk_idx_dev bf16 [T, d_I], dw_dev fp32
+ *   [T, H_I] (all fully overwritten).  workspace:
+ *   qsa_indexer_bwd_workspace_size(T, d_I) bytes (the fp32 dk accumulator;
+ *   its summation order is not fixed; dq_idx and dw are bit-identical
+ *   across runs).
+ * Supported: d_I = 128, 1 <= H_I <= 128, 1 <= topk <= 4096.  Slots that are
+ * -1 carry nothing; indices outside their sequence are treated as -1 and
+ * raise TSA_FLAG_INDEX_RANGE.
+ * ------------------------------------------------------------------------- */
+int qsa_indexer_kl(const void* q_idx_dev, const void* k_idx_dev, const float* w_dev,
+                   const int32_t* cu_seqlens, int num_seqs, int H_I, int d_I, float score_scale,
+                   const int32_t* indices_dev, int topk, const float* teacher_dev, float* loss_dev,
+                   float* dscore_dev, void* stream);
+size_t qsa_indexer_bwd_workspace_size(int64_t T, int d_I);
+int qsa_indexer_bwd(const void* q_idx_dev, const void* k_idx_dev, const float* w_dev,
+                    const int32_t* cu_seqlens, int num_seqs, int H_I, int d_I, float score_scale,
+                    const int32_t* indices_dev, int topk, const float* dscore_dev, void* dq_idx_dev,
+                    void* dk_idx_dev, float* dw_dev, void* workspace_dev, size_t workspace_bytes,
+                    void* stream);
 
 /* ---------------------------------------------------------------------------
  * sparse_gqa_fwd / sparse_gqa_bwd -- block Sparse-GQA.
@@ -215,18 +264,27 @@ int sparse_mla_bwd(const void* q_dev, const void* kv_dev, const int32_t* indices
  *
  *   q_dev bf16 [T, Hq, d], k_dev/v_dev bf16 [T, Hkv, d],
  *   block_indices_dev int32 [T, Hkv, nsel], out_dev bf16 [T, Hq, d],
- *   lse_dev fp32 [T, Hq].  Backward: dq [T,Hq,d], dk/dv [T,Hkv,d] bf16
- *   (overwritten), workspace sparse_gqa_bwd_workspace_size(T, Hq, Hkv, d,
- *   nsel) bytes: fp32 dq/dk/dv accumulators, rowsum(dO * O) and the selections
- *   inverted per (block, kv group), so that the backward visits each selected
- *   block once per chunk of the queries that chose it.
- * Supported: Hq/Hkv in {1..16}, d in {64, 128}, block_size in {32, 64}.
- * Forward deterministic; backward dq/dk/dv summation order not fixed.
+ *   lse_dev fp32 [T, Hq].  Forward workspace:
+ *   sparse_gqa_fwd_workspace_size(T, Hq, Hkv, d, nsel) bytes: the selections
+ *   inverted per (block, kv group), and per selection slot the normalised
+ *   partial output of its block (fp32, Hq/Hkv x d) with its log-sum-exp; the
+ *   slots are merged in slot order.  Backward: dq [T,Hq,d], dk/dv [T,Hkv,d]
+ *   bf16 (overwritten), workspace sparse_gqa_bwd_workspace_size(T, Hq, Hkv,
+ *   d, nsel) bytes: fp32 dq/dk/dv accumulators, rowsum(dO * O) and the
+ *   selections inverted per (block, kv group), so that the backward visits
+ *   each selected block once per chunk of the queries that chose it.
+ * Supported: Hq/Hkv in {1..16}, d in {64, 128}, block_size in {32, 64},
+ * T * Hkv * nsel < 2^31.  Block ids at or past the end of their sequence are
+ * dropped and raise TSA_FLAG_INDEX_RANGE.
+ * Forward deterministic (bit-identical across runs); backward dq/dk/dv
+ * summation order not fixed.
  * ------------------------------------------------------------------------- */
+size_t sparse_gqa_fwd_workspace_size(int64_t T, int Hq, int Hkv, int d, int nsel);
 int sparse_gqa_fwd(const void* q_dev, const void* k_dev, const void* v_dev,
                    const int32_t* block_indices_dev, const int32_t* cu_seqlens, int num_seqs,
                    int Hq, int Hkv, int d, int block_size, int nsel, float softmax_scale,
-                   void* out_dev, float* lse_dev, void* stream);
+                   void* out_dev, float* lse_dev, void* workspace_dev, size_t workspace_bytes,
+                   void* stream);
 
 size_t sparse_gqa_bwd_workspace_size(int64_t T, int Hq, int Hkv, int d, int nsel);
 int sparse_gqa_bwd(const void* q_dev, const void* k_dev, const void* v_dev,

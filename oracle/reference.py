@@ -318,22 +318,26 @@ def _selected(idx_t: np.ndarray, n: int) -> np.ndarray:
 
 
 def indexer_scores_at(q_idx, k_idx, w, cu_seqlens, idx, groups: int = 1,
-                      score_scale: float = 1.0) -> np.ndarray:
+                      score_scale: float = 1.0, rows: Optional[Iterable[int]] = None) -> np.ndarray:
     """The indexer score of every selected slot, in fp64 (not rounded to fp32):
     S[t, g, j] = score_scale * sum_{h in g} w[t,h] * max(q_I[t,h] . k_I[s0 + idx[t,g,j]], 0),
-    -inf at slots that are -1 or outside t's sequence.  idx: int [T, groups, k]."""
-    Q, K, W, I = as_f64(q_idx), as_f64(k_idx), as_f64(w), as_i64(idx)
-    T, H_I, _ = Q.shape
+    -inf at slots that are -1 or outside t's sequence.  idx: int [T, groups, k].
+    ``rows``: only those query rows, compact [len(rows), groups, k].  Row
+    inputs (q_I, w, idx) are read one row at a time."""
+    K = as_f64(k_idx)
+    T, H_I = q_idx.shape[0], q_idx.shape[1]
     hg = H_I // groups
-    out = np.full(I.shape, -np.inf)
-    for t in range(T):
+    rr = range(T) if rows is None else list(rows)
+    out = np.full((len(rr),) + tuple(idx.shape[1:]), -np.inf)
+    for i, t in enumerate(rr):
         s0, n = seq_bounds(cu_seqlens, t)
+        Qt, Wt, It = as_f64(q_idx[t]), as_f64(w[t]), as_i64(idx[t])
         for g in range(groups):
             hs = slice(g * hg, (g + 1) * hg)
-            for j, s in enumerate(I[t, g]):
+            for j, s in enumerate(It[g]):
                 if 0 <= s < n:
-                    dots = Q[t, hs] @ K[s0 + s]                 # [hg]
-                    out[t, g, j] = score_scale * float(W[t, hs] @ np.maximum(dots, 0.0))
+                    dots = Qt[hs] @ K[s0 + s]                 # [hg]
+                    out[i, g, j] = score_scale * float(Wt[hs] @ np.maximum(dots, 0.0))
     return out
 
 
@@ -341,17 +345,18 @@ def mla_teacher(q, kv, idx, cu_seqlens, scale: float, rows: Optional[Iterable[in
     """The indexer's teacher on the selected slots of each query row: the sparse
     MLA attention probabilities exp(scale q[t,h] . kv[s] - lse[t,h]) averaged over
     the heads.  0 at -1 slots; all 0 for a row without a valid slot.
-    Returns float64 [len(rows), topk]."""
-    Q, KV, I = as_f64(q), as_f64(kv), as_i64(idx)
-    T, H = Q.shape[0], Q.shape[1]
+    Returns float64 [len(rows), topk].  q and idx are read one row at a time."""
+    KV = as_f64(kv)
+    T = q.shape[0]
     rr = range(T) if rows is None else list(rows)
-    out = np.zeros((len(rr), I.shape[1]))
+    out = np.zeros((len(rr), idx.shape[1]))
     for i, t in enumerate(rr):
         s0, n = seq_bounds(cu_seqlens, t)
-        ok = _selected(I[t], n)
+        It = as_i64(idx[t])
+        ok = _selected(It, n)
         if not ok.any():
             continue
-        S = scale * (Q[t] @ KV[s0 + I[t][ok]].T)           # [H, valid slots]
+        S = scale * (as_f64(q[t]) @ KV[s0 + It[ok]].T)     # [H, valid slots]
         P = np.exp(S - S.max(axis=1, keepdims=True))
         P /= P.sum(axis=1, keepdims=True)
         out[i, ok] = P.mean(axis=0)
@@ -379,31 +384,37 @@ def sparse_kl(scores, teacher):
     return loss, grad
 
 
-def indexer_bwd(q_idx, k_idx, w, cu_seqlens, idx, dscore, groups: int = 1, score_scale: float = 1.0):
+def indexer_bwd(q_idx, k_idx, w, cu_seqlens, idx, dscore, groups: int = 1, score_scale: float = 1.0,
+                rows: Optional[Iterable[int]] = None):
     """Gradient of sum_{t,g,j} dscore[t,g,j] * I_g[t, s0 + idx[t,g,j]] (the indexer
     score definition above, taken in fp64) with respect to q_I, k_I and w:
       dw[t,h]   = score_scale * sum_j dscore * max(d, 0)
       dq_I[t,h] = score_scale * sum_j dscore * w[t,h] * [d > 0] * k_I[s]
       dk_I[s]   = score_scale * sum_{t,j} dscore * sum_h w[t,h] * [d > 0] * q_I[t,h]
     with d = q_I[t,h] . k_I[s]; slots that are -1 or outside the sequence carry
-    no gradient.  Returns float64 (dq_I [T,H_I,d_I], dk_I [T,d_I], dw [T,H_I])."""
-    Q, K, W, I, G = as_f64(q_idx), as_f64(k_idx), as_f64(w), as_i64(idx), as_f64(dscore)
-    T, H_I, _ = Q.shape
+    no gradient.  ``rows`` restricts the sum to those query rows (exact when
+    dscore is zero on every other row) and makes dq_I and dw compact.  Row
+    inputs (q_I, w, idx, dscore) are read one row at a time.
+    Returns float64 (dq_I [T,H_I,d_I], dk_I [T,d_I], dw [T,H_I])."""
+    K = as_f64(k_idx)
+    T, H_I, d_I = q_idx.shape
     hg = H_I // groups
-    dq, dk, dw = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(W)
-    for t in range(T):
+    rr = list(range(T)) if rows is None else list(rows)
+    dq, dk, dw = np.zeros((len(rr), H_I, d_I)), np.zeros_like(K), np.zeros((len(rr), H_I))
+    for i, t in enumerate(rr):
         s0, n = seq_bounds(cu_seqlens, t)
+        Qt, Wt, It, Gt = as_f64(q_idx[t]), as_f64(w[t]), as_i64(idx[t]), as_f64(dscore[t])
         for g in range(groups):
             hs = slice(g * hg, (g + 1) * hg)
-            for j, s in enumerate(I[t, g]):
-                if not (0 <= s < n) or G[t, g, j] == 0.0:
+            for j, s in enumerate(It[g]):
+                if not (0 <= s < n) or Gt[g, j] == 0.0:
                     continue
-                c = score_scale * G[t, g, j]
-                d = Q[t, hs] @ K[s0 + s]                       # [hg]
+                c = score_scale * Gt[g, j]
+                d = Qt[hs] @ K[s0 + s]                       # [hg]
                 on = (d > 0).astype(np.float64)
-                dw[t, hs] += c * np.maximum(d, 0.0)
-                dq[t, hs] += c * (W[t, hs] * on)[:, None] * K[s0 + s][None, :]
-                dk[s0 + s] += c * ((W[t, hs] * on) @ Q[t, hs])
+                dw[i, hs] += c * np.maximum(d, 0.0)
+                dq[i, hs] += c * (Wt[hs] * on)[:, None] * K[s0 + s][None, :]
+                dk[s0 + s] += c * ((Wt[hs] * on) @ Qt[hs])
     return dq, dk, dw
 
 

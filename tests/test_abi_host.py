@@ -75,11 +75,12 @@ def test_host_validation_errors(lib):
     # workspace too small
     assert lib.qsa_topk(fake, fake, fake, cu, 1, 8, 64, 1, 1, 1.0, 4, fake, fake, 1, None) == 3
     assert lib.sparse_mla_bwd(fake, fake, fake, fake, fake, fake, cu, 1, 8, 576, 64, 0.1, fake, fake,
-                              fake, 16, None) == 3
+                              None, fake, 16, None) == 3
     # GQA shapes
-    assert lib.sparse_gqa_fwd(fake, fake, fake, fake, cu, 1, 32, 3, 128, 64, 4, 0.1, fake, fake, None) == 2
-    assert lib.sparse_gqa_fwd(fake, fake, fake, fake, cu, 1, 32, 4, 96, 64, 4, 0.1, fake, fake, None) == 2
-    assert lib.sparse_gqa_fwd(fake, fake, fake, fake, cu, 1, 32, 4, 128, 16, 4, 0.1, fake, fake, None) == 2
+    assert lib.sparse_gqa_fwd(fake, fake, fake, fake, cu, 1, 32, 3, 128, 64, 4, 0.1, fake, fake, fake, 1 << 40, None) == 2
+    assert lib.sparse_gqa_fwd(fake, fake, fake, fake, cu, 1, 32, 4, 96, 64, 4, 0.1, fake, fake, fake, 1 << 40, None) == 2
+    assert lib.sparse_gqa_fwd(fake, fake, fake, fake, cu, 1, 32, 4, 128, 16, 4, 0.1, fake, fake, fake, 1 << 40, None) == 2
+    assert lib.sparse_gqa_fwd(fake, fake, fake, fake, cu, 1, 32, 4, 128, 64, 4, 0.1, fake, fake, fake, 16, None) == 3
     assert "d_qk" in lib.tsa_last_error().decode() or lib.tsa_last_error().decode()
 
 
@@ -134,9 +135,16 @@ def test_backward_and_sequence_table_validation(lib):
     fake = ctypes.c_void_p(16)
     # MLA backward: a null gradient pointer, an unsupported width
     assert lib.sparse_mla_bwd(fake, fake, fake, fake, fake, None, cu, 1, 8, 576, 64, 0.1, fake, fake,
-                              fake, 1 << 30, None) == 1
+                              None, fake, 1 << 30, None) == 1
     assert lib.sparse_mla_bwd(fake, fake, fake, fake, fake, fake, cu, 1, 8, 320, 64, 0.1, fake, fake,
-                              fake, 1 << 30, None) == 2
+                              None, fake, 1 << 30, None) == 2
+    # indexer training: d_I other than 128, topk beyond 4096, null loss, workspace too small
+    assert lib.qsa_indexer_kl(fake, fake, fake, cu, 1, 64, 64, 1.0, fake, 64, fake, fake, fake, None) == 2
+    assert lib.qsa_indexer_kl(fake, fake, fake, cu, 1, 64, 128, 1.0, fake, 5000, fake, fake, fake, None) == 2
+    assert lib.qsa_indexer_kl(fake, fake, fake, cu, 1, 64, 128, 1.0, fake, 64, fake, None, fake, None) == 1
+    assert lib.qsa_indexer_bwd_workspace_size(8, 128) == 4096
+    assert lib.qsa_indexer_bwd(fake, fake, fake, cu, 1, 64, 128, 1.0, fake, 64, fake, fake, fake, fake,
+                               fake, 16, None) == 3
     # GQA backward: group size above 16, zero selected blocks, workspace too small, null dq
     args = lambda Hq, Hkv, nsel, dq, ws_bytes: (fake, fake, fake, fake, fake, fake, fake, cu, 1, Hq, Hkv, 128,
                                                64, nsel, 0.1, dq, fake, fake, fake, ws_bytes, None)

@@ -15,13 +15,17 @@ def test_step_flops_match_closed_forms():
     pairs = T * (T + 1) // 2                      # causal (query, key) pairs, self included
     valid = k * (k + 1) // 2 + (T - k) * k        # sum over t of min(t + 1, k)
     assert valid == sum(min(t + 1, k) for t in range(T))
-    f_idx, f_fwd, f_bwd = bench.flops_of(valid, pairs)
+    f_idx, f_fwd, f_bwd, f_kl, f_ibwd = bench.flops_of(valid, pairs)
     # indexer: one multiply-add per head and channel for every causal pair
     assert f_idx == pairs * 64 * 128 * 2 == 35_184_908_959_744
     # forward: QK^T over 576 channels and PV over 512, per head and valid pair
     assert f_fwd == valid * 128 * 2 * (576 + 512) == 36_799_565_004_800
     # backward: S and dQ, dK over 576; dP and dV over 512
     assert f_bwd == valid * 128 * 2 * (3 * 576 + 2 * 512) == 93_081_252_659_200
+    # indexer KL: the student scores of every valid slot (64 heads x 128 channels)
+    assert f_kl == valid * 64 * 128 * 2 == 2_164_680_294_400
+    # indexer backward: the scores again, dq_I and dk_I
+    assert f_ibwd == 3 * f_kl
 
 
 def test_job_rate_is_ranks_times_work_over_slowest_time():

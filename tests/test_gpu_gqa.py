@@ -7,7 +7,7 @@ import torch
 
 import oracle as O
 import synth
-from _util import TOL_GRAD, check_out_lse, rel_l2
+from _util import check_grad, check_out_lse
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -42,8 +42,8 @@ def test_gqa_fwd_bwd(tsa, Hq, Hkv, d, bs, nsel, lengths):
     o_r, l_r = O.sparse_gqa_fwd(g["q"], g["k"], g["v"], blk, cu, bs, scale)
     check_out_lse(out, lse, o_r, l_r)
     dq_r, dk_r, dv_r = O.sparse_gqa_bwd(g["q"], g["k"], g["v"], blk, cu, bs, scale, g["dout"])
-    for got, ref in ((dq, dq_r), (dk, dk_r), (dv, dv_r)):
-        assert rel_l2(got, ref) <= TOL_GRAD
+    for name, got, ref in (("dq", dq, dq_r), ("dk", dk, dk_r), ("dv", dv, dv_r)):
+        check_grad(got, ref, name)
     assert torch.all(out[min(5, T - 1)] == 0)
 
 
@@ -64,8 +64,8 @@ def test_gqa_bwd_lists_longer_than_a_chunk(tsa):
     dq, dk, dv = tsa.sparse_gqa_bwd(q, k, v, blk.to(DEV), out, lse, dO, cu, bs, scale)
     torch.cuda.synchronize()
     dq_r, dk_r, dv_r = O.sparse_gqa_bwd(g["q"], g["k"], g["v"], blk, cu, bs, scale, g["dout"])
-    for got, ref in ((dq, dq_r), (dk, dk_r), (dv, dv_r)):
-        assert rel_l2(got, ref) <= TOL_GRAD
+    for name, got, ref in (("dq", dq, dq_r), ("dk", dk, dk_r), ("dv", dv, dv_r)):
+        check_grad(got, ref, name)
 
 
 def test_gqa_forward_deterministic(tsa):
@@ -97,6 +97,7 @@ def test_gqa_thd32768_sampled(tsa):
     o_r, l_r = O.sparse_gqa_fwd(g["q"], g["k"], g["v"], blk, cu, 64, scale, rows=rows)
     check_out_lse(out, lse, o_r, l_r, rows=rows)
     dq_r, dk_r, dv_r = O.sparse_gqa_bwd(g["q"], g["k"], g["v"], blk, cu, 64, scale, g["dout"], rows=rows)
-    assert rel_l2(dq[rows], dq_r) <= TOL_GRAD
-    assert rel_l2(dk, dk_r) <= TOL_GRAD and rel_l2(dv, dv_r) <= TOL_GRAD
+    check_grad(dq[rows], dq_r, "dq")
+    check_grad(dk, dk_r, "dk")
+    check_grad(dv, dv_r, "dv")
 

@@ -9,7 +9,7 @@ import torch
 
 import oracle as O
 import synth
-from _util import TOL_GRAD, TOL_OUT, check_out_lse, rel_l2
+from _util import TOL_GRAD, TOL_OUT, check_grad, check_out_lse, rel_l2
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -80,8 +80,8 @@ def test_mla_shape_sweep_t2048(tsa, D, topk, H):
     o_ref, l_ref = O.sparse_mla_fwd(m["q"], m["kv"], idx, cu, scale, rows=rows)
     check_out_lse(r["out"], r["lse"], o_ref, l_ref, rows=rows)
     dq_ref, dkv_ref = O.sparse_mla_bwd(m["q"], m["kv"], idx, cu, scale, m["dout"])
-    e_q, e_kv = rel_l2(r["dq"], dq_ref), rel_l2(r["dkv"], dkv_ref)
-    assert e_q <= TOL_GRAD and e_kv <= TOL_GRAD, (e_q, e_kv)
+    check_grad(r["dq"], dq_ref, "dq")
+    check_grad(r["dkv"], dkv_ref, "dkv")
     # all-invalid rows: zero output, -inf lse, zero dq
     for row in (0, 97, 1000, 2047):
         assert torch.all(r["out"][row] == 0) and torch.all(torch.isneginf(r["lse"][row]))
@@ -109,7 +109,8 @@ def test_mla_nope_and_topk_padding_are_exact(tsa):
     o_ref, l_ref = O.sparse_mla_fwd(m["q"], m["kv"], idx, cu, scale)
     check_out_lse(a["out"], a["lse"], o_ref, l_ref)
     dq_ref, dkv_ref = O.sparse_mla_bwd(m["q"], m["kv"], idx, cu, scale, m["dout"])
-    assert rel_l2(a["dq"], dq_ref) <= TOL_GRAD and rel_l2(a["dkv"], dkv_ref) <= TOL_GRAD
+    check_grad(a["dq"], dq_ref, "dq")
+    check_grad(a["dkv"], dkv_ref, "dkv")
 
 
 def test_mla_forward_deterministic_under_contention(tsa):
@@ -140,7 +141,8 @@ def test_mla_thd_and_index_range_flag(tsa):
     o_ref, l_ref = O.sparse_mla_fwd(m["q"], m["kv"], idx, cu, scale)
     check_out_lse(r["out"], r["lse"], o_ref, l_ref)
     dq_ref, dkv_ref = O.sparse_mla_bwd(m["q"], m["kv"], idx, cu, scale, m["dout"])
-    assert rel_l2(r["dq"], dq_ref) <= TOL_GRAD and rel_l2(r["dkv"], dkv_ref) <= TOL_GRAD
+    check_grad(r["dq"], dq_ref, "dq")
+    check_grad(r["dkv"], dkv_ref, "dkv")
     # an index beyond its sequence is treated as -1 and raises the flag (no fault)
     bad = idx.clone()
     bad[50, 3] = 100          # sequence 0 has 100 tokens: position 100 is outside it
@@ -168,8 +170,8 @@ def test_mla_t4096_h16_topk2048(tsa):
     o_ref, l_ref = O.sparse_mla_fwd(m["q"], m["kv"], idx, cu, scale, rows=rows)
     check_out_lse(r["out"], r["lse"], o_ref, l_ref, rows=rows)
     dq_ref, dkv_ref = O.sparse_mla_bwd(m["q"], m["kv"], idx, cu, scale, m["dout"], rows=rows)
-    assert rel_l2(r["dq"].cpu()[rows], dq_ref) <= TOL_GRAD
-    assert rel_l2(r["dkv"], dkv_ref) <= TOL_GRAD
+    check_grad(r["dq"].cpu()[rows], dq_ref, "dq")
+    check_grad(r["dkv"], dkv_ref, "dkv")
 
 
 @pytest.mark.slow
@@ -196,8 +198,8 @@ def test_mla_t65536_h128_sampled(tsa):
     o_ref, l_ref = O.sparse_mla_fwd(m["q"], m["kv"], idx, cu, scale, rows=rows)
     check_out_lse(out, lse, o_ref, l_ref, rows=rows)
     dq_ref, dkv_ref = O.sparse_mla_bwd(m["q"], m["kv"], idx, cu, scale, m["dout"], rows=rows)
-    assert rel_l2(dq[rows], dq_ref) <= TOL_GRAD
-    assert rel_l2(dkv, dkv_ref) <= TOL_GRAD
+    check_grad(dq[rows], dq_ref, "dq")
+    check_grad(dkv, dkv_ref, "dkv")
 
 
 @pytest.mark.parametrize("D,topk,lengths", [
@@ -268,10 +270,63 @@ def test_mla_h128_backward(tsa, D, topk, lengths):
     assert torch.equal(dq2, r["dq"])
     dq_ref, dkv_ref = O.sparse_mla_bwd(m["q"], m["kv"], idx, cu, scale, m["dout"], rows=rows)
     dq = r["dq"].cpu()
-    assert rel_l2(dq[rows], dq_ref) <= TOL_GRAD
-    assert rel_l2(r["dkv"], dkv_ref) <= TOL_GRAD
+    check_grad(dq[rows], dq_ref, "dq")
+    check_grad(r["dkv"], dkv_ref, "dkv")
     others = torch.ones(T, dtype=torch.bool)
     others[rows] = False
     assert torch.all(dq[others] == 0)
     untouched = torch.from_numpy(np.abs(np.asarray(dkv_ref)).sum(1) == 0)
     assert torch.all(r["dkv"].cpu()[untouched] == 0)
+
+
+def test_mla_h128_index_range_flag(tsa):
+    """H = 128 (the tcgen05 forward and backward): an index beyond its sequence
+    is treated as -1 and raises FLAG_INDEX_RANGE; out, lse and dq equal those
+    of the run with the bad slots set to -1 bit for bit (dkv up to the order of
+    its atomic sums), and that run matches the oracle."""
+    cu = [0, 300, 700]
+    T = cu[-1]
+    m = synth.mla_inputs(T, 128, 576, seed=21, with_grad_out=True)
+    idx = synth.random_topk_indices(cu, 256, seed=21)
+    bad = idx.clone()
+    bad[50, 3] = 300          # sequence 0 holds local positions 0..299
+    bad[400, 0] = 400         # sequence 1 holds local positions 0..399
+    bad[650, 255] = 1 << 20
+    fixed = bad.clone()
+    fixed[50, 3] = fixed[400, 0] = fixed[650, 255] = -1
+    scale = 1 / math.sqrt(576)
+    tsa.read_flags(clear=True)
+    rf = _run_fwd_bwd(tsa, m, fixed, cu, scale)
+    assert tsa.read_flags() == 0
+    rb = _run_fwd_bwd(tsa, m, bad, cu, scale)
+    assert tsa.read_flags() & tsa.FLAG_INDEX_RANGE
+    assert torch.equal(rb["out"], rf["out"]) and torch.equal(rb["lse"], rf["lse"])
+    assert torch.equal(rb["dq"], rf["dq"])
+    assert rel_l2(rb["dkv"], rf["dkv"]) <= 1e-3
+    rows = [0, 49, 50, 51, 299, 300, 399, 400, 401, 650, 699]
+    o_ref, l_ref = O.sparse_mla_fwd(m["q"], m["kv"], fixed, cu, scale, rows=rows)
+    check_out_lse(rf["out"], rf["lse"], o_ref, l_ref, rows=rows)
+
+
+@pytest.mark.parametrize("H", [64, 96])
+def test_mla_tp_head_counts_fwd_bwd(tsa, H):
+    """Head counts of a tensor-parallel slice of 128 heads (64) and a count that
+    is not a power of two (96): forward on sampled rows, dq of those rows and
+    the full dkv with dO kept on them only."""
+    cu = [0, 900, 1500]
+    T = cu[-1]
+    m = synth.mla_inputs(T, H, 576, seed=H, with_grad_out=True)
+    idx = synth.random_topk_indices(cu, 512, seed=H, invalid_rows=[3, T - 1])
+    scale = 1 / math.sqrt(576)
+    rows = sorted(set([0, 1, 3, 511, 512, 899, 900, 901, T - 1] + list(range(7, T, 97))))
+    mask = torch.zeros(T, dtype=torch.bool)
+    mask[rows] = True
+    m["dout"] = torch.where(mask[:, None, None], m["dout"], torch.zeros_like(m["dout"]))
+    r = _run_fwd_bwd(tsa, m, idx, cu, scale)
+    o_ref, l_ref = O.sparse_mla_fwd(m["q"], m["kv"], idx, cu, scale, rows=rows)
+    check_out_lse(r["out"], r["lse"], o_ref, l_ref, rows=rows)
+    dq_ref, dkv_ref = O.sparse_mla_bwd(m["q"], m["kv"], idx, cu, scale, m["dout"], rows=rows)
+    check_grad(r["dq"].cpu()[rows], dq_ref, "dq")
+    check_grad(r["dkv"], dkv_ref, "dkv")
+    for row in (3, T - 1):
+        assert torch.all(r["out"][row] == 0) and torch.all(torch.isneginf(r["lse"][row]))

@@ -160,6 +160,30 @@ def test_qsa_topk_zero_tie_stress_t4096(tsa):
     assert mism <= 0.001 * len(rows) * 2048
 
 
+@pytest.mark.parametrize("H_I,d_I,groups,bs,topk,cu", [
+    (8, 128, 1, 1, 2048, [0, 4096]),
+    (64, 128, 1, 1, 512, [0, 1000, 3000]),
+    (8, 128, 4, 64, 32, [0, 1000, 4096]),
+    (16, 64, 2, 32, 20, [0, 77, 2000]),
+])
+def test_qsa_topk_equals_topk_of_its_own_scores(tsa, H_I, d_I, groups, bs, topk, cu):
+    """On N(0,1) inputs (scores are not exact in fp32), the fused streaming
+    qsa_topk selects exactly the top-k of the fp32 scores that qsa_indexer_scores
+    produces, byte for byte: the selection itself adds no error."""
+    T = cu[-1]
+    x = {k: v.to(DEV) for k, v in synth.indexer_inputs(T, H_I, d_I, seed=T + bs, zero_key_frac=0.3).items()}
+    got = tsa.qsa_topk(x["q_idx"], x["k_idx"], x["w"], cu, topk, groups=groups, block_size=bs)
+    sc = tsa.qsa_indexer_scores(x["q_idx"], x["k_idx"], x["w"], cu, groups=groups, block_size=bs)
+    sel = tsa.qsa_topk_from_scores(sc, topk)
+    assert torch.equal(sel, got)
+    # and those scores select, on the CPU, what the GPU selects (the oracle's
+    # exact top-k of the same fp32 buffer)
+    scn = sc.cpu().numpy()
+    for t in range(0, T, max(1, T // 64)):
+        for g in range(groups):
+            np.testing.assert_array_equal(got[t, g].cpu().numpy(), O.topk_lex(scn[t, g], topk))
+
+
 def test_qsa_topk_deterministic(tsa):
     cu = [0, 3000]
     x = synth.indexer_inputs(3000, 8, 128, seed=4, zero_key_frac=0.3)
@@ -180,9 +204,19 @@ def test_qsa_topk_t65536_sampled(tsa):
     xc = {k: v.cpu() for k, v in x.items()}
     sc = O.indexer_token_scores(xc["q_idx"], xc["k_idx"], xc["w"], cu, rows)
     g = got.cpu().numpy()
+    mism = 0
     for i, t in enumerate(rows):
         tol = indexer_score_bound(xc["q_idx"], xc["k_idx"], xc["w"], cu, t)[0]
-        compare_topk_rows(g[t, 0], sc[i, 0], 2048, tol)
+        mism += compare_topk_rows(g[t, 0], sc[i, 0], 2048, tol)
+    print(f"T=65536 top-2048: {mism} of {len(rows) * 2048} sampled slots differ from the oracle "
+          "(each within the fp32 score bound)")
+    assert mism <= 0.001 * len(rows) * 2048
+    # the fused streaming call selects exactly the top-k of its own fp32 scores:
+    # one 512-query chunk through qsa_indexer_scores + qsa_topk_from_scores
+    q0, nq = 40000, 512
+    sc_gpu = tsa.qsa_indexer_scores(x["q_idx"], x["k_idx"], x["w"], cu, q_begin=q0, q_count=nq)
+    sel = tsa.qsa_topk_from_scores(sc_gpu, 2048)
+    assert torch.equal(sel, got[q0:q0 + nq])
 
 
 @pytest.mark.slow
@@ -196,7 +230,15 @@ def test_qsa_topk_block_thd32768_sampled(tsa):
     rows = [0, 63, 64, 4095, 4096, 4097, 12287, 12288, 24575, 24576, 32767] + list(range(500, T, 1999))
     xc = {k: v.cpu() for k, v in x.items()}
     sc = O.indexer_block_scores(xc["q_idx"], xc["k_idx"], xc["w"], cu, rows, 64, 4)
+    mism = 0
     for i, t in enumerate(rows):
         tol = indexer_score_bound(xc["q_idx"], xc["k_idx"], xc["w"], cu, t, 4)
         for g in range(4):
-            compare_topk_rows(got[t, g], sc[i, g], 32, tol[g])
+            mism += compare_topk_rows(got[t, g], sc[i, g], 32, tol[g])
+    print(f"THD 32768 block top-32: {mism} of {len(rows) * 4 * 32} sampled slots differ from the oracle "
+          "(each within the fp32 score bound)")
+    assert mism <= 0.001 * len(rows) * 4 * 32
+    # fused call == exact top-k of its own block scores, for every query (bit for bit)
+    sc_gpu = tsa.qsa_indexer_scores(x["q_idx"], x["k_idx"], x["w"], cu, groups=4, block_size=64)
+    sel = tsa.qsa_topk_from_scores(sc_gpu, 32).cpu().numpy()
+    np.testing.assert_array_equal(sel, got)

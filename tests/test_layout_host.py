@@ -59,4 +59,4 @@ def test_every_kernel_launch_is_counted():
             if "<<<" in ln and not ln.lstrip().startswith("//"):
                 sites += 1
                 assert lines[i + 1].strip() == "note_launch();", f"{f}:{i + 1} launch not counted"
-    assert sites >= 19
+    assert sites >= 18

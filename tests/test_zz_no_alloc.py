@@ -56,11 +56,14 @@ def test_no_alloc_matches_workspace_entry_point(tsa, H_I, d_I, groups, bs, topk,
     T = cu[-1]
     x = {k: v.to(DEV) for k, v in synth.indexer_inputs(T, H_I, d_I, seed=T + groups, zero_key_frac=0.3).items()}
     ref = tsa.qsa_topk(x["q_idx"], x["k_idx"], x["w"], cu, topk, groups=groups, block_size=bs)
+    tsa.read_flags(clear=True)
     for call in range(2):
         out = torch.full((T, groups, topk), -7, dtype=torch.int32, device=DEV)
         rc = _no_alloc(lib, x, cu, H_I, d_I, groups, bs, topk, out)
         assert rc == 0, lib.tsa_last_error().decode()
         torch.cuda.synchronize()
+        # no bounded wait gave up (a timeout would raise FLAG_TIMEOUT here)
+        assert tsa.read_flags() == 0, f"call {call}: device flags raised"
         assert torch.equal(out, ref), f"call {call}: indices differ from qsa_topk"
 
 
@@ -75,6 +78,7 @@ def test_no_alloc_second_problem_after_first(tsa):
         out = torch.empty((T, 1, 512), dtype=torch.int32, device=DEV)
         assert _no_alloc(lib, x, cu, 8, 128, 1, 1, 512, out) == 0
         torch.cuda.synchronize()
+        assert tsa.read_flags() == 0
         assert torch.equal(out, ref)
 
 

@@ -43,9 +43,16 @@ SIGNATURES = {
                                c_void_p, c_void_p, c_void_p]),
     "sparse_mla_bwd_workspace_size": (c_size_t, [c_int64, c_int, c_int, c_int]),
     "sparse_mla_bwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_i32p, c_int,
-                               c_int, c_int, c_int, c_float, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+                               c_int, c_int, c_int, c_float, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
+                               c_void_p]),
+    "qsa_indexer_kl": (c_int, [c_void_p, c_void_p, c_void_p, c_i32p, c_int, c_int, c_int, c_float, c_void_p, c_int,
+                               c_void_p, c_void_p, c_void_p, c_void_p]),
+    "qsa_indexer_bwd_workspace_size": (c_size_t, [c_int64, c_int]),
+    "qsa_indexer_bwd": (c_int, [c_void_p, c_void_p, c_void_p, c_i32p, c_int, c_int, c_int, c_float, c_void_p, c_int,
+                                c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "sparse_gqa_fwd_workspace_size": (c_size_t, [c_int64, c_int, c_int, c_int, c_int]),
     "sparse_gqa_fwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_i32p, c_int, c_int, c_int, c_int,
-                               c_int, c_int, c_float, c_void_p, c_void_p, c_void_p]),
+                               c_int, c_int, c_float, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "sparse_gqa_bwd_workspace_size": (c_size_t, [c_int64, c_int, c_int, c_int, c_int]),
     "sparse_gqa_bwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_i32p,
                                c_int, c_int, c_int, c_int, c_int, c_int, c_float, c_void_p, c_void_p, c_void_p,
@@ -207,8 +214,10 @@ def sparse_mla_bwd_workspace_size(T: int, H: int, d_qk: int, topk: int) -> int:
 
 
 def sparse_mla_bwd(q, kv, indices, out, lse, dout, cu_seqlens, softmax_scale: float, workspace=None,
-                   dq=None, dkv=None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """dq bf16 [T, H, D], dkv bf16 [T, D]."""
+                   dq=None, dkv=None, teacher=None, want_teacher: bool = False, stream=None):
+    """dq bf16 [T, H, D], dkv bf16 [T, D]; with ``want_teacher`` (or a given
+    fp32 [T, topk] ``teacher`` buffer) also the indexer's KL teacher, the head
+    mean of the attention probabilities at every slot: (dq, dkv, teacher)."""
     for t, n, dt in ((q, "q", torch.bfloat16), (kv, "kv", torch.bfloat16), (indices, "indices", torch.int32),
                      (out, "out", torch.bfloat16), (lse, "lse", torch.float32), (dout, "dout", torch.bfloat16)):
         _req(t, n, dt)
@@ -223,16 +232,81 @@ def sparse_mla_bwd(q, kv, indices, out, lse, dout, cu_seqlens, softmax_scale: fl
         dq = torch.empty_like(q)
     if dkv is None:
         dkv = torch.empty_like(kv)
+    if teacher is None and want_teacher:
+        teacher = torch.empty((T, topk), dtype=torch.float32, device=q.device)
+    if teacher is not None:
+        _req(teacher, "teacher", torch.float32)
     _check("sparse_mla_bwd", lib.sparse_mla_bwd(_ptr(q), _ptr(kv), _ptr(indices), _ptr(out), _ptr(lse), _ptr(dout),
                                                 cu, nseq, H, D, topk, softmax_scale, _ptr(dq), _ptr(dkv),
-                                                _ptr(workspace), workspace.numel(), _stream(stream)))
-    return dq, dkv
+                                                _ptr(teacher), _ptr(workspace), workspace.numel(),
+                                                _stream(stream)))
+    return (dq, dkv, teacher) if teacher is not None else (dq, dkv)
+
+
+# ------------------------------------------------------------------ indexer training
+
+def _sel_indices(indices) -> Tuple[torch.Tensor, int]:
+    _req(indices, "indices", torch.int32)
+    return indices, indices.shape[-1]
+
+
+def qsa_indexer_kl(q_idx, k_idx, w, cu_seqlens, indices, teacher, score_scale: float = 1.0, loss=None,
+                   dscore=None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Sparse KL of the indexer against the teacher on the selected slots:
+    (loss fp32 [T], dscore fp32 [T, topk] = softmax(student) - teacher)."""
+    _req(q_idx, "q_idx", torch.bfloat16, 3)
+    _req(k_idx, "k_idx", torch.bfloat16, 2)
+    _req(w, "w", torch.float32, 2)
+    indices, topk = _sel_indices(indices)
+    _req(teacher, "teacher", torch.float32)
+    T, H_I, d_I = q_idx.shape
+    cu, nseq = _cu(cu_seqlens)
+    if loss is None:
+        loss = torch.empty((T,), dtype=torch.float32, device=q_idx.device)
+    if dscore is None:
+        dscore = torch.empty((T, topk), dtype=torch.float32, device=q_idx.device)
+    _check("qsa_indexer_kl", load_library().qsa_indexer_kl(
+        _ptr(q_idx), _ptr(k_idx), _ptr(w), cu, nseq, H_I, d_I, score_scale, _ptr(indices), topk, _ptr(teacher),
+        _ptr(loss), _ptr(dscore), _stream(stream)))
+    return loss, dscore
+
+
+def qsa_indexer_bwd_workspace_size(T: int, d_I: int) -> int:
+    return int(load_library().qsa_indexer_bwd_workspace_size(T, d_I))
+
+
+def qsa_indexer_bwd(q_idx, k_idx, w, cu_seqlens, indices, dscore, score_scale: float = 1.0, workspace=None,
+                    dq=None, dk=None, dw=None, stream=None):
+    """Backward of the indexer score on the selected slots: (dq_idx bf16
+    [T, H_I, d_I], dk_idx bf16 [T, d_I], dw fp32 [T, H_I])."""
+    _req(q_idx, "q_idx", torch.bfloat16, 3)
+    _req(k_idx, "k_idx", torch.bfloat16, 2)
+    _req(w, "w", torch.float32, 2)
+    indices, topk = _sel_indices(indices)
+    _req(dscore, "dscore", torch.float32)
+    T, H_I, d_I = q_idx.shape
+    cu, nseq = _cu(cu_seqlens)
+    lib = load_library()
+    need = int(lib.qsa_indexer_bwd_workspace_size(T, d_I))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q_idx.device)
+    dq = torch.empty_like(q_idx) if dq is None else dq
+    dk = torch.empty_like(k_idx) if dk is None else dk
+    dw = torch.empty_like(w) if dw is None else dw
+    _check("qsa_indexer_bwd", lib.qsa_indexer_bwd(
+        _ptr(q_idx), _ptr(k_idx), _ptr(w), cu, nseq, H_I, d_I, score_scale, _ptr(indices), topk, _ptr(dscore),
+        _ptr(dq), _ptr(dk), _ptr(dw), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return dq, dk, dw
 
 
 # ------------------------------------------------------------------ sparse GQA
 
+def sparse_gqa_fwd_workspace_size(T: int, Hq: int, Hkv: int, d: int, nsel: int) -> int:
+    return int(load_library().sparse_gqa_fwd_workspace_size(T, Hq, Hkv, d, nsel))
+
+
 def sparse_gqa_fwd(q, k, v, block_indices, cu_seqlens, block_size: int, softmax_scale: float, out=None,
-                   lse=None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+                   lse=None, workspace=None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """out bf16 [T, Hq, d], lse fp32 [T, Hq]."""
     _req(q, "q", torch.bfloat16, 3)
     _req(k, "k", torch.bfloat16, 3)
@@ -247,9 +321,12 @@ def sparse_gqa_fwd(q, k, v, block_indices, cu_seqlens, block_size: int, softmax_
     if lse is None:
         lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device)
     lib = load_library()
+    need = int(lib.sparse_gqa_fwd_workspace_size(T, Hq, Hkv, d, nsel))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     _check("sparse_gqa_fwd", lib.sparse_gqa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(block_indices), cu, nseq, Hq, Hkv,
                                                 d, block_size, nsel, softmax_scale, _ptr(out), _ptr(lse),
-                                                _stream(stream)))
+                                                _ptr(workspace), workspace.numel(), _stream(stream)))
     return out, lse
 
 

@@ -19,7 +19,7 @@ LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libtsa.so")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 
-SOURCES = ["api.cu", "topk.cu", "indexer.cu", "indexer_tc.cu", "mla_fwd.cu", "mla_fwd_tc.cu", "mla_bwd.cu", "mla_bwd_tc.cu", "mla_bwd_pds_tc.cu", "gqa.cu", "gqa_bwd_kv.cu", "noalloc.cu", "selftest.cu"]
+SOURCES = ["api.cu", "topk.cu", "indexer.cu", "indexer_tc.cu", "mla_fwd.cu", "mla_fwd_tc.cu", "mla_bwd.cu", "mla_bwd_tc.cu", "mla_bwd_pds_tc.cu", "gqa_tc.cu", "indexer_kl.cu", "noalloc.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-Xptxas", "-v", "-I", INCLUDE]

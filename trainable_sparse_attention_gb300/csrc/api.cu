@@ -18,15 +18,6 @@ namespace {
 // Error flag word raised by kernels (never a trap); read by tsa_read_flags.
 __device__ unsigned int g_flags = 0;
 
-unsigned int* flags_ptr() {
-  void* p = nullptr;
-  if (cudaGetSymbolAddress(&p, g_flags) != cudaSuccess) {
-    cudaGetLastError();
-    return nullptr;
-  }
-  return static_cast<unsigned int*>(p);
-}
-
 thread_local std::string g_last_error;
 
 int fail(int code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
@@ -61,8 +52,45 @@ std::atomic<unsigned long long> g_launches{0};
     if (_e != cudaSuccess) return cuda_status(_e, where); \
   } while (0)
 
+// Score scratch of one query chunk of the streaming indexer + top-k.  Large
+// enough that a chunk's top-k launch has thousands of rows (one CTA each) in
+// flight; far below the T x T scores it replaces.
+static constexpr int64_t kScoreChunkBytes = int64_t(512) << 20;
+
+// Query rows per streamed chunk: the chunk's scores stay within kScoreChunkBytes.
+int64_t chunk_rows(int max_len, int groups, int block_size) {
+  int64_t w = score_width(max_len, block_size);
+  if (w < 1) w = 1;
+  int64_t c = kScoreChunkBytes / (4 * w * groups);
+  c = (c / 128) * 128;
+  if (c < 128) c = 128;
+  if (c > max_len) c = max_len;
+  if (c < 1) c = 1;
+  return c;
+}
+
+}  // namespace
+
+namespace tsa {
+// Record a detail message for tsa_last_error() (entry points of other
+// translation units), and account for a kernel launch (every launch site).
+int note_error(int code, const char* msg) {
+  g_last_error = msg;
+  return code;
+}
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+unsigned int* device_flags() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_flags) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return static_cast<unsigned int*>(p);
+}
+
 // Validate cu_seqlens and fill the kernel-side table.
-int make_seqs(const int32_t* cu, int num_seqs, SeqTable* st, int64_t* T_out) {
+int make_seq_table(const int32_t* cu, int num_seqs, SeqTable* st, int64_t* T_out) {
   if (cu == nullptr) return fail(TSA_ERR_INVALID_ARG, "cu_seqlens is null");
   if (num_seqs < 1 || num_seqs > TSA_MAX_SEQS)
     return fail(TSA_ERR_INVALID_ARG, "num_seqs=%d outside [1, %d]", num_seqs, TSA_MAX_SEQS);
@@ -97,33 +125,6 @@ int64_t score_width(int max_len, int block_size) {
   return block_size == 1 ? max_len : (max_len + block_size - 1) / block_size;
 }
 
-// Score scratch of one query chunk of the streaming indexer + top-k.  Large
-// enough that a chunk's top-k launch has thousands of rows (one CTA each) in
-// flight; far below the T x T scores it replaces.
-static constexpr int64_t kScoreChunkBytes = int64_t(512) << 20;
-
-// Query rows per streamed chunk: the chunk's scores stay within kScoreChunkBytes.
-int64_t chunk_rows(int max_len, int groups, int block_size) {
-  int64_t w = score_width(max_len, block_size);
-  if (w < 1) w = 1;
-  int64_t c = kScoreChunkBytes / (4 * w * groups);
-  c = (c / 128) * 128;
-  if (c < 128) c = 128;
-  if (c > max_len) c = max_len;
-  if (c < 1) c = 1;
-  return c;
-}
-
-}  // namespace
-
-namespace tsa {
-// Record a detail message for tsa_last_error() (entry points of other
-// translation units), and account for a kernel launch (every launch site).
-int note_error(int code, const char* msg) {
-  g_last_error = msg;
-  return code;
-}
-void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 }  // namespace tsa
 
 extern "C" {
@@ -163,7 +164,7 @@ int tsa_read_flags(uint32_t* flags, int clear, void* stream) {
 }
 
 int tsa_selftest_bounded_wait(void* stream) {
-  unsigned int* f = flags_ptr();
+  unsigned int* f = device_flags();
   if (f == nullptr) return fail(TSA_ERR_CUDA, "device flag word unavailable");
   TSA_LAUNCH(launch_bounded_wait_selftest(f, static_cast<cudaStream_t>(stream)), "self-test launch");
   return TSA_OK;
@@ -176,7 +177,7 @@ int qsa_indexer_scores(const void* q_idx, const void* k_idx, const float* w, con
                        int64_t q_begin, int64_t q_count, float* scores, int64_t width, void* stream) {
   SeqTable st;
   int64_t T;
-  int rc = make_seqs(cu_seqlens, num_seqs, &st, &T);
+  int rc = make_seq_table(cu_seqlens, num_seqs, &st, &T);
   if (rc) return rc;
   if ((rc = check_indexer_shape(H_I, d_I, groups, block_size))) return rc;
   if (q_begin < 0 || q_count < 0 || q_begin + q_count > T)
@@ -205,7 +206,7 @@ int qsa_indexer_scores(const void* q_idx, const void* k_idx, const float* w, con
     a.out = scores + (lo - q_begin) * groups * width;
     a.width = width;
       a.T_total = static_cast<int>(T);
-      a.flags = flags_ptr();
+      a.flags = device_flags();
     TSA_LAUNCH(launch_indexer(a, s), "indexer launch");
   }
   return TSA_OK;
@@ -231,7 +232,7 @@ int qsa_topk_from_scores(const float* scores, int64_t rows, int64_t width, int64
 size_t qsa_topk_workspace_size(const int32_t* cu_seqlens, int num_seqs, int groups, int block_size) {
   SeqTable st;
   int64_t T;
-  if (make_seqs(cu_seqlens, num_seqs, &st, &T) || groups < 1 || block_size < 1) return 0;
+  if (make_seq_table(cu_seqlens, num_seqs, &st, &T) || groups < 1 || block_size < 1) return 0;
   int64_t C = chunk_rows(st.max_len, groups, block_size);
   return static_cast<size_t>(C * groups * score_width(st.max_len, block_size) * sizeof(float));
 }
@@ -241,7 +242,7 @@ int qsa_topk(const void* q_idx, const void* k_idx, const float* w, const int32_t
              void* workspace, size_t workspace_bytes, void* stream) {
   SeqTable st;
   int64_t T;
-  int rc = make_seqs(cu_seqlens, num_seqs, &st, &T);
+  int rc = make_seq_table(cu_seqlens, num_seqs, &st, &T);
   if (rc) return rc;
   if ((rc = check_indexer_shape(H_I, d_I, groups, block_size))) return rc;
   if (topk < 1 || topk > kTopkMaxK) return fail(TSA_ERR_UNSUPPORTED, "topk=%d outside [1, %d]", topk, kTopkMaxK);
@@ -270,7 +271,7 @@ int qsa_topk(const void* q_idx, const void* k_idx, const float* w, const int32_t
       a.out = scratch;
       a.width = width;
       a.T_total = static_cast<int>(T);
-      a.flags = flags_ptr();
+      a.flags = device_flags();
       TSA_LAUNCH(launch_indexer(a, s), "indexer launch");
       TopkRows r;
       r.scores = scratch; r.ld = width; r.width = width;
@@ -299,7 +300,7 @@ int sparse_mla_fwd(const void* q, const void* kv, const int32_t* indices, const 
                    int H, int d_qk, int topk, float softmax_scale, void* out, float* lse, void* stream) {
   MlaFwdArgs a;
   int64_t T;
-  int rc = make_seqs(cu_seqlens, num_seqs, &a.st, &T);
+  int rc = make_seq_table(cu_seqlens, num_seqs, &a.st, &T);
   if (rc) return rc;
   if ((rc = check_mla(T, H, d_qk, topk))) return rc;
   if (T == 0) return TSA_OK;
@@ -311,7 +312,7 @@ int sparse_mla_fwd(const void* q, const void* kv, const int32_t* indices, const 
   a.scale_log2 = softmax_scale * kLog2e;
   a.out = static_cast<__nv_bfloat16*>(out);
   a.lse = lse;
-  a.flags = flags_ptr();
+  a.flags = device_flags();
   TSA_LAUNCH(launch_mla_fwd(a, d_qk, static_cast<cudaStream_t>(stream)), "mla fwd launch");
   return TSA_OK;
 }
@@ -341,11 +342,11 @@ size_t sparse_mla_bwd_workspace_size(int64_t T, int H, int d_qk, int topk) {
 
 int sparse_mla_bwd(const void* q, const void* kv, const int32_t* indices, const void* out, const float* lse,
                    const void* dout, const int32_t* cu_seqlens, int num_seqs, int H, int d_qk, int topk,
-                   float softmax_scale, void* dq, void* dkv, void* workspace, size_t workspace_bytes,
-                   void* stream) {
+                   float softmax_scale, void* dq, void* dkv, float* teacher, void* workspace,
+                   size_t workspace_bytes, void* stream) {
   MlaBwdArgs a;
   int64_t T;
-  int rc = make_seqs(cu_seqlens, num_seqs, &a.st, &T);
+  int rc = make_seq_table(cu_seqlens, num_seqs, &a.st, &T);
   if (rc) return rc;
   if ((rc = check_mla(T, H, d_qk, topk))) return rc;
   if (T == 0) return TSA_OK;
@@ -379,7 +380,7 @@ int sparse_mla_bwd(const void* q, const void* kv, const int32_t* indices, const 
     const int64_t kp = mla_kp(topk);
     auto* stage = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(workspace) + dkv_bytes + dlt_bytes);
     a.kp = static_cast<int>(kp);
-    a.flags = flags_ptr();
+    a.flags = device_flags();
     a.p_out = stage;
     a.ds_out = stage + chunk * H * kp;
     MlaBwdTcArgs b;
@@ -390,19 +391,96 @@ int sparse_mla_bwd(const void* q, const void* kv, const int32_t* indices, const 
     b.idx = indices;
     b.T = a.T; b.D = d_qk; b.topk = topk; b.kp = a.kp;
     b.dkv_acc = dkv_acc;
-    b.flags = flags_ptr();
+    b.flags = device_flags();
     b.st = a.st;
     for (int64_t q0 = 0; q0 < T; q0 += chunk) {
       const int nq = static_cast<int>(std::min(chunk, T - q0));
       a.q0 = b.q0 = static_cast<int>(q0);
       TSA_LAUNCH(launch_mla_bwd_pds_tc(a, d_qk, nq, s), "mla bwd recompute launch");
+      if (teacher != nullptr)
+        TSA_LAUNCH(launch_mla_teacher_from_p(a.p_out, nq, H, a.kp, topk, a.q0, teacher, s), "teacher launch");
       TSA_LAUNCH(launch_mla_bwd_dq_tc(a, d_qk, nq, s), "mla bwd dq launch");
       TSA_LAUNCH(launch_mla_bwd_dkv_tc(b, nq, s), "mla bwd dkv launch");
     }
   } else {
+    if (teacher != nullptr) {
+      TSA_CHECK_CUDA(cudaMemsetAsync(teacher, 0, static_cast<size_t>(T) * topk * sizeof(float), s), "memset");
+      a.teacher = teacher;
+    }
     TSA_LAUNCH(launch_mla_bwd(a, d_qk, s), "mla bwd launch");
   }
   TSA_LAUNCH(launch_f32_to_bf16(dkv_acc, static_cast<__nv_bfloat16*>(dkv), T * d_qk, s), "convert launch");
+  return TSA_OK;
+}
+
+// ---------------------------------------------------------------- indexer training
+
+static int check_indexer_sel(int64_t T, int H_I, int d_I, int topk) {
+  if (!indexer_sel_supported(H_I, d_I))
+    return fail(TSA_ERR_UNSUPPORTED, "H_I=%d d_I=%d: need d_I = 128 and 1 <= H_I <= 128", H_I, d_I);
+  if (topk < 1 || topk > kTopkMaxK) return fail(TSA_ERR_UNSUPPORTED, "topk=%d outside [1, %d]", topk, kTopkMaxK);
+  if (T > 0x7fffffffLL / 128) return fail(TSA_ERR_UNSUPPORTED, "T too large");
+  return TSA_OK;
+}
+
+int qsa_indexer_kl(const void* q_idx, const void* k_idx, const float* w, const int32_t* cu_seqlens, int num_seqs,
+                   int H_I, int d_I, float score_scale, const int32_t* indices, int topk, const float* teacher,
+                   float* loss, float* dscore, void* stream) {
+  IndexerSelArgs a;
+  memset(static_cast<void*>(&a), 0, sizeof(a) - sizeof(SeqTable));
+  int64_t T;
+  int rc = make_seq_table(cu_seqlens, num_seqs, &a.st, &T);
+  if (rc) return rc;
+  if ((rc = check_indexer_sel(T, H_I, d_I, topk))) return rc;
+  if (T == 0) return TSA_OK;
+  if (!q_idx || !k_idx || !w || !indices || !teacher || !loss || !dscore)
+    return fail(TSA_ERR_INVALID_ARG, "null tensor pointer");
+  a.w = w;
+  a.idx = indices;
+  a.teacher = teacher;
+  a.loss = loss;
+  a.dscore_out = dscore;
+  a.T = static_cast<int>(T); a.H_I = H_I; a.topk = topk;
+  a.score_scale = score_scale;
+  a.flags = device_flags();
+  TSA_LAUNCH(launch_indexer_sel(a, q_idx, k_idx, false, static_cast<cudaStream_t>(stream)), "indexer kl launch");
+  return TSA_OK;
+}
+
+size_t qsa_indexer_bwd_workspace_size(int64_t T, int d_I) {
+  if (T < 0 || d_I < 1) return 0;
+  return align256(static_cast<size_t>(T) * d_I * sizeof(float));
+}
+
+int qsa_indexer_bwd(const void* q_idx, const void* k_idx, const float* w, const int32_t* cu_seqlens, int num_seqs,
+                    int H_I, int d_I, float score_scale, const int32_t* indices, int topk, const float* dscore,
+                    void* dq_idx, void* dk_idx, float* dw, void* workspace, size_t workspace_bytes, void* stream) {
+  IndexerSelArgs a;
+  memset(static_cast<void*>(&a), 0, sizeof(a) - sizeof(SeqTable));
+  int64_t T;
+  int rc = make_seq_table(cu_seqlens, num_seqs, &a.st, &T);
+  if (rc) return rc;
+  if ((rc = check_indexer_sel(T, H_I, d_I, topk))) return rc;
+  if (T == 0) return TSA_OK;
+  if (!q_idx || !k_idx || !w || !indices || !dscore || !dq_idx || !dk_idx || !dw)
+    return fail(TSA_ERR_INVALID_ARG, "null tensor pointer");
+  const size_t need = qsa_indexer_bwd_workspace_size(T, d_I);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(TSA_ERR_WORKSPACE, "workspace %zu bytes < %zu", workspace_bytes, need);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* dk_acc = static_cast<float*>(workspace);
+  TSA_CHECK_CUDA(cudaMemsetAsync(dk_acc, 0, static_cast<size_t>(T) * d_I * sizeof(float), s), "memset");
+  a.w = w;
+  a.idx = indices;
+  a.dscore = dscore;
+  a.dq = static_cast<__nv_bfloat16*>(dq_idx);
+  a.dw = dw;
+  a.dk_acc = dk_acc;
+  a.T = static_cast<int>(T); a.H_I = H_I; a.topk = topk;
+  a.score_scale = score_scale;
+  a.flags = device_flags();
+  TSA_LAUNCH(launch_indexer_sel(a, q_idx, k_idx, true, s), "indexer bwd launch");
+  TSA_LAUNCH(launch_f32_to_bf16(dk_acc, static_cast<__nv_bfloat16*>(dk_idx), T * d_I, s), "convert launch");
   return TSA_OK;
 }
 
@@ -418,35 +496,79 @@ static int check_gqa(int64_t T, int Hq, int Hkv, int d, int block_size, int nsel
   return TSA_OK;
 }
 
+// Workspace of the tcgen05 forward: the inverted selections and, per selection
+// slot (t, g, j), the normalised partial output of its block (fp32, G x d) and
+// its log2-sum-exp.
+static size_t gqa_ws_align(size_t x) { return (x + 255) & ~size_t(255); }
+
+static size_t gqa_inv_bytes(size_t t, int Hkv, int nsel) {
+  const size_t nb = t * Hkv + 1;
+  return gqa_ws_align(t * Hkv * nsel * sizeof(int)) + 4 * gqa_ws_align((nb + 1) * sizeof(int));
+}
+
+size_t sparse_gqa_fwd_workspace_size(int64_t T, int Hq, int Hkv, int d, int nsel) {
+  if (T < 0 || Hq < 1 || Hkv < 1 || d < 1 || nsel < 1) return 0;
+  const size_t t = static_cast<size_t>(T);
+  return gqa_inv_bytes(t, Hkv, nsel) + gqa_ws_align(t * Hq * nsel * d * sizeof(float)) +
+         gqa_ws_align(t * Hq * nsel * sizeof(float));
+}
+
+// Per-sequence first global block, and the total.
+static int gqa_block_bases(const SeqTable& st, int block_size, int* base) {
+  int nblk = 0;
+  for (int i = 0; i < st.num_seqs; ++i) {
+    base[i] = nblk;
+    nblk += (st.cu[i + 1] - st.cu[i] + block_size - 1) / block_size;
+  }
+  base[st.num_seqs] = nblk;
+  return nblk;
+}
+
 int sparse_gqa_fwd(const void* q, const void* k, const void* v, const int32_t* block_indices,
                    const int32_t* cu_seqlens, int num_seqs, int Hq, int Hkv, int d, int block_size, int nsel,
-                   float softmax_scale, void* out, float* lse, void* stream) {
-  GqaArgs a;
-  memset(static_cast<void*>(&a), 0, sizeof(a) - sizeof(SeqTable));
+                   float softmax_scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+  GqaTcArgs a;
+  memset(static_cast<void*>(&a), 0, sizeof(a));
   int64_t T;
-  int rc = make_seqs(cu_seqlens, num_seqs, &a.st, &T);
+  int rc = make_seq_table(cu_seqlens, num_seqs, &a.st, &T);
   if (rc) return rc;
   if ((rc = check_gqa(T, Hq, Hkv, d, block_size, nsel))) return rc;
+  if (T * Hkv * nsel > 0x7fffffffLL) return fail(TSA_ERR_UNSUPPORTED, "T * Hkv * nsel beyond 2^31-1");
   if (T == 0) return TSA_OK;
   if (!q || !k || !v || !block_indices || !out || !lse) return fail(TSA_ERR_INVALID_ARG, "null tensor pointer");
+  const size_t need = sparse_gqa_fwd_workspace_size(T, Hq, Hkv, d, nsel);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(TSA_ERR_WORKSPACE, "workspace %zu bytes < %zu", workspace_bytes, need);
+  a.nblk = gqa_block_bases(a.st, block_size, a.blk_base);
+  const size_t t = static_cast<size_t>(T);
+  const size_t nb = t * Hkv + 1;
+  char* w = static_cast<char*>(workspace);
+  auto take = [&](size_t bytes) { char* p = w; w += gqa_ws_align(bytes); return p; };
+  a.list = reinterpret_cast<int*>(take(t * Hkv * nsel * sizeof(int)));
+  a.cnt = reinterpret_cast<int*>(take((nb + 1) * sizeof(int)));
+  a.off = reinterpret_cast<int*>(take((nb + 1) * sizeof(int)));
+  a.cur = reinterpret_cast<int*>(take((nb + 1) * sizeof(int)));
+  a.choff = reinterpret_cast<int*>(take((nb + 1) * sizeof(int)));
+  a.part_o = reinterpret_cast<float*>(take(t * Hq * nsel * d * sizeof(float)));
+  a.part_l = reinterpret_cast<float*>(take(t * Hq * nsel * sizeof(float)));
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.k = static_cast<const __nv_bfloat16*>(k);
   a.v = static_cast<const __nv_bfloat16*>(v);
   a.blk = block_indices;
-  a.T = static_cast<int>(T); a.Hq = Hq; a.Hkv = Hkv; a.G = Hq / Hkv; a.nsel = nsel;
+  a.T = static_cast<int>(T); a.Hq = Hq; a.Hkv = Hkv; a.G = Hq / Hkv; a.nsel = nsel; a.bs = block_size; a.d = d;
   a.scale = softmax_scale;
   a.scale_log2 = softmax_scale * kLog2e;
   a.out = static_cast<__nv_bfloat16*>(out);
   a.lse = lse;
-  a.flags = flags_ptr();
-  TSA_LAUNCH(launch_gqa(a, block_size, d, static_cast<cudaStream_t>(stream)), "gqa fwd launch");
+  a.flags = device_flags();
+  TSA_LAUNCH(launch_gqa_fwd_tc(a, static_cast<cudaStream_t>(stream)), "gqa fwd launch");
   return TSA_OK;
 }
 
 // Workspace of the key-centric backward: fp32 dQ, dK, dV accumulators, Delta,
 // the inverted selections and their offsets.  At most one block per token, so
 // T * Hkv bounds the number of (block, group) lists.
-static size_t gqa_ws_align(size_t x) { return (x + 255) & ~size_t(255); }
 
 size_t sparse_gqa_bwd_workspace_size(int64_t T, int Hq, int Hkv, int d, int nsel) {
   if (T < 0 || Hq < 1 || Hkv < 1 || d < 1 || nsel < 1) return 0;
@@ -461,12 +583,13 @@ int sparse_gqa_bwd(const void* q, const void* k, const void* v, const int32_t* b
                    const float* lse, const void* dout, const int32_t* cu_seqlens, int num_seqs, int Hq, int Hkv,
                    int d, int block_size, int nsel, float softmax_scale, void* dq, void* dk, void* dv,
                    void* workspace, size_t workspace_bytes, void* stream) {
-  GqaKvArgs a;
+  GqaTcArgs a;
   memset(static_cast<void*>(&a), 0, sizeof(a));
   int64_t T;
-  int rc = make_seqs(cu_seqlens, num_seqs, &a.st, &T);
+  int rc = make_seq_table(cu_seqlens, num_seqs, &a.st, &T);
   if (rc) return rc;
   if ((rc = check_gqa(T, Hq, Hkv, d, block_size, nsel))) return rc;
+  if (T * Hkv * nsel > 0x7fffffffLL) return fail(TSA_ERR_UNSUPPORTED, "T * Hkv * nsel beyond 2^31-1");
   if (T == 0) return TSA_OK;
   if (!q || !k || !v || !block_indices || !out || !lse || !dout || !dq || !dk || !dv)
     return fail(TSA_ERR_INVALID_ARG, "null tensor pointer");
@@ -474,13 +597,7 @@ int sparse_gqa_bwd(const void* q, const void* k, const void* v, const int32_t* b
   if (workspace == nullptr || workspace_bytes < need)
     return fail(TSA_ERR_WORKSPACE, "workspace %zu bytes < %zu", workspace_bytes, need);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // first global block of every sequence
-  int nblk = 0;
-  for (int i = 0; i < a.st.num_seqs; ++i) {
-    a.blk_base[i] = nblk;
-    nblk += (a.st.cu[i + 1] - a.st.cu[i] + block_size - 1) / block_size;
-  }
-  a.blk_base[a.st.num_seqs] = nblk;
+  a.nblk = gqa_block_bases(a.st, block_size, a.blk_base);
   const size_t t = static_cast<size_t>(T);
   const size_t nb = t * Hkv + 1;
   char* w = static_cast<char*>(workspace);
@@ -506,15 +623,14 @@ int sparse_gqa_bwd(const void* q, const void* k, const void* v, const int32_t* b
   a.blk = block_indices;
   a.lse_in = lse;
   a.dlt = dlt;
-  a.T = static_cast<int>(T); a.Hq = Hq; a.Hkv = Hkv; a.G = Hq / Hkv; a.nsel = nsel; a.bs = block_size;
+  a.T = static_cast<int>(T); a.Hq = Hq; a.Hkv = Hkv; a.G = Hq / Hkv; a.nsel = nsel; a.bs = block_size; a.d = d;
   a.scale = softmax_scale;
   a.scale_log2 = softmax_scale * kLog2e;
-  a.nblk = nblk;
   a.dq_acc = dq_acc;
   a.dk_acc = dk_acc;
   a.dv_acc = dv_acc;
-  a.flags = flags_ptr();
-  TSA_LAUNCH(launch_gqa_bwd_kv(a, d, s), "gqa bwd launch");
+  a.flags = device_flags();
+  TSA_LAUNCH(launch_gqa_bwd_tc(a, s), "gqa bwd launch");
   TSA_LAUNCH(launch_f32_to_bf16(dq_acc, static_cast<__nv_bfloat16*>(dq), (int64_t)(t * Hq * d), s), "convert");
   TSA_LAUNCH(launch_f32_to_bf16(dk_acc, static_cast<__nv_bfloat16*>(dk), (int64_t)(t * Hkv * d), s), "convert");
   TSA_LAUNCH(launch_f32_to_bf16(dv_acc, static_cast<__nv_bfloat16*>(dv), (int64_t)(t * Hkv * d), s), "convert");

@@ -1,0 +1,876 @@
+// Block Sparse-GQA forward and backward on tcgen05 (TMEM accumulators, TMA
+// tile::gather4 staging, mbarrier pipelines), key-centric.
+//
+// Megatron-LM issue #7060 "Add trainable QSA sparse attention with a TileLang
+// backend" ("Describe the solution you'd like": Sparse-GQA forward and backward
+// kernels over exact block top-k selections, BSHD and packed THD).
+//
+// A query selects nsel blocks per kv group, each a run of block_size keys it
+// attends causally.  Gathered per query, every (query, group, block) triple
+// moves a block_size x d tile of K and of V for only G = Hq / Hkv heads of the
+// query (8 bytes of gather per flop at G = 8): the work is bound by row copies,
+// and the G rows of one query fill at most 16 of the 128 rows of an MMA.
+// Inverted, it is dense: the selections are turned into one list per (block,
+// group) of the queries that chose that block (count, scan, fill), and a CTA
+// takes a chunk of a list.  The block's K and V are staged once; the chunk's
+// queries pass through in batches of 128 (query, head) rows -- 128 / G queries
+// of G heads -- so every MMA is M = 128 rows x N = 64 keys:
+//
+//   forward, per batch:   S = Q K^T (TMEM), P = exp(scale S - m) on the causal
+//                         keys (rows on TMEM lanes: one thread per row, the row
+//                         maximum and sum never leave the thread), P to TMEM as
+//                         bf16, O = P V (A operand read from TMEM);
+//                         the normalised partial O / l and its log-sum-exp go to
+//                         the slot (query, group, j) of the selection in the
+//                         caller's workspace;
+//   combine:              per (query, head), the partials of the selected
+//                         blocks are merged in slot order: the result does not
+//                         depend on the order of the inverted lists, so the
+//                         forward replays bit for bit;
+//   backward, per batch:  S = Q K^T and dP = dO V^T (TMEM), P = exp(scale S - lse)
+//                         and dS = scale P (dP - Delta) written to shared memory
+//                         in bf16, then dV^T += dO^T P and dK^T += Q^T dS
+//                         (accumulated in TMEM over the whole chunk, reduced once
+//                         per chunk) and dQ^T = K^T dS^T, whose channels sit on
+//                         TMEM lanes so that each warp's fp32 reductions into the
+//                         dQ accumulator cover whole 128-byte lines.
+//
+// Head dimension 64 runs as 128 with channels 64..127 zero in shared memory,
+// and blocks of 32 keys as 64-key tiles whose upper half is masked: the MMA
+// shapes stay M = 128, N = 64 / 128.
+#include <algorithm>
+
+#include "kernels.cuh"
+#include "tc.cuh"
+
+namespace tsa {
+
+cudaError_t make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                              uint32_t box_cols);
+
+namespace {
+
+constexpr int GT_ROWS = 128;              // (query, head) rows per batch = MMA M
+constexpr int GT_KEYS = 64;               // key tile = MMA N (a 32-key block is padded)
+constexpr int GT_DP = 128;                // head dimension in shared memory (64 is zero padded)
+constexpr int GT_THREADS = 192;           // warps 0-3 rows / drain, warp 4 producer, warp 5 MMA
+constexpr int GT_QBOX = GT_ROWS * 128;    // 128 rows x 64 channels bf16: 16 KB
+constexpr int GT_QT = 2 * GT_QBOX;        // a Q (or dO) batch: 32 KB
+constexpr int GT_KBOX = GT_KEYS * 128;    // 64 keys x 64 channels: 8 KB
+constexpr int GT_KT = 2 * GT_KBOX;        // the K (or V) tile: 16 KB
+constexpr int GT_PT = GT_ROWS * 128;      // P or dS: 128 rows x 64 keys bf16: 16 KB
+
+// forward: K, V, two Q buffers, two row tables
+constexpr int GF_OFF_K = 0;
+constexpr int GF_OFF_V = GF_OFF_K + GT_KT;
+constexpr int GF_OFF_Q = GF_OFF_V + GT_KT;
+constexpr int GF_OFF_TAB = GF_OFF_Q + 2 * GT_QT;       // int [2][128]: selection entry of each row, -1 = none
+constexpr int GF_OFF_BAR = GF_OFF_TAB + 2 * GT_ROWS * 4;
+constexpr int GF_SMEM = 1024 + GF_OFF_BAR + 256;
+// TMEM (forward): S 64 columns, P 32 (bf16 pairs), O 128
+constexpr int GF_T_S = 0, GF_T_P = 64, GF_T_O = 128, GF_TMEM = 256;
+
+__device__ __forceinline__ int gt_block_seq(const GqaTcArgs& a, int gb) {
+  int lo = 0, hi = a.st.num_seqs - 1;  // last sequence whose first block is <= gb
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (a.blk_base[mid] <= gb) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Byte offset of 16-byte chunk c (0..7) of row r inside a 128-byte-swizzled box.
+__device__ __forceinline__ uint32_t sw128(int r, int c) {
+  return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ void red_f32(float* p, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- selection inversion
+
+// Selection entries e = (t, g, j) that name a causal block of t's sequence:
+// count them per (global block, group), or (FILL) append e itself (the flat
+// index (t * Hkv + g) * nsel + j, which is also the entry's partial slot) to
+// that list.  Entries outside the sequence raise TSA_FLAG_INDEX_RANGE and are dropped.
+template <bool FILL>
+__global__ void gqa_tc_inv_kernel(const __grid_constant__ GqaTcArgs a) {
+  const int64_t total = static_cast<int64_t>(a.T) * a.Hkv * a.nsel;
+  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int b = __ldg(a.blk + e);
+    if (b < 0) continue;
+    const int t = static_cast<int>(e / (static_cast<int64_t>(a.Hkv) * a.nsel));
+    const int g = static_cast<int>((e / a.nsel) % a.Hkv);
+    const int s = seq_of(a.st, t);
+    const int p = t - a.st.cu[s];
+    const int n = a.st.cu[s + 1] - a.st.cu[s];
+    if (static_cast<int64_t>(b) * a.bs >= n) {
+      if (!FILL) raise_flag(a.flags, TSA_FLAG_INDEX_RANGE);
+      continue;
+    }
+    if (static_cast<int64_t>(b) * a.bs > p) continue;  // not a causal block of this query
+    const int idx = (a.blk_base[s] + b) * a.Hkv + g;
+    if (!FILL) {
+      atomicAdd(a.cnt + idx, 1);
+    } else {
+      const int pos = atomicAdd(a.cur + idx, 1);
+      a.list[a.off[idx] + pos] = static_cast<int>(e);
+    }
+  }
+}
+
+// Exclusive scans of the list sizes (offsets) and of the chunks per list;
+// clears the fill cursors.  One CTA of 1024 threads.
+__global__ void __launch_bounds__(1024) gqa_tc_scan_kernel(const __grid_constant__ GqaTcArgs a, int nB, int chunk) {
+  __shared__ int warp_tot[2][32];
+  __shared__ int carry[2];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x < 2) carry[threadIdx.x] = 0;
+  __syncthreads();
+  for (int base = 0; base < nB; base += 1024) {
+    const int i = base + threadIdx.x;
+    const int c = i < nB ? a.cnt[i] : 0;
+    const int ch = (c + chunk - 1) / chunk;
+    if (i < nB) a.cur[i] = 0;
+    int x = c, y = ch;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int xv = __shfl_up_sync(0xffffffffu, x, o), yv = __shfl_up_sync(0xffffffffu, y, o);
+      if (lane >= o) { x += xv; y += yv; }
+    }
+    if (lane == 31) { warp_tot[0][warp] = x; warp_tot[1][warp] = y; }
+    __syncthreads();
+    int px = carry[0], py = carry[1];
+    for (int w = 0; w < warp; ++w) { px += warp_tot[0][w]; py += warp_tot[1][w]; }
+    if (i < nB) { a.off[i] = px + x - c; a.choff[i] = py + y - ch; }
+    __syncthreads();
+    if (threadIdx.x == 1023) { carry[0] = px + x; carry[1] = py + y; }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) { a.off[nB] = carry[0]; a.choff[nB] = carry[1]; }
+}
+
+// The chunk of CTA c: its list (block, group) and entry range.  Returns false if c is past the last chunk.
+struct GtChunk {
+  int g, s0, n, kbase, e0, e1;
+};
+__device__ __forceinline__ bool gt_chunk(const GqaTcArgs& a, int c, int chunk, GtChunk& ck) {
+  const int nB = a.nblk * a.Hkv;
+  if (c >= a.choff[nB]) return false;
+  int lo = 0, hi = nB - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (a.choff[mid] <= c) lo = mid; else hi = mid - 1;
+  }
+  const int gb = lo / a.Hkv;
+  ck.g = lo % a.Hkv;
+  const int sq = gt_block_seq(a, gb);
+  ck.s0 = a.st.cu[sq];
+  ck.n = a.st.cu[sq + 1] - ck.s0;
+  ck.kbase = (gb - a.blk_base[sq]) * a.bs;
+  ck.e0 = a.off[lo] + (c - a.choff[lo]) * chunk;
+  ck.e1 = min(a.off[lo + 1], ck.e0 + chunk);
+  return true;
+}
+
+// ---------------------------------------------------------------- forward: partials
+
+// Producer helper: gather the block's 64 key rows (K or V, [T * Hkv, d] view)
+// into a 64 x 128-channel tile; rows past the block or the sequence repeat the
+// block's first row (masked by the consumers).
+__device__ __forceinline__ void gt_gather_kv(uint32_t dst, const CUtensorMap* map, uint64_t* bar, const GqaTcArgs& a,
+                                             const GtChunk& ck, int lane) {
+  if (lane < 16) {
+    int r[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int key = 4 * lane + i;
+      const int kp = ck.kbase + key;
+      const bool ok = key < a.bs && kp < ck.n;
+      r[i] = (ck.s0 + (ok ? kp : ck.kbase)) * a.Hkv + ck.g;
+    }
+    tc::tma_gather4(dst + 4 * lane * 128, map, bar, 0, r[0], r[1], r[2], r[3]);
+    if (a.d == 128) tc::tma_gather4(dst + GT_KBOX + 4 * lane * 128, map, bar, 64, r[0], r[1], r[2], r[3]);
+  }
+}
+
+// Producer helpers: the rows of one batch (entries eb .. eb + qb of the chunk,
+// G heads each); lane l owns rows 4l .. 4l+3.  gt_batch_rows computes their
+// source rows of the [T * Hq, d] view (and, if tab is given, records each row's
+// selection entry (t * Hkv + g) * nsel + j, or -1); gt_gather_batch issues the
+// gathers into a 128-row Q (or dO) buffer.
+__device__ __forceinline__ void gt_batch_rows(const GqaTcArgs& a, const GtChunk& ck, int eb, int* tab, int lane,
+                                              int (&r)[4]) {
+  const int G = a.G, qb = GT_ROWS / G;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int row = 4 * lane + i;
+    const int qi = row / G, hh = row - qi * G;
+    const int ei = eb + qi;
+    const bool ok = qi < qb && ei < ck.e1;
+    const int e = ok ? __ldg(a.list + ei) : -1;
+    if (tab != nullptr) tab[row] = e;
+    r[i] = (ok ? e / (a.Hkv * a.nsel) : 0) * a.Hq + ck.g * G + hh;
+  }
+}
+__device__ __forceinline__ void gt_gather_batch(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int d,
+                                                const int (&r)[4], int lane) {
+  tc::tma_gather4(dst + 4 * lane * 128, map, bar, 0, r[0], r[1], r[2], r[3]);
+  if (d == 128) tc::tma_gather4(dst + GT_QBOX + 4 * lane * 128, map, bar, 64, r[0], r[1], r[2], r[3]);
+}
+
+__global__ void __launch_bounds__(GT_THREADS, 2)
+    gqa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ GqaTcArgs a, int chunk) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  unsigned char* gbase = smem_raw + (base - raw);
+  const uint32_t sK = base + GF_OFF_K, sV = base + GF_OFF_V, sQ = base + GF_OFF_Q;
+  int* tab = reinterpret_cast<int*>(gbase + GF_OFF_TAB);  // [2][128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + GF_OFF_BAR);
+  uint64_t* kvfull = bars;        // [1]
+  uint64_t* qfull = bars + 1;     // [2]
+  uint64_t* qempty = qfull + 2;   // [2] S MMA done with the Q buffer and rows done with its table
+  uint64_t* sfull = qempty + 2;   // [1]
+  uint64_t* sempty = sfull + 1;   // [1] rows read S (4 warps)
+  uint64_t* pfull = sempty + 1;   // [1] rows wrote P (4 warps)
+  uint64_t* pempty = pfull + 1;   // [1] PV done with P
+  uint64_t* ofull = pempty + 1;   // [1]
+  uint64_t* oempty = ofull + 1;   // [1] rows read O (4 warps)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(oempty + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  GtChunk ck;
+  if (!gt_chunk(a, blockIdx.x, chunk, ck)) return;  // uniform
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int qb = GT_ROWS / a.G;
+  const int nbatch = (ck.e1 - ck.e0 + qb - 1) / qb;
+  int issued = 0;  // producer: batches whose gathers were issued
+
+  if (tid == 0) {
+    tc::mbar_init(kvfull, 1);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&qfull[i], 1);
+      tc::mbar_init(&qempty[i], 1 + 4);  // the MMA commit and the four row warps
+    }
+    tc::mbar_init(sfull, 1);
+    tc::mbar_init(sempty, 4);
+    tc::mbar_init(pfull, 4);
+    tc::mbar_init(pempty, 1);
+    tc::mbar_init(ofull, 1);
+    tc::mbar_init(oempty, 4);
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  if (a.d == 64) {
+    // channels 64..127 of every operand tile are never loaded: zero them once
+    for (int i = tid; i < GT_KBOX / 16; i += GT_THREADS) {
+      reinterpret_cast<uint4*>(gbase + GF_OFF_K + GT_KBOX)[i] = make_uint4(0u, 0u, 0u, 0u);
+      reinterpret_cast<uint4*>(gbase + GF_OFF_V + GT_KBOX)[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    for (int i = tid; i < GT_QBOX / 16; i += GT_THREADS) {
+      reinterpret_cast<uint4*>(gbase + GF_OFF_Q + GT_QBOX)[i] = make_uint4(0u, 0u, 0u, 0u);
+      reinterpret_cast<uint4*>(gbase + GF_OFF_Q + GT_QT + GT_QBOX)[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    tc::fence_proxy_async_smem();
+  }
+  if (warp == 5) tc::tmem_alloc(tmem_slot, GF_TMEM);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t kv_bytes = (a.d == 128 ? 2 : 1) * 2 * GT_KBOX;
+  const uint32_t q_bytes = (a.d == 128 ? 2 : 1) * GT_QBOX;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tc::prefetch_tmap(&tm_q);
+      tc::prefetch_tmap(&tm_k);
+      tc::prefetch_tmap(&tm_v);
+      tc::mbar_arrive_expect_tx(kvfull, kv_bytes);
+    }
+    __syncwarp();
+    gt_gather_kv(sK, &tm_k, kvfull, a, ck, lane);
+    gt_gather_kv(sV, &tm_v, kvfull, a, ck, lane);
+    bool ok = true;
+    for (int i = 0; i < nbatch; ++i) {
+      const int buf = i & 1;
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&qempty[buf], ((i >> 1) & 1) ^ 1u, abort_flag))) {
+        ok = false;
+        break;
+      }
+      // the row table is read by the row warps after they see qfull: every lane
+      // writes its rows' entries before lane 0's arrival releases them
+      int r[4];
+      gt_batch_rows(a, ck, ck.e0 + i * qb, tab + buf * GT_ROWS, lane, r);
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_expect_tx(&qfull[buf], q_bytes);
+      __syncwarp();
+      gt_gather_batch(sQ + buf * GT_QT, &tm_q, &qfull[buf], a.d, r, lane);
+      issued = i + 1;
+    }
+    if (!ok) *abort_flag = 1;
+    if (lane == 0) {  // copies still in flight land before the CTA exits (bounded by time only)
+      volatile int keep_waiting = 0;
+      (void)tc::mbar_wait(kvfull, 0, &keep_waiting);
+      for (int g = issued > 2 ? issued - 2 : 0; g < issued; ++g)
+        (void)tc::mbar_wait(&qfull[g & 1], (g >> 1) & 1, &keep_waiting);
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = tc::idesc_bf16_f32(GT_ROWS, GT_KEYS);
+      constexpr uint32_t id_o = tc::idesc_bf16_f32_bmn(GT_ROWS, GT_DP);
+      bool ok = tc::mbar_wait(kvfull, 0, abort_flag);
+      for (int i = 0; ok && i < nbatch; ++i) {
+        const int buf = i & 1;
+        const uint32_t ph = i & 1;
+        if (!tc::mbar_wait(&qfull[buf], (i >> 1) & 1, abort_flag) ||
+            (i > 0 && !tc::mbar_wait(sempty, ph ^ 1u, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t qt = sQ + buf * GT_QT;
+#pragma unroll
+        for (int ks = 0; ks < GT_DP / 16; ++ks) {
+          const int c = ks >> 2, kk = ks & 3;
+          tc::mma_bf16_ss(tmem + GF_T_S, tc::desc_sw128(qt + c * GT_QBOX + kk * 32),
+                          tc::desc_sw128(sK + c * GT_KBOX + kk * 32), id_s, ks > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(sfull);
+        tc::mma_commit(&qempty[buf]);
+        if (!tc::mbar_wait(pfull, ph, abort_flag) || (i > 0 && !tc::mbar_wait(oempty, ph ^ 1u, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+#pragma unroll
+        for (int ks = 0; ks < GT_KEYS / 16; ++ks)
+          tc::mma_bf16_ts(tmem + GF_T_O, tmem + GF_T_P + ks * 8, tc::desc_sw128_mn(sV + ks * 2048, GT_KBOX), id_o,
+                          ks > 0 ? 1u : 0u);
+        tc::mma_commit(pempty);
+        tc::mma_commit(ofull);
+      }
+      if (!ok) *abort_flag = 1;
+    }
+  } else {
+    // ------------------------------------------------------------ rows (warps 0-3): softmax and partials
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const int row = warp * 32 + lane;
+    const int hh = row % a.G;
+    for (int i = 0; i < nbatch; ++i) {
+      const int buf = i & 1;
+      const uint32_t ph = i & 1;
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&qfull[buf], (i >> 1) & 1, abort_flag)) ||
+          !__all_sync(0xffffffffu, tc::mbar_wait(sfull, ph, abort_flag))) {
+        *abort_flag = 1;
+        break;
+      }
+      tc::fence_after_sync();
+      const int e = tab[buf * GT_ROWS + row];  // the producer wrote it before arriving on qfull
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&qempty[buf]);  // the table may be rewritten for batch i + 2
+      const int t = e >= 0 ? e / (a.Hkv * a.nsel) : 0;
+      const int p = t - ck.s0;
+      // causal keys of this row in the tile: key c < lim
+      const int lim = e < 0 ? 0 : min(min(a.bs, ck.n - ck.kbase), p - ck.kbase + 1);
+      uint32_t sr[GT_KEYS];
+      __syncwarp();
+      tc::tmem_ld32(tmem + lane_base + GF_T_S, sr);
+      tc::tmem_ld32(tmem + lane_base + GF_T_S + 32, sr + 32);
+      tc::tmem_ld_wait();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(sempty);
+      float m = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < GT_KEYS; ++c)
+        if (c < lim) m = fmaxf(m, __uint_as_float(sr[c]) * a.scale_log2);
+      float l = 0.f;
+      uint32_t pk[GT_KEYS / 2];
+#pragma unroll
+      for (int c = 0; c < GT_KEYS; c += 2) {
+        const float p0 = c < lim ? exp2f(__uint_as_float(sr[c]) * a.scale_log2 - m) : 0.f;
+        const float p1 = c + 1 < lim ? exp2f(__uint_as_float(sr[c + 1]) * a.scale_log2 - m) : 0.f;
+        l += p0 + p1;
+        pk[c / 2] = pack_bf16(p0, p1);
+      }
+      // P -> TMEM once PV of the previous batch is done with it
+      if (i > 0 && !__all_sync(0xffffffffu, tc::mbar_wait(pempty, ph ^ 1u, abort_flag))) {
+        *abort_flag = 1;
+        break;
+      }
+      tc::fence_after_sync();
+      __syncwarp();
+      tc::tmem_st32(tmem + lane_base + GF_T_P, pk);
+      tc::tmem_st_wait();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(pfull);
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(ofull, ph, abort_flag))) {
+        *abort_flag = 1;
+        break;
+      }
+      tc::fence_after_sync();
+      // partial O / l and its log2-sum-exp into the selection slot of this row
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      float* dst = e >= 0 ? a.part_o + ((int64_t)e * a.G + hh) * a.d : nullptr;
+#pragma unroll 1
+      for (int cb = 0; cb < a.d / 32; ++cb) {
+        uint32_t r[32];
+        __syncwarp();
+        tc::tmem_ld32(tmem + lane_base + GF_T_O + cb * 32, r);
+        tc::tmem_ld_wait();
+        if (dst != nullptr) {
+#pragma unroll
+          for (int k = 0; k < 32; k += 4)
+            *reinterpret_cast<float4*>(dst + cb * 32 + k) =
+                make_float4(__uint_as_float(r[k]) * inv, __uint_as_float(r[k + 1]) * inv,
+                            __uint_as_float(r[k + 2]) * inv, __uint_as_float(r[k + 3]) * inv);
+        }
+      }
+      if (e >= 0) a.part_l[(int64_t)e * a.G + hh] = l > 0.f ? m + log2f(l) : -INFINITY;
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(oempty);
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (*abort_flag && tid == 0) raise_flag(a.flags, TSA_FLAG_TIMEOUT);
+  if (warp == 5) {
+    __syncwarp();
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, GF_TMEM);
+  }
+}
+
+// Merge of the partials: one warp per (query, head), the selected blocks in
+// slot order (fixed, so the result is bit-identical across runs).
+__global__ void __launch_bounds__(256) gqa_combine_kernel(const __grid_constant__ GqaTcArgs a) {
+  const int64_t rowid = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (rowid >= (int64_t)a.T * a.Hq) return;
+  const int t = static_cast<int>(rowid / a.Hq), h = static_cast<int>(rowid % a.Hq);
+  const int g = h / a.G, hh = h % a.G;
+  const int s = seq_of(a.st, t);
+  const int p = t - a.st.cu[s];
+  const int n = a.st.cu[s + 1] - a.st.cu[s];
+  const int32_t* brow = a.blk + ((int64_t)t * a.Hkv + g) * a.nsel;
+  const int64_t e0 = ((int64_t)t * a.Hkv + g) * a.nsel;
+  float M = -INFINITY;
+  for (int j = 0; j < a.nsel; ++j) {
+    const int b = __ldg(brow + j);
+    if (b < 0 || (int64_t)b * a.bs >= n || (int64_t)b * a.bs > p) continue;
+    M = fmaxf(M, __ldg(a.part_l + (e0 + j) * a.G + hh));
+  }
+  float W = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int nv = a.d / 4;  // float4 per row
+  if (M != -INFINITY) {
+    for (int j = 0; j < a.nsel; ++j) {
+      const int b = __ldg(brow + j);
+      if (b < 0 || (int64_t)b * a.bs >= n || (int64_t)b * a.bs > p) continue;
+      const float wj = exp2f(__ldg(a.part_l + (e0 + j) * a.G + hh) - M);
+      W += wj;
+      if (lane < nv) {
+        const float4 o = __ldg(reinterpret_cast<const float4*>(a.part_o + ((e0 + j) * a.G + hh) * a.d) + lane);
+        acc.x = fmaf(wj, o.x, acc.x);
+        acc.y = fmaf(wj, o.y, acc.y);
+        acc.z = fmaf(wj, o.z, acc.z);
+        acc.w = fmaf(wj, o.w, acc.w);
+      }
+    }
+  }
+  const float inv = W > 0.f ? 1.f / W : 0.f;
+  if (lane < nv) {
+    __nv_bfloat16* orow = a.out + ((int64_t)t * a.Hq + h) * a.d + 4 * lane;
+    *reinterpret_cast<uint2*>(orow) = make_uint2(pack_bf16(acc.x * inv, acc.y * inv), pack_bf16(acc.z * inv, acc.w * inv));
+  }
+  if (lane == 0) a.lse[(int64_t)t * a.Hq + h] = W > 0.f ? (M + log2f(W)) * kLn2 : -INFINITY;
+}
+
+// ---------------------------------------------------------------- host side
+
+namespace {
+
+// Inversion of the selections into per-(block, group) lists, shared by the
+// forward and the backward.
+cudaError_t gt_invert(const GqaTcArgs& a, int chunk, cudaStream_t stream) {
+  const int nB = a.nblk * a.Hkv;
+  const int64_t entries = static_cast<int64_t>(a.T) * a.Hkv * a.nsel;
+  cudaError_t e;
+  const unsigned ig = static_cast<unsigned>(std::min<int64_t>((entries + 255) / 256, 4096));
+  if ((e = cudaMemsetAsync(a.cnt, 0, sizeof(int) * nB, stream)) != cudaSuccess) return e;
+  gqa_tc_inv_kernel<false><<<ig, 256, 0, stream>>>(a);
+  note_launch();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  gqa_tc_scan_kernel<<<1, 1024, 0, stream>>>(a, nB, chunk);
+  note_launch();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  gqa_tc_inv_kernel<true><<<ig, 256, 0, stream>>>(a);
+  note_launch();
+  return cudaGetLastError();
+}
+
+constexpr int GT_FWD_CHUNK = 256;  // list entries (queries) per forward CTA
+
+}  // namespace
+
+cudaError_t launch_gqa_fwd_tc(const GqaTcArgs& a, cudaStream_t stream) {
+  const int nB = a.nblk * a.Hkv;
+  const int64_t entries = static_cast<int64_t>(a.T) * a.Hkv * a.nsel;
+  if (entries <= 0 || nB <= 0) return cudaSuccess;
+  cudaError_t e = gt_invert(a, GT_FWD_CHUNK, stream);
+  if (e != cudaSuccess) return e;
+  CUtensorMap tq, tk, tv;
+  if ((e = make_tmap_bf16_2d(&tq, a.q, (uint64_t)a.T * a.Hq, a.d, 1, 64)) != cudaSuccess) return e;
+  if ((e = make_tmap_bf16_2d(&tk, a.k, (uint64_t)a.T * a.Hkv, a.d, 1, 64)) != cudaSuccess) return e;
+  if ((e = make_tmap_bf16_2d(&tv, a.v, (uint64_t)a.T * a.Hkv, a.d, 1, 64)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(gqa_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, GF_SMEM)) !=
+      cudaSuccess)
+    return e;
+  // chunks: at most one partial chunk per list plus entries / chunk full ones
+  const int64_t grid = nB + (entries + GT_FWD_CHUNK - 1) / GT_FWD_CHUNK;
+  gqa_fwd_tc_kernel<<<static_cast<unsigned>(grid), GT_THREADS, GF_SMEM, stream>>>(tq, tk, tv, a, GT_FWD_CHUNK);
+  note_launch();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int64_t rows = static_cast<int64_t>(a.T) * a.Hq;
+  gqa_combine_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(a);
+  note_launch();
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- backward
+
+namespace {
+
+// K, V, two Q and two dO buffers, P, dS, two row tables
+constexpr int GB_OFF_K = 0;
+constexpr int GB_OFF_V = GB_OFF_K + GT_KT;
+constexpr int GB_OFF_Q = GB_OFF_V + GT_KT;
+constexpr int GB_OFF_DO = GB_OFF_Q + 2 * GT_QT;
+constexpr int GB_OFF_P = GB_OFF_DO + 2 * GT_QT;
+constexpr int GB_OFF_DS = GB_OFF_P + GT_PT;
+constexpr int GB_OFF_TAB = GB_OFF_DS + GT_PT;          // int [2][128]
+constexpr int GB_OFF_BAR = GB_OFF_TAB + 2 * GT_ROWS * 4;
+constexpr int GB_SMEM = 1024 + GB_OFF_BAR + 256;
+static_assert(GB_SMEM <= 227 * 1024, "GQA backward shared memory");
+constexpr int GB_THREADS = 320;  // warps 0-7 rows / drains (two per TMEM lane quadrant), 8 producer, 9 MMA
+// TMEM: S and dP double-buffered, dV^T, dK^T (accumulated over the chunk), dQ^T
+constexpr int GB_T_S = 0, GB_T_DP = 128, GB_T_DV = 256, GB_T_DK = 320, GB_T_DQ = 384, GB_TMEM = 512;
+constexpr int GT_BWD_CHUNK = 512;  // list entries (queries) per backward CTA
+
+}  // namespace
+
+__global__ void __launch_bounds__(GB_THREADS, 1)
+    gqa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ GqaTcArgs a, int chunk) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  unsigned char* gbase = smem_raw + (base - raw);
+  const uint32_t sK = base + GB_OFF_K, sV = base + GB_OFF_V, sQ = base + GB_OFF_Q, sO = base + GB_OFF_DO;
+  const uint32_t sP = base + GB_OFF_P, sS = base + GB_OFF_DS;
+  int* tab = reinterpret_cast<int*>(gbase + GB_OFF_TAB);  // [2][128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + GB_OFF_BAR);
+  uint64_t* kvfull = bars;          // [1]
+  uint64_t* qfull = bars + 1;       // [2] Q, dO and the row table of a batch landed
+  uint64_t* qempty = qfull + 2;     // [2] MMAs done with Q / dO, rows done with the table
+  uint64_t* sfull = qempty + 2;     // [2] S and dP ready
+  uint64_t* sempty = sfull + 2;     // [2] rows read S and dP (8 warps)
+  uint64_t* psfull = sempty + 2;    // [1] rows wrote P and dS (8 warps)
+  uint64_t* psempty = psfull + 1;   // [1] MMAs done reading P and dS
+  uint64_t* dqfull = psempty + 1;   // [1]
+  uint64_t* dqempty = dqfull + 1;   // [1] rows drained dQ^T (8 warps)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dqempty + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  GtChunk ck;
+  if (!gt_chunk(a, blockIdx.x, chunk, ck)) return;  // uniform
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int qb = GT_ROWS / a.G;
+  const int nbatch = (ck.e1 - ck.e0 + qb - 1) / qb;
+  int issued = 0;
+
+  if (tid == 0) {
+    tc::mbar_init(kvfull, 1);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&qfull[i], 1);
+      tc::mbar_init(&qempty[i], 1 + 8);  // the MMA commit and the eight row warps
+      tc::mbar_init(&sfull[i], 1);
+      tc::mbar_init(&sempty[i], 8);
+    }
+    tc::mbar_init(psfull, 8);
+    tc::mbar_init(psempty, 1);
+    tc::mbar_init(dqfull, 1);
+    tc::mbar_init(dqempty, 8);
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  if (a.d == 64) {
+    // channels 64..127 of every operand tile are never loaded: zero them once
+    for (int i = tid; i < GT_KBOX / 16; i += GB_THREADS) {
+      reinterpret_cast<uint4*>(gbase + GB_OFF_K + GT_KBOX)[i] = make_uint4(0u, 0u, 0u, 0u);
+      reinterpret_cast<uint4*>(gbase + GB_OFF_V + GT_KBOX)[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    for (int i = tid; i < GT_QBOX / 16; i += GB_THREADS)
+      for (int b = 0; b < 2; ++b) {
+        reinterpret_cast<uint4*>(gbase + GB_OFF_Q + b * GT_QT + GT_QBOX)[i] = make_uint4(0u, 0u, 0u, 0u);
+        reinterpret_cast<uint4*>(gbase + GB_OFF_DO + b * GT_QT + GT_QBOX)[i] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    tc::fence_proxy_async_smem();
+  }
+  if (warp == 9) tc::tmem_alloc(tmem_slot, GB_TMEM);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t kv_bytes = (a.d == 128 ? 2 : 1) * 2 * GT_KBOX;
+  const uint32_t q_bytes = (a.d == 128 ? 2 : 1) * 2 * GT_QBOX;  // Q and dO
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tc::prefetch_tmap(&tm_q);
+      tc::prefetch_tmap(&tm_do);
+      tc::prefetch_tmap(&tm_k);
+      tc::prefetch_tmap(&tm_v);
+      tc::mbar_arrive_expect_tx(kvfull, kv_bytes);
+    }
+    __syncwarp();
+    gt_gather_kv(sK, &tm_k, kvfull, a, ck, lane);
+    gt_gather_kv(sV, &tm_v, kvfull, a, ck, lane);
+    bool ok = true;
+    for (int i = 0; i < nbatch; ++i) {
+      const int buf = i & 1;
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&qempty[buf], ((i >> 1) & 1) ^ 1u, abort_flag))) {
+        ok = false;
+        break;
+      }
+      int r[4];
+      gt_batch_rows(a, ck, ck.e0 + i * qb, tab + buf * GT_ROWS, lane, r);
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_expect_tx(&qfull[buf], q_bytes);
+      __syncwarp();
+      gt_gather_batch(sQ + buf * GT_QT, &tm_q, &qfull[buf], a.d, r, lane);
+      gt_gather_batch(sO + buf * GT_QT, &tm_do, &qfull[buf], a.d, r, lane);
+      issued = i + 1;
+    }
+    if (!ok) *abort_flag = 1;
+    if (lane == 0) {  // copies still in flight land before the CTA exits (bounded by time only)
+      volatile int keep_waiting = 0;
+      (void)tc::mbar_wait(kvfull, 0, &keep_waiting);
+      for (int g = issued > 2 ? issued - 2 : 0; g < issued; ++g)
+        (void)tc::mbar_wait(&qfull[g & 1], (g >> 1) & 1, &keep_waiting);
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = tc::idesc_bf16_f32(GT_ROWS, GT_KEYS);
+      constexpr uint32_t id_kv = tc::idesc_bf16_f32(GT_DP, GT_KEYS) | (1u << 15) | (1u << 16);  // A, B MN-major
+      constexpr uint32_t id_q = tc::idesc_bf16_f32(GT_DP, GT_ROWS) | (1u << 15);                // A MN-major
+      bool ok = tc::mbar_wait(kvfull, 0, abort_flag);
+      for (int i = 0; ok && i < nbatch; ++i) {
+        const int buf = i & 1;
+        const uint32_t ph = i & 1;
+        if (!tc::mbar_wait(&qfull[buf], (i >> 1) & 1, abort_flag) ||
+            (i >= 2 && !tc::mbar_wait(&sempty[buf], ((i >> 1) & 1) ^ 1u, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t qt = sQ + buf * GT_QT, ot = sO + buf * GT_QT;
+        // S = Q K^T and dP = dO V^T (K = the head dimension)
+#pragma unroll
+        for (int ks = 0; ks < GT_DP / 16; ++ks) {
+          const int c = ks >> 2, kk = ks & 3;
+          tc::mma_bf16_ss(tmem + GB_T_S + buf * GT_KEYS, tc::desc_sw128(qt + c * GT_QBOX + kk * 32),
+                          tc::desc_sw128(sK + c * GT_KBOX + kk * 32), id_s, ks > 0 ? 1u : 0u);
+          tc::mma_bf16_ss(tmem + GB_T_DP + buf * GT_KEYS, tc::desc_sw128(ot + c * GT_QBOX + kk * 32),
+                          tc::desc_sw128(sV + c * GT_KBOX + kk * 32), id_s, ks > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(&sfull[buf]);
+        // the rows' P and dS of this batch, and the drained dQ^T of the previous one
+        if (!tc::mbar_wait(psfull, ph, abort_flag) || (i > 0 && !tc::mbar_wait(dqempty, ph ^ 1u, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        // dV^T += dO^T P, dK^T += Q^T dS (K = the batch's 128 rows)
+#pragma unroll
+        for (int ks = 0; ks < GT_ROWS / 16; ++ks) {
+          tc::mma_bf16_ss(tmem + GB_T_DV, tc::desc_sw128_mn(ot + ks * 2048, GT_QBOX),
+                          tc::desc_sw128_mn(sP + ks * 2048, GT_PT), id_kv, (i > 0 || ks > 0) ? 1u : 0u);
+          tc::mma_bf16_ss(tmem + GB_T_DK, tc::desc_sw128_mn(qt + ks * 2048, GT_QBOX),
+                          tc::desc_sw128_mn(sS + ks * 2048, GT_PT), id_kv, (i > 0 || ks > 0) ? 1u : 0u);
+        }
+        tc::mma_commit(&qempty[buf]);
+        // dQ^T = K^T dS^T (K = the 64 keys)
+#pragma unroll
+        for (int ks = 0; ks < GT_KEYS / 16; ++ks)
+          tc::mma_bf16_ss(tmem + GB_T_DQ, tc::desc_sw128_mn(sK + ks * 2048, GT_KBOX), tc::desc_sw128(sS + ks * 32),
+                          id_q, ks > 0 ? 1u : 0u);
+        tc::mma_commit(psempty);
+        tc::mma_commit(dqfull);
+      }
+      if (!ok) *abort_flag = 1;
+    }
+  } else {
+    // ------------------------------------------------------------ rows / drains (warps 0-7)
+    // warp w: TMEM lane quadrant qd = w % 4 (batch rows, or channels in the
+    // transposed products), half hf = w / 4 (keys 32 hf .. +31 of S / dP, batch
+    // rows 64 hf .. +63 of dQ^T, keys 32 hf .. +31 of dK^T / dV^T)
+    const int qd = warp & 3, hf = warp >> 2;
+    const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
+    const int row = qd * 32 + lane;
+    const int hh = row % a.G;
+    const int ch = qd * 32 + lane;  // channel in the transposed products
+    for (int i = 0; i < nbatch; ++i) {
+      const int buf = i & 1;
+      const uint32_t ph = i & 1;
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&qfull[buf], (i >> 1) & 1, abort_flag)) ||
+          !__all_sync(0xffffffffu, tc::mbar_wait(&sfull[buf], (i >> 1) & 1, abort_flag))) {
+        *abort_flag = 1;
+        break;
+      }
+      tc::fence_after_sync();
+      const int* tb = tab + buf * GT_ROWS;
+      const int e = tb[row];
+      const int t = e >= 0 ? e / (a.Hkv * a.nsel) : 0;
+      const int h = ck.g * a.G + hh;
+      const int lim = e < 0 ? 0 : min(min(a.bs, ck.n - ck.kbase), t - ck.s0 - ck.kbase + 1);
+      const float lse2 = e >= 0 ? __ldg(a.lse_in + (int64_t)t * a.Hq + h) * kLog2e : 0.f;
+      const float dl = e >= 0 ? __ldg(a.dlt + (int64_t)t * a.Hq + h) : 0.f;
+      uint32_t sr[32], dr[32];
+      __syncwarp();
+      tc::tmem_ld32(tmem + lane_base + GB_T_S + buf * GT_KEYS + hf * 32, sr);
+      tc::tmem_ld32(tmem + lane_base + GB_T_DP + buf * GT_KEYS + hf * 32, dr);
+      tc::tmem_ld_wait();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&sempty[buf]);
+      uint32_t pk[16], dk[16];
+#pragma unroll
+      for (int c = 0; c < 32; c += 2) {
+        const int k0 = hf * 32 + c;
+        const float p0 = k0 < lim ? exp2f(__uint_as_float(sr[c]) * a.scale_log2 - lse2) : 0.f;
+        const float p1 = k0 + 1 < lim ? exp2f(__uint_as_float(sr[c + 1]) * a.scale_log2 - lse2) : 0.f;
+        pk[c / 2] = pack_bf16(p0, p1);
+        dk[c / 2] = pack_bf16(a.scale * p0 * (__uint_as_float(dr[c]) - dl),
+                              a.scale * p1 * (__uint_as_float(dr[c + 1]) - dl));
+      }
+      // P and dS into shared memory once the previous batch's MMAs have read them
+      if (i > 0 && !__all_sync(0xffffffffu, tc::mbar_wait(psempty, ph ^ 1u, abort_flag))) {
+        *abort_flag = 1;
+        break;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        *reinterpret_cast<uint4*>(gbase + GB_OFF_P + sw128(row, hf * 4 + q)) =
+            make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        *reinterpret_cast<uint4*>(gbase + GB_OFF_DS + sw128(row, hf * 4 + q)) =
+            make_uint4(dk[4 * q], dk[4 * q + 1], dk[4 * q + 2], dk[4 * q + 3]);
+      }
+      tc::fence_proxy_async_smem();  // generic writes before the MMAs (async proxy) read them
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(psfull);
+      // dQ^T of this batch: channel ch of batch rows 64 hf .. +63, one fp32
+      // reduction per (row, channel); a warp instruction covers 32 channels of a row
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(dqfull, ph, abort_flag))) {
+        *abort_flag = 1;
+        break;
+      }
+      tc::fence_after_sync();
+#pragma unroll 1
+      for (int cb = 0; cb < 2; ++cb) {
+        uint32_t r[32];
+        __syncwarp();
+        tc::tmem_ld32(tmem + lane_base + GB_T_DQ + hf * 64 + cb * 32, r);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int rr = hf * 64 + cb * 32 + k;
+          const int er = tb[rr];
+          if (er >= 0 && ch < a.d) {
+            const int tr = er / (a.Hkv * a.nsel);
+            red_f32(a.dq_acc + ((int64_t)tr * a.Hq + ck.g * a.G + rr % a.G) * a.d + ch, __uint_as_float(r[k]));
+          }
+        }
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        tc::mbar_arrive(dqempty);
+        tc::mbar_arrive(&qempty[buf]);  // the row table may be rewritten for batch i + 2
+      }
+    }
+    // ---- this chunk's dK, dV of the block's keys: channel ch, keys 32 hf .. +31
+    if (!*abort_flag && nbatch > 0) {
+      // the last dQ^T commit follows every MMA of the chunk
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(dqfull, (nbatch - 1) & 1, abort_flag))) {
+        *abort_flag = 1;
+      } else {
+        tc::fence_after_sync();
+        uint32_t rk[32], rv[32];
+        __syncwarp();
+        tc::tmem_ld32(tmem + lane_base + GB_T_DK + hf * 32, rk);
+        tc::tmem_ld32(tmem + lane_base + GB_T_DV + hf * 32, rv);
+        tc::tmem_ld_wait();
+        if (ch < a.d) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const int key = hf * 32 + k;
+            const int kp = ck.kbase + key;
+            if (key < a.bs && kp < ck.n) {
+              const int64_t o = ((int64_t)(ck.s0 + kp) * a.Hkv + ck.g) * a.d + ch;
+              red_f32(a.dk_acc + o, __uint_as_float(rk[k]));
+              red_f32(a.dv_acc + o, __uint_as_float(rv[k]));
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (*abort_flag && tid == 0) raise_flag(a.flags, TSA_FLAG_TIMEOUT);
+  if (warp == 9) {
+    __syncwarp();
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, GB_TMEM);
+  }
+}
+
+cudaError_t launch_gqa_bwd_tc(const GqaTcArgs& a, cudaStream_t stream) {
+  const int nB = a.nblk * a.Hkv;
+  const int64_t entries = static_cast<int64_t>(a.T) * a.Hkv * a.nsel;
+  if (entries <= 0 || nB <= 0) return cudaSuccess;
+  cudaError_t e = gt_invert(a, GT_BWD_CHUNK, stream);
+  if (e != cudaSuccess) return e;
+  CUtensorMap tq, tdo, tk, tv;
+  if ((e = make_tmap_bf16_2d(&tq, a.q, (uint64_t)a.T * a.Hq, a.d, 1, 64)) != cudaSuccess) return e;
+  if ((e = make_tmap_bf16_2d(&tdo, a.dout, (uint64_t)a.T * a.Hq, a.d, 1, 64)) != cudaSuccess) return e;
+  if ((e = make_tmap_bf16_2d(&tk, a.k, (uint64_t)a.T * a.Hkv, a.d, 1, 64)) != cudaSuccess) return e;
+  if ((e = make_tmap_bf16_2d(&tv, a.v, (uint64_t)a.T * a.Hkv, a.d, 1, 64)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(gqa_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, GB_SMEM)) !=
+      cudaSuccess)
+    return e;
+  const int64_t grid = nB + (entries + GT_BWD_CHUNK - 1) / GT_BWD_CHUNK;
+  const unsigned nblocks = static_cast<unsigned>(grid);
+  gqa_bwd_tc_kernel<<<nblocks, GB_THREADS, GB_SMEM, stream>>>(tq, tdo, tk, tv, a, GT_BWD_CHUNK);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace tsa

@@ -23,6 +23,16 @@
 // as soon as the MMAs of the previous one are done, and the head weights go
 // to the other half of a double buffer.
 //
+// Block scores (block_size bs in {16, 32, 64, 128}, the QSA block top-k input)
+// come from the same MMAs with a different epilogue: each thread masks its
+// key's group scores to -inf where the key is not causal for the query, and the
+// maximum over the bs consecutive keys of a block is taken across TMEM lanes --
+// inside a warp by recursive halving (at each xor-shuffle step a lane keeps half
+// of its values and takes the partner's copy of that half, so 64 values need 62
+// shuffles instead of 320), across the 2 or 4 warps of a 64- or 128-key block
+// through shared memory, handed over on an mbarrier (bounded wait).  Only the
+// block maxima are written: the [T, T] token scores never exist.
+//
 // Warp roles (320 threads): warps 0-7 epilogue (warp w: TMEM lanes 32 (w % 4)
 // .. +31, accumulator columns 128 (w / 4) .. +127, so two warps share each
 // sub-partition and hide each other's latencies), warp 8 TMA producer, warp 9
@@ -48,7 +58,8 @@ struct ItLayout {
   static constexpr int KB = DI / 64;                    // 128-byte column blocks along d_I
   static constexpr int B_BYTES = KB * IT_N * 128;       // q_I block
   static constexpr int A_BYTES = KB * IT_M * 128;       // one key tile
-  static constexpr int USED = 1024 + B_BYTES + IT_STAGES * A_BYTES + 2 * IT_N * 4 + 256;
+  static constexpr int XBUF = 2 * 8 * 4 * 32 * 4;        // block epilogue partials [acc][warp][<=4][32 lanes]
+  static constexpr int USED = 1024 + B_BYTES + IT_STAGES * A_BYTES + 2 * IT_N * 4 + XBUF + 256;
   // at least 120 KB so that a single CTA (the only TMEM owner) fits on an SM
   static constexpr int SMEM = USED > 120 * 1024 ? USED : 120 * 1024;
 };
@@ -77,7 +88,88 @@ __device__ __forceinline__ void fma2(float& c0, float& c1, float a0, float a1, f
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
-template <int DI, int HG>
+// Recursive-halving maximum over aligned groups of 2*O lanes (O a power of two):
+// N values per lane in, and after log2(min(N, 2*O)) halving steps each lane
+// holds N / 2^steps of them, each the maximum over its lane group.  The value
+// v[i] of lane L then belongs to the original index i + NF * ((L & (2O-1)) >> R),
+// with NF the values left and R = log2(2O) - steps (lanes differing only in
+// their R low bits hold the same values).
+template <int N, int O>
+__device__ __forceinline__ void lane_group_max(float* v, int lane) {
+  if constexpr (O >= 1) {
+    if constexpr (N >= 2) {
+      const bool up = (lane & O) != 0;
+#pragma unroll
+      for (int i = 0; i < N / 2; ++i) {
+        const float send = up ? v[i] : v[N / 2 + i];
+        const float keep = up ? v[N / 2 + i] : v[i];
+        v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, O));
+      }
+      lane_group_max<N / 2, O / 2>(v, lane);
+    } else {
+      v[0] = fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], O));
+      lane_group_max<1, O / 2>(v, lane);
+    }
+  }
+}
+
+__host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
+
+// Block-maximum epilogue of one warp for one key tile.  vals[NSEG]: the masked
+// scores of this lane's key for the warp's NSEG (query, group) segments.  G = the
+// lanes of one block inside the warp (16, or 32 for blocks of 32 keys and more).
+// Blocks of 64 / 128 keys span 2 / 4 warps: the partner warps leave their
+// partials in xbuf and arrive on xbar; the first warp of the block waits
+// (bounded) and writes.  Returns false if that wait gave up.
+template <int NSEG, int G>
+__device__ __forceinline__ bool block_max_epilogue(float* vals, const IndexerArgs& a, int lane, int warp, int qd,
+                                                   int ch, int acc, uint32_t aph, int kt, int q0, int qn,
+                                                   int p_first, float* xbuf, uint64_t* xbar,
+                                                   volatile int* abort_flag) {
+  constexpr int LG = ilog2(G), LN = ilog2(NSEG);
+  constexpr int HS = LG < LN ? LG : LN;  // halving steps
+  constexpr int NF = NSEG >> HS;         // values left per lane
+  constexpr int R = LG - HS;
+  lane_group_max<NSEG, G / 2>(vals, lane);
+  const int sub = (lane & (G - 1)) >> R;
+  const bool dup = (lane & ((1 << R) - 1)) != 0;
+  const int bs = a.bs;
+  int blk;  // local block of this lane's key
+  if (bs <= 32) {
+    blk = (kt * IT_M + qd * 32 + lane) / bs;
+  } else {
+    const int bsw = bs / 32;  // warps per block
+    const int grp = qd / bsw;
+    uint64_t* xb = &xbar[(acc * 2 + ch) * 2 + grp];
+    float* mine = xbuf + (acc * 8 + warp) * (4 * 32);
+    if (qd % bsw != 0) {  // partner: hand the partials over and go on
+#pragma unroll
+      for (int i = 0; i < NF; ++i) mine[i * 32 + lane] = vals[i];
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(xb);
+      return true;
+    }
+    if (!__all_sync(0xffffffffu, tc::mbar_wait(xb, aph, abort_flag))) return false;
+    for (int p = 1; p < bsw; ++p) {
+      const float* other = mine + p * (4 * 32);  // warp + p: same column half, next lane quadrant
+#pragma unroll
+      for (int i = 0; i < NF; ++i) vals[i] = fmaxf(vals[i], other[i * 32 + lane]);
+    }
+    blk = (kt * IT_M + qd * 32) / bs;
+  }
+  if (!dup) {
+#pragma unroll
+    for (int i = 0; i < NF; ++i) {
+      const int sg = ch * NSEG + i + NF * sub;  // (query, group) segment of the block's half
+      const int qq = sg / a.groups, gg = sg % a.groups;
+      if (qq < qn && blk * bs <= p_first + qq)
+        a.out[((int64_t)(q0 + qq) * a.groups + gg) * a.width + blk] = vals[i];
+    }
+  }
+  return true;
+}
+
+template <int DI, int HG, bool BLK>
 __global__ void __launch_bounds__(IT_THREADS, 1)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ IndexerArgs a, int total) {
@@ -89,7 +181,7 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
   const uint32_t sB = base;
   const uint32_t sA = base + L::B_BYTES;
   float* Ws = reinterpret_cast<float*>(gbase + L::B_BYTES + IT_STAGES * L::A_BYTES);  // [2][IT_N]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(Ws + 2 * IT_N);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<unsigned char*>(Ws + 2 * IT_N) + L::XBUF);
   uint64_t* full = bars;                       // [IT_STAGES] key tile landed
   uint64_t* empty = bars + IT_STAGES;          // [IT_STAGES]
   uint64_t* bfull = empty + IT_STAGES;         // [1] q_I block landed (one phase per block change)
@@ -98,7 +190,9 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
   uint64_t* acce = accf + 2;                   // [2]
   uint64_t* wsfull = acce + 2;                 // [2] head weights of a block written (32 lanes)
   uint64_t* wsempty = wsfull + 2;              // [2] epilogue done with a weight buffer (8 warps)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wsempty + 2);
+  uint64_t* xbar = wsempty + 2;                // [2 acc][2 halves][2 blocks] block partials handed over
+  float* xbuf = reinterpret_cast<float*>(gbase + L::B_BYTES + IT_STAGES * L::A_BYTES + 2 * IT_N * 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int H_I = a.H_I;
@@ -151,6 +245,8 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
       tc::mbar_init(&wsfull[i], 32);
       tc::mbar_init(&wsempty[i], 8);
     }
+    // partner warps of a block: 1 (64-key blocks) or 3 (128-key blocks)
+    for (int i = 0; i < 8; ++i) tc::mbar_init(&xbar[i], a.bs >= 64 ? a.bs / 32 - 1 : 1);
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -269,6 +365,8 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
       // dependency chain; the TMEM load of block cb+1 is in flight while block
       // cb is reduced; the head weights come four at a time
       float run[4] = {0.f, 0.f, 0.f, 0.f};
+      constexpr int NSEG = (IT_N / 2) / HG;  // (query, group) segments of this warp's column half
+      float vals[BLK ? NSEG : 1];
       uint32_t rbuf[2][32];
       constexpr int NCB = IT_N / 64;  // 32-column blocks of this warp's half
       __syncwarp();
@@ -297,10 +395,24 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
             const float tot = (run[0] + run[1]) + (run[2] + run[3]);
             const int sg = col / HG;
             const int qq = sg / a.groups, gg = sg % a.groups;
-            if (qq < qn && s <= p_first + qq)
-              a.out[((int64_t)(q0 + qq) * a.groups + gg) * a.width + s] = tot * a.score_scale + 0.f;
+            if constexpr (BLK) {
+              vals[(cb * 32 + j) / HG] = (qq < qn && s <= p_first + qq) ? tot * a.score_scale + 0.f : -INFINITY;
+            } else {
+              if (qq < qn && s <= p_first + qq)
+                a.out[((int64_t)(q0 + qq) * a.groups + gg) * a.width + s] = tot * a.score_scale + 0.f;
+            }
             run[0] = run[1] = run[2] = run[3] = 0.f;
           }
+        }
+      }
+      if constexpr (BLK) {
+        const bool ok = a.bs == 16 ? block_max_epilogue<NSEG, 16>(vals, a, lane, warp, qd, ch, acc, aph, w.kt, q0,
+                                                                   qn, p_first, xbuf, xbar, abort_flag)
+                                   : block_max_epilogue<NSEG, 32>(vals, a, lane, warp, qd, ch, acc, aph, w.kt, q0,
+                                                                   qn, p_first, xbuf, xbar, abort_flag);
+        if (!ok) {
+          *abort_flag = 1;
+          break;
         }
       }
       tc::fence_before_sync();
@@ -370,13 +482,14 @@ cudaError_t make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, u
 }
 
 bool indexer_tc_supported(int H_I, int d_I, int groups, int bs) {
-  if (bs != 1 || (d_I != 64 && d_I != 128)) return false;
+  if (bs != 1 && bs != 16 && bs != 32 && bs != 64 && bs != 128) return false;
+  if (d_I != 64 && d_I != 128) return false;
   if (H_I < 2 || H_I > IT_N || (IT_N % H_I) != 0) return false;
   const int hg = H_I / groups;
   return hg >= 2 && hg <= 128 && (hg & (hg - 1)) == 0 && hg * groups == H_I;
 }
 
-template <int DI, int HG>
+template <int DI, int HG, bool BLK>
 static cudaError_t launch_tc_t(const IndexerArgs& a, cudaStream_t stream) {
   CUtensorMap tq, tk;
   cudaError_t e = make_tmap_bf16_2d(&tq, a.q, (uint64_t)a.T_total * a.H_I, DI, IT_N, 64);
@@ -384,7 +497,7 @@ static cudaError_t launch_tc_t(const IndexerArgs& a, cudaStream_t stream) {
   e = make_tmap_bf16_2d(&tk, a.k, (uint64_t)a.T_total, DI, IT_M, 64);
   if (e != cudaSuccess) return e;
   constexpr int smem = ItLayout<DI>::SMEM;
-  e = cudaFuncSetAttribute(indexer_tc_kernel<DI, HG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  e = cudaFuncSetAttribute(indexer_tc_kernel<DI, HG, BLK>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   // total (query block, key tile) pairs of the launch; one persistent CTA per SM
   const int QB = IT_N / a.H_I;
@@ -395,34 +508,33 @@ static cudaError_t launch_tc_t(const IndexerArgs& a, cudaStream_t stream) {
     total += (a.p_begin + qb * QB + qn - 1) / IT_M + 1;
   }
   if (total > 0x7fffffffLL) return cudaErrorInvalidValue;
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  }
+  // SM count of the current device, read per launch (devices may differ)
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const int grid = static_cast<int>(std::min<int64_t>(total, sms));
-  indexer_tc_kernel<DI, HG><<<grid, IT_THREADS, smem, stream>>>(tq, tk, a, static_cast<int>(total));
+  indexer_tc_kernel<DI, HG, BLK><<<grid, IT_THREADS, smem, stream>>>(tq, tk, a, static_cast<int>(total));
   note_launch();
   return cudaGetLastError();
 }
 
-template <int DI>
+template <int DI, bool BLK>
 static cudaError_t launch_tc_d(const IndexerArgs& a, cudaStream_t stream) {
   switch (a.H_I / a.groups) {
-    case 2: return launch_tc_t<DI, 2>(a, stream);
-    case 4: return launch_tc_t<DI, 4>(a, stream);
-    case 8: return launch_tc_t<DI, 8>(a, stream);
-    case 16: return launch_tc_t<DI, 16>(a, stream);
-    case 32: return launch_tc_t<DI, 32>(a, stream);
-    case 64: return launch_tc_t<DI, 64>(a, stream);
-    default: return launch_tc_t<DI, 128>(a, stream);
+    case 2: return launch_tc_t<DI, 2, BLK>(a, stream);
+    case 4: return launch_tc_t<DI, 4, BLK>(a, stream);
+    case 8: return launch_tc_t<DI, 8, BLK>(a, stream);
+    case 16: return launch_tc_t<DI, 16, BLK>(a, stream);
+    case 32: return launch_tc_t<DI, 32, BLK>(a, stream);
+    case 64: return launch_tc_t<DI, 64, BLK>(a, stream);
+    default: return launch_tc_t<DI, 128, BLK>(a, stream);
   }
 }
 
 cudaError_t launch_indexer_tc(const IndexerArgs& a, cudaStream_t stream) {
   if (a.nq <= 0) return cudaSuccess;
-  return a.d_I == 128 ? launch_tc_d<128>(a, stream) : launch_tc_d<64>(a, stream);
+  if (a.bs > 1) return a.d_I == 128 ? launch_tc_d<128, true>(a, stream) : launch_tc_d<64, true>(a, stream);
+  return a.d_I == 128 ? launch_tc_d<128, false>(a, stream) : launch_tc_d<64, false>(a, stream);
 }
 
 }  // namespace tsa

@@ -65,6 +65,9 @@ struct MlaBwdArgs {
   __nv_bfloat16* p_out = nullptr;
   __nv_bfloat16* ds_out = nullptr;
   unsigned int* flags = nullptr;  // device error flags
+  // optional indexer teacher [T, topk]: head mean of P at each slot (zeroed by the
+  // caller for the H < 128 kernel, which adds each head block's share)
+  float* teacher = nullptr;
 };
 
 // Inputs of the tcgen05 dKV GEMM: P and dS of queries q0 .. q0+nq in bf16,
@@ -81,45 +84,62 @@ struct MlaBwdTcArgs {
   SeqTable st;
 };
 
-struct GqaArgs {            // Sparse-GQA forward (gqa.cu)
-  const __nv_bfloat16* q;   // [T, Hq, d]
-  const __nv_bfloat16* k;   // [T, Hkv, d]
-  const __nv_bfloat16* v;   // [T, Hkv, d]
-  const int32_t* blk;       // [T, Hkv, nsel]
-  int T, Hq, Hkv, G, nsel;
-  float scale, scale_log2;
-  __nv_bfloat16* out;       // [T, Hq, d]
-  float* lse;               // [T, Hq]
-  unsigned int* flags;      // device error flags
-  SeqTable st;
-};
-
-// Key-centric Sparse-GQA backward (gqa_bwd_kv.cu): inverted selections and
-// fp32 gradient accumulators, all in the caller's workspace.
-struct GqaKvArgs {
+// Key-centric Sparse-GQA on tcgen05 (gqa_tc.cu): selections inverted into
+// per-(block, group) lists of entries t * nsel + j; the forward writes per-slot
+// partials that a combine pass merges in slot order.  All buffers are the
+// caller's workspace.
+struct GqaTcArgs {
   const __nv_bfloat16* q;     // [T, Hq, d]
   const __nv_bfloat16* k;     // [T, Hkv, d]
   const __nv_bfloat16* v;     // [T, Hkv, d]
-  const __nv_bfloat16* dout;  // [T, Hq, d]
+  const __nv_bfloat16* dout;  // backward: [T, Hq, d]
   const int32_t* blk;         // [T, Hkv, nsel] local block ids, -1 = none
-  const float* lse_in;        // [T, Hq] natural log
-  const float* dlt;           // [T, Hq] rowsum(dO * O)
-  int T, Hq, Hkv, G, nsel, bs;
+  const float* lse_in;        // backward: [T, Hq] natural log
+  const float* dlt;           // backward: [T, Hq] rowsum(dO * O)
+  int T, Hq, Hkv, G, nsel, bs, d;
   float scale, scale_log2;
   int nblk;                   // blocks over all sequences
-  int* cnt;                   // [nblk * Hkv] queries per (block, group)
+  int* cnt;                   // [nblk * Hkv] entries per (block, group)
   int* off;                   // [nblk * Hkv + 1] list offsets
   int* cur;                   // [nblk * Hkv] fill cursors
   int* choff;                 // [nblk * Hkv + 1] chunk offsets
-  int* list;                  // [T * Hkv * nsel] query tokens per (block, group)
-  float* dq_acc;              // [T, Hq, d] fp32
-  float* dk_acc;              // [T, Hkv, d] fp32
-  float* dv_acc;
+  int* list;                  // [T * Hkv * nsel] per (block, group): flat selection indices (t * Hkv + g) * nsel + j
+  float* part_o;              // forward: [T * Hkv * nsel, G, d] normalised partial outputs
+  float* part_l;              // forward: [T * Hkv * nsel, G] their log2-sum-exp
+  __nv_bfloat16* out;         // forward: [T, Hq, d]
+  float* lse;                 // forward: [T, Hq]
+  float* dq_acc;              // backward: [T, Hq, d] fp32
+  float* dk_acc;              // backward: [T, Hkv, d] fp32
+  float* dv_acc;              // backward: [T, Hkv, d] fp32
   unsigned int* flags;
   SeqTable st;
   int blk_base[TSA_MAX_SEQS + 1];  // first global block of each sequence
 };
-cudaError_t launch_gqa_bwd_kv(const GqaKvArgs& a, int d, cudaStream_t stream);
+cudaError_t launch_gqa_fwd_tc(const GqaTcArgs& a, cudaStream_t stream);
+cudaError_t launch_gqa_bwd_tc(const GqaTcArgs& a, cudaStream_t stream);
+
+// Indexer training on the selected slots (indexer_kl.cu): the sparse KL of the
+// student scores against the attention teacher, and the indexer backward.
+struct IndexerSelArgs {
+  const float* w;             // [T, H_I]
+  const int32_t* idx;         // [T, topk] local positions, -1 = none
+  const float* teacher;       // KL: [T, topk]
+  const float* dscore;        // backward: [T, topk]
+  float* loss;                // KL: [T]
+  float* dscore_out;          // KL: [T, topk]
+  __nv_bfloat16* dq;          // backward: [T, H_I, 128]
+  float* dw;                  // backward: [T, H_I]
+  float* dk_acc;              // backward: [T, 128] fp32, zeroed by the caller
+  int T, H_I, topk;
+  float score_scale;
+  unsigned int* flags;
+  SeqTable st;
+};
+bool indexer_sel_supported(int H_I, int d_I);
+cudaError_t launch_indexer_sel(const IndexerSelArgs& a, const void* q, const void* k, bool bwd, cudaStream_t stream);
+// Head mean of the staged bf16 P of one 128-head backward chunk -> teacher rows q0 .. q0+nq.
+cudaError_t launch_mla_teacher_from_p(const __nv_bfloat16* P, int nq, int H, int kp, int topk, int q0,
+                                      float* teacher, cudaStream_t stream);
 
 cudaError_t launch_topk_rows(const TopkRows& a, int64_t rows, cudaStream_t stream);
 cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t stream);
@@ -129,6 +149,18 @@ cudaError_t launch_indexer_tc(const IndexerArgs& a, cudaStream_t stream);
 // Account for one kernel launch of this library (the count tsa_kernel_launches reports);
 // every launch site calls it right after its <<<...>>> statement.
 void note_launch();
+
+// Host helpers of the C-ABI layer (api.cu), shared by every entry-point file.
+// note_error records the detail message tsa_last_error() returns and passes the
+// status through; device_flags is the current device's flag word (null if it
+// cannot be looked up); make_seq_table validates cu_seqlens and fills the
+// kernel-side table; check_indexer_shape refuses indexer shapes that are not
+// built; score_width is the score-row width for the longest sequence.
+int note_error(int code, const char* msg);
+unsigned int* device_flags();
+int make_seq_table(const int32_t* cu, int num_seqs, SeqTable* st, int64_t* T_out);
+int check_indexer_shape(int H_I, int d_I, int groups, int block_size);
+int64_t score_width(int max_len, int block_size);
 cudaError_t launch_fill(float* p, int64_t n, float v, cudaStream_t stream);
 cudaError_t launch_bounded_wait_selftest(unsigned int* flags, cudaStream_t stream);
 cudaError_t launch_mla_fwd(const MlaFwdArgs& a, int D, cudaStream_t stream);
@@ -141,7 +173,6 @@ cudaError_t launch_mla_bwd_dq_tc(const MlaBwdArgs& a, int D, int nq, cudaStream_
 cudaError_t launch_bwd_delta(const __nv_bfloat16* o, const __nv_bfloat16* dout, float* dlt, int64_t rows, int dv,
                              cudaStream_t stream);
 cudaError_t launch_f32_to_bf16(const float* src, __nv_bfloat16* dst, int64_t n, cudaStream_t stream);
-cudaError_t launch_gqa(const GqaArgs& a, int bs, int d, cudaStream_t stream);
 
 constexpr int kIndexerKTile = 128;  // keys per indexer tile (block sizes must divide it)
 constexpr int kTopkMaxK = 4096;

@@ -183,6 +183,15 @@ __global__ void __launch_bounds__(128 * MW) mla_bwd_mma_kernel(const __grid_cons
     *reinterpret_cast<uint32_t*>(dSs + prow * PRS + key0) = pack_bf16(dS[0], dS[1]);
     *reinterpret_cast<uint32_t*>(dSs + (prow + 8) * PRS + key0) = pack_bf16(dS[2], dS[3]);
     __syncthreads();
+    if (a.teacher != nullptr && tid < MB_KT) {
+      // indexer teacher: this head block's share of the head mean of P at the tile's slots
+      const int slot = jt * MB_KT + tid;
+      if (slot < a.topk) {
+        float sp = 0.f;
+        for (int h = 0; h < HB; ++h) sp += __bfloat162float(Ps[h * PRS + tid]);
+        if (sp != 0.f) atomicAdd(a.teacher + (int64_t)t * a.topk + slot, sp / static_cast<float>(a.H));
+      }
+    }
 
     // dQ[mt rows, quarter kq of D] += (scale dS) K
     {
@@ -267,7 +276,8 @@ static size_t mla_bwd_smem() {
 template <int D, int MW>
 static cudaError_t launch_bwd_main(const MlaBwdArgs& a, cudaStream_t stream) {
   size_t smem = mla_bwd_smem<D, MW>();
-  cudaFuncSetAttribute(mla_bwd_mma_kernel<D, MW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(mla_bwd_mma_kernel<D, MW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
   dim3 grid(a.T, (a.H + 16 * MW - 1) / (16 * MW));
   mla_bwd_mma_kernel<D, MW><<<grid, 128 * MW, smem, stream>>>(a);
   note_launch();

@@ -193,12 +193,14 @@ cudaError_t launch_mla_fwd(const MlaFwdArgs& a, int D, cudaStream_t stream) {
   dim3 grid(a.T, (a.H + MF_HB - 1) / MF_HB);
   if (D == 576) {
     size_t smem = mla_fwd_smem<576>();
-    cudaFuncSetAttribute(mla_fwd_mma_kernel<576>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(mla_fwd_mma_kernel<576>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     mla_fwd_mma_kernel<576><<<grid, MF_THREADS, smem, stream>>>(a);
     note_launch();
   } else {
     size_t smem = mla_fwd_smem<512>();
-    cudaFuncSetAttribute(mla_fwd_mma_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(mla_fwd_mma_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     mla_fwd_mma_kernel<512><<<grid, MF_THREADS, smem, stream>>>(a);
     note_launch();
   }

@@ -30,11 +30,6 @@
 
 #include "kernels.cuh"
 
-namespace tsa {
-int note_error(int code, const char* msg);
-void note_launch();
-}  // namespace tsa
-
 using namespace tsa;
 
 namespace {
@@ -68,30 +63,21 @@ int scratch_address(void** out) {
   return TSA_OK;
 }
 
-bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
-
 }  // namespace
 
 extern "C" int qsa_topk_no_alloc(const void* q_idx, const void* k_idx, const float* w, const int32_t* cu_seqlens,
                                  int num_seqs, int H_I, int d_I, int groups, int block_size, float score_scale,
                                  int topk, int32_t* indices, void* stream) {
-  // ---- host-side validation (nothing is launched or looked up on failure)
-  if (cu_seqlens == nullptr) return note_error(TSA_ERR_INVALID_ARG, "cu_seqlens is null");
-  if (num_seqs < 1 || num_seqs > TSA_MAX_SEQS) return note_error(TSA_ERR_INVALID_ARG, "num_seqs out of range");
-  if (cu_seqlens[0] != 0) return note_error(TSA_ERR_INVALID_ARG, "cu_seqlens[0] must be 0");
-  int max_len = 0;
-  for (int i = 1; i <= num_seqs; ++i) {
-    if (cu_seqlens[i] < cu_seqlens[i - 1]) return note_error(TSA_ERR_INVALID_ARG, "cu_seqlens must not decrease");
-    max_len = std::max(max_len, cu_seqlens[i] - cu_seqlens[i - 1]);
-  }
-  if (!pow2(H_I) || H_I < 2 || H_I > 128) return note_error(TSA_ERR_UNSUPPORTED, "H_I must be 2..128, power of two");
-  if (d_I != 64 && d_I != 128) return note_error(TSA_ERR_UNSUPPORTED, "d_I must be 64 or 128");
-  if (groups < 1 || H_I % groups != 0 || H_I / groups < 2)
-    return note_error(TSA_ERR_UNSUPPORTED, "groups must divide H_I with H_I/groups >= 2");
-  if (block_size != 1 && block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128)
-    return note_error(TSA_ERR_UNSUPPORTED, "block_size must be 1, 16, 32, 64 or 128");
+  // ---- host-side validation (nothing is launched or looked up on failure):
+  // the same checks, in the same helpers, as qsa_topk
+  SeqTable st;
+  int64_t T = 0;
+  int rc = make_seq_table(cu_seqlens, num_seqs, &st, &T);
+  if (rc != TSA_OK) return rc;
+  if ((rc = check_indexer_shape(H_I, d_I, groups, block_size)) != TSA_OK) return rc;
   if (topk < 1 || topk > kTopkMaxK) return note_error(TSA_ERR_UNSUPPORTED, "topk must be 1..4096");
-  const int64_t width = block_size == 1 ? max_len : (max_len + block_size - 1) / block_size;
+  const int max_len = st.max_len;
+  const int64_t width = score_width(max_len, block_size);
   const int64_t row_bytes = int64_t(4) * groups * (width > 0 ? width : 1);
   if (row_bytes > static_cast<int64_t>(kNoAllocScratchBytes)) {
     char msg[200];
@@ -100,11 +86,11 @@ extern "C" int qsa_topk_no_alloc(const void* q_idx, const void* k_idx, const flo
              (long long)row_bytes, kNoAllocScratchBytes);
     return note_error(TSA_ERR_UNSUPPORTED, msg);
   }
-  if (cu_seqlens[num_seqs] == 0) return TSA_OK;
+  if (T == 0) return TSA_OK;
   if (!q_idx || !k_idx || !w || !indices) return note_error(TSA_ERR_INVALID_ARG, "null tensor pointer");
 
   void* scratch = nullptr;
-  int rc = scratch_address(&scratch);
+  rc = scratch_address(&scratch);
   if (rc != TSA_OK) return rc;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -125,7 +111,8 @@ extern "C" int qsa_topk_no_alloc(const void* q_idx, const void* k_idx, const flo
       a.nq = nq;
       a.out = static_cast<float*>(scratch);
       a.width = width;
-      a.T_total = cu_seqlens[num_seqs];
+      a.T_total = static_cast<int>(T);
+      a.flags = device_flags();  // a bounded wait that gives up raises TSA_FLAG_TIMEOUT, as in qsa_topk
       cudaError_t e = launch_indexer(a, s);
       if (e != cudaSuccess) return note_error(TSA_ERR_CUDA, cudaGetErrorString(e));
       TopkRows r;
