@@ -394,8 +394,8 @@ def run_gpu(args):
     if rank == 0 and world >= 1 and not args.no_cpu_baseline:
         dt, f, _ = oracle_sample(args.ref_rows)
         cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-               "sample": f"{args.ref_rows} random query rows of the same workload (indexer+top-k, fwd, bwd), "
-                         f"numpy fp64, {dt:.1f} s"}
+               "sample": f"{args.ref_rows} random query rows of the same workload (indexer+top-k, fwd, bwd, "
+                         f"teacher, indexer KL and backward), numpy fp64, {dt:.1f} s"}
 
     if rank == 0:
         line = {

@@ -267,14 +267,15 @@ int qsa_indexer_bwd(const void* q_idx_dev, const void* k_idx_dev, const float* w
  *   lse_dev fp32 [T, Hq].  Forward workspace:
  *   sparse_gqa_fwd_workspace_size(T, Hq, Hkv, d, nsel) bytes: the selections
  *   inverted per (block, kv group), and per selection slot the normalised
- *   partial output of its block (fp32, Hq/Hkv x d) with its log-sum-exp; the
- *   slots are merged in slot order.  Backward: dq [T,Hq,d], dk/dv [T,Hkv,d]
+ *   partial output of its block (bf16, Hq/Hkv x d: a convex combination of
+ *   value rows) with its log-sum-exp (fp32); the slots are merged in slot
+ *   order.  Backward: dq [T,Hq,d], dk/dv [T,Hkv,d]
  *   bf16 (overwritten), workspace sparse_gqa_bwd_workspace_size(T, Hq, Hkv,
  *   d, nsel) bytes: fp32 dq/dk/dv accumulators, rowsum(dO * O) and the
  *   selections inverted per (block, kv group), so that the backward visits
  *   each selected block once per chunk of the queries that chose it.
  * Supported: Hq/Hkv in {1..16}, d in {64, 128}, block_size in {32, 64},
- * T * Hkv * nsel < 2^31.  Block ids at or past the end of their sequence are
+ * T * Hkv * nsel < 2^31, T * Hq < 2^31.  Block ids at or past the end of their sequence are
  * dropped and raise TSA_FLAG_INDEX_RANGE.
  * Forward deterministic (bit-identical across runs); backward dq/dk/dv
  * summation order not fixed.

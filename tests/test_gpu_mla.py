@@ -308,11 +308,13 @@ def test_mla_h128_index_range_flag(tsa):
     check_out_lse(rf["out"], rf["lse"], o_ref, l_ref, rows=rows)
 
 
-@pytest.mark.parametrize("H", [64, 96])
+@pytest.mark.parametrize("H", [48, 64, 96])
 def test_mla_tp_head_counts_fwd_bwd(tsa, H):
-    """Head counts of a tensor-parallel slice of 128 heads (64) and a count that
-    is not a power of two (96): forward on sampled rows, dq of those rows and
-    the full dkv with dO kept on them only."""
+    """Head counts of a tensor-parallel slice of 128 heads (64), a count that is
+    not a power of two (96) and one that splits a warp of rows (48): the forward
+    runs on the tcgen05 kernel with the heads padded to 128 rows.  Forward on
+    sampled rows (and bit-identical on replay), dq of those rows and the full
+    dkv with dO kept on them only."""
     cu = [0, 900, 1500]
     T = cu[-1]
     m = synth.mla_inputs(T, H, 576, seed=H, with_grad_out=True)
@@ -323,6 +325,9 @@ def test_mla_tp_head_counts_fwd_bwd(tsa, H):
     mask[rows] = True
     m["dout"] = torch.where(mask[:, None, None], m["dout"], torch.zeros_like(m["dout"]))
     r = _run_fwd_bwd(tsa, m, idx, cu, scale)
+    out2, lse2 = tsa.sparse_mla_fwd(m["q"].to(DEV), m["kv"].to(DEV), idx.to(DEV), cu, scale)
+    torch.cuda.synchronize()
+    assert torch.equal(out2, r["out"]) and torch.equal(lse2, r["lse"])
     o_ref, l_ref = O.sparse_mla_fwd(m["q"], m["kv"], idx, cu, scale, rows=rows)
     check_out_lse(r["out"], r["lse"], o_ref, l_ref, rows=rows)
     dq_ref, dkv_ref = O.sparse_mla_bwd(m["q"], m["kv"], idx, cu, scale, m["dout"], rows=rows)

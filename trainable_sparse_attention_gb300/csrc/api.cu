@@ -497,8 +497,8 @@ static int check_gqa(int64_t T, int Hq, int Hkv, int d, int block_size, int nsel
 }
 
 // Workspace of the tcgen05 forward: the inverted selections and, per selection
-// slot (t, g, j), the normalised partial output of its block (fp32, G x d) and
-// its log2-sum-exp.
+// slot (t, g, j), the normalised partial output of its block (bf16, G x d) and
+// its log2-sum-exp (fp32).
 static size_t gqa_ws_align(size_t x) { return (x + 255) & ~size_t(255); }
 
 static size_t gqa_inv_bytes(size_t t, int Hkv, int nsel) {
@@ -509,7 +509,7 @@ static size_t gqa_inv_bytes(size_t t, int Hkv, int nsel) {
 size_t sparse_gqa_fwd_workspace_size(int64_t T, int Hq, int Hkv, int d, int nsel) {
   if (T < 0 || Hq < 1 || Hkv < 1 || d < 1 || nsel < 1) return 0;
   const size_t t = static_cast<size_t>(T);
-  return gqa_inv_bytes(t, Hkv, nsel) + gqa_ws_align(t * Hq * nsel * d * sizeof(float)) +
+  return gqa_inv_bytes(t, Hkv, nsel) + gqa_ws_align(t * Hq * nsel * d * sizeof(__nv_bfloat16)) +
          gqa_ws_align(t * Hq * nsel * sizeof(float));
 }
 
@@ -534,7 +534,8 @@ int sparse_gqa_fwd(const void* q, const void* k, const void* v, const int32_t* b
   int rc = make_seq_table(cu_seqlens, num_seqs, &a.st, &T);
   if (rc) return rc;
   if ((rc = check_gqa(T, Hq, Hkv, d, block_size, nsel))) return rc;
-  if (T * Hkv * nsel > 0x7fffffffLL) return fail(TSA_ERR_UNSUPPORTED, "T * Hkv * nsel beyond 2^31-1");
+  if (T * Hkv * nsel > 0x7fffffffLL || T * Hq > 0x7fffffffLL)
+    return fail(TSA_ERR_UNSUPPORTED, "T * Hkv * nsel or T * Hq beyond 2^31-1");
   if (T == 0) return TSA_OK;
   if (!q || !k || !v || !block_indices || !out || !lse) return fail(TSA_ERR_INVALID_ARG, "null tensor pointer");
   const size_t need = sparse_gqa_fwd_workspace_size(T, Hq, Hkv, d, nsel);
@@ -550,7 +551,7 @@ int sparse_gqa_fwd(const void* q, const void* k, const void* v, const int32_t* b
   a.off = reinterpret_cast<int*>(take((nb + 1) * sizeof(int)));
   a.cur = reinterpret_cast<int*>(take((nb + 1) * sizeof(int)));
   a.choff = reinterpret_cast<int*>(take((nb + 1) * sizeof(int)));
-  a.part_o = reinterpret_cast<float*>(take(t * Hq * nsel * d * sizeof(float)));
+  a.part_o = reinterpret_cast<__nv_bfloat16*>(take(t * Hq * nsel * d * sizeof(__nv_bfloat16)));
   a.part_l = reinterpret_cast<float*>(take(t * Hq * nsel * sizeof(float)));
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.k = static_cast<const __nv_bfloat16*>(k);
@@ -589,7 +590,8 @@ int sparse_gqa_bwd(const void* q, const void* k, const void* v, const int32_t* b
   int rc = make_seq_table(cu_seqlens, num_seqs, &a.st, &T);
   if (rc) return rc;
   if ((rc = check_gqa(T, Hq, Hkv, d, block_size, nsel))) return rc;
-  if (T * Hkv * nsel > 0x7fffffffLL) return fail(TSA_ERR_UNSUPPORTED, "T * Hkv * nsel beyond 2^31-1");
+  if (T * Hkv * nsel > 0x7fffffffLL || T * Hq > 0x7fffffffLL)
+    return fail(TSA_ERR_UNSUPPORTED, "T * Hkv * nsel or T * Hq beyond 2^31-1");
   if (T == 0) return TSA_OK;
   if (!q || !k || !v || !block_indices || !out || !lse || !dout || !dq || !dk || !dv)
     return fail(TSA_ERR_INVALID_ARG, "null tensor pointer");

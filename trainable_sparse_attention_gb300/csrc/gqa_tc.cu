@@ -20,9 +20,9 @@
 //                         keys (rows on TMEM lanes: one thread per row, the row
 //                         maximum and sum never leave the thread), P to TMEM as
 //                         bf16, O = P V (A operand read from TMEM);
-//                         the normalised partial O / l and its log-sum-exp go to
-//                         the slot (query, group, j) of the selection in the
-//                         caller's workspace;
+//                         the normalised partial O / l (bf16) and its
+//                         log-sum-exp (fp32) go to the slot (query, group, j)
+//                         of the selection in the caller's workspace;
 //   combine:              per (query, head), the partials of the selected
 //                         blocks are merged in slot order: the result does not
 //                         depend on the order of the inverted lists, so the
@@ -200,11 +200,12 @@ __device__ __forceinline__ void gt_gather_kv(uint32_t dst, const CUtensorMap* ma
 
 // Producer helpers: the rows of one batch (entries eb .. eb + qb of the chunk,
 // G heads each); lane l owns rows 4l .. 4l+3.  gt_batch_rows computes their
-// source rows of the [T * Hq, d] view (and, if tab is given, records each row's
-// selection entry (t * Hkv + g) * nsel + j, or -1); gt_gather_batch issues the
-// gathers into a 128-row Q (or dO) buffer.
-__device__ __forceinline__ void gt_batch_rows(const GqaTcArgs& a, const GtChunk& ck, int eb, int* tab, int lane,
-                                              int (&r)[4]) {
+// source rows of the [T * Hq, d] view and, if tab is given, records for each
+// row its selection entry (t * Hkv + g) * nsel + j, or with tab_rows that
+// source row t * Hq + h, or -1; gt_gather_batch issues the gathers into a
+// 128-row Q (or dO) buffer.
+__device__ __forceinline__ void gt_batch_rows(const GqaTcArgs& a, const GtChunk& ck, int eb, int* tab, bool tab_rows,
+                                              int lane, int (&r)[4]) {
   const int G = a.G, qb = GT_ROWS / G;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -213,8 +214,8 @@ __device__ __forceinline__ void gt_batch_rows(const GqaTcArgs& a, const GtChunk&
     const int ei = eb + qi;
     const bool ok = qi < qb && ei < ck.e1;
     const int e = ok ? __ldg(a.list + ei) : -1;
-    if (tab != nullptr) tab[row] = e;
     r[i] = (ok ? e / (a.Hkv * a.nsel) : 0) * a.Hq + ck.g * G + hh;
+    if (tab != nullptr) tab[row] = ok ? (tab_rows ? r[i] : e) : -1;
   }
 }
 __device__ __forceinline__ void gt_gather_batch(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int d,
@@ -308,7 +309,7 @@ __global__ void __launch_bounds__(GT_THREADS, 2)
       // the row table is read by the row warps after they see qfull: every lane
       // writes its rows' entries before lane 0's arrival releases them
       int r[4];
-      gt_batch_rows(a, ck, ck.e0 + i * qb, tab + buf * GT_ROWS, lane, r);
+      gt_batch_rows(a, ck, ck.e0 + i * qb, tab + buf * GT_ROWS, false, lane, r);
       __syncwarp();
       if (lane == 0) tc::mbar_arrive_expect_tx(&qfull[buf], q_bytes);
       __syncwarp();
@@ -419,9 +420,10 @@ __global__ void __launch_bounds__(GT_THREADS, 2)
         break;
       }
       tc::fence_after_sync();
-      // partial O / l and its log2-sum-exp into the selection slot of this row
+      // partial O / l (bf16: a convex combination of value rows) and its
+      // log2-sum-exp (fp32) into the selection slot of this row
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      float* dst = e >= 0 ? a.part_o + ((int64_t)e * a.G + hh) * a.d : nullptr;
+      __nv_bfloat16* dst = e >= 0 ? a.part_o + ((int64_t)e * a.G + hh) * a.d : nullptr;
 #pragma unroll 1
       for (int cb = 0; cb < a.d / 32; ++cb) {
         uint32_t r[32];
@@ -430,10 +432,12 @@ __global__ void __launch_bounds__(GT_THREADS, 2)
         tc::tmem_ld_wait();
         if (dst != nullptr) {
 #pragma unroll
-          for (int k = 0; k < 32; k += 4)
-            *reinterpret_cast<float4*>(dst + cb * 32 + k) =
-                make_float4(__uint_as_float(r[k]) * inv, __uint_as_float(r[k + 1]) * inv,
-                            __uint_as_float(r[k + 2]) * inv, __uint_as_float(r[k + 3]) * inv);
+          for (int k = 0; k < 32; k += 8)
+            *reinterpret_cast<uint4*>(dst + cb * 32 + k) =
+                make_uint4(pack_bf16(__uint_as_float(r[k]) * inv, __uint_as_float(r[k + 1]) * inv),
+                           pack_bf16(__uint_as_float(r[k + 2]) * inv, __uint_as_float(r[k + 3]) * inv),
+                           pack_bf16(__uint_as_float(r[k + 4]) * inv, __uint_as_float(r[k + 5]) * inv),
+                           pack_bf16(__uint_as_float(r[k + 6]) * inv, __uint_as_float(r[k + 7]) * inv));
         }
       }
       if (e >= 0) a.part_l[(int64_t)e * a.G + hh] = l > 0.f ? m + log2f(l) : -INFINITY;
@@ -482,11 +486,13 @@ __global__ void __launch_bounds__(256) gqa_combine_kernel(const __grid_constant_
       const float wj = exp2f(__ldg(a.part_l + (e0 + j) * a.G + hh) - M);
       W += wj;
       if (lane < nv) {
-        const float4 o = __ldg(reinterpret_cast<const float4*>(a.part_o + ((e0 + j) * a.G + hh) * a.d) + lane);
-        acc.x = fmaf(wj, o.x, acc.x);
-        acc.y = fmaf(wj, o.y, acc.y);
-        acc.z = fmaf(wj, o.z, acc.z);
-        acc.w = fmaf(wj, o.w, acc.w);
+        const uint2 raw = __ldg(reinterpret_cast<const uint2*>(a.part_o + ((e0 + j) * a.G + hh) * a.d) + lane);
+        const float2 o01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+        const float2 o23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+        acc.x = fmaf(wj, o01.x, acc.x);
+        acc.y = fmaf(wj, o01.y, acc.y);
+        acc.z = fmaf(wj, o23.x, acc.z);
+        acc.w = fmaf(wj, o23.y, acc.w);
       }
     }
   }
@@ -658,7 +664,7 @@ __global__ void __launch_bounds__(GB_THREADS, 1)
         break;
       }
       int r[4];
-      gt_batch_rows(a, ck, ck.e0 + i * qb, tab + buf * GT_ROWS, lane, r);
+      gt_batch_rows(a, ck, ck.e0 + i * qb, tab + buf * GT_ROWS, true, lane, r);
       __syncwarp();
       if (lane == 0) tc::mbar_arrive_expect_tx(&qfull[buf], q_bytes);
       __syncwarp();
@@ -679,18 +685,10 @@ __global__ void __launch_bounds__(GB_THREADS, 1)
       constexpr uint32_t id_s = tc::idesc_bf16_f32(GT_ROWS, GT_KEYS);
       constexpr uint32_t id_kv = tc::idesc_bf16_f32(GT_DP, GT_KEYS) | (1u << 15) | (1u << 16);  // A, B MN-major
       constexpr uint32_t id_q = tc::idesc_bf16_f32(GT_DP, GT_ROWS) | (1u << 15);                // A MN-major
-      bool ok = tc::mbar_wait(kvfull, 0, abort_flag);
-      for (int i = 0; ok && i < nbatch; ++i) {
+      // S = Q K^T and dP = dO V^T of batch i into buffer i & 1 (K = the head dimension)
+      auto issue_s = [&](int i) {
         const int buf = i & 1;
-        const uint32_t ph = i & 1;
-        if (!tc::mbar_wait(&qfull[buf], (i >> 1) & 1, abort_flag) ||
-            (i >= 2 && !tc::mbar_wait(&sempty[buf], ((i >> 1) & 1) ^ 1u, abort_flag))) {
-          ok = false;
-          break;
-        }
-        tc::fence_after_sync();
         const uint32_t qt = sQ + buf * GT_QT, ot = sO + buf * GT_QT;
-        // S = Q K^T and dP = dO V^T (K = the head dimension)
 #pragma unroll
         for (int ks = 0; ks < GT_DP / 16; ++ks) {
           const int c = ks >> 2, kk = ks & 3;
@@ -700,12 +698,39 @@ __global__ void __launch_bounds__(GB_THREADS, 1)
                           tc::desc_sw128(sV + c * GT_KBOX + kk * 32), id_s, ks > 0 ? 1u : 0u);
         }
         tc::mma_commit(&sfull[buf]);
+      };
+      // batch i's rows landed and its S / dP buffer free (rows read batch i-2's)
+      auto s_ready = [&](int i, bool block) {
+        const int buf = i & 1;
+        if (block)
+          return tc::mbar_wait(&qfull[buf], (i >> 1) & 1, abort_flag) &&
+                 (i < 2 || tc::mbar_wait(&sempty[buf], ((i >> 1) & 1) ^ 1u, abort_flag));
+        return tc::mbar_try_wait(&qfull[buf], (i >> 1) & 1) &&
+               (i < 2 || tc::mbar_try_wait(&sempty[buf], ((i >> 1) & 1) ^ 1u));
+      };
+      bool ok = tc::mbar_wait(kvfull, 0, abort_flag) && (nbatch == 0 || s_ready(0, true));
+      if (ok && nbatch > 0) {
+        tc::fence_after_sync();
+        issue_s(0);
+      }
+      for (int i = 0; ok && i < nbatch; ++i) {
+        const int buf = i & 1;
+        const uint32_t ph = i & 1;
+        // S / dP of the next batch first if its rows are already here, so the
+        // row warps find it ready when they finish this batch
+        bool next_done = false;
+        if (i + 1 < nbatch && s_ready(i + 1, false)) {
+          tc::fence_after_sync();
+          issue_s(i + 1);
+          next_done = true;
+        }
         // the rows' P and dS of this batch, and the drained dQ^T of the previous one
         if (!tc::mbar_wait(psfull, ph, abort_flag) || (i > 0 && !tc::mbar_wait(dqempty, ph ^ 1u, abort_flag))) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
+        const uint32_t qt = sQ + buf * GT_QT, ot = sO + buf * GT_QT;
         // dV^T += dO^T P, dK^T += Q^T dS (K = the batch's 128 rows)
 #pragma unroll
         for (int ks = 0; ks < GT_ROWS / 16; ++ks) {
@@ -722,6 +747,14 @@ __global__ void __launch_bounds__(GB_THREADS, 1)
                           id_q, ks > 0 ? 1u : 0u);
         tc::mma_commit(psempty);
         tc::mma_commit(dqfull);
+        if (i + 1 < nbatch && !next_done) {
+          if (!s_ready(i + 1, true)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          issue_s(i + 1);
+        }
       }
       if (!ok) *abort_flag = 1;
     }
@@ -733,7 +766,6 @@ __global__ void __launch_bounds__(GB_THREADS, 1)
     const int qd = warp & 3, hf = warp >> 2;
     const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
     const int row = qd * 32 + lane;
-    const int hh = row % a.G;
     const int ch = qd * 32 + lane;  // channel in the transposed products
     for (int i = 0; i < nbatch; ++i) {
       const int buf = i & 1;
@@ -744,13 +776,12 @@ __global__ void __launch_bounds__(GB_THREADS, 1)
         break;
       }
       tc::fence_after_sync();
-      const int* tb = tab + buf * GT_ROWS;
-      const int e = tb[row];
-      const int t = e >= 0 ? e / (a.Hkv * a.nsel) : 0;
-      const int h = ck.g * a.G + hh;
-      const int lim = e < 0 ? 0 : min(min(a.bs, ck.n - ck.kbase), t - ck.s0 - ck.kbase + 1);
-      const float lse2 = e >= 0 ? __ldg(a.lse_in + (int64_t)t * a.Hq + h) * kLog2e : 0.f;
-      const float dl = e >= 0 ? __ldg(a.dlt + (int64_t)t * a.Hq + h) : 0.f;
+      const int* tb = tab + buf * GT_ROWS;  // per batch row: its row t * Hq + h of q / dO / dq, or -1
+      const int qrow = tb[row];
+      const int t = qrow >= 0 ? qrow / a.Hq : 0;
+      const int lim = qrow < 0 ? 0 : min(min(a.bs, ck.n - ck.kbase), t - ck.s0 - ck.kbase + 1);
+      const float lse2 = qrow >= 0 ? __ldg(a.lse_in + qrow) * kLog2e : 0.f;
+      const float dl = qrow >= 0 ? __ldg(a.dlt + qrow) : 0.f;
       uint32_t sr[32], dr[32];
       __syncwarp();
       tc::tmem_ld32(tmem + lane_base + GB_T_S + buf * GT_KEYS + hf * 32, sr);
@@ -799,12 +830,8 @@ __global__ void __launch_bounds__(GB_THREADS, 1)
         tc::tmem_ld_wait();
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          const int rr = hf * 64 + cb * 32 + k;
-          const int er = tb[rr];
-          if (er >= 0 && ch < a.d) {
-            const int tr = er / (a.Hkv * a.nsel);
-            red_f32(a.dq_acc + ((int64_t)tr * a.Hq + ck.g * a.G + rr % a.G) * a.d + ch, __uint_as_float(r[k]));
-          }
+          const int qr = tb[hf * 64 + cb * 32 + k];
+          if (qr >= 0 && ch < a.d) red_f32(a.dq_acc + (int64_t)qr * a.d + ch, __uint_as_float(r[k]));
         }
       }
       tc::fence_before_sync();

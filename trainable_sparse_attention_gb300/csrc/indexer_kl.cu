@@ -58,17 +58,22 @@ namespace {
 
 constexpr int KL_M = 128;       // slots per tile
 constexpr int KL_DI = 128;      // indexer head dimension (the only one built here)
-constexpr int KL_STAGES = 3;
 constexpr int KL_THREADS = 192;
 constexpr int KL_KBOX = KL_M * 128;          // one 64-channel box of a gathered tile: 16 KB
 constexpr int KL_KSTAGE = 2 * KL_KBOX;       // d_I = 128: two boxes
 
+// NP = 64: two CTAs per SM (two gather stages, at most 256 TMEM columns each,
+// D^T single-buffered in the backward), so that one query's pipeline fill and
+// final row pass overlap the other's tiles.  NP = 128: one CTA per SM.
 template <int NP, bool BWD>
 struct KlLayout {
+  static constexpr int CTAS = NP == 64 ? 2 : 1;          // resident CTAs per SM
+  static constexpr int STAGES = NP == 64 ? 2 : 3;        // gather ring
+  static constexpr int DB = (BWD && NP == 64) ? 1 : 2;   // D^T buffers
   static constexpr int QBOX = NP * 128;                  // one 64-channel box of q_I[t] (NP rows)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + 2 * QBOX;
-  static constexpr int OFF_C = OFF_K + KL_STAGES * KL_KSTAGE;
+  static constexpr int OFF_C = OFF_K + STAGES * KL_KSTAGE;
   static constexpr int CBOX = KL_M * 128;                // 64 heads of C for the tile's 128 slots
   static constexpr int C_BYTES = BWD ? (NP / 64) * CBOX : 0;
   static constexpr int OFF_W = OFF_C + C_BYTES;          // head weights [NP]
@@ -77,11 +82,14 @@ struct KlLayout {
   static constexpr int OFF_RED = OFF_SC + SC_BYTES;      // block reductions [8]
   static constexpr int OFF_BAR = OFF_RED + 64;
   static constexpr int SMEM = 1024 + OFF_BAR + 256;
-  // TMEM columns: D^T double-buffered, then (backward) dq^T and dk^T
+  // TMEM columns: D^T (DB buffers), then (backward) dq^T and dk^T
   static constexpr int T_D = 0;
-  static constexpr int T_DQ = 2 * NP;
-  static constexpr int T_DK = 3 * NP;
-  static constexpr int TMEM_COLS = BWD ? 512 : (2 * NP <= 128 ? 128 : 256);
+  static constexpr int T_DQ = DB * NP;
+  static constexpr int T_DK = T_DQ + NP;
+  static constexpr int USED_COLS = BWD ? T_DK + KL_M : DB * NP;
+  static constexpr int TMEM_COLS = USED_COLS <= 128 ? 128 : USED_COLS <= 256 ? 256 : 512;
+  static_assert(CTAS * TMEM_COLS <= 512, "TMEM columns of the resident CTAs");
+  static_assert(CTAS * (SMEM + 1024) <= 228 * 1024, "shared memory of the resident CTAs");
 };
 
 // Sum over the 32 lanes of N values per lane by recursive halving: afterwards
@@ -115,7 +123,7 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
 
 
 template <int NP, bool BWD>
-__global__ void __launch_bounds__(KL_THREADS, 1)
+__global__ void __launch_bounds__(KL_THREADS, KlLayout<NP, BWD>::CTAS)
     indexer_sel_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ IndexerSelArgs a) {
   using L = KlLayout<NP, BWD>;
@@ -130,9 +138,9 @@ __global__ void __launch_bounds__(KL_THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + L::OFF_BAR);
   uint64_t* qfull = bars;                      // [1] q_I[t] landed
   uint64_t* kfull = bars + 1;                  // [STAGES] gathered tile landed
-  uint64_t* kempty = kfull + KL_STAGES;        // [STAGES] its MMAs are done
-  uint64_t* dfull = kempty + KL_STAGES;        // [2] D^T ready
-  uint64_t* dempty = dfull + 2;                // [2] epilogue read D^T (4 warps)
+  uint64_t* kempty = kfull + L::STAGES;        // [STAGES] its MMAs are done
+  uint64_t* dfull = kempty + L::STAGES;        // [DB] D^T ready
+  uint64_t* dempty = dfull + 2;                // [DB] epilogue read D^T (4 warps)
   uint64_t* cfull = dempty + 2;                // [1] C tile written (4 warps)
   uint64_t* cempty = cfull + 1;                // [1] MMAs reading C done
   uint64_t* dkfull = cempty + 1;               // [1] dk^T ready
@@ -151,7 +159,7 @@ __global__ void __launch_bounds__(KL_THREADS, 1)
 
   if (tid == 0) {
     tc::mbar_init(qfull, 1);
-    for (int i = 0; i < KL_STAGES; ++i) {
+    for (int i = 0; i < L::STAGES; ++i) {
       tc::mbar_init(&kfull[i], 1);
       tc::mbar_init(&kempty[i], 1);
     }
@@ -187,8 +195,8 @@ __global__ void __launch_bounds__(KL_THREADS, 1)
     }
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
-      const int st = j % KL_STAGES;
-      if (!__all_sync(0xffffffffu, tc::mbar_wait(&kempty[st], ((j / KL_STAGES) & 1) ^ 1u, abort_flag))) {
+      const int st = j % L::STAGES;
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&kempty[st], ((j / L::STAGES) & 1) ^ 1u, abort_flag))) {
         ok = false;
         break;
       }
@@ -211,8 +219,8 @@ __global__ void __launch_bounds__(KL_THREADS, 1)
     // gathers still in flight land before the CTA exits (bounded by time only)
     if (lane == 0) {
       volatile int keep_waiting = 0;
-      for (int g = issued > KL_STAGES ? issued - KL_STAGES : 0; g < issued; ++g)
-        (void)tc::mbar_wait(&kfull[g % KL_STAGES], (g / KL_STAGES) & 1, &keep_waiting);
+      for (int g = issued > L::STAGES ? issued - L::STAGES : 0; g < issued; ++g)
+        (void)tc::mbar_wait(&kfull[g % L::STAGES], (g / L::STAGES) & 1, &keep_waiting);
       (void)tc::mbar_wait(qfull, 0, &keep_waiting);
     }
   } else if (warp == 5) {
@@ -223,9 +231,9 @@ __global__ void __launch_bounds__(KL_THREADS, 1)
       constexpr uint32_t id_dk = tc::idesc_bf16_f32(KL_DI, KL_M) | (1u << 15);               // A MN-major
       bool ok = tc::mbar_wait(qfull, 0, abort_flag);
       for (int j = 0; ok && j < ntiles; ++j) {
-        const int st = j % KL_STAGES, acc = j & 1;
-        if (!tc::mbar_wait(&kfull[st], (j / KL_STAGES) & 1, abort_flag) ||
-            !tc::mbar_wait(&dempty[acc], ((j >> 1) & 1) ^ 1u, abort_flag)) {
+        const int st = j % L::STAGES, acc = j % L::DB;
+        if (!tc::mbar_wait(&kfull[st], (j / L::STAGES) & 1, abort_flag) ||
+            (j >= L::DB && !tc::mbar_wait(&dempty[acc], ((j / L::DB) & 1) ^ 1u, abort_flag))) {
           ok = false;
           break;
         }
@@ -273,13 +281,13 @@ __global__ void __launch_bounds__(KL_THREADS, 1)
 #pragma unroll
     for (int i = 0; i < NP / 32; ++i) dwacc[i] = 0.f;
     for (int j = 0; j < ntiles; ++j) {
-      const int acc = j & 1;
+      const int acc = j % L::DB;
       const int slot = j * KL_M + slot_in_tile;
       const int id = slot < a.topk ? __ldg(idx_row + slot) : -1;
       const bool valid = id >= 0 && id < n;
       float g = 0.f;
       if constexpr (BWD) g = valid ? a.score_scale * __ldg(a.dscore + (int64_t)t * a.topk + slot) : 0.f;
-      if (!__all_sync(0xffffffffu, tc::mbar_wait(&dfull[acc], (j >> 1) & 1, abort_flag))) {
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&dfull[acc], (j / L::DB) & 1, abort_flag))) {
         *abort_flag = 1;
         break;
       }

@@ -104,7 +104,7 @@ struct GqaTcArgs {
   int* cur;                   // [nblk * Hkv] fill cursors
   int* choff;                 // [nblk * Hkv + 1] chunk offsets
   int* list;                  // [T * Hkv * nsel] per (block, group): flat selection indices (t * Hkv + g) * nsel + j
-  float* part_o;              // forward: [T * Hkv * nsel, G, d] normalised partial outputs
+  __nv_bfloat16* part_o;      // forward: [T * Hkv * nsel, G, d] normalised partial outputs (bf16)
   float* part_l;              // forward: [T * Hkv * nsel, G] their log2-sum-exp
   __nv_bfloat16* out;         // forward: [T, Hq, d]
   float* lse;                 // forward: [T, Hq]
@@ -174,6 +174,7 @@ cudaError_t launch_bwd_delta(const __nv_bfloat16* o, const __nv_bfloat16* dout, 
                              cudaStream_t stream);
 cudaError_t launch_f32_to_bf16(const float* src, __nv_bfloat16* dst, int64_t n, cudaStream_t stream);
 
+constexpr int kMlaFwdTcMinHeads = 32;  // the forward runs on tcgen05 (heads padded to 128) above this
 constexpr int kIndexerKTile = 128;  // keys per indexer tile (block sizes must divide it)
 constexpr int kTopkMaxK = 4096;
 

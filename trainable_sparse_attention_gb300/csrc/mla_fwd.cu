@@ -185,11 +185,12 @@ static size_t mla_fwd_smem() {
          sizeof(float) * 8 * MF_HB;
 }
 
-// H = 128 runs on the tcgen05 cluster kernel (mla_fwd_tc.cu); other head
-// counts, which leave most of a 128-row MMA empty, run here.
+// H > 32 runs on the tcgen05 cluster kernel (mla_fwd_tc.cu), heads padded to
+// its 128 MMA rows; fewer heads, which would leave most of a 128-row MMA empty,
+// run here (one CTA per query and 16 heads).
 cudaError_t launch_mla_fwd(const MlaFwdArgs& a, int D, cudaStream_t stream) {
   if (a.T <= 0) return cudaSuccess;
-  if (a.H == 128) return launch_mla_fwd_tc(a, D, stream);
+  if (a.H > kMlaFwdTcMinHeads) return launch_mla_fwd_tc(a, D, stream);
   dim3 grid(a.T, (a.H + MF_HB - 1) / MF_HB);
   if (D == 576) {
     size_t smem = mla_fwd_smem<576>();

@@ -1,5 +1,9 @@
 // Sparse MLA forward for H = 128 heads on tcgen05 (TMEM accumulators, 2-CTA
-// cluster, TMA gathers into swizzled tiles).
+// cluster, TMA gathers into swizzled tiles).  Tensor-parallel head counts
+// H < 128 (64 for a two-way split of 128 heads) run on the same kernel with the
+// heads padded to the MMA's 128 rows: rows h >= H get a zero q row and write
+// nothing (Megatron-LM PR #7617 backport commit message: the FlashMLA route pads
+// TP-local heads to the kernel's head tile).
 //
 // Megatron-LM PR #3674 "Enable DSA CP/absorbed/THD paths with TileLang fused
 // ops" (sparse MLA forward over the absorbed latent) and Megatron-LM PR #7617
@@ -300,12 +304,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     // q slice row h -> TMEM columns [MT_QCOL, MT_QCOL + 32 kb)
     {
-      const uint4* qrow = reinterpret_cast<const uint4*>(a.q + ((int64_t)t * MT_H + h) * D + ch0);
+      // heads h >= H (a tensor-parallel slice padded to the MMA's 128 rows) get a
+      // zero q row: their logits are 0, and nothing of them is written
+      const bool real = h < a.H;
+      const uint4* qrow = reinterpret_cast<const uint4*>(a.q + ((int64_t)t * a.H + (real ? h : 0)) * D + ch0);
       for (int c = 0; c < kb; ++c) {
         uint32_t r[32];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const uint4 v = __ldg(qrow + c * 8 + i);
+          const uint4 v = real ? __ldg(qrow + c * 8 + i) : make_uint4(0u, 0u, 0u, 0u);
           r[4 * i] = v.x;
           r[4 * i + 1] = v.y;
           r[4 * i + 2] = v.z;
@@ -451,8 +458,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
     // epilogue: O row / l -> bf16, lse
     const int lb = (ntiles - 1) & 1;
     const bool last_ok = ok && __all_sync(0xffffffffu, tc::mbar_wait(&p_empty[lb], ((ntiles - 1) >> 1) & 1, abort_flag));
-    __nv_bfloat16* orow = a.out + ((int64_t)t * MT_H + h) * MT_DV + ch0;
+    const bool real_head = h < a.H;
+    __nv_bfloat16* orow = a.out + ((int64_t)t * a.H + (real_head ? h : 0)) * MT_DV + ch0;
     if (last_ok) {
+      // every lane takes part in the (warp-collective) TMEM loads; only the
+      // rows of real heads are stored
       tc::fence_after_sync();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       for (int cb = 0; cb < MT_OCOLS / 32; ++cb) {
@@ -461,6 +471,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
         tc::tmem_ld32(tmem + lane_base + cb * 32, o);
         tc::tmem_ld_wait();
         uint4* dst = reinterpret_cast<uint4*>(orow + cb * 32);
+        if (real_head)
 #pragma unroll
         for (int q = 0; q < 4; ++q)
           dst[q] = make_uint4(pack_bf16(__uint_as_float(o[8 * q]) * inv, __uint_as_float(o[8 * q + 1]) * inv),
@@ -468,12 +479,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
                               pack_bf16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv),
                               pack_bf16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv));
       }
-      if (rank == 0) a.lse[(int64_t)t * MT_H + h] = l > 0.f ? (m_use + log2f(l)) * kLn2 : NEG_INF;
+      if (rank == 0 && real_head) a.lse[(int64_t)t * a.H + h] = l > 0.f ? (m_use + log2f(l)) * kLn2 : NEG_INF;
     } else {
       // wound down after a timeout: zero output row, -inf lse
       *abort_flag = 1;
-      for (int c = 0; c < MT_OCOLS; c += 8) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
-      if (rank == 0) a.lse[(int64_t)t * MT_H + h] = NEG_INF;
+      if (real_head) {
+        for (int c = 0; c < MT_OCOLS; c += 8) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
+        if (rank == 0) a.lse[(int64_t)t * a.H + h] = NEG_INF;
+      }
     }
   }
 
