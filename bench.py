@@ -438,7 +438,8 @@ def run_gqa(args, tsa, dev, world):
     2 d bf16 per triple."""
     import torch
     import synth
-    cu = synth.cu_seqlens_thd(GQA_LENGTHS)
+    lengths = GQA_LENGTHS if args.gqa_lengths is None else [int(v) for v in args.gqa_lengths.split(",")]
+    cu = synth.cu_seqlens_thd(lengths)
     T = cu[-1]
     g = synth.gqa_inputs(T, GQA_HQ, GQA_HKV, GQA_D, seed=8, device=dev, with_grad_out=True)
     x = synth.indexer_inputs(T, GQA_HI, GQA_DI, seed=6, device=dev)
@@ -475,7 +476,7 @@ def run_gqa(args, tsa, dev, world):
     b = blk.long()
     ntok = torch.where(b >= 0, torch.clamp(p[:, None, None] - b * GQA_BS + 1, 0, GQA_BS), torch.zeros_like(b))
     triples = int(ntok.sum().item())
-    pairs = sum(n * (n + 1) // 2 for n in GQA_LENGTHS)
+    pairs = sum(n * (n + 1) // 2 for n in lengths)
     G = GQA_HQ // GQA_HKV
     f_idx = pairs * GQA_HI * GQA_DI * 2
     f_fwd = triples * 4 * GQA_D * G
@@ -491,8 +492,8 @@ def run_gqa(args, tsa, dev, world):
     del g, x, ws, ws_f, ws_b, blk
     torch.cuda.empty_cache()
     return {
-        "workload": "qsa_gqa_thd32768_hq32_hkv4_bs64_top32",
-        "lengths": GQA_LENGTHS, "Hq": GQA_HQ, "Hkv": GQA_HKV, "d": GQA_D, "block_size": GQA_BS,
+        "workload": f"qsa_gqa_thd{T}_hq32_hkv4_bs64_top32",
+        "lengths": lengths, "Hq": GQA_HQ, "Hkv": GQA_HKV, "d": GQA_D, "block_size": GQA_BS,
         "blocks_selected": GQA_NSEL, "indexer_heads": GQA_HI, "d_I": GQA_DI, "steps": steps,
         "note": "timed separately after the main step; not part of value",
         "block_indexer_topk": {"ms": ms[0], "tflops": job_tflops(world, f_idx, ms[0]),
@@ -636,6 +637,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-gqa", action="store_true", help="skip the separately timed block Sparse-GQA workload")
+    ap.add_argument("--gqa-lengths", default=None,
+                    help="profiling aid: comma-separated sequence lengths of the GQA workload (default 4096,8192,12288,8192)")
     ap.add_argument("--gqa-only", action="store_true",
                     help="profiling aid: time only the block Sparse-GQA workload and print its object")
     args = ap.parse_args()

@@ -194,8 +194,19 @@ __global__ void __launch_bounds__(KL_THREADS, KlLayout<NP, BWD>::CTAS)
       for (int c = 0; c < 2; ++c) tc::tma_load_2d(sQ + c * L::QBOX, &tm_q, qfull, c * 64, t * a.H_I);
     }
     bool ok = true;
+    // the slot indices of tile j + 1 are loaded while tile j's stage frees up
+    int id_next[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) id_next[i] = 4 * lane + i < a.topk ? __ldg(idx_row + 4 * lane + i) : -1;
     for (int j = 0; j < ntiles; ++j) {
       const int st = j % L::STAGES;
+      int id[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        id[i] = id_next[i];
+        const int slot = (j + 1) * KL_M + 4 * lane + i;
+        id_next[i] = slot < a.topk ? __ldg(idx_row + slot) : -1;
+      }
       if (!__all_sync(0xffffffffu, tc::mbar_wait(&kempty[st], ((j / L::STAGES) & 1) ^ 1u, abort_flag))) {
         ok = false;
         break;
@@ -203,10 +214,8 @@ __global__ void __launch_bounds__(KL_THREADS, KlLayout<NP, BWD>::CTAS)
       int r[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int slot = j * KL_M + 4 * lane + i;
-        const int id = slot < a.topk ? __ldg(idx_row + slot) : -1;
-        if (id >= n) raise_flag(a.flags, TSA_FLAG_INDEX_RANGE);
-        r[i] = s0 + ((id >= 0 && id < n) ? id : 0);
+        if (id[i] >= n) raise_flag(a.flags, TSA_FLAG_INDEX_RANGE);
+        r[i] = s0 + ((id[i] >= 0 && id[i] < n) ? id[i] : 0);
       }
       if (lane == 0) tc::mbar_arrive_expect_tx(&kfull[st], KL_KSTAGE);
       __syncwarp();
@@ -348,18 +357,24 @@ __global__ void __launch_bounds__(KL_THREADS, KlLayout<NP, BWD>::CTAS)
         for (int i = 0; i < NP / 32; ++i) dwacc[i] += dwv[i];
         // dk^T tile: this warp's 32 channels (TMEM lanes) x the tile's 128 slots, one reduction per
         // (slot, channel): every warp instruction covers one 128-byte line of a key row
+        // key rows of the tile's slots cb*32 + lane (cb = 0..3), one per lane and
+        // block, loaded before the wait and broadcast below
+        int rowq[KL_M / 32];
+#pragma unroll
+        for (int cb = 0; cb < KL_M / 32; ++cb) {
+          const int sl = j * KL_M + cb * 32 + lane;
+          const int idc = sl < a.topk ? __ldg(idx_row + sl) : -1;
+          rowq[cb] = (idc >= 0 && idc < n) ? s0 + idc : -1;
+        }
         if (!__all_sync(0xffffffffu, tc::mbar_wait(dkfull, j & 1, abort_flag))) {
           *abort_flag = 1;
           break;
         }
         tc::fence_after_sync();
         const int ch = warp * 32 + lane;
-#pragma unroll 1
+#pragma unroll
         for (int cb = 0; cb < KL_M / 32; ++cb) {
-          // key rows of slots cb*32 .. +31 of the tile, one per lane, broadcast below
-          const int sl = j * KL_M + cb * 32 + lane;
-          const int idc = sl < a.topk ? __ldg(idx_row + sl) : -1;
-          const int rowc = (idc >= 0 && idc < n) ? s0 + idc : -1;
+          const int rowc = rowq[cb];
           uint32_t r[32];
           __syncwarp();
           tc::tmem_ld32(tmem + lane_base + L::T_DK + cb * 32, r);
@@ -410,16 +425,27 @@ __global__ void __launch_bounds__(KL_THREADS, KlLayout<NP, BWD>::CTAS)
       float lsum = 0.f;
       const float* arow = a.teacher + (int64_t)t * a.topk;
       float* grow = a.dscore_out + (int64_t)t * a.topk;
-      for (int s = tid; s < a.topk; s += KL_THREADS) {
-        const float z_s = sc[s];
-        float gval = 0.f;
-        if (z_s != -INFINITY) {
-          const float lp = z_s - lz;
-          const float av = __ldg(arow + s);
-          gval = expf(lp) - av;
-          if (av > 0.f) lsum += av * (logf(av) - lp);
+      // four teacher loads per thread in flight at a time
+      for (int s4 = tid; s4 < a.topk; s4 += 4 * KL_THREADS) {
+        float av[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int s = s4 + u * KL_THREADS;
+          av[u] = s < a.topk ? __ldg(arow + s) : 0.f;
         }
-        grow[s] = gval;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int s = s4 + u * KL_THREADS;
+          if (s >= a.topk) break;
+          const float z_s = sc[s];
+          float gval = 0.f;
+          if (z_s != -INFINITY) {
+            const float lp = z_s - lz;
+            gval = expf(lp) - av[u];
+            if (av[u] > 0.f) lsum += av[u] * (logf(av[u]) - lp);
+          }
+          grow[s] = gval;
+        }
       }
       lsum = warp_sum(lsum);
       if (lane == 0) red[warp] = lsum;
