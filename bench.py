@@ -632,7 +632,7 @@ def main():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--ref-rows", type=int, default=48, help="oracle rows per CPU sample")
+    ap.add_argument("--ref-rows", type=int, default=192, help="oracle rows per CPU sample")
     ap.add_argument("--T", type=int, default=T_TOK, help="sequence length (smaller only for profiling captures)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

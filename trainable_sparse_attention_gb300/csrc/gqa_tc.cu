@@ -458,7 +458,9 @@ __global__ void __launch_bounds__(GT_THREADS, 2)
 }
 
 // Merge of the partials: one warp per (query, head), the selected blocks in
-// slot order (fixed, so the result is bit-identical across runs).
+// slot order (fixed, so the result is bit-identical across runs).  Lane j holds
+// slot j's log-sum-exp (32 slots per round), the weights come from warp
+// reductions, and the partial rows are read eight slots at a time.
 __global__ void __launch_bounds__(256) gqa_combine_kernel(const __grid_constant__ GqaTcArgs a) {
   const int64_t rowid = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -470,31 +472,50 @@ __global__ void __launch_bounds__(256) gqa_combine_kernel(const __grid_constant_
   const int n = a.st.cu[s + 1] - a.st.cu[s];
   const int32_t* brow = a.blk + ((int64_t)t * a.Hkv + g) * a.nsel;
   const int64_t e0 = ((int64_t)t * a.Hkv + g) * a.nsel;
+  const int nv = a.d / 4;  // four channels per lane
+  // pass 1: the maximum log-sum-exp over the valid slots
   float M = -INFINITY;
-  for (int j = 0; j < a.nsel; ++j) {
-    const int b = __ldg(brow + j);
-    if (b < 0 || (int64_t)b * a.bs >= n || (int64_t)b * a.bs > p) continue;
-    M = fmaxf(M, __ldg(a.part_l + (e0 + j) * a.G + hh));
+  for (int j0 = 0; j0 < a.nsel; j0 += 32) {
+    const int j = j0 + lane;
+    const int b = j < a.nsel ? __ldg(brow + j) : -1;
+    const bool ok = b >= 0 && (int64_t)b * a.bs < n && (int64_t)b * a.bs <= p;
+    M = fmaxf(M, ok ? __ldg(a.part_l + (e0 + j) * a.G + hh) : -INFINITY);
   }
+  M = warp_max(M);
   float W = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int nv = a.d / 4;  // float4 per row
   if (M != -INFINITY) {
-    for (int j = 0; j < a.nsel; ++j) {
-      const int b = __ldg(brow + j);
-      if (b < 0 || (int64_t)b * a.bs >= n || (int64_t)b * a.bs > p) continue;
-      const float wj = exp2f(__ldg(a.part_l + (e0 + j) * a.G + hh) - M);
-      W += wj;
-      if (lane < nv) {
-        const uint2 raw = __ldg(reinterpret_cast<const uint2*>(a.part_o + ((e0 + j) * a.G + hh) * a.d) + lane);
-        const float2 o01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
-        const float2 o23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
-        acc.x = fmaf(wj, o01.x, acc.x);
-        acc.y = fmaf(wj, o01.y, acc.y);
-        acc.z = fmaf(wj, o23.x, acc.z);
-        acc.w = fmaf(wj, o23.y, acc.w);
+    for (int j0 = 0; j0 < a.nsel; j0 += 32) {
+      const int j = j0 + lane;
+      const int b = j < a.nsel ? __ldg(brow + j) : -1;
+      const bool ok = b >= 0 && (int64_t)b * a.bs < n && (int64_t)b * a.bs <= p;
+      const float wl = ok ? exp2f(__ldg(a.part_l + (e0 + j) * a.G + hh) - M) : 0.f;
+      W += wl;
+      const int cnt = min(32, a.nsel - j0);
+      for (int k0 = 0; k0 < cnt; k0 += 8) {
+        uint2 raw[8];
+        float wk[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {  // slot order within a round: k0 + u
+          const int k = k0 + u;
+          wk[u] = __shfl_sync(0xffffffffu, wl, k & 31);
+          raw[u] = make_uint2(0u, 0u);
+          if (k < cnt && wk[u] != 0.f && lane < nv)
+            raw[u] = __ldg(reinterpret_cast<const uint2*>(a.part_o + ((e0 + j0 + k) * a.G + hh) * a.d) + lane);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if (k0 + u >= cnt || wk[u] == 0.f) continue;
+          const float2 o01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[u].x));
+          const float2 o23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[u].y));
+          acc.x = fmaf(wk[u], o01.x, acc.x);
+          acc.y = fmaf(wk[u], o01.y, acc.y);
+          acc.z = fmaf(wk[u], o23.x, acc.z);
+          acc.w = fmaf(wk[u], o23.y, acc.w);
+        }
       }
     }
+    W = warp_sum(W);
   }
   const float inv = W > 0.f ? 1.f / W : 0.f;
   if (lane < nv) {
