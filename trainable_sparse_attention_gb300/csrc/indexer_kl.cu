@@ -34,8 +34,10 @@
 // dq^T and the K-major B operand of dk^T), and two more MMAs per tile give
 //   dq_I[t]^T += K_sel^T C      (M = d_I, N = NP, K = 128 slots; accumulated over tiles)
 //   dk^T       = q_I[t]^T C^T   (M = d_I, N = 128 slots, K = NP)
-// dk^T has channels on TMEM lanes, so each warp's fp32 reductions into the
-// caller's dk accumulator cover whole 128-byte lines of one key row.  dw is the
+// dk^T has channels on TMEM lanes; each warp turns its 32 channels x 32 slots
+// around in shared memory so that its fp32 reductions into the caller's dk
+// accumulator are 16-byte vectors, 8 lanes covering one 128-byte line of a key
+// row.  dw is the
 // slot sum of G ReLU(D): a recursive-halving shuffle sum per tile, combined over
 // the four epilogue warps at the end.
 //
@@ -108,10 +110,6 @@ __device__ __forceinline__ void lane_sum_halving(float* v, int lane) {
     }
     lane_sum_halving<N / 2, O / 2>(v, lane);
   }
-}
-
-__device__ __forceinline__ void red_f32(float* p, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
 // Byte offset of 16-byte chunk c (0..7) of row r inside a 128-byte-swizzled box.
@@ -371,19 +369,29 @@ __global__ void __launch_bounds__(KL_THREADS, KlLayout<NP, BWD>::CTAS)
           break;
         }
         tc::fence_after_sync();
-        const int ch = warp * 32 + lane;
+        // Each 32-slot block goes through shared memory (this warp's 32 rows of
+        // the C tile, whose MMAs are complete) so that a lane adds four
+        // channels of one key row with a 16-byte reduction: 8 lanes cover the
+        // warp's 128-byte line of a row, 4 rows per instruction.
+        const int ch0 = warp * 32;
+        float* tb = reinterpret_cast<float*>(gbase + L::OFF_C + warp * (32 * 128));
 #pragma unroll
         for (int cb = 0; cb < KL_M / 32; ++cb) {
-          const int rowc = rowq[cb];
           uint32_t r[32];
           __syncwarp();
           tc::tmem_ld32(tmem + lane_base + L::T_DK + cb * 32, r);
           tc::tmem_ld_wait();
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const int rk = __shfl_sync(0xffffffffu, rowc, k);
-            if (rk >= 0) red_f32(a.dk_acc + (int64_t)rk * KL_DI + ch, __uint_as_float(r[k]));
+          for (int k = 0; k < 32; ++k) tb[k * 32 + lane] = __uint_as_float(r[k]);  // [slot][channel]
+          __syncwarp();
+#pragma unroll
+          for (int m = 0; m < 8; ++m) {
+            const int k = 4 * m + (lane >> 3);
+            const int rk = __shfl_sync(0xffffffffu, rowq[cb], k);
+            const float4 v = *reinterpret_cast<const float4*>(tb + k * 32 + 4 * (lane & 7));
+            if (rk >= 0) red_add_v4(a.dk_acc + (int64_t)rk * KL_DI + ch0 + 4 * (lane & 7), v.x, v.y, v.z, v.w);
           }
+          __syncwarp();  // read before the next block overwrites it
         }
         tc::fence_before_sync();
         __syncwarp();
