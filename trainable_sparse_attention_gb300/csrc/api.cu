@@ -393,11 +393,14 @@ int sparse_mla_bwd(const void* q, const void* kv, const int32_t* indices, const 
     b.dkv_acc = dkv_acc;
     b.flags = device_flags();
     b.st = a.st;
+    b.teacher = d_qk == 576 ? teacher : nullptr;
     for (int64_t q0 = 0; q0 < T; q0 += chunk) {
       const int nq = static_cast<int>(std::min(chunk, T - q0));
       a.q0 = b.q0 = static_cast<int>(q0);
       TSA_LAUNCH(launch_mla_bwd_pds_tc(a, d_qk, nq, s), "mla bwd recompute launch");
-      if (teacher != nullptr)
+      // the teacher comes out of the dKV GEMM's rope block for d_qk = 576, and
+      // from a pass over the staged P otherwise
+      if (teacher != nullptr && d_qk != 576)
         TSA_LAUNCH(launch_mla_teacher_from_p(a.p_out, nq, H, a.kp, topk, a.q0, teacher, s), "teacher launch");
       TSA_LAUNCH(launch_mla_bwd_dq_tc(a, d_qk, nq, s), "mla bwd dq launch");
       TSA_LAUNCH(launch_mla_bwd_dkv_tc(b, nq, s), "mla bwd dkv launch");

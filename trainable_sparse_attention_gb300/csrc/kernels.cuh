@@ -82,6 +82,9 @@ struct MlaBwdTcArgs {
   float* dkv_acc;             // [T, D] fp32
   unsigned int* flags;        // device error flags
   SeqTable st;
+  // optional indexer teacher [T, topk] (D = 576 only): the head mean of P, from
+  // the rope block's spare accumulator lane
+  float* teacher = nullptr;
 };
 
 // Key-centric Sparse-GQA on tcgen05 (gqa_tc.cu): selections inverted into

@@ -80,6 +80,11 @@ __global__ void __launch_bounds__(DK_THREADS, 1)
   const int ch0 = (blockIdx.x % nblk) * 128;
   const int nch = min(128, a.D - ch0);  // 128, or 64 for the rope block of D = 576
   const bool has_v = ch0 < 512;         // the block holds value channels (the dO term applies)
+  // The rope block of D = 576 (64 channels) leaves accumulator lanes 64..127
+  // empty: with the indexer's teacher requested, its P term runs against a
+  // constant A whose channel 64 is 1/128 for every head, so accumulator lane 64
+  // is (1/128) sum_h P[h, slot], the head mean of the probabilities.
+  const bool has_t = a.teacher != nullptr && nch == 64;
   const int ntiles = a.kp / DK_NS;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int b_issued = 0;  // P / dS tiles whose TMA loads the producer issued
@@ -101,6 +106,17 @@ __global__ void __launch_bounds__(DK_THREADS, 1)
     // the second 64-channel box of a 64-channel block is never loaded: zero it (rows 64..127 of A)
     uint4* z = reinterpret_cast<uint4*>(gbase + DK_OFF_AQ + DK_BOX);
     for (int i = tid; i < DK_BOX / 16; i += DK_THREADS) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (has_t) {
+      // the teacher's constant A (MN-major, head rows of 128 bytes, 128-byte
+      // swizzle): zero, then 1/128 (bf16 0x3C00) at channel 64 of every head
+      // row -- element 0 of the second box, whose 16-byte chunk 0 sits at
+      // chunk (0 ^ (row & 7)) of the row
+      uint4* zo = reinterpret_cast<uint4*>(gbase + DK_OFF_AO);
+      for (int i = tid; i < 2 * DK_BOX / 16; i += DK_THREADS) zo[i] = make_uint4(0u, 0u, 0u, 0u);
+      __syncthreads();
+      for (int h = tid; h < BH; h += DK_THREADS)
+        *reinterpret_cast<unsigned short*>(gbase + DK_OFF_AO + DK_BOX + h * 128 + ((h & 7) << 4)) = 0x3C00u;
+    }
     tc::fence_proxy_async_smem();
   }
   if (warp == 17) tc::tmem_alloc(tmem_slot, 256);
@@ -123,12 +139,12 @@ __global__ void __launch_bounds__(DK_THREADS, 1)
           *abort_flag = 1;
           break;
         }
-        tc::mbar_arrive_expect_tx(&bfull[st], (has_v ? 2 : 1) * DK_B);
+        tc::mbar_arrive_expect_tx(&bfull[st], (has_v || has_t ? 2 : 1) * DK_B);
         const uint32_t dst = base + DK_OFF_B + st * 2 * DK_B;
         const uint64_t pol = tc::policy_evict_first();  // P / dS tiles: read by this query's CTAs only
         for (int c = 0; c < 2; ++c) {
           tc::tma_load_2d_hint(dst + c * DK_BOX, &tm_ds, &bfull[st], j * DK_NS + c * 64, lq * BH, pol);
-          if (has_v)
+          if (has_v || has_t)
             tc::tma_load_2d_hint(dst + DK_B + c * DK_BOX, &tm_p, &bfull[st], j * DK_NS + c * 64, lq * BH, pol);
         }
         ++b_issued;
@@ -154,7 +170,7 @@ __global__ void __launch_bounds__(DK_THREADS, 1)
         for (int ks = 0; ks < BH / 16; ++ks)
           tc::mma_bf16_ss(d, tc::desc_sw128_mn(sAq + ks * 2048, DK_BOX), tc::desc_sw128_mn(bS + ks * 2048, DK_BOX),
                           idesc, ks > 0 ? 1u : 0u);
-        if (has_v) {
+        if (has_v || has_t) {
 #pragma unroll
           for (int ks = 0; ks < BH / 16; ++ks)
             tc::mma_bf16_ss(d, tc::desc_sw128_mn(sAo + ks * 2048, DK_BOX), tc::desc_sw128_mn(bP + ks * 2048, DK_BOX),
@@ -196,6 +212,18 @@ __global__ void __launch_bounds__(DK_THREADS, 1)
         break;
       }
       tc::fence_after_sync();
+      if (has_t && qd == 2) {
+        // accumulator lane 64 (this quadrant's lane 0): the teacher of slots pc*32 .. +31 of the tile
+        uint32_t r[32];
+        tc::tmem_ld32(tmem + (static_cast<uint32_t>(qd * 32) << 16) + acc * DK_NS + pc * 32, r);
+        tc::tmem_ld_wait();
+        if (lane == 0) {
+          float* trow = a.teacher + (int64_t)t * a.topk + j * DK_NS + pc * 32;
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            if (j * DK_NS + pc * 32 + k < a.topk) trow[k] = __uint_as_float(r[k]);
+        }
+      }
       if (live) {
         uint32_t r[32];
         tc::tmem_ld32(tmem + (static_cast<uint32_t>(qd * 32) << 16) + acc * DK_NS + pc * 32, r);
