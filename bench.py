@@ -365,7 +365,7 @@ def run_gpu(args):
                     "frac_of_measured_bf16_sustained": f_fwd / (st_fwd * 1e-3) / 1e12 / psus},
         "mla_bwd": {"ms": st_bwd, "tflops": f_bwd / (st_bwd * 1e-3) / 1e12,
                     "frac_of_measured_bf16_sustained": f_bwd / (st_bwd * 1e-3) / 1e12 / psus,
-                    "note": "includes the indexer teacher (head mean of the staged P)"},
+                    "note": "includes the indexer teacher (head mean of P, from the dKV GEMM of the 576-channel rows)"},
         "indexer_kl": {"ms": st_kl, "tflops": f_kl / (st_kl * 1e-3) / 1e12,
                        "frac_of_measured_bf16_sustained": f_kl / (st_kl * 1e-3) / 1e12 / psus},
         "indexer_bwd": {"ms": st_ibwd, "tflops": f_ibwd / (st_ibwd * 1e-3) / 1e12,

@@ -126,9 +126,15 @@ int qsa_topk_from_scores(const float* scores_dev, int64_t rows, int64_t width, i
  *
  *   indices_dev int32 [T, groups, topk]: the row for (t, g) is
  *   qsa_topk_from_scores applied to qsa_indexer_scores(t, g).  Scores live
- *   only in the caller's workspace, one query chunk at a time
- *   (qsa_topk_workspace_size bytes, independent of T beyond the longest
- *   sequence).
+ *   only in the caller's workspace, two query chunks at a time
+ *   (qsa_topk_workspace_size bytes: two score buffers of at most 512 MB each,
+ *   independent of T beyond the longest sequence): the top-k of one chunk
+ *   runs while the indexer scores the next into the other buffer.  The work
+ *   goes to two library-owned streams of this device (created on the first
+ *   call; the indexer's on the highest priority), forked from `stream` and
+ *   joined back into it by events, so the call is ordered on `stream` like a
+ *   single kernel.  Calls from several host threads are serialised while they
+ *   enqueue.
  * ------------------------------------------------------------------------- */
 size_t qsa_topk_workspace_size(const int32_t* cu_seqlens, int num_seqs, int groups, int block_size);
 int qsa_topk(const void* q_idx_dev, const void* k_idx_dev, const float* w_dev,

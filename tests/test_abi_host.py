@@ -93,10 +93,11 @@ def test_empty_inputs_are_noops(lib):
 
 
 def test_workspace_sizes_are_bounded(lib):
-    # streaming top-k scratch stays bounded by one query chunk, far below T x T
+    # streaming top-k scratch stays bounded by two query chunks (one being
+    # scored while the other is selected), far below T x T
     cu = _cu([0, 65536])
     ws = lib.qsa_topk_workspace_size(cu, 1, 1, 1)
-    assert 0 < ws <= 512 * 2 ** 20 and ws < 65536 * 65536 * 4 // 30
+    assert 0 < ws <= 2 * 512 * 2 ** 20 and ws < 65536 * 65536 * 4 // 15
     assert lib.sparse_mla_bwd_workspace_size(1000, 16, 576, 2048) >= 1000 * 576 * 4 + 1000 * 16 * 4
     # the 128-head P/dS staging is one bounded chunk of queries, not T x topk
     big = lib.sparse_mla_bwd_workspace_size(65536, 128, 576, 2048)

@@ -73,6 +73,23 @@ def test_topk_from_scores_selection_branches(tsa, L, k):
     np.testing.assert_array_equal(got, O.topk_rows(s.numpy(), k))
 
 
+def test_topk_from_scores_bucket_ranking_and_its_fallback(tsa):
+    """Long rows whose guided candidates are ranked by buckets of their order
+    key: distinct scores packed into a narrow range (small buckets), 200 exact
+    ties inside the top k (one bucket over its limit: the sort instead), and
+    one huge outlier that squeezes every other candidate into a few buckets."""
+    g = torch.Generator().manual_seed(77)
+    L, k = 30000, 2048
+    tight = (1.0 + 1e-7 * torch.arange(L, dtype=torch.float64))[torch.randperm(L, generator=g)].float()
+    tied = torch.randn(L, generator=g)
+    tied[torch.randperm(L, generator=g)[:200]] = 2.0           # inside the top 2048 of N(0, 1)
+    outlier = torch.randn(L, generator=g)
+    outlier[123] = 1e30
+    s = torch.stack([tight, tied, outlier, torch.randn(L, generator=g)]).contiguous()
+    got = tsa.qsa_topk_from_scores(s.to(DEV), k).cpu().numpy()
+    np.testing.assert_array_equal(got, O.topk_rows(s.numpy(), k))
+
+
 def test_topk_deterministic_replay_under_contention(tsa):
     s = synth.tie_stress_scores(256, 12000, seed=9).to(DEV)
     a = tsa.qsa_topk_from_scores(s, 2048)

@@ -7,6 +7,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include "kernels.cuh"
@@ -234,8 +235,49 @@ size_t qsa_topk_workspace_size(const int32_t* cu_seqlens, int num_seqs, int grou
   int64_t T;
   if (make_seq_table(cu_seqlens, num_seqs, &st, &T) || groups < 1 || block_size < 1) return 0;
   int64_t C = chunk_rows(st.max_len, groups, block_size);
-  return static_cast<size_t>(C * groups * score_width(st.max_len, block_size) * sizeof(float));
+  // two score buffers: the top-k of one chunk runs while the indexer fills the other
+  return 2 * static_cast<size_t>(C * groups * score_width(st.max_len, block_size) * sizeof(float));
 }
+
+namespace {
+
+// The two internal streams of the streamed indexer (per device, created on
+// first use): the indexer's on the highest stream priority, so that its
+// persistent CTAs take an SM as soon as one frees up, and the top-k's on the
+// lowest, whose CTAs fill the room the indexer leaves.  Both fork from the
+// caller's stream and join back into it with events, so the caller sees one
+// ordered operation on its own stream.
+struct TopkPipe {
+  cudaStream_t idx = nullptr, sel = nullptr;
+  cudaEvent_t start = nullptr, filled[2] = {nullptr, nullptr}, drained[2] = {nullptr, nullptr};
+};
+constexpr int kMaxPipeDevices = 64;
+TopkPipe g_pipes[kMaxPipeDevices];
+std::mutex g_pipe_mu;
+
+int topk_pipe(TopkPipe** out) {
+  int dev = 0;
+  TSA_CHECK_CUDA(cudaGetDevice(&dev), "current device");
+  if (dev < 0 || dev >= kMaxPipeDevices) return fail(TSA_ERR_UNSUPPORTED, "device %d beyond the stream table", dev);
+  TopkPipe& p = g_pipes[dev];
+  if (p.idx == nullptr) {
+    int least = 0, greatest = 0;
+    TSA_CHECK_CUDA(cudaDeviceGetStreamPriorityRange(&least, &greatest), "stream priorities");
+    TopkPipe q;
+    TSA_CHECK_CUDA(cudaStreamCreateWithPriority(&q.idx, cudaStreamNonBlocking, greatest), "indexer stream");
+    TSA_CHECK_CUDA(cudaStreamCreateWithPriority(&q.sel, cudaStreamNonBlocking, least), "top-k stream");
+    TSA_CHECK_CUDA(cudaEventCreateWithFlags(&q.start, cudaEventDisableTiming), "event");
+    for (int i = 0; i < 2; ++i) {
+      TSA_CHECK_CUDA(cudaEventCreateWithFlags(&q.filled[i], cudaEventDisableTiming), "event");
+      TSA_CHECK_CUDA(cudaEventCreateWithFlags(&q.drained[i], cudaEventDisableTiming), "event");
+    }
+    p = q;
+  }
+  *out = &p;
+  return TSA_OK;
+}
+
+}  // namespace
 
 int qsa_topk(const void* q_idx, const void* k_idx, const float* w, const int32_t* cu_seqlens, int num_seqs,
              int H_I, int d_I, int groups, int block_size, float score_scale, int topk, int32_t* indices,
@@ -254,11 +296,24 @@ int qsa_topk(const void* q_idx, const void* k_idx, const float* w, const int32_t
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t C = chunk_rows(st.max_len, groups, block_size);
   const int64_t width = score_width(st.max_len, block_size);
-  float* scratch = static_cast<float*>(workspace);
+  // Chunk i: the indexer writes score buffer i % 2 on the indexer stream, and
+  // the top-k reads it on the top-k stream, which the indexer of chunk i + 2
+  // waits for before it overwrites the buffer.
+  std::lock_guard<std::mutex> lock(g_pipe_mu);
+  TopkPipe* pp = nullptr;
+  if ((rc = topk_pipe(&pp))) return rc;
+  TSA_CHECK_CUDA(cudaEventRecord(pp->start, s), "fork");
+  TSA_CHECK_CUDA(cudaStreamWaitEvent(pp->idx, pp->start, 0), "fork");
+  TSA_CHECK_CUDA(cudaStreamWaitEvent(pp->sel, pp->start, 0), "fork");
+  const size_t buf_floats = static_cast<size_t>(C) * groups * width;
+  int64_t chunk = 0;
   for (int b = 0; b < num_seqs; ++b) {
     const int len = st.cu[b + 1] - st.cu[b];
-    for (int64_t p0 = 0; p0 < len; p0 += C) {
+    for (int64_t p0 = 0; p0 < len; p0 += C, ++chunk) {
       const int nq = static_cast<int>(std::min<int64_t>(C, len - p0));
+      const int nb = static_cast<int>(chunk & 1);
+      float* scratch = static_cast<float*>(workspace) + nb * buf_floats;
+      if (chunk >= 2) TSA_CHECK_CUDA(cudaStreamWaitEvent(pp->idx, pp->drained[nb], 0), "buffer reuse");
       IndexerArgs a;
       a.q = static_cast<const __nv_bfloat16*>(q_idx);
       a.k = static_cast<const __nv_bfloat16*>(k_idx);
@@ -272,7 +327,9 @@ int qsa_topk(const void* q_idx, const void* k_idx, const float* w, const int32_t
       a.width = width;
       a.T_total = static_cast<int>(T);
       a.flags = device_flags();
-      TSA_LAUNCH(launch_indexer(a, s), "indexer launch");
+      TSA_LAUNCH(launch_indexer(a, pp->idx), "indexer launch");
+      TSA_CHECK_CUDA(cudaEventRecord(pp->filled[nb], pp->idx), "chunk scored");
+      TSA_CHECK_CUDA(cudaStreamWaitEvent(pp->sel, pp->filled[nb], 0), "chunk scored");
       TopkRows r;
       r.scores = scratch; r.ld = width; r.width = width;
       r.mode = block_size == 1 ? 1 : 2;
@@ -280,9 +337,12 @@ int qsa_topk(const void* q_idx, const void* k_idx, const float* w, const int32_t
       r.out = indices + (st.cu[b] + p0) * groups * topk;
       r.out_ld = topk;
       r.k = topk;
-      TSA_LAUNCH(launch_topk_rows(r, (int64_t)nq * groups, s), "topk launch");
+      TSA_LAUNCH(launch_topk_rows(r, (int64_t)nq * groups, pp->sel), "topk launch");
+      TSA_CHECK_CUDA(cudaEventRecord(pp->drained[nb], pp->sel), "chunk selected");
     }
   }
+  // join: the last top-k follows every indexer launch (through its event)
+  TSA_CHECK_CUDA(cudaStreamWaitEvent(s, pp->drained[(chunk - 1) & 1], 0), "join");
   return TSA_OK;
 }
 

@@ -9,7 +9,11 @@
 //
 // A query block is QB = 256 / H_I consecutive queries: their q_I rows form the
 // MMA's B operand (N = 256 columns = (query, head)); key tiles of 128 keys (the
-// A operand, M = 128) stream through a 4-stage TMA ring.  Keys sit on TMEM
+// A operand, M = 128) stream through a 2-stage TMA ring.  Two stages keep the
+// CTA's shared memory (~139 KB at d_I = 128) small enough for one top-k CTA to
+// run beside it on the same SM: the streamed runner selects chunk i while this
+// kernel scores chunk i + 1 (with four stages and the two kernels in turn the
+// T = 65536 indexer + top-k took 31.3 ms, with two stages side by side 29.9 ms).  Keys sit on TMEM
 // lanes, so each epilogue thread owns one key and reduces the heads of a group
 // inside its own registers: ReLU, head weight and group sum never leave the
 // thread, and only causal scores are written ("cleaned" logits are never
@@ -50,7 +54,7 @@ namespace {
 
 constexpr int IT_M = 128;
 constexpr int IT_N = 256;
-constexpr int IT_STAGES = 4;
+constexpr int IT_STAGES = 2;  // see the header: room for a top-k CTA beside this one
 constexpr int IT_THREADS = 320;
 
 template <int DI>
@@ -498,6 +502,10 @@ static cudaError_t launch_tc_t(const IndexerArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   constexpr int smem = ItLayout<DI>::SMEM;
   e = cudaFuncSetAttribute(indexer_tc_kernel<DI, HG, BLK>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  // the whole shared-memory carveout, so that a top-k CTA fits beside this one
+  e = cudaFuncSetAttribute(indexer_tc_kernel<DI, HG, BLK>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   // total (query block, key tile) pairs of the launch; one persistent CTA per SM
   const int QB = IT_N / a.H_I;

@@ -21,6 +21,12 @@
 //    sweeps (10 + 9 bits) find the k-th largest u = tau, and an ordered sweep
 //    keeps every u > tau and the lowest-index (k - count(u > tau)) entries
 //    with u == tau, ranked by a block prefix sum in index order;
+//  * the usual path for long rows gathers about 1.25 k candidates above a
+//    threshold guessed from a sample and orders them without a sort: buckets
+//    of the candidates' u range, a scan of the bucket counts, and each key's
+//    rank inside its bucket (a bucket holding more than TK_BUCKET_MAX keys --
+//    exact ties in u, or a dense spot under an outlier -- sends the row to the
+//    sort instead);
 //  * the sort is bitonic: strides below 32 elements exchange registers between
 //    lanes, strides inside one warp's chunk exchange a thread's own registers,
 //    and only the longer strides go through shared memory with a block barrier.
@@ -37,6 +43,10 @@ constexpr int TK_BINS = 1 << TK_BITS1;
 constexpr int TK_SH1 = 32 - TK_BITS1;
 constexpr int TK_PER = 8;       // consecutive entries per thread in the sweeps over long rows
 constexpr int TK_SMEM = TK_MAXK * 8 + TK_BINS * 4;
+constexpr int TK_NB = 2048;          // buckets of the final ranking (4 per thread)
+constexpr int TK_BUCKET_MAX = 128;   // a fuller bucket (ties in u, a dense spot) sends the row to the sort
+static_assert(TK_NB == 4 * TK_THREADS, "bucket scan: four buckets per thread");
+static_assert(TK_NB * 4 + TK_MAXK * 2 <= TK_MAXK * 8, "bucket scratch fits the key buffer");
 
 
 __device__ __forceinline__ uint32_t order_key(float s) {
@@ -349,6 +359,76 @@ __device__ __forceinline__ void finish_row(uint64_t* keys, int m, int k, int32_t
   emit(keys, m, k, out);
 }
 
+// Writes the first k of the m keys packed[0..m) in descending order as
+// indices (m >= k), without a sort: every key falls in one of TK_NB buckets
+// by its u (the range [u_lo, u_hi] of the keys scaled to the buckets, higher
+// u in lower buckets), a scan of the bucket counts gives each bucket's place
+// in the output, and a key's rank inside its bucket is the number of keys of
+// the bucket above it.  The keys are unique, so the ranks are a permutation
+// and the result equals the sorted order.  Returns false (block-uniform,
+// nothing written) when a bucket holds more than TK_BUCKET_MAX keys; packed
+// is left unchanged either way.  Scratch: cnt[TK_NB] and pos[m].
+__device__ bool rank_by_buckets(const uint64_t* packed, int m, int k, uint32_t u_lo, uint32_t u_hi, uint32_t* cnt,
+                                uint16_t* pos, uint32_t* warp_tot, int* sh, int32_t* out) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t range = u_hi - u_lo;
+  int sft = 0;
+  while ((range >> sft) >= static_cast<uint32_t>(TK_NB)) ++sft;
+  auto bucket = [&](uint64_t key) {
+    return TK_NB - 1 - static_cast<int>((static_cast<uint32_t>(key >> 32) - u_lo) >> sft);
+  };
+  for (int i = threadIdx.x; i < TK_NB; i += TK_THREADS) cnt[i] = 0;
+  if (threadIdx.x == 0) sh[3] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < m; i += TK_THREADS) atomicAdd(&cnt[bucket(packed[i])], 1u);
+  __syncthreads();
+  // exclusive scan of the counts (buckets 4t .. 4t+3 on thread t) and their maximum
+  uint32_t c[4], tsum = 0, tmax = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    c[e] = cnt[4 * threadIdx.x + e];
+    tsum += c[e];
+    tmax = c[e] > tmax ? c[e] : tmax;
+  }
+  uint32_t x = tsum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint32_t y = __shfl_xor_sync(0xffffffffu, tmax, o);
+    tmax = y > tmax ? y : tmax;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  if (lane == 0) atomicMax(&sh[3], static_cast<int>(tmax));
+  __syncthreads();
+  if (sh[3] > TK_BUCKET_MAX) return false;
+  uint32_t off = x - tsum;
+  for (int w = 0; w < warp; ++w) off += warp_tot[w];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    cnt[4 * threadIdx.x + e] = off;
+    off += c[e];
+  }
+  __syncthreads();
+  // place every key in its bucket's range (any order inside a bucket); cnt[b]
+  // then holds the end of bucket b, the start of bucket b + 1
+  for (int i = threadIdx.x; i < m; i += TK_THREADS) pos[atomicAdd(&cnt[bucket(packed[i])], 1u)] = static_cast<uint16_t>(i);
+  __syncthreads();
+  for (int i = threadIdx.x; i < m; i += TK_THREADS) {
+    const uint64_t key = packed[i];
+    const int b = bucket(key);
+    const uint32_t st = b > 0 ? cnt[b - 1] : 0u, en = cnt[b];
+    if (st >= static_cast<uint32_t>(k)) continue;
+    uint32_t r = st;
+    for (uint32_t j = st; j < en; ++j) r += packed[pos[j]] > key ? 1u : 0u;
+    if (r < static_cast<uint32_t>(k)) out[r] = static_cast<int32_t>(~static_cast<uint32_t>(key & 0xffffffffull));
+  }
+  return true;
+}
+
 // The lower edge of first-digit bin b as a score (inverse of order_key).
 __device__ __forceinline__ float bin_floor(int b) {
   const uint32_t u = static_cast<uint32_t>(b) << TK_SH1;
@@ -467,10 +547,38 @@ __global__ void __launch_bounds__(TK_THREADS, 3) topk_rows_kernel(TopkRows a) {
     }
     if (!over && cnt >= static_cast<uint32_t>(k)) {
       // the k largest are among the gathered keys: pack the regions into the
-      // (now free) histogram area and sort there
+      // (now free) histogram area, with the range of their u, and rank them
+      // there by buckets (the sort when a bucket is too full)
       uint64_t* packed = reinterpret_cast<uint64_t*>(hist);
-      for (uint32_t i = lane; i < wcnt; i += 32) packed[before + i] = wk[i];
-      finish_row(packed, static_cast<int>(cnt), k, out);
+      if (threadIdx.x == 0) {
+        slots[0] = 0xffffffffu;
+        slots[1] = 0u;
+      }
+      __syncthreads();
+      uint32_t ulo = 0xffffffffu, uhi = 0u;
+      for (uint32_t i = lane; i < wcnt; i += 32) {
+        const uint64_t key = wk[i];
+        packed[before + i] = key;
+        const uint32_t u = static_cast<uint32_t>(key >> 32);
+        ulo = u < ulo ? u : ulo;
+        uhi = u > uhi ? u : uhi;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const uint32_t a = __shfl_xor_sync(0xffffffffu, ulo, o), b = __shfl_xor_sync(0xffffffffu, uhi, o);
+        ulo = a < ulo ? a : ulo;
+        uhi = b > uhi ? b : uhi;
+      }
+      if (lane == 0) {
+        atomicMin(&slots[0], ulo);
+        atomicMax(&slots[1], uhi);
+      }
+      __syncthreads();  // packed and the range are complete; the key buffer is free
+      const uint32_t u_lo = slots[0], u_hi = slots[1];
+      if (!rank_by_buckets(packed, static_cast<int>(cnt), k, u_lo, u_hi, reinterpret_cast<uint32_t*>(keys),
+                           reinterpret_cast<uint16_t*>(reinterpret_cast<uint32_t*>(keys) + TK_NB), warp_tot, sh,
+                           out))
+        finish_row(packed, static_cast<int>(cnt), k, out);
       return;
     }
     __syncthreads();  // every thread has read warp_tot
@@ -592,6 +700,11 @@ __global__ void __launch_bounds__(TK_THREADS, 3) topk_rows_kernel(TopkRows a) {
 cudaError_t launch_topk_rows(const TopkRows& a, int64_t rows, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TK_SMEM);
+  if (e != cudaSuccess) return e;
+  // the whole shared-memory carveout: the rows of one chunk run beside the
+  // indexer's persistent CTAs of the next
+  e = cudaFuncSetAttribute(topk_rows_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   topk_rows_kernel<<<static_cast<unsigned>(rows), TK_THREADS, TK_SMEM, stream>>>(a);
   note_launch();
