@@ -32,8 +32,10 @@
 //                         in bf16, then dV^T += dO^T P and dK^T += Q^T dS
 //                         (accumulated in TMEM over the whole chunk, reduced once
 //                         per chunk) and dQ^T = K^T dS^T, whose channels sit on
-//                         TMEM lanes so that each warp's fp32 reductions into the
-//                         dQ accumulator cover whole 128-byte lines.
+//                         TMEM lanes; each warp turns its 32 channels x 32 rows
+//                         around in shared memory so that its fp32 reductions
+//                         into the dQ accumulator are 16-byte vectors, 8 lanes
+//                         per 128-byte line.
 //
 // Head dimension 64 runs as 128 with channels 64..127 zero in shared memory,
 // and blocks of 32 keys as 64-key tiles whose upper half is masked: the MMA
@@ -836,30 +838,47 @@ __global__ void __launch_bounds__(GB_THREADS, 1)
       tc::fence_proxy_async_smem();  // generic writes before the MMAs (async proxy) read them
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(psfull);
-      // dQ^T of this batch: channel ch of batch rows 64 hf .. +63, one fp32
-      // reduction per (row, channel); a warp instruction covers 32 channels of a row
+      // dQ^T of this batch: channels 32 qd .. +31 of batch rows 64 hf .. +63.
+      // Each 32-row block is turned around in shared memory so that a lane adds
+      // four channels of one row with a 16-byte reduction: 8 lanes cover the
+      // warp's 128-byte line of a row, 4 rows per instruction.  The space is
+      // this warp's 4 KB of the batch's own Q / dO buffers (their first
+      // 64-channel boxes, which the producer reloads for every batch): every
+      // MMA that reads them is complete once dQ^T is, and the producer refills
+      // them only after all eight row warps have released the batch below.
       if (!__all_sync(0xffffffffu, tc::mbar_wait(dqfull, ph, abort_flag))) {
         *abort_flag = 1;
         break;
       }
       tc::fence_after_sync();
+      float* xb = reinterpret_cast<float*>(gbase + (hf ? GB_OFF_DO : GB_OFF_Q) + buf * GT_QT + qd * (32 * 32 * 4));
+      const bool live = qd * 32 < a.d;  // d = 64: quadrants 2, 3 hold the zero padding
 #pragma unroll 1
       for (int cb = 0; cb < 2; ++cb) {
         uint32_t r[32];
         __syncwarp();
         tc::tmem_ld32(tmem + lane_base + GB_T_DQ + hf * 64 + cb * 32, r);
         tc::tmem_ld_wait();
+        if (live) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int qr = tb[hf * 64 + cb * 32 + k];
-          if (qr >= 0 && ch < a.d) red_f32(a.dq_acc + (int64_t)qr * a.d + ch, __uint_as_float(r[k]));
+          for (int k = 0; k < 32; ++k) xb[k * 32 + lane] = __uint_as_float(r[k]);
+          __syncwarp();
+#pragma unroll
+          for (int m = 0; m < 8; ++m) {
+            const int k = 4 * m + (lane >> 3);
+            const int qr = tb[hf * 64 + cb * 32 + k];
+            const float4 v = *reinterpret_cast<const float4*>(xb + k * 32 + 4 * (lane & 7));
+            if (qr >= 0) red_add_v4(a.dq_acc + (int64_t)qr * a.d + qd * 32 + 4 * (lane & 7), v.x, v.y, v.z, v.w);
+          }
+          __syncwarp();  // read before the next block overwrites it
         }
       }
+      tc::fence_proxy_async_smem();  // the transpose writes before the producer's next TMA into the buffer
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) {
         tc::mbar_arrive(dqempty);
-        tc::mbar_arrive(&qempty[buf]);  // the row table may be rewritten for batch i + 2
+        tc::mbar_arrive(&qempty[buf]);  // the buffers and the row table may be rewritten for batch i + 2
       }
     }
     // ---- this chunk's dK, dV of the block's keys: channel ch, keys 32 hf .. +31
