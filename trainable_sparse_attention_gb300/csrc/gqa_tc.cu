@@ -35,7 +35,13 @@
 //                         TMEM lanes; each warp turns its 32 channels x 32 rows
 //                         around in shared memory so that its fp32 reductions
 //                         into the dQ accumulator are 16-byte vectors, 8 lanes
-//                         per 128-byte line.
+//                         per 128-byte line.  The backward's batches flow
+//                         through three groups of warps at once: two loader
+//                         warps copy the next batches' Q and dO rows with
+//                         cp.async (the TMA gathers' one-instruction-per-4-rows
+//                         rate bound the kernel), eight row warps turn S / dP
+//                         into P / dS, and four drain warps reduce the previous
+//                         batch's dQ^T from the second of two TMEM buffers.
 //
 // Head dimension 64 runs as 128 with channels 64..127 zero in shared memory,
 // and blocks of 32 keys as 64-key tiles whose upper half is masked: the MMA
@@ -593,16 +599,17 @@ constexpr int GB_OFF_TAB = GB_OFF_DS + GT_PT;          // int [2][128]
 constexpr int GB_OFF_BAR = GB_OFF_TAB + 2 * GT_ROWS * 4;
 constexpr int GB_SMEM = 1024 + GB_OFF_BAR + 256;
 static_assert(GB_SMEM <= 227 * 1024, "GQA backward shared memory");
-constexpr int GB_THREADS = 320;  // warps 0-7 rows / drains (two per TMEM lane quadrant), 8 producer, 9 MMA
-// TMEM: S and dP double-buffered, dV^T, dK^T (accumulated over the chunk), dQ^T
-constexpr int GB_T_S = 0, GB_T_DP = 128, GB_T_DV = 256, GB_T_DK = 320, GB_T_DQ = 384, GB_TMEM = 512;
+constexpr int GB_THREADS = 480;  // warps 0-7 rows (two per TMEM lane quadrant), 8-11 dQ drains, 12-13 loaders, 14 MMA
+constexpr int GB_W_DRAIN = 8, GB_W_LOAD = 12, GB_W_MMA = 14;
+constexpr int GB_LOADERS = 64;   // loader threads: one regular and one cp.async arrival each on qfull
+// TMEM: S, dP, dV^T, dK^T (accumulated over the chunk), dQ^T double-buffered
+constexpr int GB_T_S = 0, GB_T_DP = 64, GB_T_DV = 128, GB_T_DK = 192, GB_T_DQ = 256, GB_TMEM = 512;
 constexpr int GT_BWD_CHUNK = 512;  // list entries (queries) per backward CTA
 
 }  // namespace
 
 __global__ void __launch_bounds__(GB_THREADS, 1)
-    gqa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
-                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+    gqa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ GqaTcArgs a, int chunk) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -613,15 +620,15 @@ __global__ void __launch_bounds__(GB_THREADS, 1)
   int* tab = reinterpret_cast<int*>(gbase + GB_OFF_TAB);  // [2][128]
   uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + GB_OFF_BAR);
   uint64_t* kvfull = bars;          // [1]
-  uint64_t* qfull = bars + 1;       // [2] Q, dO and the row table of a batch landed
-  uint64_t* qempty = qfull + 2;     // [2] MMAs done with Q / dO, rows done with the table
-  uint64_t* sfull = qempty + 2;     // [2] S and dP ready
-  uint64_t* sempty = sfull + 2;     // [2] rows read S and dP (8 warps)
-  uint64_t* psfull = sempty + 2;    // [1] rows wrote P and dS (8 warps)
+  uint64_t* qfull = bars + 1;       // [2] Q, dO and the row table of a batch landed (loader arrivals)
+  uint64_t* qempty = qfull + 2;     // [2] MMAs done with Q / dO, row and drain warps done with the table
+  uint64_t* sfull = qempty + 2;     // [1] S and dP ready
+  uint64_t* sempty = sfull + 1;     // [1] rows read S and dP (8 warps)
+  uint64_t* psfull = sempty + 1;    // [1] rows wrote P and dS (8 warps)
   uint64_t* psempty = psfull + 1;   // [1] MMAs done reading P and dS
-  uint64_t* dqfull = psempty + 1;   // [1]
-  uint64_t* dqempty = dqfull + 1;   // [1] rows drained dQ^T (8 warps)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dqempty + 1);
+  uint64_t* dqfull = psempty + 1;   // [2] dQ^T of a batch complete
+  uint64_t* dqempty = dqfull + 2;   // [2] drain warps read it (4 warps)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dqempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   GtChunk ck;
@@ -629,20 +636,19 @@ __global__ void __launch_bounds__(GB_THREADS, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qb = GT_ROWS / a.G;
   const int nbatch = (ck.e1 - ck.e0 + qb - 1) / qb;
-  int issued = 0;
 
   if (tid == 0) {
     tc::mbar_init(kvfull, 1);
     for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&qfull[i], 1);
-      tc::mbar_init(&qempty[i], 1 + 8);  // the MMA commit and the eight row warps
-      tc::mbar_init(&sfull[i], 1);
-      tc::mbar_init(&sempty[i], 8);
+      tc::mbar_init(&qfull[i], 2 * GB_LOADERS);
+      tc::mbar_init(&qempty[i], 1 + 8 + 4);  // the MMA commit, the eight row and the four drain warps
+      tc::mbar_init(&dqfull[i], 1);
+      tc::mbar_init(&dqempty[i], 4);
     }
+    tc::mbar_init(sfull, 1);
+    tc::mbar_init(sempty, 8);
     tc::mbar_init(psfull, 8);
     tc::mbar_init(psempty, 1);
-    tc::mbar_init(dqfull, 1);
-    tc::mbar_init(dqempty, 8);
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -659,26 +665,40 @@ __global__ void __launch_bounds__(GB_THREADS, 1)
       }
     tc::fence_proxy_async_smem();
   }
-  if (warp == 9) tc::tmem_alloc(tmem_slot, GB_TMEM);
+  if (warp == GB_W_MMA) tc::tmem_alloc(tmem_slot, GB_TMEM);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   const uint32_t kv_bytes = (a.d == 128 ? 2 : 1) * 2 * GT_KBOX;
-  const uint32_t q_bytes = (a.d == 128 ? 2 : 1) * 2 * GT_QBOX;  // Q and dO
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      tc::prefetch_tmap(&tm_q);
-      tc::prefetch_tmap(&tm_do);
-      tc::prefetch_tmap(&tm_k);
-      tc::prefetch_tmap(&tm_v);
-      tc::mbar_arrive_expect_tx(kvfull, kv_bytes);
+  if (warp == GB_W_LOAD || warp == GB_W_LOAD + 1) {
+    // ------------------------------------------------------------ loaders (2 warps)
+    // The block's K and V rows by TMA gathers, once per chunk.  Then per batch,
+    // loader warp wl owns batch rows 64 wl .. +63: lane l finds the sources of
+    // rows 64 wl + 2l and +1 and writes them to the row table, and the warp
+    // copies the rows' Q and dO by cp.async, 16 lanes per row (two whole rows
+    // per instruction; the sources travel by shuffle), each 16-byte chunk
+    // straight to its place in the 128-byte-swizzled K-major tile (chunk j of
+    // row r at r * 128 + (j ^ (r & 7)) * 16 of its 64-channel box).  Rows
+    // without a query are zero-filled.  Each thread arrives on qfull once after
+    // its table entries and once (noinc) when its copies have landed.
+    const int wl = warp - GB_W_LOAD;
+    if (wl == 0) {
+      if (lane == 0) {
+        tc::prefetch_tmap(&tm_k);
+        tc::prefetch_tmap(&tm_v);
+        tc::mbar_arrive_expect_tx(kvfull, kv_bytes);
+      }
+      __syncwarp();
+      gt_gather_kv(sK, &tm_k, kvfull, a, ck, lane);
+      gt_gather_kv(sV, &tm_v, kvfull, a, ck, lane);
     }
-    __syncwarp();
-    gt_gather_kv(sK, &tm_k, kvfull, a, ck, lane);
-    gt_gather_kv(sV, &tm_v, kvfull, a, ck, lane);
+    const int nch = a.d / 8;  // 16-byte chunks per row: 16 or 8
+    const int c16 = lane & 15, h = lane >> 4;
+    const int cb = c16 >> 3, jj = c16 & 7;
+    const char* qsrc = reinterpret_cast<const char*>(a.q);
+    const char* osrc = reinterpret_cast<const char*>(a.dout);
     bool ok = true;
     for (int i = 0; i < nbatch; ++i) {
       const int buf = i & 1;
@@ -686,50 +706,68 @@ __global__ void __launch_bounds__(GB_THREADS, 1)
         ok = false;
         break;
       }
-      int r[4];
-      gt_batch_rows(a, ck, ck.e0 + i * qb, tab + buf * GT_ROWS, true, lane, r);
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive_expect_tx(&qfull[buf], q_bytes);
-      __syncwarp();
-      gt_gather_batch(sQ + buf * GT_QT, &tm_q, &qfull[buf], a.d, r, lane);
-      gt_gather_batch(sO + buf * GT_QT, &tm_do, &qfull[buf], a.d, r, lane);
-      issued = i + 1;
+      int src[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int row = 64 * wl + 2 * lane + k;
+        const int qi = row / a.G, hh = row - qi * a.G;
+        const int ei = ck.e0 + i * qb + qi;
+        const bool okr = qi < qb && ei < ck.e1;
+        const int e = okr ? __ldg(a.list + ei) : -1;
+        src[k] = okr ? (e / (a.Hkv * a.nsel)) * a.Hq + ck.g * a.G + hh : -1;
+        tab[buf * GT_ROWS + row] = src[k];
+      }
+      tc::mbar_arrive(&qfull[buf]);  // this thread's table entries
+      const uint32_t qdst = sQ + buf * GT_QT, odst = sO + buf * GT_QT;
+#pragma unroll 4
+      for (int m = 0; m < 32; ++m) {
+        const int s0 = __shfl_sync(0xffffffffu, src[0], m), s1 = __shfl_sync(0xffffffffu, src[1], m);
+        const int sr = h ? s1 : s0;
+        const int row = 64 * wl + 2 * m + h;
+        if (c16 < nch) {
+          const int64_t off = (int64_t)(sr >= 0 ? sr : 0) * a.d * 2 + c16 * 16;
+          const uint32_t o = cb * GT_QBOX + row * 128 + ((jj ^ (row & 7)) << 4);
+          cp_async16(qdst + o, qsrc + off, sr >= 0 ? 16u : 0u);
+          cp_async16(odst + o, osrc + off, sr >= 0 ? 16u : 0u);
+        }
+      }
+      cp_async_commit();
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&qfull[buf])) : "memory");
     }
+    cp_async_wait<0>();  // this thread's copies land before the CTA can exit
     if (!ok) *abort_flag = 1;
-    if (lane == 0) {  // copies still in flight land before the CTA exits (bounded by time only)
+    if (wl == 0 && lane == 0) {  // the K / V gathers land before the CTA exits (bounded by time only)
       volatile int keep_waiting = 0;
       (void)tc::mbar_wait(kvfull, 0, &keep_waiting);
-      for (int g = issued > 2 ? issued - 2 : 0; g < issued; ++g)
-        (void)tc::mbar_wait(&qfull[g & 1], (g >> 1) & 1, &keep_waiting);
     }
-  } else if (warp == 9) {
+  } else if (warp == GB_W_MMA) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_s = tc::idesc_bf16_f32(GT_ROWS, GT_KEYS);
       constexpr uint32_t id_kv = tc::idesc_bf16_f32(GT_DP, GT_KEYS) | (1u << 15) | (1u << 16);  // A, B MN-major
       constexpr uint32_t id_q = tc::idesc_bf16_f32(GT_DP, GT_ROWS) | (1u << 15);                // A MN-major
-      // S = Q K^T and dP = dO V^T of batch i into buffer i & 1 (K = the head dimension)
+      // S = Q K^T and dP = dO V^T of batch i (K = the head dimension)
       auto issue_s = [&](int i) {
         const int buf = i & 1;
         const uint32_t qt = sQ + buf * GT_QT, ot = sO + buf * GT_QT;
+        tc::fence_proxy_async_smem();  // the rows arrived by cp.async (generic proxy); the MMAs read them
 #pragma unroll
         for (int ks = 0; ks < GT_DP / 16; ++ks) {
           const int c = ks >> 2, kk = ks & 3;
-          tc::mma_bf16_ss(tmem + GB_T_S + buf * GT_KEYS, tc::desc_sw128(qt + c * GT_QBOX + kk * 32),
+          tc::mma_bf16_ss(tmem + GB_T_S, tc::desc_sw128(qt + c * GT_QBOX + kk * 32),
                           tc::desc_sw128(sK + c * GT_KBOX + kk * 32), id_s, ks > 0 ? 1u : 0u);
-          tc::mma_bf16_ss(tmem + GB_T_DP + buf * GT_KEYS, tc::desc_sw128(ot + c * GT_QBOX + kk * 32),
+          tc::mma_bf16_ss(tmem + GB_T_DP, tc::desc_sw128(ot + c * GT_QBOX + kk * 32),
                           tc::desc_sw128(sV + c * GT_KBOX + kk * 32), id_s, ks > 0 ? 1u : 0u);
         }
-        tc::mma_commit(&sfull[buf]);
+        tc::mma_commit(sfull);
       };
-      // batch i's rows landed and its S / dP buffer free (rows read batch i-2's)
+      // batch i's rows landed and the rows have read S / dP of batch i - 1
       auto s_ready = [&](int i, bool block) {
         const int buf = i & 1;
         if (block)
           return tc::mbar_wait(&qfull[buf], (i >> 1) & 1, abort_flag) &&
-                 (i < 2 || tc::mbar_wait(&sempty[buf], ((i >> 1) & 1) ^ 1u, abort_flag));
-        return tc::mbar_try_wait(&qfull[buf], (i >> 1) & 1) &&
-               (i < 2 || tc::mbar_try_wait(&sempty[buf], ((i >> 1) & 1) ^ 1u));
+                 (i < 1 || tc::mbar_wait(sempty, (i - 1) & 1, abort_flag));
+        return tc::mbar_try_wait(&qfull[buf], (i >> 1) & 1) && (i < 1 || tc::mbar_try_wait(sempty, (i - 1) & 1));
       };
       bool ok = tc::mbar_wait(kvfull, 0, abort_flag) && (nbatch == 0 || s_ready(0, true));
       if (ok && nbatch > 0) {
@@ -738,17 +776,17 @@ __global__ void __launch_bounds__(GB_THREADS, 1)
       }
       for (int i = 0; ok && i < nbatch; ++i) {
         const int buf = i & 1;
-        const uint32_t ph = i & 1;
-        // S / dP of the next batch first if its rows are already here, so the
-        // row warps find it ready when they finish this batch
+        // S / dP of the next batch first if the rows have read this one's and
+        // its rows are here, so the row warps find it ready
         bool next_done = false;
         if (i + 1 < nbatch && s_ready(i + 1, false)) {
           tc::fence_after_sync();
           issue_s(i + 1);
           next_done = true;
         }
-        // the rows' P and dS of this batch, and the drained dQ^T of the previous one
-        if (!tc::mbar_wait(psfull, ph, abort_flag) || (i > 0 && !tc::mbar_wait(dqempty, ph ^ 1u, abort_flag))) {
+        // the rows' P and dS of this batch, and dQ^T buffer i & 1 drained (batch i - 2)
+        if (!tc::mbar_wait(psfull, i & 1, abort_flag) ||
+            (i > 1 && !tc::mbar_wait(&dqempty[buf], ((i >> 1) & 1) ^ 1u, abort_flag))) {
           ok = false;
           break;
         }
@@ -763,13 +801,13 @@ __global__ void __launch_bounds__(GB_THREADS, 1)
                           tc::desc_sw128_mn(sS + ks * 2048, GT_PT), id_kv, (i > 0 || ks > 0) ? 1u : 0u);
         }
         tc::mma_commit(&qempty[buf]);
-        // dQ^T = K^T dS^T (K = the 64 keys)
+        // dQ^T = K^T dS^T (K = the 64 keys) into buffer i & 1
 #pragma unroll
         for (int ks = 0; ks < GT_KEYS / 16; ++ks)
-          tc::mma_bf16_ss(tmem + GB_T_DQ, tc::desc_sw128_mn(sK + ks * 2048, GT_KBOX), tc::desc_sw128(sS + ks * 32),
-                          id_q, ks > 0 ? 1u : 0u);
+          tc::mma_bf16_ss(tmem + GB_T_DQ + buf * GT_ROWS, tc::desc_sw128_mn(sK + ks * 2048, GT_KBOX),
+                          tc::desc_sw128(sS + ks * 32), id_q, ks > 0 ? 1u : 0u);
         tc::mma_commit(psempty);
-        tc::mma_commit(dqfull);
+        tc::mma_commit(&dqfull[buf]);
         if (i + 1 < nbatch && !next_done) {
           if (!s_ready(i + 1, true)) {
             ok = false;
@@ -781,38 +819,34 @@ __global__ void __launch_bounds__(GB_THREADS, 1)
       }
       if (!ok) *abort_flag = 1;
     }
-  } else {
-    // ------------------------------------------------------------ rows / drains (warps 0-7)
-    // warp w: TMEM lane quadrant qd = w % 4 (batch rows, or channels in the
-    // transposed products), half hf = w / 4 (keys 32 hf .. +31 of S / dP, batch
-    // rows 64 hf .. +63 of dQ^T, keys 32 hf .. +31 of dK^T / dV^T)
+  } else if (warp < GB_W_DRAIN) {
+    // ------------------------------------------------------------ rows (warps 0-7)
+    // warp w: TMEM lane quadrant qd = w % 4 (batch rows), keys 32 hf .. +31 of
+    // S / dP with hf = w / 4
     const int qd = warp & 3, hf = warp >> 2;
     const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
     const int row = qd * 32 + lane;
-    const int ch = qd * 32 + lane;  // channel in the transposed products
     for (int i = 0; i < nbatch; ++i) {
       const int buf = i & 1;
-      const uint32_t ph = i & 1;
       if (!__all_sync(0xffffffffu, tc::mbar_wait(&qfull[buf], (i >> 1) & 1, abort_flag)) ||
-          !__all_sync(0xffffffffu, tc::mbar_wait(&sfull[buf], (i >> 1) & 1, abort_flag))) {
+          !__all_sync(0xffffffffu, tc::mbar_wait(sfull, i & 1, abort_flag))) {
         *abort_flag = 1;
         break;
       }
       tc::fence_after_sync();
-      const int* tb = tab + buf * GT_ROWS;  // per batch row: its row t * Hq + h of q / dO / dq, or -1
-      const int qrow = tb[row];
+      const int qrow = tab[buf * GT_ROWS + row];  // its row t * Hq + h of q / dO, or -1
       const int t = qrow >= 0 ? qrow / a.Hq : 0;
       const int lim = qrow < 0 ? 0 : min(min(a.bs, ck.n - ck.kbase), t - ck.s0 - ck.kbase + 1);
       const float lse2 = qrow >= 0 ? __ldg(a.lse_in + qrow) * kLog2e : 0.f;
       const float dl = qrow >= 0 ? __ldg(a.dlt + qrow) : 0.f;
       uint32_t sr[32], dr[32];
       __syncwarp();
-      tc::tmem_ld32(tmem + lane_base + GB_T_S + buf * GT_KEYS + hf * 32, sr);
-      tc::tmem_ld32(tmem + lane_base + GB_T_DP + buf * GT_KEYS + hf * 32, dr);
+      tc::tmem_ld32(tmem + lane_base + GB_T_S + hf * 32, sr);
+      tc::tmem_ld32(tmem + lane_base + GB_T_DP + hf * 32, dr);
       tc::tmem_ld_wait();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&sempty[buf]);
+      if (lane == 0) tc::mbar_arrive(sempty);
       uint32_t pk[16], dk[16];
 #pragma unroll
       for (int c = 0; c < 32; c += 2) {
@@ -824,7 +858,7 @@ __global__ void __launch_bounds__(GB_THREADS, 1)
                               a.scale * p1 * (__uint_as_float(dr[c + 1]) - dl));
       }
       // P and dS into shared memory once the previous batch's MMAs have read them
-      if (i > 0 && !__all_sync(0xffffffffu, tc::mbar_wait(psempty, ph ^ 1u, abort_flag))) {
+      if (i > 0 && !__all_sync(0xffffffffu, tc::mbar_wait(psempty, (i - 1) & 1, abort_flag))) {
         *abort_flag = 1;
         break;
       }
@@ -837,27 +871,41 @@ __global__ void __launch_bounds__(GB_THREADS, 1)
       }
       tc::fence_proxy_async_smem();  // generic writes before the MMAs (async proxy) read them
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(psfull);
-      // dQ^T of this batch: channels 32 qd .. +31 of batch rows 64 hf .. +63.
-      // Each 32-row block is turned around in shared memory so that a lane adds
-      // four channels of one row with a 16-byte reduction: 8 lanes cover the
-      // warp's 128-byte line of a row, 4 rows per instruction.  The space is
-      // this warp's 4 KB of the batch's own Q / dO buffers (their first
-      // 64-channel boxes, which the producer reloads for every batch): every
-      // MMA that reads them is complete once dQ^T is, and the producer refills
-      // them only after all eight row warps have released the batch below.
-      if (!__all_sync(0xffffffffu, tc::mbar_wait(dqfull, ph, abort_flag))) {
+      if (lane == 0) {
+        tc::mbar_arrive(psfull);
+        tc::mbar_arrive(&qempty[buf]);  // done with the batch's row table
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ dQ drains (warps 8-11)
+    // warp 8 + qd: channels 32 qd .. +31 (its TMEM lane quadrant of dQ^T) of all
+    // 128 batch rows, 32 rows at a time.  Each 32-row block is turned around in
+    // shared memory so that a lane adds four channels of one row with a 16-byte
+    // reduction: 8 lanes cover the warp's 128-byte line of a row, 4 rows per
+    // instruction.  The space is this warp's 4 KB of the batch's own Q buffer
+    // (its first 64-channel box, which the producer reloads for every batch):
+    // every MMA that reads it is complete once dQ^T is, and the producer refills
+    // it only after this warp has released the batch.
+    const int qd = warp - GB_W_DRAIN;
+    const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
+    const bool live = qd * 32 < a.d;  // d = 64: quadrants 2, 3 hold the zero padding
+    for (int i = 0; i < nbatch; ++i) {
+      const int buf = i & 1;
+      // qfull orders the producer's row-table writes before this warp's reads
+      // (the phase cannot move on before this warp releases the batch)
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&qfull[buf], (i >> 1) & 1, abort_flag)) ||
+          !__all_sync(0xffffffffu, tc::mbar_wait(&dqfull[buf], (i >> 1) & 1, abort_flag))) {
         *abort_flag = 1;
         break;
       }
       tc::fence_after_sync();
-      float* xb = reinterpret_cast<float*>(gbase + (hf ? GB_OFF_DO : GB_OFF_Q) + buf * GT_QT + qd * (32 * 32 * 4));
-      const bool live = qd * 32 < a.d;  // d = 64: quadrants 2, 3 hold the zero padding
+      const int* tb = tab + buf * GT_ROWS;
+      float* xb = reinterpret_cast<float*>(gbase + GB_OFF_Q + buf * GT_QT + qd * (32 * 32 * 4));  // [row][channel]
 #pragma unroll 1
-      for (int cb = 0; cb < 2; ++cb) {
+      for (int cb = 0; cb < GT_ROWS / 32; ++cb) {
         uint32_t r[32];
         __syncwarp();
-        tc::tmem_ld32(tmem + lane_base + GB_T_DQ + hf * 64 + cb * 32, r);
+        tc::tmem_ld32(tmem + lane_base + GB_T_DQ + buf * GT_ROWS + cb * 32, r);
         tc::tmem_ld_wait();
         if (live) {
 #pragma unroll
@@ -866,7 +914,7 @@ __global__ void __launch_bounds__(GB_THREADS, 1)
 #pragma unroll
           for (int m = 0; m < 8; ++m) {
             const int k = 4 * m + (lane >> 3);
-            const int qr = tb[hf * 64 + cb * 32 + k];
+            const int qr = tb[cb * 32 + k];
             const float4 v = *reinterpret_cast<const float4*>(xb + k * 32 + 4 * (lane & 7));
             if (qr >= 0) red_add_v4(a.dq_acc + (int64_t)qr * a.d + qd * 32 + 4 * (lane & 7), v.x, v.y, v.z, v.w);
           }
@@ -877,31 +925,36 @@ __global__ void __launch_bounds__(GB_THREADS, 1)
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) {
-        tc::mbar_arrive(dqempty);
+        tc::mbar_arrive(&dqempty[buf]);
         tc::mbar_arrive(&qempty[buf]);  // the buffers and the row table may be rewritten for batch i + 2
       }
     }
-    // ---- this chunk's dK, dV of the block's keys: channel ch, keys 32 hf .. +31
+    // ---- this chunk's dK, dV of the block's keys: channels 32 qd .. +31, all 64 keys
     if (!*abort_flag && nbatch > 0) {
       // the last dQ^T commit follows every MMA of the chunk
-      if (!__all_sync(0xffffffffu, tc::mbar_wait(dqfull, (nbatch - 1) & 1, abort_flag))) {
+      const int last = nbatch - 1;
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&dqfull[last & 1], (last >> 1) & 1, abort_flag))) {
         *abort_flag = 1;
       } else {
         tc::fence_after_sync();
-        uint32_t rk[32], rv[32];
-        __syncwarp();
-        tc::tmem_ld32(tmem + lane_base + GB_T_DK + hf * 32, rk);
-        tc::tmem_ld32(tmem + lane_base + GB_T_DV + hf * 32, rv);
-        tc::tmem_ld_wait();
-        if (ch < a.d) {
+        const int ch = qd * 32 + lane;
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t rk[32], rv[32];
+          __syncwarp();
+          tc::tmem_ld32(tmem + lane_base + GB_T_DK + hf * 32, rk);
+          tc::tmem_ld32(tmem + lane_base + GB_T_DV + hf * 32, rv);
+          tc::tmem_ld_wait();
+          if (ch < a.d) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const int key = hf * 32 + k;
-            const int kp = ck.kbase + key;
-            if (key < a.bs && kp < ck.n) {
-              const int64_t o = ((int64_t)(ck.s0 + kp) * a.Hkv + ck.g) * a.d + ch;
-              red_f32(a.dk_acc + o, __uint_as_float(rk[k]));
-              red_f32(a.dv_acc + o, __uint_as_float(rv[k]));
+            for (int k = 0; k < 32; ++k) {
+              const int key = hf * 32 + k;
+              const int kp = ck.kbase + key;
+              if (key < a.bs && kp < ck.n) {
+                const int64_t o = ((int64_t)(ck.s0 + kp) * a.Hkv + ck.g) * a.d + ch;
+                red_f32(a.dk_acc + o, __uint_as_float(rk[k]));
+                red_f32(a.dv_acc + o, __uint_as_float(rv[k]));
+              }
             }
           }
         }
@@ -912,7 +965,7 @@ __global__ void __launch_bounds__(GB_THREADS, 1)
   tc::fence_before_sync();
   __syncthreads();
   if (*abort_flag && tid == 0) raise_flag(a.flags, TSA_FLAG_TIMEOUT);
-  if (warp == 9) {
+  if (warp == GB_W_MMA) {
     __syncwarp();
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, GB_TMEM);
@@ -925,9 +978,7 @@ cudaError_t launch_gqa_bwd_tc(const GqaTcArgs& a, cudaStream_t stream) {
   if (entries <= 0 || nB <= 0) return cudaSuccess;
   cudaError_t e = gt_invert(a, GT_BWD_CHUNK, stream);
   if (e != cudaSuccess) return e;
-  CUtensorMap tq, tdo, tk, tv;
-  if ((e = make_tmap_bf16_2d(&tq, a.q, (uint64_t)a.T * a.Hq, a.d, 1, 64)) != cudaSuccess) return e;
-  if ((e = make_tmap_bf16_2d(&tdo, a.dout, (uint64_t)a.T * a.Hq, a.d, 1, 64)) != cudaSuccess) return e;
+  CUtensorMap tk, tv;
   if ((e = make_tmap_bf16_2d(&tk, a.k, (uint64_t)a.T * a.Hkv, a.d, 1, 64)) != cudaSuccess) return e;
   if ((e = make_tmap_bf16_2d(&tv, a.v, (uint64_t)a.T * a.Hkv, a.d, 1, 64)) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(gqa_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, GB_SMEM)) !=
@@ -935,7 +986,7 @@ cudaError_t launch_gqa_bwd_tc(const GqaTcArgs& a, cudaStream_t stream) {
     return e;
   const int64_t grid = nB + (entries + GT_BWD_CHUNK - 1) / GT_BWD_CHUNK;
   const unsigned nblocks = static_cast<unsigned>(grid);
-  gqa_bwd_tc_kernel<<<nblocks, GB_THREADS, GB_SMEM, stream>>>(tq, tdo, tk, tv, a, GT_BWD_CHUNK);
+  gqa_bwd_tc_kernel<<<nblocks, GB_THREADS, GB_SMEM, stream>>>(tk, tv, a, GT_BWD_CHUNK);
   note_launch();
   return cudaGetLastError();
 }
