@@ -467,9 +467,11 @@ __global__ void __launch_bounds__(GT_THREADS, 2)
 
 // Merge of the partials: one warp per (query, head), the selected blocks in
 // slot order (fixed, so the result is bit-identical across runs).  Lane j holds
-// slot j's log-sum-exp (32 slots per round), the weights come from warp
-// reductions, and the partial rows are read eight slots at a time.
-__global__ void __launch_bounds__(256) gqa_combine_kernel(const __grid_constant__ GqaTcArgs a) {
+// slot j's log-sum-exp (32 slots per round) and the weights come from warp
+// reductions.  Up to 32 selected blocks, the partial rows are loaded together
+// with the log-sum-exps (one memory latency per row); more blocks take two
+// passes, the partial rows eight slots at a time.
+__global__ void __launch_bounds__(256, 2) gqa_combine_kernel(const __grid_constant__ GqaTcArgs a) {
   const int64_t rowid = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (rowid >= (int64_t)a.T * a.Hq) return;
@@ -481,49 +483,75 @@ __global__ void __launch_bounds__(256) gqa_combine_kernel(const __grid_constant_
   const int32_t* brow = a.blk + ((int64_t)t * a.Hkv + g) * a.nsel;
   const int64_t e0 = ((int64_t)t * a.Hkv + g) * a.nsel;
   const int nv = a.d / 4;  // four channels per lane
-  // pass 1: the maximum log-sum-exp over the valid slots
-  float M = -INFINITY;
-  for (int j0 = 0; j0 < a.nsel; j0 += 32) {
-    const int j = j0 + lane;
-    const int b = j < a.nsel ? __ldg(brow + j) : -1;
-    const bool ok = b >= 0 && (int64_t)b * a.bs < n && (int64_t)b * a.bs <= p;
-    M = fmaxf(M, ok ? __ldg(a.part_l + (e0 + j) * a.G + hh) : -INFINITY);
-  }
-  M = warp_max(M);
-  float W = 0.f;
+  float M = -INFINITY, W = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (M != -INFINITY) {
+  auto accumulate = [&](const uint2& r, float w) {
+    const float2 o01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.x));
+    const float2 o23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.y));
+    acc.x = fmaf(w, o01.x, acc.x);
+    acc.y = fmaf(w, o01.y, acc.y);
+    acc.z = fmaf(w, o23.x, acc.z);
+    acc.w = fmaf(w, o23.y, acc.w);
+  };
+  if (a.nsel <= 32) {
+    // one round: the block ids, the log-sum-exps and every slot's partial row
+    // are loaded together (one memory latency); a slot without a partial
+    // (invalid or not causal) gets weight 0 and its row, whatever it holds, is
+    // never summed
+    uint2 raw[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      raw[k] = (k < a.nsel && lane < nv)
+                   ? __ldg(reinterpret_cast<const uint2*>(a.part_o + ((e0 + k) * a.G + hh) * a.d) + lane)
+                   : make_uint2(0u, 0u);
+    const int b = lane < a.nsel ? __ldg(brow + lane) : -1;
+    const float lj = lane < a.nsel ? __ldg(a.part_l + (e0 + lane) * a.G + hh) : -INFINITY;
+    const bool ok = b >= 0 && (int64_t)b * a.bs < n && (int64_t)b * a.bs <= p;
+    M = warp_max(ok ? lj : -INFINITY);
+    if (M != -INFINITY) {
+      const float wl = ok ? exp2f(lj - M) : 0.f;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const float w = __shfl_sync(0xffffffffu, wl, k);
+        if (w != 0.f) accumulate(raw[k], w);
+      }
+      W = warp_sum(wl);
+    }
+  } else {
+    // pass 1: the maximum log-sum-exp over the valid slots
     for (int j0 = 0; j0 < a.nsel; j0 += 32) {
       const int j = j0 + lane;
       const int b = j < a.nsel ? __ldg(brow + j) : -1;
       const bool ok = b >= 0 && (int64_t)b * a.bs < n && (int64_t)b * a.bs <= p;
-      const float wl = ok ? exp2f(__ldg(a.part_l + (e0 + j) * a.G + hh) - M) : 0.f;
-      W += wl;
-      const int cnt = min(32, a.nsel - j0);
-      for (int k0 = 0; k0 < cnt; k0 += 8) {
-        uint2 raw[8];
-        float wk[8];
+      M = fmaxf(M, ok ? __ldg(a.part_l + (e0 + j) * a.G + hh) : -INFINITY);
+    }
+    M = warp_max(M);
+    if (M != -INFINITY) {
+      for (int j0 = 0; j0 < a.nsel; j0 += 32) {
+        const int j = j0 + lane;
+        const int b = j < a.nsel ? __ldg(brow + j) : -1;
+        const bool ok = b >= 0 && (int64_t)b * a.bs < n && (int64_t)b * a.bs <= p;
+        const float wl = ok ? exp2f(__ldg(a.part_l + (e0 + j) * a.G + hh) - M) : 0.f;
+        W += wl;
+        const int cnt = min(32, a.nsel - j0);
+        for (int k0 = 0; k0 < cnt; k0 += 8) {
+          uint2 raw[8];
+          float wk[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {  // slot order within a round: k0 + u
-          const int k = k0 + u;
-          wk[u] = __shfl_sync(0xffffffffu, wl, k & 31);
-          raw[u] = make_uint2(0u, 0u);
-          if (k < cnt && wk[u] != 0.f && lane < nv)
-            raw[u] = __ldg(reinterpret_cast<const uint2*>(a.part_o + ((e0 + j0 + k) * a.G + hh) * a.d) + lane);
-        }
+          for (int u = 0; u < 8; ++u) {  // slot order within a round: k0 + u
+            const int k = k0 + u;
+            wk[u] = __shfl_sync(0xffffffffu, wl, k & 31);
+            raw[u] = make_uint2(0u, 0u);
+            if (k < cnt && wk[u] != 0.f && lane < nv)
+              raw[u] = __ldg(reinterpret_cast<const uint2*>(a.part_o + ((e0 + j0 + k) * a.G + hh) * a.d) + lane);
+          }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          if (k0 + u >= cnt || wk[u] == 0.f) continue;
-          const float2 o01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[u].x));
-          const float2 o23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[u].y));
-          acc.x = fmaf(wk[u], o01.x, acc.x);
-          acc.y = fmaf(wk[u], o01.y, acc.y);
-          acc.z = fmaf(wk[u], o23.x, acc.z);
-          acc.w = fmaf(wk[u], o23.y, acc.w);
+          for (int u = 0; u < 8; ++u)
+            if (k0 + u < cnt && wk[u] != 0.f) accumulate(raw[u], wk[u]);
         }
       }
+      W = warp_sum(W);
     }
-    W = warp_sum(W);
   }
   const float inv = W > 0.f ? 1.f / W : 0.f;
   if (lane < nv) {
