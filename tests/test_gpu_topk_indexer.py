@@ -27,8 +27,12 @@ DEV = "cuda"
 # ------------------------------------------------------------ top-k from scores
 
 @pytest.mark.parametrize("rows,L,k", [(64, 50, 7), (64, 333, 64), (32, 4096, 2048), (16, 5000, 65),
-                                      (8, 20011, 2048), (4, 65536, 2048), (8, 70000, 4096), (3, 9000, 1)])
+                                      (8, 20011, 2048), (4, 65536, 2048), (8, 70000, 4096), (3, 9000, 1),
+                                      (128, 256, 64), (40, 129, 200), (9, 31, 31), (5, 1, 3)])
 def test_topk_from_scores_bit_exact(tsa, rows, L, k):
+    """Tie-stress rows (+-0, -inf, repeated values) of every length class: one
+    warp per row up to 256 entries, one CTA per row beyond; k above the row
+    length pads with -1."""
     s = synth.tie_stress_scores(rows, L, seed=rows + L + k)
     got = tsa.qsa_topk_from_scores(s.to(DEV), k).cpu().numpy()
     ref = O.topk_rows(s.numpy(), k)

@@ -697,8 +697,56 @@ __global__ void __launch_bounds__(TK_THREADS, 3) topk_rows_kernel(TopkRows a) {
   finish_row(keys, k, k, out);
 }
 
+// Launches whose rows hold at most 256 entries (the block scores of the QSA
+// selection, short sequences): one warp per row, its 32 E keys in registers (E
+// per lane) ordered by the warp-level bitonic network (lane shuffles and
+// in-register exchanges, no block barrier).  Keys are the same composite keys
+// as above, so the order is the same.
+template <int E>
+__global__ void __launch_bounds__(256) topk_warp_rows_kernel(TopkRows a, int64_t rows) {
+  const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (r >= rows) return;  // warp-uniform
+  const int lane = threadIdx.x & 31;
+  const float NEG_INF = __int_as_float(0xff800000);
+  const float* row = a.scores + r * a.ld;
+  int32_t* out = a.out + r * a.out_ld;
+  int64_t n = a.width;
+  if (a.mode != 0) {
+    const int64_t p = a.p0 + r / a.groups;
+    const int64_t c = (a.mode == 1) ? p + 1 : p / a.bs + 1;
+    n = c < n ? c : n;
+  }
+  uint64_t v[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int i = 32 * e + lane;
+    uint64_t key = 0;
+    if (i < n) {
+      const float sc = row[i];
+      if (sc != NEG_INF) key = comp_key(order_key(sc), static_cast<uint32_t>(i));
+    }
+    v[e] = key;
+  }
+  for (int size = 2; size <= 32 * E; size <<= 1) bitonic_reg_steps<E>(v, 0, size, size >> 1);
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int j = 32 * e + lane;
+    if (j < a.k) out[j] = v[e] ? static_cast<int32_t>(~static_cast<uint32_t>(v[e] & 0xffffffffull)) : -1;
+  }
+  for (int j = 32 * E + lane; j < a.k; j += 32) out[j] = -1;
+}
+
 cudaError_t launch_topk_rows(const TopkRows& a, int64_t rows, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
+  if (a.width <= 256) {
+    const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
+    auto kern = a.width <= 32 ? topk_warp_rows_kernel<1>
+                : a.width <= 64 ? topk_warp_rows_kernel<2>
+                : a.width <= 128 ? topk_warp_rows_kernel<4> : topk_warp_rows_kernel<8>;
+    kern<<<grid, 256, 0, stream>>>(a, rows);
+    note_launch();
+    return cudaGetLastError();
+  }
   cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TK_SMEM);
   if (e != cudaSuccess) return e;
   // the whole shared-memory carveout: the rows of one chunk run beside the
