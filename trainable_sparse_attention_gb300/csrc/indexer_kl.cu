@@ -19,9 +19,9 @@
 //     dq_I[t,h] = score_scale * sum_j G * w[t,h] * [D > 0] * k_I[s]
 //     dk_I[s]  += score_scale * sum_h G * w[t,h] * [D > 0] * q_I[t,h]
 //
-// One CTA per query.  The selected key rows k_I[s0 + idx[t, j]] are gathered
-// 128 at a time (TMA tile::gather4 into the 128-byte-swizzled K-major layout)
-// through a three-stage ring, and
+// One CTA per query.  The selected key rows k_I[s0 + idx[t, j]] are copied
+// 128 at a time (cp.async into the 128-byte-swizzled K-major layout) through a
+// two- or three-stage ring, and
 //   D^T = K_sel q_I[t]^T        (M = 128 slots, N = NP heads, K = d_I = 128)
 // lands in TMEM with slots on lanes, so every epilogue thread owns one slot and
 // works on its own row of head values (ReLU, head weight, the head sum of the
@@ -43,7 +43,7 @@
 //
 // Heads are padded to NP = 64 or 128 (w = 0 on the padding, so padded heads add
 // exactly nothing).  Warp roles (192 threads): warps 0-3 epilogue (TMEM lane
-// quadrants; slot of the tile = 32 w + lane), warp 4 TMA producer, warp 5 TMEM
+// quadrants; slot of the tile = 32 w + lane), warp 4 producer, warp 5 TMEM
 // allocator + MMA issuer.  Every wait is bounded; a timeout raises
 // TSA_FLAG_TIMEOUT and the CTA winds down, releasing its TMEM.
 #include <algorithm>
@@ -122,7 +122,7 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
 
 template <int NP, bool BWD>
 __global__ void __launch_bounds__(KL_THREADS, KlLayout<NP, BWD>::CTAS)
-    indexer_sel_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    indexer_sel_kernel(const __grid_constant__ CUtensorMap tm_q, const __nv_bfloat16* __restrict__ kI,
                        const __grid_constant__ IndexerSelArgs a) {
   using L = KlLayout<NP, BWD>;
   extern __shared__ unsigned char smem_raw[];
@@ -153,12 +153,11 @@ __global__ void __launch_bounds__(KL_THREADS, KlLayout<NP, BWD>::CTAS)
   const int n = a.st.cu[sq + 1] - s0;
   const int ntiles = (a.topk + KL_M - 1) / KL_M;
   const int* idx_row = a.idx + (int64_t)t * a.topk;
-  int issued = 0;  // producer: tiles whose gathers were issued
 
   if (tid == 0) {
     tc::mbar_init(qfull, 1);
     for (int i = 0; i < L::STAGES; ++i) {
-      tc::mbar_init(&kfull[i], 1);
+      tc::mbar_init(&kfull[i], 32);  // one cp.async arrival per producer lane
       tc::mbar_init(&kempty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -181,16 +180,23 @@ __global__ void __launch_bounds__(KL_THREADS, KlLayout<NP, BWD>::CTAS)
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer
-    // q_I[t] once (NP rows from row t * H_I; rows past this query's heads meet
-    // w = 0), then each tile's 128 slot rows: lane l gathers rows 4l .. 4l+3 of
-    // both 64-channel boxes.  A slot that is -1 or outside the sequence fetches
-    // the sequence's first row; the epilogue masks it.
+    // q_I[t] once by TMA (NP rows from row t * H_I; rows past this query's heads
+    // meet w = 0), then each tile's 128 slot rows of k_I by cp.async: 16 lanes
+    // per row, so that a warp instruction copies two whole 256-byte rows, each
+    // 16-byte chunk straight to its place in the 128-byte-swizzled K-major tile
+    // (chunk j of row r at r * 128 + (j ^ (r & 7)) * 16 of its 64-channel box).
+    // Lane l holds the slot indices of rows 4l .. 4l+3; they travel to the
+    // copying lanes by shuffle.  A slot that is -1 or outside the sequence is
+    // zero-filled; the epilogue masks it.  (One TMA gather4 per 4 rows had
+    // bound these kernels.)  Each lane's copies of a tile arrive on its kfull.
     if (lane == 0) {
       tc::prefetch_tmap(&tm_q);
-      tc::prefetch_tmap(&tm_k);
       tc::mbar_arrive_expect_tx(qfull, 2 * L::QBOX);
       for (int c = 0; c < 2; ++c) tc::tma_load_2d(sQ + c * L::QBOX, &tm_q, qfull, c * 64, t * a.H_I);
     }
+    const int c16 = lane & 15, h = lane >> 4;
+    const int cb = c16 >> 3, jj = c16 & 7;
+    const char* ksrc = reinterpret_cast<const char*>(kI);
     bool ok = true;
     // the slot indices of tile j + 1 are loaded while tile j's stage frees up
     int id_next[4];
@@ -213,21 +219,26 @@ __global__ void __launch_bounds__(KL_THREADS, KlLayout<NP, BWD>::CTAS)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         if (id[i] >= n) raise_flag(a.flags, TSA_FLAG_INDEX_RANGE);
-        r[i] = s0 + ((id[i] >= 0 && id[i] < n) ? id[i] : 0);
+        r[i] = (id[i] >= 0 && id[i] < n) ? s0 + id[i] : -1;
       }
-      if (lane == 0) tc::mbar_arrive_expect_tx(&kfull[st], KL_KSTAGE);
-      __syncwarp();
-      const uint32_t dst = sK + st * KL_KSTAGE + 4 * lane * 128;
-      tc::tma_gather4(dst, &tm_k, &kfull[st], 0, r[0], r[1], r[2], r[3]);
-      tc::tma_gather4(dst + KL_KBOX, &tm_k, &kfull[st], 64, r[0], r[1], r[2], r[3]);
-      issued = j + 1;
+      const uint32_t dst = sK + st * KL_KSTAGE + cb * KL_KBOX;
+#pragma unroll 8
+      for (int m = 0; m < KL_M / 2; ++m) {
+        // row 2m + h is row 2 (m & 1) + h of lane m / 2
+        const int ra = __shfl_sync(0xffffffffu, r[2 * (m & 1)], m >> 1);
+        const int rb = __shfl_sync(0xffffffffu, r[2 * (m & 1) + 1], m >> 1);
+        const int src = h ? rb : ra;
+        const int row = 2 * m + h;
+        cp_async16(dst + row * 128 + ((jj ^ (row & 7)) << 4), ksrc + (int64_t)(src >= 0 ? src : s0) * (KL_DI * 2) + c16 * 16,
+                   src >= 0 ? 16u : 0u);
+      }
+      cp_async_commit();
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&kfull[st])) : "memory");
     }
     if (!ok) *abort_flag = 1;
-    // gathers still in flight land before the CTA exits (bounded by time only)
-    if (lane == 0) {
+    cp_async_wait<0>();  // this lane's copies land before the CTA can exit
+    if (lane == 0) {     // and the q_I block (bounded by time only)
       volatile int keep_waiting = 0;
-      for (int g = issued > L::STAGES ? issued - L::STAGES : 0; g < issued; ++g)
-        (void)tc::mbar_wait(&kfull[g % L::STAGES], (g / L::STAGES) & 1, &keep_waiting);
       (void)tc::mbar_wait(qfull, 0, &keep_waiting);
     }
   } else if (warp == 5) {
@@ -245,6 +256,7 @@ __global__ void __launch_bounds__(KL_THREADS, KlLayout<NP, BWD>::CTAS)
           break;
         }
         tc::fence_after_sync();
+        tc::fence_proxy_async_smem();  // the rows arrived by cp.async (generic proxy); the MMAs read them
         const uint32_t kst = sK + st * KL_KSTAGE;
         // D^T = K_sel q_I^T (both K-major)
 #pragma unroll
@@ -548,14 +560,13 @@ static cudaError_t launch_sel_t(const IndexerSelArgs& a, const void* q, const vo
                                 cudaStream_t stream) {
   using L = KlLayout<NP, BWD>;
   static_assert(L::SMEM <= 227 * 1024, "indexer selection kernel shared memory");
-  CUtensorMap tq, tk;
+  CUtensorMap tq;
   cudaError_t e = make_tmap_bf16_2d(&tq, q, (uint64_t)T_total * a.H_I, KL_DI, NP, 64);
   if (e != cudaSuccess) return e;
-  if ((e = make_tmap_bf16_2d(&tk, k, (uint64_t)T_total, KL_DI, 1, 64)) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(indexer_sel_kernel<NP, BWD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 L::SMEM)) != cudaSuccess)
     return e;
-  indexer_sel_kernel<NP, BWD><<<a.T, KL_THREADS, L::SMEM, stream>>>(tq, tk, a);
+  indexer_sel_kernel<NP, BWD><<<a.T, KL_THREADS, L::SMEM, stream>>>(tq, static_cast<const __nv_bfloat16*>(k), a);
   note_launch();
   return cudaGetLastError();
 }
