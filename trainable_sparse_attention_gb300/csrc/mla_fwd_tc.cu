@@ -389,19 +389,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
           ok = false;
           break;
         }
+        // the logits stay unscaled here: the softmax scale (> 0) goes into the
+        // exponent's FMA, and rounding is monotone, so the scaled maximum is the
+        // maximum of the scaled logits
         const uint32_t mask = masks[st];
-        if (mask == 0xffffffffu) {
+        if (mask != 0xffffffffu) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) x2[i] *= a.scale_log2;
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) x2[i] = ((mask >> i) & 1u) ? x2[i] * a.scale_log2 : NEG_INF;
+          for (int i = 0; i < 32; ++i) x2[i] = ((mask >> i) & 1u) ? x2[i] : NEG_INF;
         }
         float mx[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx[i] = fmaxf(fmaxf(x2[i], x2[i + 8]), fmaxf(x2[i + 16], x2[i + 24]));
-        const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        const float tmax = a.scale_log2 * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         float alpha = 1.f;
         const bool resc = tmax > m_use + kRescaleLog2;
         if (resc) {
@@ -414,7 +414,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float p0 = ex2(x2[i] - mu), p1 = ex2(x2[i + 1] - mu);
+          const float p0 = ex2(fmaf(x2[i], a.scale_log2, -mu)), p1 = ex2(fmaf(x2[i + 1], a.scale_log2, -mu));
           ps[(i >> 1) & 3] += p0 + p1;
           pk[i / 2] = pack_bf16(p0, p1);
         }
