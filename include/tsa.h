@@ -134,7 +134,9 @@ int qsa_topk_from_scores(const float* scores_dev, int64_t rows, int64_t width, i
  *   call; the indexer's on the highest priority), forked from `stream` and
  *   joined back into it by events, so the call is ordered on `stream` like a
  *   single kernel.  Calls from several host threads are serialised while they
- *   enqueue.
+ *   enqueue.  The first call on a device creates those streams and events:
+ *   make it before any stream capture (later calls may be captured; the fork
+ *   and the join are ordinary event dependencies of the captured graph).
  * ------------------------------------------------------------------------- */
 size_t qsa_topk_workspace_size(const int32_t* cu_seqlens, int num_seqs, int groups, int block_size);
 int qsa_topk(const void* q_idx_dev, const void* k_idx_dev, const float* w_dev,
