@@ -208,6 +208,7 @@ def test_mla_t65536_h128_sampled(tsa):
     (576, 1000, [700]),          # top-k wider than the sequence: -1 tails
     (512, 96, [257]),            # NoPE layout
     (576, 2048, [2100]),         # 64 tiles of 32 keys
+    (576, 4096, [4200]),         # the widest top-k: 128 tiles
 ])
 def test_mla_h128_forward(tsa, D, topk, lengths):
     """H = 128 (the tcgen05 cluster path): parity with the oracle on sampled rows,
@@ -227,6 +228,26 @@ def test_mla_h128_forward(tsa, D, topk, lengths):
     check_out_lse(out, lse, o_ref, l_ref, rows=rows)
     for r in (3, T - 1):
         assert torch.all(out[r] == 0) and torch.all(torch.isneginf(lse[r]))
+
+
+def test_mla_h128_tiny_sequences(tsa):
+    """H = 128 on sequences of 1, 2 and 5 tokens (THD): most slots are -1, the
+    first query of each sequence has one valid key; forward and backward on every
+    row against the oracle."""
+    cu = synth.cu_seqlens_thd([1, 2, 5])
+    T = cu[-1]
+    m = synth.mla_inputs(T, 128, 576, seed=21, with_grad_out=True)
+    idx = synth.random_topk_indices(cu, 64, seed=21)
+    scale = 1 / math.sqrt(576)
+    q, kv, ids, dO = m["q"].to(DEV), m["kv"].to(DEV), idx.to(DEV), m["dout"].to(DEV)
+    out, lse = tsa.sparse_mla_fwd(q, kv, ids, cu, scale)
+    dq, dkv = tsa.sparse_mla_bwd(q, kv, ids, out, lse, dO, cu, scale)
+    torch.cuda.synchronize()
+    o_ref, l_ref = O.sparse_mla_fwd(m["q"], m["kv"], idx, cu, scale)
+    check_out_lse(out, lse, o_ref, l_ref)
+    dq_ref, dkv_ref = O.sparse_mla_bwd(m["q"], m["kv"], idx, cu, scale, m["dout"])
+    check_grad(dq, dq_ref, "dq")
+    check_grad(dkv, dkv_ref, "dkv")
 
 
 def test_mla_h128_large_logits_rescale(tsa):
