@@ -250,6 +250,7 @@ namespace {
 struct TopkPipe {
   cudaStream_t idx = nullptr, sel = nullptr;
   cudaEvent_t start = nullptr, filled[2] = {nullptr, nullptr}, drained[2] = {nullptr, nullptr};
+  cudaEvent_t joined[2] = {nullptr, nullptr};  // the ends of the two streams, waited by the caller's
 };
 constexpr int kMaxPipeDevices = 64;
 TopkPipe g_pipes[kMaxPipeDevices];
@@ -270,6 +271,7 @@ int topk_pipe(TopkPipe** out) {
     for (int i = 0; i < 2; ++i) {
       TSA_CHECK_CUDA(cudaEventCreateWithFlags(&q.filled[i], cudaEventDisableTiming), "event");
       TSA_CHECK_CUDA(cudaEventCreateWithFlags(&q.drained[i], cudaEventDisableTiming), "event");
+      TSA_CHECK_CUDA(cudaEventCreateWithFlags(&q.joined[i], cudaEventDisableTiming), "event");
     }
     p = q;
   }
@@ -306,6 +308,7 @@ int qsa_topk(const void* q_idx, const void* k_idx, const float* w, const int32_t
   TSA_CHECK_CUDA(cudaStreamWaitEvent(pp->idx, pp->start, 0), "fork");
   TSA_CHECK_CUDA(cudaStreamWaitEvent(pp->sel, pp->start, 0), "fork");
   const size_t buf_floats = static_cast<size_t>(C) * groups * width;
+  auto enqueue = [&]() -> int {
   int64_t chunk = 0;
   for (int b = 0; b < num_seqs; ++b) {
     const int len = st.cu[b + 1] - st.cu[b];
@@ -341,8 +344,18 @@ int qsa_topk(const void* q_idx, const void* k_idx, const float* w, const int32_t
       TSA_CHECK_CUDA(cudaEventRecord(pp->drained[nb], pp->sel), "chunk selected");
     }
   }
-  // join: the last top-k follows every indexer launch (through its event)
-  TSA_CHECK_CUDA(cudaStreamWaitEvent(s, pp->drained[(chunk - 1) & 1], 0), "join");
+  return TSA_OK;
+  };
+  const int erc = enqueue();
+  // join both streams into the caller's, also after a failed launch, so that
+  // everything enqueued so far is ordered before the caller's next use of the
+  // workspace and the indices
+  cudaError_t je = cudaEventRecord(pp->joined[0], pp->idx);
+  if (je == cudaSuccess) je = cudaEventRecord(pp->joined[1], pp->sel);
+  if (je == cudaSuccess) je = cudaStreamWaitEvent(s, pp->joined[0], 0);
+  if (je == cudaSuccess) je = cudaStreamWaitEvent(s, pp->joined[1], 0);
+  if (erc) return erc;
+  TSA_CHECK_CUDA(je, "join");
   return TSA_OK;
 }
 
