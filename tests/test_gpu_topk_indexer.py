@@ -214,6 +214,27 @@ def test_qsa_topk_deterministic(tsa):
     assert torch.equal(a, b)
 
 
+def test_qsa_topk_on_a_side_stream(tsa):
+    """The streamed runner forks from and joins back into the caller's stream:
+    called on a side stream (several chunks: two score buffers reused), its
+    indices are complete once that stream is, and equal the default stream's;
+    work queued on the side stream after the call sees the finished indices."""
+    T = 24000
+    cu = [0, 3000, T]  # 512 MB score chunks of 6272 rows: one chunk, then four
+    x = synth.indexer_inputs(T, 64, 128, seed=8)
+    args = (x["q_idx"].to(DEV), x["k_idx"].to(DEV), x["w"].to(DEV), cu, 1024)
+    ref = tsa.qsa_topk(*args)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        got = tsa.qsa_topk(*args, stream=side)
+        total = got.to(torch.int64).sum()          # ordered after the call on the side stream
+    side.synchronize()
+    assert torch.equal(got, ref)
+    assert total.item() == ref.to(torch.int64).sum().item()
+
+
 @pytest.mark.slow
 def test_qsa_topk_t65536_sampled(tsa):
     """T=65536, 64 indexer heads, d_I=128, k=2048; sampled rows vs the oracle."""
