@@ -619,6 +619,8 @@ int sparse_gqa_fwd(const void* q, const void* k, const void* v, const int32_t* b
     return fail(TSA_ERR_WORKSPACE, "workspace %zu bytes < %zu", workspace_bytes, need);
   a.nblk = gqa_block_bases(a.st, block_size, a.blk_base);
   const size_t t = static_cast<size_t>(T);
+  a.nseg = 1;  // the forward writes partials, no reductions: one query segment
+  a.qseg = static_cast<int>(T);
   const size_t nb = t * Hkv + 1;
   char* w = static_cast<char*>(workspace);
   auto take = [&](size_t bytes) { char* p = w; w += gqa_ws_align(bytes); return p; };
@@ -645,15 +647,25 @@ int sparse_gqa_fwd(const void* q, const void* k, const void* v, const int32_t* b
 
 // Workspace of the key-centric backward: fp32 dQ, dK, dV accumulators, Delta,
 // the inverted selections and their offsets.  At most one block per token, so
-// T * Hkv bounds the number of (block, group) lists.
+// T * Hkv bounds the number of (block, group) lists of one query segment.
+//
+// The backward's lists are split by query segment (up to 8) so that the CTAs
+// running together reduce into one segment's slice of the fp32 dQ accumulator,
+// about 48 MB or less: at the THD 32768 workload (537 MB of dQ) the reductions
+// otherwise missed L2 and went to DRAM as read-modify-writes.
+static int gqa_bwd_segments(int64_t T, int Hq, int d) {
+  const int64_t dq_bytes = T * Hq * d * static_cast<int64_t>(sizeof(float));
+  const int64_t want = (dq_bytes + (int64_t(48) << 20) - 1) / (int64_t(48) << 20);
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(8, want)));
+}
 
 size_t sparse_gqa_bwd_workspace_size(int64_t T, int Hq, int Hkv, int d, int nsel) {
   if (T < 0 || Hq < 1 || Hkv < 1 || d < 1 || nsel < 1) return 0;
   const size_t t = static_cast<size_t>(T);
-  const size_t nb = t * Hkv + 1;
+  const size_t nl = static_cast<size_t>(gqa_bwd_segments(T, Hq, d)) * (t * Hkv + 1);
   return gqa_ws_align(t * Hq * d * sizeof(float)) + 2 * gqa_ws_align(t * Hkv * d * sizeof(float)) +
          gqa_ws_align(t * Hq * sizeof(float)) + gqa_ws_align(t * Hkv * nsel * sizeof(int)) +
-         4 * gqa_ws_align((nb + 1) * sizeof(int));
+         4 * gqa_ws_align((nl + 1) * sizeof(int));
 }
 
 int sparse_gqa_bwd(const void* q, const void* k, const void* v, const int32_t* block_indices, const void* out,
@@ -677,7 +689,10 @@ int sparse_gqa_bwd(const void* q, const void* k, const void* v, const int32_t* b
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   a.nblk = gqa_block_bases(a.st, block_size, a.blk_base);
   const size_t t = static_cast<size_t>(T);
-  const size_t nb = t * Hkv + 1;
+  a.nseg = gqa_bwd_segments(T, Hq, d);
+  while (a.nseg > 1 && static_cast<int64_t>(a.nseg) * a.nblk * Hkv >= 0x7fffffffLL) --a.nseg;  // int list indices
+  a.qseg = static_cast<int>((T + a.nseg - 1) / a.nseg);
+  const size_t nb = static_cast<size_t>(a.nseg) * (t * Hkv + 1);
   char* w = static_cast<char*>(workspace);
   auto take = [&](size_t bytes) { char* p = w; w += gqa_ws_align(bytes); return p; };
   float* dq_acc = reinterpret_cast<float*>(take(t * Hq * d * sizeof(float)));

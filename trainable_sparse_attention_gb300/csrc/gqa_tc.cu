@@ -101,9 +101,13 @@ __device__ __forceinline__ void red_f32(float* p, float v) {
 // ---------------------------------------------------------------- selection inversion
 
 // Selection entries e = (t, g, j) that name a causal block of t's sequence:
-// count them per (global block, group), or (FILL) append e itself (the flat
-// index (t * Hkv + g) * nsel + j, which is also the entry's partial slot) to
-// that list.  Entries outside the sequence raise TSA_FLAG_INDEX_RANGE and are dropped.
+// count them per (query segment t / qseg, global block, group), or (FILL)
+// append e itself (the flat index (t * Hkv + g) * nsel + j, which is also the
+// entry's partial slot) to that list.  Lists are numbered segment-major, so the
+// grid takes the lists of one segment of queries before the next: the
+// backward's CTAs running together then reduce into one segment's slice of the
+// dQ accumulator, which fits in L2.  Entries outside the sequence raise
+// TSA_FLAG_INDEX_RANGE and are dropped.
 template <bool FILL>
 __global__ void gqa_tc_inv_kernel(const __grid_constant__ GqaTcArgs a) {
   const int64_t total = static_cast<int64_t>(a.T) * a.Hkv * a.nsel;
@@ -121,7 +125,7 @@ __global__ void gqa_tc_inv_kernel(const __grid_constant__ GqaTcArgs a) {
       continue;
     }
     if (static_cast<int64_t>(b) * a.bs > p) continue;  // not a causal block of this query
-    const int idx = (a.blk_base[s] + b) * a.Hkv + g;
+    const int idx = ((t / a.qseg) * a.nblk + a.blk_base[s] + b) * a.Hkv + g;
     if (!FILL) {
       atomicAdd(a.cnt + idx, 1);
     } else {
@@ -168,14 +172,16 @@ struct GtChunk {
 };
 __device__ __forceinline__ bool gt_chunk(const GqaTcArgs& a, int c, int chunk, GtChunk& ck) {
   const int nB = a.nblk * a.Hkv;
-  if (c >= a.choff[nB]) return false;
-  int lo = 0, hi = nB - 1;
+  const int nL = a.nseg * nB;
+  if (c >= a.choff[nL]) return false;
+  int lo = 0, hi = nL - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (a.choff[mid] <= c) lo = mid; else hi = mid - 1;
   }
-  const int gb = lo / a.Hkv;
-  ck.g = lo % a.Hkv;
+  const int bg = lo % nB;  // (block, group) of the list
+  const int gb = bg / a.Hkv;
+  ck.g = bg % a.Hkv;
   const int sq = gt_block_seq(a, gb);
   ck.s0 = a.st.cu[sq];
   ck.n = a.st.cu[sq + 1] - ck.s0;
@@ -568,7 +574,7 @@ namespace {
 // Inversion of the selections into per-(block, group) lists, shared by the
 // forward and the backward.
 cudaError_t gt_invert(const GqaTcArgs& a, int chunk, cudaStream_t stream) {
-  const int nB = a.nblk * a.Hkv;
+  const int nB = a.nseg * a.nblk * a.Hkv;  // lists
   const int64_t entries = static_cast<int64_t>(a.T) * a.Hkv * a.nsel;
   cudaError_t e;
   const unsigned ig = static_cast<unsigned>(std::min<int64_t>((entries + 255) / 256, 4096));
@@ -589,7 +595,7 @@ constexpr int GT_FWD_CHUNK = 256;  // list entries (queries) per forward CTA
 }  // namespace
 
 cudaError_t launch_gqa_fwd_tc(const GqaTcArgs& a, cudaStream_t stream) {
-  const int nB = a.nblk * a.Hkv;
+  const int nB = a.nseg * a.nblk * a.Hkv;  // lists
   const int64_t entries = static_cast<int64_t>(a.T) * a.Hkv * a.nsel;
   if (entries <= 0 || nB <= 0) return cudaSuccess;
   cudaError_t e = gt_invert(a, GT_FWD_CHUNK, stream);
@@ -1001,7 +1007,7 @@ __global__ void __launch_bounds__(GB_THREADS, 1)
 }
 
 cudaError_t launch_gqa_bwd_tc(const GqaTcArgs& a, cudaStream_t stream) {
-  const int nB = a.nblk * a.Hkv;
+  const int nB = a.nseg * a.nblk * a.Hkv;  // lists
   const int64_t entries = static_cast<int64_t>(a.T) * a.Hkv * a.nsel;
   if (entries <= 0 || nB <= 0) return cudaSuccess;
   cudaError_t e = gt_invert(a, GT_BWD_CHUNK, stream);

@@ -102,11 +102,12 @@ struct GqaTcArgs {
   int T, Hq, Hkv, G, nsel, bs, d;
   float scale, scale_log2;
   int nblk;                   // blocks over all sequences
-  int* cnt;                   // [nblk * Hkv] entries per (block, group)
-  int* off;                   // [nblk * Hkv + 1] list offsets
-  int* cur;                   // [nblk * Hkv] fill cursors
-  int* choff;                 // [nblk * Hkv + 1] chunk offsets
-  int* list;                  // [T * Hkv * nsel] per (block, group): flat selection indices (t * Hkv + g) * nsel + j
+  int qseg, nseg;             // lists per query segment of qseg tokens (segment-major), nseg segments
+  int* cnt;                   // [nseg * nblk * Hkv] entries per (segment, block, group)
+  int* off;                   // [nseg * nblk * Hkv + 1] list offsets
+  int* cur;                   // [nseg * nblk * Hkv] fill cursors
+  int* choff;                 // [nseg * nblk * Hkv + 1] chunk offsets
+  int* list;                  // [T * Hkv * nsel] per list: flat selection indices (t * Hkv + g) * nsel + j
   __nv_bfloat16* part_o;      // forward: [T * Hkv * nsel, G, d] normalised partial outputs (bf16)
   float* part_l;              // forward: [T * Hkv * nsel, G] their log2-sum-exp
   __nv_bfloat16* out;         // forward: [T, Hq, d]
