@@ -27,6 +27,8 @@ def tsa():
     (4, 4, 64, 32, 5, [33, 250]),
     (16, 1, 64, 64, 3, [500]),
     (12, 2, 128, 32, 7, [129, 64, 400]),
+    (8, 2, 128, 64, 1, [300, 90]),         # one selected block per query and group
+    (8, 4, 64, 64, 3, [1, 3, 70]),         # sequences of 1 and 3 tokens
 ])
 def test_gqa_fwd_bwd(tsa, Hq, Hkv, d, bs, nsel, lengths):
     cu = synth.cu_seqlens_thd(lengths)

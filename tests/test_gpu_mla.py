@@ -209,6 +209,8 @@ def test_mla_t65536_h128_sampled(tsa):
     (512, 96, [257]),            # NoPE layout
     (576, 2048, [2100]),         # 64 tiles of 32 keys
     (576, 4096, [4200]),         # the widest top-k: 128 tiles
+    (576, 1, [200]),             # one slot: a single 32-key tile, 31 slots past topk
+    (512, 17, [100, 50]),        # NoPE, a partial first tile, THD
 ])
 def test_mla_h128_forward(tsa, D, topk, lengths):
     """H = 128 (the tcgen05 cluster path): parity with the oracle on sampled rows,
@@ -270,6 +272,8 @@ def test_mla_h128_large_logits_rescale(tsa):
     (512, 96, [257]),            # NoPE layout: four 128-channel dKV blocks
     (576, 2048, [2100]),         # 33 tiles of 64 slots
     (576, 4000, [2100, 300]),    # kp = 4096: 2048-query P/dS chunks, a boundary inside sequence 0
+    (576, 1, [200]),             # one slot
+    (512, 17, [100, 50]),        # NoPE, 17 slots padded to 128
 ])
 def test_mla_h128_backward(tsa, D, topk, lengths):
     """H = 128 backward (recompute of P/dS + tcgen05 dKV GEMM): dO is kept on
