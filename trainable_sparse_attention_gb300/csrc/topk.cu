@@ -511,8 +511,10 @@ __global__ void __launch_bounds__(TK_THREADS, 3) topk_rows_kernel(TopkRows a) {
     // ---- guided sweep: gather every candidate >= g (float order; -0.0 ==
     // +0.0).  g interpolates inside the sample's bin, assuming its entries
     // spread evenly over the bin's score range.  Warp w appends to its own
-    // region of WCAP keys: ballots rank the lanes and the warp's count stays
-    // in a register, so the sweep has no atomics and no shuffles.
+    // region of WCAP keys: per run, each thread marks its hits in a bit mask,
+    // one warp prefix sum of the hit counts places them, and the warp's count
+    // stays in a register (no atomics; the order of the keys inside the region
+    // does not matter: the ranking and the sort depend only on the keys).
     float g = bin_floor(gbin);
     if (gbin + 1 < TK_BINS) {
       const float top = bin_floor(gbin + 1);
@@ -521,18 +523,30 @@ __global__ void __launch_bounds__(TK_THREADS, 3) topk_rows_kernel(TopkRows a) {
     }
     constexpr int WCAP = TK_MAXK / TK_WARPS;
     uint64_t* wk = keys + warp * WCAP;
-    const uint32_t lt = (1u << lane) - 1u;
     uint32_t wcnt = 0;  // warp-uniform
     for_runs_from(row, n, vec, v0, [&](const float (&v)[TK_PER], int64_t i0) {
+      uint32_t msk = 0;
 #pragma unroll
-      for (int e = 0; e < TK_PER; ++e) {
-        const bool hit = v[e] >= g && v[e] != NEG_INF;
-        const uint32_t bal = __ballot_sync(0xffffffffu, hit);
-        if (hit) {
-          const uint32_t pos = wcnt + static_cast<uint32_t>(__popc(bal & lt));
-          if (pos < static_cast<uint32_t>(WCAP)) wk[pos] = comp_key(order_key(v[e]), static_cast<uint32_t>(i0 + e));
+      for (int e = 0; e < TK_PER; ++e) msk |= (v[e] >= g && v[e] != NEG_INF) ? (1u << e) : 0u;
+      if (__any_sync(0xffffffffu, msk != 0u)) {
+        const uint32_t mine = static_cast<uint32_t>(__popc(msk));
+        uint32_t x = mine;  // inclusive scan of the hit counts over the lanes
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
         }
-        wcnt += static_cast<uint32_t>(__popc(bal));
+        uint32_t pos = wcnt + x - mine;
+        while (msk) {
+          const int e = __ffs(msk) - 1;
+          msk &= msk - 1u;
+          float sv = v[0];
+#pragma unroll
+          for (int j = 1; j < TK_PER; ++j) sv = (e == j) ? v[j] : sv;
+          if (pos < static_cast<uint32_t>(WCAP)) wk[pos] = comp_key(order_key(sv), static_cast<uint32_t>(i0 + e));
+          ++pos;
+        }
+        wcnt += __shfl_sync(0xffffffffu, x, 31);
       }
     });
     if (lane == 0) warp_tot[warp] = wcnt;
