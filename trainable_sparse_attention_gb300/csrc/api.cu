@@ -304,7 +304,16 @@ int qsa_topk(const void* q_idx, const void* k_idx, const float* w, const int32_t
   std::lock_guard<std::mutex> lock(g_pipe_mu);
   TopkPipe* pp = nullptr;
   if ((rc = topk_pipe(&pp))) return rc;
-  TSA_CHECK_CUDA(cudaEventRecord(pp->start, s), "fork");
+  cudaError_t fe = cudaEventRecord(pp->start, s);
+  if (fe == cudaErrorInvalidResourceHandle || fe == cudaErrorContextIsDestroyed) {
+    // the context that owned the streams and events is gone (the application
+    // reset the device): make a new set for the current context
+    cudaGetLastError();
+    *pp = TopkPipe();
+    if ((rc = topk_pipe(&pp))) return rc;
+    fe = cudaEventRecord(pp->start, s);
+  }
+  TSA_CHECK_CUDA(fe, "fork");
   TSA_CHECK_CUDA(cudaStreamWaitEvent(pp->idx, pp->start, 0), "fork");
   TSA_CHECK_CUDA(cudaStreamWaitEvent(pp->sel, pp->start, 0), "fork");
   const size_t buf_floats = static_cast<size_t>(C) * groups * width;
