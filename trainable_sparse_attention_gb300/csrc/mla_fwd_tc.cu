@@ -29,9 +29,9 @@
 // lane) owning all 32 key columns of a tile, so a row's maximum and sum stay
 // in one thread (two warps per quadrant, agreeing on each tile's maximum
 // through shared memory, were slower); each rescales and writes its row of
-// the O slice.  Warp 4: TMEM owner and QK^T issuer; warp 5: PV issuer (two
-// issuing threads, so that QK^T waiting for a gather never delays a ready
-// PV); warps 6-9: TMA gathers (tile::gather4, issued from several lanes at
+// the O slice.  Warp 4: TMEM owner and QK^T issuer of the even tiles, warp 11
+// of the odd ones; warp 5: PV issuer (separate issuing threads, so that QK^T
+// waiting for a gather never delays a ready PV); warps 6-9: TMA gathers (tile::gather4, issued from several lanes at
 // once) of the selected rows into a 6-stage ring of 32-key tiles; warp 10:
 // sender, one bulk copy per tile of the staged partial
 // logits into the peer's exchange buffer (per-thread stores into the peer's
@@ -56,13 +56,14 @@ namespace {
 
 constexpr int MT_H = 128;        // heads = MMA M
 constexpr int MT_N = 32;         // keys per tile
-constexpr int MT_STAGES = 6;
+constexpr int MT_STAGES = 6;     // even: tile j's stage is used only by tiles of j's parity
 constexpr int MT_SOFTMAX = 4;    // softmax warps, one per TMEM lane quadrant
 constexpr int MT_W_QK = 4;       // QK^T issuer and TMEM owner
 constexpr int MT_W_PV = 5;       // PV issuer
 constexpr int MT_W_PROD = 6;     // first of the four gather producer warps
 constexpr int MT_W_SEND = 10;    // sender of the staged partial logits
-constexpr int MT_THREADS = 352;
+constexpr int MT_W_QK2 = 11;     // QK^T issuer of the odd tiles (another SM sub-partition than warp 4)
+constexpr int MT_THREADS = 384;
 constexpr int MT_DV = 512;
 constexpr int MT_OCOLS = 256;    // value channels per CTA (TMEM columns [0, 256))
 constexpr int MT_SCOL = 256;     // TMEM column of the two S buffers
@@ -84,6 +85,7 @@ struct MtLayout {
   static constexpr int OFF_BAR = OFF_SB + 2 * X_BYTES;
   static constexpr int SMEM = 1024 + OFF_BAR + 512;
   static_assert(MT_QCOL + 32 * KBMAX <= MT_PCOL && MT_PCOL + 2 * 16 <= 512, "TMEM columns");
+  static_assert(MT_STAGES % 2 == 0, "each QK^T issuer owns the stages of its tiles");
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -219,22 +221,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
     volatile int keep_waiting = 0;
     for (int g = issued > MT_STAGES ? issued - MT_STAGES : 0; g < issued; ++g)
       (void)tc::mbar_wait(&kv_full[g % MT_STAGES], (g / MT_STAGES) & 1, &keep_waiting);
-  } else if (warp == MT_W_QK) {
-    // ------------------------------------------------------------ QK^T issuer (A = q slice in TMEM)
+  } else if (warp == MT_W_QK || warp == MT_W_QK2) {
+    // ------------------------------------------------------------ QK^T issuers (A = q slice in TMEM)
+    // One thread keeps only one tcgen05.mma in issue at a time (~50 ns each,
+    // whatever N is), so the 16 to 20 MMAs of a tile's QK^T take most of a
+    // tile period from one thread; two threads on different SM sub-partitions
+    // take the even and the odd tiles (S buffer j & 1), and each tile's MMAs
+    // still accumulate in order on one thread.  With an even number of stages
+    // each issuer also owns the stages of its tiles.
     if (lane == 0) {
       constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(MT_H, MT_N);
       bool ok = tc::mbar_wait(qready, 0, abort_flag);
       tc::fence_after_sync();
-      // QK^T of every tile, as soon as its rows have landed and an S buffer is
-      // free (the softmax frees one as soon as it has read it).
-      for (int j = 0; ok && j < ntiles; ++j) {
+      // QK^T of each of this issuer's tiles, as soon as its rows have landed and
+      // its S buffer is free (the softmax frees one as soon as it has read it).
+      for (int j = warp == MT_W_QK ? 0 : 1; ok && j < ntiles; j += 2) {
         const int st = j % MT_STAGES, b = j & 1;
         if (!tc::mbar_wait(&kv_full[st], (j / MT_STAGES) & 1, abort_flag) ||
             !tc::mbar_wait(&s_empty[b], ((j >> 1) & 1) ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
-        tc::fence_proxy_async_smem();  // kept from the cp.async version: the rows now arrive by TMA (async proxy) and need no proxy fence
         tc::fence_after_sync();
         const uint32_t d = tmem + MT_SCOL + b * MT_N;
         for (int c = 0; c < kb; ++c) {
