@@ -38,10 +38,13 @@
 // shared memory held up the softmax warps' next shared-memory accesses by
 // ~0.5 us per tile).
 //
-// The softmax is software-pipelined: while tile j is normalised, the partial
-// logits of tile j+1 are already on their way to the peer (two exchange
-// buffers), and P is double-buffered so PV(j) never waits for the softmax of
-// tile j+1.  The running max is rescaled lazily (only when it grows by more
+// The softmax is software-pipelined: a tile's partial logits are staged for
+// the peer before the peer's half of the previous tile is awaited, so the
+// exchange (a bulk copy lands ~0.6 us after its issue) overlaps a whole
+// normalisation; four exchange buffers keep the peer's sends ordered by the
+// exchange itself (the peer stages tile j only after it received this CTA's
+// tile j - 2, staged after this CTA read buffer j % 4 for tile j - 4).  P is
+// double-buffered so PV(j) never waits for the softmax of tile j+1.  The running max is rescaled lazily (only when it grows by more
 // than 2^8), so the O slice in TMEM is rarely touched.  Every wait is bounded;
 // a timeout raises TSA_FLAG_TIMEOUT and both CTAs wind down.
 #include "kernels.cuh"
@@ -69,6 +72,7 @@ constexpr int MT_OCOLS = 256;    // value channels per CTA (TMEM columns [0, 256
 constexpr int MT_SCOL = 256;     // TMEM column of the two S buffers
 constexpr int MT_QCOL = 320;     // TMEM column of the q slice (up to 160 columns)
 constexpr int MT_PCOL = 480;     // TMEM column of the two P buffers (32 keys of bf16 pairs = 16 columns each)
+constexpr int MT_XBUF = 4;       // exchange buffers: the peer's half of tile j lands in buffer j % 4
 constexpr float kRescaleLog2 = 8.f;
 
 template <int D>
@@ -81,7 +85,7 @@ struct MtLayout {
   static constexpr int X_BYTES = MT_H * MT_N * 4;    // one exchange buffer
   static constexpr int OFF_KV = 0;
   static constexpr int OFF_X = OFF_KV + MT_STAGES * KV_STAGE;
-  static constexpr int OFF_SB = OFF_X + 2 * X_BYTES;  // two staging buffers of this CTA's partials (same layout as X)
+  static constexpr int OFF_SB = OFF_X + MT_XBUF * X_BYTES;  // two staging buffers of this CTA's partials (same layout as X)
   static constexpr int OFF_BAR = OFF_SB + 2 * X_BYTES;
   static constexpr int SMEM = 1024 + OFF_BAR + 512;
   static_assert(MT_QCOL + 32 * KBMAX <= MT_PCOL && MT_PCOL + 2 * 16 <= 512, "TMEM columns");
@@ -105,7 +109,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* gbase = smem_raw + (base - raw);
   const uint32_t sKV = base + L::OFF_KV;
-  // [2][128][32] partial logits written by the peer; chunk q (4 floats) of row h
+  // [4][128][32] partial logits written by the peer; chunk q (4 floats) of row h
   // sits at chunk q ^ (h & 7), so the 16-byte stores and loads of a warp spread
   // over all banks
   float* X = reinterpret_cast<float*>(gbase + L::OFF_X);
@@ -117,8 +121,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
   uint64_t* s_empty = s_full + 2;                     // [2] (one arrival per softmax warp)
   uint64_t* p_full = s_empty + 2;                     // [2] (one arrival per softmax warp)
   uint64_t* p_empty = p_full + 2;                     // [2] (PV of that buffer completed)
-  uint64_t* xfull = p_empty + 2;                      // [2] the peer's half of a tile landed in my X[b]
-  uint64_t* sb_full = xfull + 2;                      // [2] staging buffer written (one arrival per softmax warp)
+  uint64_t* xfull = p_empty + 2;                      // [4] the peer's half of tile j landed in my X[j % 4]
+  uint64_t* sb_full = xfull + MT_XBUF;                // [2] staging buffer written (one arrival per softmax warp)
   uint64_t* sb_empty = sb_full + 2;                   // [2] bulk copy of the staging buffer has read it
   uint64_t* mask_full = sb_empty + 2;                 // [STAGES] valid-slot bits of the stage written
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mask_full + MT_STAGES);
@@ -150,16 +154,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
       tc::mbar_init(&s_empty[i], MT_SOFTMAX);
       tc::mbar_init(&p_full[i], MT_SOFTMAX);
       tc::mbar_init(&p_empty[i], 1);
-      tc::mbar_init(&xfull[i], 1);  // own expect_tx arrival + the peer's st.async bytes
     }
+    for (int i = 0; i < MT_XBUF; ++i) tc::mbar_init(&xfull[i], 1);  // own expect_tx arrival + the peer's bulk copy
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&sb_full[i], MT_SOFTMAX);
       tc::mbar_init(&sb_empty[i], 1);
     }
     *abort_flag = 0;
     tc::fence_barrier_init();
-    tc::mbar_arrive_expect_tx(&xfull[0], L::X_BYTES);  // tiles 0 and 1
-    tc::mbar_arrive_expect_tx(&xfull[1], L::X_BYTES);
+    for (int i = 0; i < MT_XBUF; ++i) tc::mbar_arrive_expect_tx(&xfull[i], L::X_BYTES);  // tiles 0 .. 3
   }
   if (warp == MT_W_QK) tc::tmem_alloc(tmem_slot, 512);
   tc::fence_before_sync();
@@ -270,8 +273,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
           ok = false;
           break;
         }
-        tc::bulk_copy_to_peer(x_peer + b * L::X_BYTES, base + L::OFF_SB + b * L::X_BYTES, L::X_BYTES,
-                              peer_xfull + b * 8);
+        const int xb = j & (MT_XBUF - 1);
+        tc::bulk_copy_to_peer(x_peer + xb * L::X_BYTES, base + L::OFF_SB + b * L::X_BYTES, L::X_BYTES,
+                              peer_xfull + xb * 8);
         tc::bulk_commit();
         tc::bulk_wait_read0();
         tc::mbar_arrive(&sb_empty[b]);
@@ -304,9 +308,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
     // ------------------------------------------------------------ softmax (warps 0-3)
     // Thread h (warp h / 32 reads its TMEM lane quadrant) owns row h: all 32
     // key columns of every tile, so a row's maximum and sum never leave the
-    // thread.  Iteration j: fetch tile j's partial logits from TMEM, receive
-    // the peer's half of tile j-1, stage this CTA's half of tile j for the
-    // sender, then normalise tile j-1 while it travels.
+    // thread.  Iteration j: fetch tile j's partial logits from TMEM and stage
+    // them for the sender, then add the peer's half of tile j-1 to this CTA's
+    // (read back from the staging row) and normalise tile j-1.
     const int h = warp * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     // q slice row h -> TMEM columns [MT_QCOL, MT_QCOL + 32 kb)
@@ -335,11 +339,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
     }
     float m_use = NEG_INF, l = 0.f;  // running max and row sum
     bool ok = true;
-    uint32_t cur[32];
     for (int j = 0; j <= ntiles; ++j) {
-      uint32_t nxt[32];
       if (j < ntiles) {
+        // tile j's partial logits, staged for the sender at once (same swizzled
+        // layout as the peer's exchange buffer), before this thread waits for
+        // the peer's half of tile j - 1: the exchange then takes a tile period
+        // per two tiles instead of setting every period.  Staging buffer b is
+        // free once the bulk copy of tile j - 2 has read it (this thread read
+        // its own row of tile j - 2 back from it in the previous iteration).
         const int b = j & 1;
+        uint32_t nxt[32];
         if (!__all_sync(0xffffffffu, tc::mbar_wait(&s_full[b], (j >> 1) & 1, abort_flag))) { ok = false; break; }
         tc::fence_after_sync();
         __syncwarp();
@@ -348,33 +357,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&s_empty[b]);
-      }
-      // receive the peer's half of tile j-1 (published at the end of its previous iteration)
-      float x2[32];
-      if (j > 0) {
-        const int jj = j - 1, bb = jj & 1;
-        if (!__all_sync(0xffffffffu, tc::mbar_wait_cluster(&xfull[bb], (jj >> 1) & 1, abort_flag))) {
-          ok = false;
-          break;
-        }
-        const float4* xr = reinterpret_cast<const float4*>(X + bb * (MT_H * MT_N) + h * MT_N);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float4 v = xr[q ^ (h & 7)];  // 16-byte chunks of a row are swizzled by the row
-          x2[4 * q] = __uint_as_float(cur[4 * q]) + v.x;
-          x2[4 * q + 1] = __uint_as_float(cur[4 * q + 1]) + v.y;
-          x2[4 * q + 2] = __uint_as_float(cur[4 * q + 2]) + v.z;
-          x2[4 * q + 3] = __uint_as_float(cur[4 * q + 3]) + v.w;
-        }
-        // the next use of X[bb] is tile jj+2; the peer can send it only after
-        // all of this CTA's threads sent tile jj+1, i.e. after they read X[bb]
-        if (h == 0 && jj + 2 < ntiles) tc::mbar_arrive_expect_tx(&xfull[bb], L::X_BYTES);
-      }
-      // stage this thread's row of tile j for the sender (same swizzled layout
-      // as the peer's exchange buffer); staging buffer b is free once the bulk
-      // copy of tile j-2 has read it
-      if (j < ntiles) {
-        const int b = j & 1;
         if (!__all_sync(0xffffffffu, tc::mbar_wait(&sb_empty[b], ((j >> 1) & 1) ^ 1u, abort_flag))) {
           ok = false;
           break;
@@ -387,6 +369,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
         tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&sb_full[b]);
+      }
+      // tile j - 1: this CTA's half (its staging row) plus the peer's
+      float x2[32];
+      if (j > 0) {
+        const int jj = j - 1, bb = jj & 1, xb = jj & (MT_XBUF - 1);
+        if (!__all_sync(0xffffffffu, tc::mbar_wait_cluster(&xfull[xb], (jj >> 2) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        const float4* xr = reinterpret_cast<const float4*>(X + xb * (MT_H * MT_N) + h * MT_N);
+        const float4* mr = reinterpret_cast<const float4*>(gbase + L::OFF_SB + bb * L::X_BYTES + h * (MT_N * 4));
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 v = xr[q ^ (h & 7)];  // 16-byte chunks of a row are swizzled by the row
+          const float4 u = mr[q ^ (h & 7)];
+          x2[4 * q] = u.x + v.x;
+          x2[4 * q + 1] = u.y + v.y;
+          x2[4 * q + 2] = u.z + v.z;
+          x2[4 * q + 3] = u.w + v.w;
+        }
+        // the next use of X[xb] is tile jj + 4; the peer sends it only after it
+        // received this CTA's tile jj + 2, which this CTA stages after reading X[xb]
+        if (h == 0 && jj + MT_XBUF < ntiles) tc::mbar_arrive_expect_tx(&xfull[xb], L::X_BYTES);
       }
       if (j > 0) {
         const int jj = j - 1, bb = jj & 1;
@@ -458,8 +463,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&p_full[bb]);
       }
-#pragma unroll
-      for (int i = 0; i < 32; ++i) cur[i] = nxt[i];
     }
     if (!ok) *abort_flag = 1;
     // epilogue: O row / l -> bf16, lse
