@@ -310,7 +310,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
     // key columns of every tile, so a row's maximum and sum never leave the
     // thread.  Iteration j: fetch tile j's partial logits from TMEM and stage
     // them for the sender, then add the peer's half of tile j-1 to this CTA's
-    // (read back from the staging row) and normalise tile j-1.
+    // and normalise tile j-1.
     const int h = warp * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     // q slice row h -> TMEM columns [MT_QCOL, MT_QCOL + 32 kb)
@@ -339,16 +339,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
     }
     float m_use = NEG_INF, l = 0.f;  // running max and row sum
     bool ok = true;
+    uint32_t cur[32];  // this CTA's partial logits of tile j - 1 (staged in the previous iteration)
     for (int j = 0; j <= ntiles; ++j) {
+      uint32_t nxt[32];
       if (j < ntiles) {
         // tile j's partial logits, staged for the sender at once (same swizzled
         // layout as the peer's exchange buffer), before this thread waits for
         // the peer's half of tile j - 1: the exchange then takes a tile period
         // per two tiles instead of setting every period.  Staging buffer b is
-        // free once the bulk copy of tile j - 2 has read it (this thread read
-        // its own row of tile j - 2 back from it in the previous iteration).
+        // free once the bulk copy of tile j - 2 has read it.
         const int b = j & 1;
-        uint32_t nxt[32];
         if (!__all_sync(0xffffffffu, tc::mbar_wait(&s_full[b], (j >> 1) & 1, abort_flag))) { ok = false; break; }
         tc::fence_after_sync();
         __syncwarp();
@@ -370,7 +370,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&sb_full[b]);
       }
-      // tile j - 1: this CTA's half (its staging row) plus the peer's
+      // tile j - 1: this CTA's half plus the peer's
       float x2[32];
       if (j > 0) {
         const int jj = j - 1, bb = jj & 1, xb = jj & (MT_XBUF - 1);
@@ -379,15 +379,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
           break;
         }
         const float4* xr = reinterpret_cast<const float4*>(X + xb * (MT_H * MT_N) + h * MT_N);
-        const float4* mr = reinterpret_cast<const float4*>(gbase + L::OFF_SB + bb * L::X_BYTES + h * (MT_N * 4));
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const float4 v = xr[q ^ (h & 7)];  // 16-byte chunks of a row are swizzled by the row
-          const float4 u = mr[q ^ (h & 7)];
-          x2[4 * q] = u.x + v.x;
-          x2[4 * q + 1] = u.y + v.y;
-          x2[4 * q + 2] = u.z + v.z;
-          x2[4 * q + 3] = u.w + v.w;
+          x2[4 * q] = __uint_as_float(cur[4 * q]) + v.x;
+          x2[4 * q + 1] = __uint_as_float(cur[4 * q + 1]) + v.y;
+          x2[4 * q + 2] = __uint_as_float(cur[4 * q + 2]) + v.z;
+          x2[4 * q + 3] = __uint_as_float(cur[4 * q + 3]) + v.w;
         }
         // the next use of X[xb] is tile jj + 4; the peer sends it only after it
         // received this CTA's tile jj + 2, which this CTA stages after reading X[xb]
@@ -463,6 +461,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&p_full[bb]);
       }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) cur[i] = nxt[i];
     }
     if (!ok) *abort_flag = 1;
     // epilogue: O row / l -> bf16, lse
