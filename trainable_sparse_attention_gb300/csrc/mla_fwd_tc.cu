@@ -340,6 +340,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MT_THREADS, 1)
     float m_use = NEG_INF, l = 0.f;  // running max and row sum
     bool ok = true;
     uint32_t cur[32];  // this CTA's partial logits of tile j - 1 (staged in the previous iteration)
+#pragma unroll 2
     for (int j = 0; j <= ntiles; ++j) {
       uint32_t nxt[32];
       if (j < ntiles) {
