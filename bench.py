@@ -50,7 +50,7 @@ TOPK = 2048
 # DRAM bytes (read + write) of one forward launch per query, from an ncu capture
 # of the current forward kernel on the same workload at T=4096 (scaled by the
 # number of queries); None when the kernel changed since the capture.
-FWD_TRAFFIC_BYTES_PER_QUERY = 277641  # (0.642514 + 0.494703) GB / 4096 queries; re-captured for each forward kernel change
+FWD_TRAFFIC_BYTES_PER_QUERY = 277630  # (0.642460 + 0.494712) GB / 4096 queries; re-captured for each forward kernel change
 SCALE = 1.0 / math.sqrt(192)
 H_I = 64
 D_I = 128
