@@ -61,7 +61,7 @@ constexpr int MT_H = 128;        // heads = MMA M
 constexpr int MT_N = 32;         // keys per tile
 constexpr int MT_STAGES = 6;     // even: tile j's stage is used only by tiles of j's parity
 constexpr int MT_SOFTMAX = 4;    // softmax warps, one per TMEM lane quadrant
-constexpr int MT_W_QK = 4;       // QK^T issuer and TMEM owner
+constexpr int MT_W_QK = 4;       // QK^T issuer of the even tiles and TMEM owner
 constexpr int MT_W_PV = 5;       // PV issuer
 constexpr int MT_W_PROD = 6;     // first of the four gather producer warps
 constexpr int MT_W_SEND = 10;    // sender of the staged partial logits
