@@ -31,12 +31,12 @@
 // through shared memory, were slower); each rescales and writes its row of
 // the O slice.  Warp 4: TMEM owner and QK^T issuer of the even tiles, warp 11
 // of the odd ones; warp 5: PV issuer (separate issuing threads, so that QK^T
-// waiting for a gather never delays a ready PV); warps 6-9: TMA gathers (tile::gather4, issued from several lanes at
-// once) of the selected rows into a 6-stage ring of 32-key tiles; warp 10:
-// sender, one bulk copy per tile of the staged partial
-// logits into the peer's exchange buffer (per-thread stores into the peer's
-// shared memory held up the softmax warps' next shared-memory accesses by
-// ~0.5 us per tile).
+// waiting for a gather never delays a ready PV); warps 6-9: TMA gathers
+// (tile::gather4, issued from several lanes at once) of the selected rows into
+// a 6-stage ring of 32-key tiles; warp 10: sender, one bulk copy per tile of
+// the staged partial logits into the peer's exchange buffer (per-thread stores
+// into the peer's shared memory held up the softmax warps' next shared-memory
+// accesses by ~0.5 us per tile).
 //
 // The softmax is software-pipelined: a tile's partial logits are staged for
 // the peer before the peer's half of the previous tile is awaited, so the
@@ -44,9 +44,10 @@
 // normalisation; four exchange buffers keep the peer's sends ordered by the
 // exchange itself (the peer stages tile j only after it received this CTA's
 // tile j - 2, staged after this CTA read buffer j % 4 for tile j - 4).  P is
-// double-buffered so PV(j) never waits for the softmax of tile j+1.  The running max is rescaled lazily (only when it grows by more
-// than 2^8), so the O slice in TMEM is rarely touched.  Every wait is bounded;
-// a timeout raises TSA_FLAG_TIMEOUT and both CTAs wind down.
+// double-buffered so PV(j) never waits for the softmax of tile j+1.  The
+// running max is rescaled lazily (only when it grows by more than 2^8), so the
+// O slice in TMEM is rarely touched.  Every wait is bounded; a timeout raises
+// TSA_FLAG_TIMEOUT and both CTAs wind down.
 #include "kernels.cuh"
 #include "tc.cuh"
 
